@@ -1,0 +1,176 @@
+"""fp64 CPU oracle of the test-time memory update (Titans / Miras / ATLAS family).
+
+TEST INFRASTRUCTURE ONLY.  The tests, the package smoke check and the
+benchmark's CPU-baseline leg are the only callers; the CUDA library never
+imports, loads or links anything here, and nothing here imports the CUDA
+library.  The arithmetic lives in ``atlas_oracle.c`` (plain C, fp64, literal
+token loops, threads over heads); this module only compiles it with gcc and
+marshals numpy arrays through ctypes.
+
+What each C function follows (page title, section) is stated in the C file.
+Every function here is pinned by a ``-m "not gpu"`` test against a closed form,
+an invariant, a library routine or brute force; see ``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "atlas_oracle.c")
+_LIB = os.path.join(_HERE, "_build", "libatlas_oracle.so")
+
+MEM_LINEAR, MEM_MLP = 0, 1
+PHI_IDENTITY, PHI_POLY2 = 0, 1
+LOSS_L2, LOSS_DOT = 0, 1
+
+
+class OrcCfg(ctypes.Structure):
+    _fields_ = [
+        ("N", ctypes.c_int), ("d_k", ctypes.c_int), ("d_v", ctypes.c_int),
+        ("d_h", ctypes.c_int), ("mem", ctypes.c_int), ("phi", ctypes.c_int),
+        ("loss", ctypes.c_int), ("c", ctypes.c_int), ("b", ctypes.c_int),
+        ("ns_steps", ctypes.c_int), ("ns_a", ctypes.c_double),
+        ("ns_b", ctypes.c_double), ("ns_c", ctypes.c_double),
+        ("ns_eps", ctypes.c_double),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (portable flags: no -march, no intrinsics)."""
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fno-fast-math",
+                           "-ffp-contract=off", "-o", tmp, _SRC, "-lm", "-lpthread"])
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            dp = ctypes.POINTER(ctypes.c_double)
+            cp = ctypes.POINTER(OrcCfg)
+            lib.orc_feature_dim.argtypes = [cp]
+            lib.orc_feature_dim.restype = ctypes.c_int
+            lib.orc_state_size.argtypes = [cp]
+            lib.orc_state_size.restype = ctypes.c_long
+            lib.orc_phi.argtypes = [cp, dp, dp]
+            lib.orc_gelu.argtypes = [ctypes.c_double]
+            lib.orc_gelu.restype = ctypes.c_double
+            lib.orc_gelu_prime.argtypes = [ctypes.c_double]
+            lib.orc_gelu_prime.restype = ctypes.c_double
+            lib.orc_memory_apply.argtypes = [cp, dp, dp, dp]
+            lib.orc_grad.argtypes = [cp, dp, dp, dp, dp]
+            lib.orc_newton_schulz.argtypes = [ctypes.c_int, ctypes.c_int, dp, ctypes.c_int,
+                                              ctypes.c_double, ctypes.c_double,
+                                              ctypes.c_double, ctypes.c_double, dp]
+            fwd = [cp, ctypes.c_int] + [dp] * 10 + [ctypes.c_int]
+            lib.orc_forward_chunked.argtypes = fwd
+            lib.orc_forward_chunked.restype = ctypes.c_int
+            lib.orc_forward_recurrent.argtypes = fwd
+            lib.orc_forward_recurrent.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def make_cfg(N, d_k, d_v, d_h=0, mem=MEM_LINEAR, phi=PHI_IDENTITY, loss=LOSS_L2, c=1, b=1,
+             ns_steps=0, ns_a=0.0, ns_b=0.0, ns_c=0.0, ns_eps=0.0) -> OrcCfg:
+    return OrcCfg(int(N), int(d_k), int(d_v), int(d_h), int(mem), int(phi), int(loss),
+                  int(c), int(b), int(ns_steps), float(ns_a), float(ns_b), float(ns_c),
+                  float(ns_eps))
+
+
+def feature_dim(cfg: OrcCfg) -> int:
+    return _load().orc_feature_dim(ctypes.byref(cfg))
+
+
+def state_size(cfg: OrcCfg) -> int:
+    return _load().orc_state_size(ctypes.byref(cfg))
+
+
+def phi(cfg: OrcCfg, x) -> np.ndarray:
+    x = _f64(x)
+    out = np.zeros(feature_dim(cfg))
+    _load().orc_phi(ctypes.byref(cfg), _p(x), _p(out))
+    return out
+
+
+def gelu(x: float) -> float:
+    return _load().orc_gelu(float(x))
+
+
+def gelu_prime(x: float) -> float:
+    return _load().orc_gelu_prime(float(x))
+
+
+def memory_apply(cfg: OrcCfg, state, x) -> np.ndarray:
+    state, x = _f64(state), _f64(x)
+    out = np.zeros(cfg.d_v)
+    _load().orc_memory_apply(ctypes.byref(cfg), _p(state), _p(x), _p(out))
+    return out
+
+
+def grad(cfg: OrcCfg, state, k, v) -> np.ndarray:
+    state, k, v = _f64(state), _f64(k), _f64(v)
+    G = np.zeros(state_size(cfg))
+    _load().orc_grad(ctypes.byref(cfg), _p(state), _p(k), _p(v), _p(G))
+    return G
+
+
+def newton_schulz(S, steps, a, b, c, eps) -> np.ndarray:
+    S = _f64(S)
+    rows, cols = S.shape
+    out = np.zeros_like(S)
+    _load().orc_newton_schulz(rows, cols, _p(S), int(steps), float(a), float(b), float(c),
+                              float(eps), _p(out))
+    return out
+
+
+def forward(cfg: OrcCfg, K, Q, V, alpha, eta, theta, gamma, M0=None, S0=None,
+            recurrent: bool = False, n_threads: int = 0):
+    """Run the oracle over H independent heads.
+
+    K, Q: [H, N, d_k]; V: [H, N, d_v]; alpha, eta, theta: [H, N]; gamma: [c];
+    M0, S0: [H, state] or None (zeros).  Returns (Y [H, N, d_v], M [H, state],
+    S [H, state]), all fp64.
+    """
+    K, Q, V = _f64(K), _f64(Q), _f64(V)
+    H = K.shape[0]
+    assert K.shape == (H, cfg.N, cfg.d_k) and Q.shape == K.shape
+    assert V.shape == (H, cfg.N, cfg.d_v)
+    alpha, eta, theta = _f64(alpha), _f64(eta), _f64(theta)
+    assert alpha.shape == (H, cfg.N) and eta.shape == alpha.shape and theta.shape == alpha.shape
+    gamma = _f64(gamma)
+    assert gamma.shape == (cfg.c,)
+    ns = state_size(cfg)
+    M = np.zeros((H, ns)) if M0 is None else _f64(M0).reshape(H, ns).copy()
+    S = np.zeros((H, ns)) if S0 is None else _f64(S0).reshape(H, ns).copy()
+    Y = np.zeros((H, cfg.N, cfg.d_v))
+    fn = _load().orc_forward_recurrent if recurrent else _load().orc_forward_chunked
+    rc = fn(ctypes.byref(cfg), H, _p(K), _p(Q), _p(V), _p(alpha), _p(eta), _p(theta),
+            _p(gamma), _p(M), _p(S), _p(Y), int(n_threads))
+    if rc != 0:
+        raise ValueError("oracle rejected the problem description")
+    return Y, M, S

@@ -1,0 +1,439 @@
+/*
+ * atlas_oracle.c -- plain, slow, fp64 CPU oracle of the test-time memory update
+ * (Titans / Miras / ATLAS family).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls
+ * this file; only the tests, the package's smoke check and the benchmark's CPU
+ * baseline leg do.  It shares no code, header, table or helper with the CUDA
+ * library: every formula here is written out again from the pages.
+ *
+ * Sources (page title, section):
+ *   [Titans]  "[Paper Review] Titans 논문 이해하기" (rahites.tistory.com),
+ *             "Learning Process and Surprise Metric" (momentum S_t),
+ *             "Objective" (l2 attentional bias), "Forgetting Mechanism"
+ *             (M_t = (1-alpha_t) M_{t-1} + S_t), "Retrieving a Memory"
+ *             (y_t = M*(q_t), a forward pass without update).
+ *   [ATLAS]   "논문 리뷰 Google ATLAS" (velog.io), §3.1 (polynomial feature
+ *             map Phi_p, l2 bias on Phi(k)), §3.2 (Omega rule: sliding-window
+ *             loss sum_{i=t-c+1..t} gamma_i ||M(Phi(k_i)) - v_i||^2),
+ *             §3.3 (chunked form: gradients inside a chunk taken at the state
+ *             the previous chunk ended with).
+ *   [ATLAS-s] "ATLAS: Learning to Optimally Memorize the Context at Test
+ *             Time" (paperlayer.ai summary), §5 Memory Optimization (Muon /
+ *             Newton-Schulz in place of plain GD), App. E (2-layer residual
+ *             MLP memory, expansion 4, GELU).
+ *   [Miras]   "It's All Connected: A Journey Through Test-Time Memorization,
+ *             ..." (still-with-you.github.io), Associative Memory & Attentional
+ *             Bias (linear attention = GD on -2<Mk, v>), Training (chunk-wise
+ *             parallelisation at the chunk-start state, Miras layer outputs
+ *             M(q_t)).
+ *
+ * Readings taken where the pages are silent or disagree (each one is listed
+ * in the design notes of the repository):
+ *   - gate names follow [Titans]/[Miras]: S_t = eta_t S_{t-1} - theta_t g_t,
+ *     M_t = (1 - alpha_t) M_{t-1} + S_t;
+ *   - the loss is ||.||^2 with no 1/2, so the gradient carries the factor 2;
+ *   - the chunk-start state is the state after the last token of the
+ *     previous chunk, so b = 1 is the token recurrence;
+ *   - gamma is fixed per lag j = t - i (gamma[0] weighs the current token),
+ *     not renormalised, and the window is clipped at the first token;
+ *   - readout is after the write: y_t = M_t(Phi(q_t));
+ *   - Phi_2(x) = [x_1..x_d, x_i x_j for i <= j, i-major], no constant term and
+ *     no multinomial weights (d = 32 gives 560 features);
+ *   - MLP memory M(x) = x + W1 GELU(W2 x) without LayerNorm, exact (erf) GELU;
+ *   - Newton-Schulz (when enabled) acts on the momentum of each weight matrix
+ *     separately, per token: M_t = (1 - alpha_t) M_{t-1} + NS(S_t), with
+ *     X_0 = S / (||S||_F + eps) and the literal X X^T Gram.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#define ORC_MEM_LINEAR 0
+#define ORC_MEM_MLP 1
+#define ORC_PHI_IDENTITY 0
+#define ORC_PHI_POLY2 1
+#define ORC_LOSS_L2 0
+#define ORC_LOSS_DOT 1
+
+/* Per-head problem description.  All tensors handed to the oracle are fp64,
+ * one head after another. */
+typedef struct {
+  int N;        /* tokens */
+  int d_k;      /* key / query width before the feature map */
+  int d_v;      /* value width */
+  int d_h;      /* MLP hidden width (MLP memory only) */
+  int mem;      /* ORC_MEM_LINEAR or ORC_MEM_MLP */
+  int phi;      /* ORC_PHI_IDENTITY or ORC_PHI_POLY2 (linear memory only) */
+  int loss;     /* ORC_LOSS_L2 or ORC_LOSS_DOT */
+  int c;        /* Omega window length, >= 1 */
+  int b;        /* chunk length, >= 1 (1 = token recurrence) */
+  int ns_steps; /* Newton-Schulz iterations on the momentum, 0 = none */
+  double ns_a, ns_b, ns_c, ns_eps;
+} orc_cfg;
+
+/* ------------------------------------------------------------------ sizes */
+
+/* Width of Phi(x).  [ATLAS] §3.1: Phi_p(x) = [x^beta]_{|beta| <= p}; with the
+ * constant dropped and p = 2 that is d linear terms and d(d+1)/2 products. */
+int orc_feature_dim(const orc_cfg* g) {
+  if (g->mem == ORC_MEM_MLP) return g->d_k;
+  if (g->phi == ORC_PHI_POLY2) return g->d_k + g->d_k * (g->d_k + 1) / 2;
+  return g->d_k;
+}
+
+/* Number of fp64 entries in one head's memory state (and in its momentum). */
+long orc_state_size(const orc_cfg* g) {
+  if (g->mem == ORC_MEM_MLP) return 2L * g->d_k * g->d_h;
+  return (long)g->d_v * orc_feature_dim(g);
+}
+
+/* --------------------------------------------------------- feature map Phi */
+
+/* [ATLAS] §3.1 polynomial map, degree 2, read as described above. */
+void orc_phi(const orc_cfg* g, const double* x, double* out) {
+  int d = g->d_k;
+  for (int i = 0; i < d; ++i) out[i] = x[i];
+  if (g->mem == ORC_MEM_MLP || g->phi == ORC_PHI_IDENTITY) return;
+  int p = d;
+  for (int i = 0; i < d; ++i)
+    for (int j = i; j < d; ++j) out[p++] = x[i] * x[j];
+}
+
+/* ------------------------------------------------------------------- GELU */
+
+/* GELU(x) = x * P(X <= x), X ~ N(0,1), written with erf. */
+double orc_gelu(double x) { return 0.5 * x * (1.0 + erf(x / sqrt(2.0))); }
+
+/* d/dx GELU(x) = P(X <= x) + x * pdf(x). */
+double orc_gelu_prime(double x) {
+  const double inv_sqrt_2pi = 0.39894228040143267794;
+  return 0.5 * (1.0 + erf(x / sqrt(2.0))) + x * inv_sqrt_2pi * exp(-0.5 * x * x);
+}
+
+/* ------------------------------------------------------- memory forward */
+
+/* Memory output M(x) for a key/query x (before Phi).
+ * Linear: M Phi(x).  MLP: x + W1 GELU(W2 x)  ([ATLAS-s] App. E; [Titans]
+ * Memory Architecture).  `out` has d_v entries. */
+void orc_memory_apply(const orc_cfg* g, const double* state, const double* x, double* out) {
+  if (g->mem == ORC_MEM_LINEAR) {
+    int D = orc_feature_dim(g);
+    double* f = (double*)malloc(sizeof(double) * D);
+    orc_phi(g, x, f);
+    for (int r = 0; r < g->d_v; ++r) {
+      double s = 0.0;
+      for (int j = 0; j < D; ++j) s += state[(long)r * D + j] * f[j];
+      out[r] = s;
+    }
+    free(f);
+    return;
+  }
+  int d = g->d_k, dh = g->d_h;
+  const double* W1 = state;                  /* d  x dh */
+  const double* W2 = state + (long)d * dh;   /* dh x d  */
+  double* h = (double*)malloc(sizeof(double) * dh);
+  for (int j = 0; j < dh; ++j) {
+    double z = 0.0;
+    for (int i = 0; i < d; ++i) z += W2[(long)j * d + i] * x[i];
+    h[j] = orc_gelu(z);
+  }
+  for (int r = 0; r < d; ++r) {
+    double s = x[r];
+    for (int j = 0; j < dh; ++j) s += W1[(long)r * dh + j] * h[j];
+    out[r] = s;
+  }
+  free(h);
+}
+
+/* ------------------------------------------------------- loss gradient */
+
+/* Gradient of the attentional bias with respect to the memory state, written
+ * into G (state layout).
+ *   l2  ([Titans] Objective; [ATLAS] §3.1):  l = ||M(Phi(k)) - v||^2.
+ *   dot ([Miras] Associative Memory & Attentional Bias): l = -2 <M(Phi(k)), v>.
+ * For the MLP the gradient is plain backpropagation through
+ * y = k + W1 h, h = GELU(z), z = W2 k. */
+void orc_grad(const orc_cfg* g, const double* state, const double* k, const double* v, double* G) {
+  if (g->mem == ORC_MEM_LINEAR) {
+    int D = orc_feature_dim(g), dv = g->d_v;
+    double* f = (double*)malloc(sizeof(double) * D);
+    double* e = (double*)malloc(sizeof(double) * dv);
+    orc_phi(g, k, f);
+    for (int r = 0; r < dv; ++r) {
+      if (g->loss == ORC_LOSS_DOT) {
+        e[r] = -v[r];               /* dl/d(M Phi) = -2 v */
+      } else {
+        double s = 0.0;
+        for (int j = 0; j < D; ++j) s += state[(long)r * D + j] * f[j];
+        e[r] = s - v[r];            /* dl/d(M Phi) = 2 (M Phi - v) */
+      }
+    }
+    for (int r = 0; r < dv; ++r)
+      for (int j = 0; j < D; ++j) G[(long)r * D + j] = 2.0 * e[r] * f[j];
+    free(f);
+    free(e);
+    return;
+  }
+  int d = g->d_k, dh = g->d_h;
+  const double* W1 = state;
+  const double* W2 = state + (long)d * dh;
+  double* G1 = G;
+  double* G2 = G + (long)d * dh;
+  double* z = (double*)malloc(sizeof(double) * dh);
+  double* h = (double*)malloc(sizeof(double) * dh);
+  double* dy = (double*)malloc(sizeof(double) * d);
+  double* dz = (double*)malloc(sizeof(double) * dh);
+  for (int j = 0; j < dh; ++j) {
+    double s = 0.0;
+    for (int i = 0; i < d; ++i) s += W2[(long)j * d + i] * k[i];
+    z[j] = s;
+    h[j] = orc_gelu(s);
+  }
+  for (int r = 0; r < d; ++r) {
+    if (g->loss == ORC_LOSS_DOT) {
+      dy[r] = -2.0 * v[r];
+    } else {
+      double y = k[r];
+      for (int j = 0; j < dh; ++j) y += W1[(long)r * dh + j] * h[j];
+      dy[r] = 2.0 * (y - v[r]);
+    }
+  }
+  /* dl/dW1 = dy h^T */
+  for (int r = 0; r < d; ++r)
+    for (int j = 0; j < dh; ++j) G1[(long)r * dh + j] = dy[r] * h[j];
+  /* dl/dz = (W1^T dy) * GELU'(z) */
+  for (int j = 0; j < dh; ++j) {
+    double s = 0.0;
+    for (int r = 0; r < d; ++r) s += W1[(long)r * dh + j] * dy[r];
+    dz[j] = s * orc_gelu_prime(z[j]);
+  }
+  /* dl/dW2 = dz k^T */
+  for (int j = 0; j < dh; ++j)
+    for (int i = 0; i < d; ++i) G2[(long)j * d + i] = dz[j] * k[i];
+  free(z);
+  free(h);
+  free(dy);
+  free(dz);
+}
+
+/* ------------------------------------------------------ Newton-Schulz */
+
+/* C (m x n) = A (m x p) * B (p x n), all row-major. */
+static void orc_matmul(int m, int p, int n, const double* A, const double* B, double* C) {
+  for (int i = 0; i < m; ++i) {
+    for (int j = 0; j < n; ++j) C[(long)i * n + j] = 0.0;
+    for (int l = 0; l < p; ++l) {
+      double a = A[(long)i * p + l];
+      for (int j = 0; j < n; ++j) C[(long)i * n + j] += a * B[(long)l * n + j];
+    }
+  }
+}
+
+/* Newton-Schulz orthogonalisation of one rows x cols matrix ([ATLAS-s] §5,
+ * Muon): X_0 = S / (||S||_F + eps); repeat X <- a X + b (X X^T) X +
+ * c (X X^T)^2 X, where (X X^T)^2 X is evaluated as (X X^T)((X X^T) X). */
+void orc_newton_schulz(int rows, int cols, const double* S, int steps, double a, double b,
+                       double c, double eps, double* out) {
+  long n = (long)rows * cols;
+  double nrm = 0.0;
+  for (long i = 0; i < n; ++i) nrm += S[i] * S[i];
+  nrm = sqrt(nrm);
+  double* X = out;
+  for (long i = 0; i < n; ++i) X[i] = S[i] / (nrm + eps);
+  double* Xt = (double*)malloc(sizeof(double) * n);
+  double* A = (double*)malloc(sizeof(double) * (long)rows * rows);
+  double* AX = (double*)malloc(sizeof(double) * n);
+  double* AAX = (double*)malloc(sizeof(double) * n);
+  for (int it = 0; it < steps; ++it) {
+    for (int i = 0; i < rows; ++i)
+      for (int j = 0; j < cols; ++j) Xt[(long)j * rows + i] = X[(long)i * cols + j];
+    orc_matmul(rows, cols, rows, X, Xt, A);     /* A = X X^T */
+    orc_matmul(rows, rows, cols, A, X, AX);     /* A X */
+    orc_matmul(rows, rows, cols, A, AX, AAX);   /* A (A X) */
+    for (long i = 0; i < n; ++i) X[i] = a * X[i] + b * AX[i] + c * AAX[i];
+  }
+  free(Xt);
+  free(A);
+  free(AX);
+  free(AAX);
+}
+
+/* The update a momentum contributes to the memory: S itself, or NS(S) applied
+ * to each weight matrix of the state on its own. */
+static void orc_momentum_update(const orc_cfg* g, const double* S, double* out) {
+  long n = orc_state_size(g);
+  if (g->ns_steps <= 0) {
+    memcpy(out, S, sizeof(double) * n);
+    return;
+  }
+  if (g->mem == ORC_MEM_LINEAR) {
+    orc_newton_schulz(g->d_v, orc_feature_dim(g), S, g->ns_steps, g->ns_a, g->ns_b, g->ns_c,
+                      g->ns_eps, out);
+    return;
+  }
+  long half = (long)g->d_k * g->d_h;
+  orc_newton_schulz(g->d_k, g->d_h, S, g->ns_steps, g->ns_a, g->ns_b, g->ns_c, g->ns_eps, out);
+  orc_newton_schulz(g->d_h, g->d_k, S + half, g->ns_steps, g->ns_a, g->ns_b, g->ns_c, g->ns_eps,
+                    out + half);
+}
+
+/* ------------------------------------------------------- one head, one token */
+
+/* Shared token step: S = eta S - theta g; M = (1 - alpha) M + U(S);
+ * y = M(Phi(q)).  ([Titans] Surprise Metric, Forgetting Mechanism, Retrieving.) */
+static void orc_token_step(const orc_cfg* g, double alpha, double eta, double theta,
+                           const double* grad, const double* q, double* M, double* S,
+                           double* upd, double* y) {
+  long n = orc_state_size(g);
+  for (long j = 0; j < n; ++j) S[j] = eta * S[j] - theta * grad[j];
+  orc_momentum_update(g, S, upd);
+  for (long j = 0; j < n; ++j) M[j] = (1.0 - alpha) * M[j] + upd[j];
+  orc_memory_apply(g, M, q, y);
+}
+
+/* Chunked Omega rule for one head ([ATLAS] §3.3, [Miras] Training): for every
+ * chunk of b tokens, M0 is the state the previous chunk ended with, and every
+ * token n of the chunk uses g_n = sum_{i=n-c+1..n, i>=0} gamma[n-i] grad(M0; k_i, v_i).
+ * b = 1 makes M0 the state right before each token. */
+static void orc_head_chunked(const orc_cfg* g, const double* K, const double* Q, const double* V,
+                             const double* alpha, const double* eta, const double* theta,
+                             const double* gamma, double* M, double* S, double* Y) {
+  long n = orc_state_size(g);
+  double* M0 = (double*)malloc(sizeof(double) * n);
+  double* gsum = (double*)malloc(sizeof(double) * n);
+  double* Gi = (double*)malloc(sizeof(double) * n);
+  double* upd = (double*)malloc(sizeof(double) * n);
+  int dk = g->d_k, dv = g->d_v;
+  for (int t0 = 0; t0 < g->N; t0 += g->b) {
+    memcpy(M0, M, sizeof(double) * n);
+    int t1 = t0 + g->b < g->N ? t0 + g->b : g->N;
+    for (int t = t0; t < t1; ++t) {
+      for (long j = 0; j < n; ++j) gsum[j] = 0.0;
+      int i0 = t - g->c + 1 < 0 ? 0 : t - g->c + 1;
+      for (int i = i0; i <= t; ++i) {
+        orc_grad(g, M0, K + (long)i * dk, V + (long)i * dv, Gi);
+        double w = gamma[t - i];
+        for (long j = 0; j < n; ++j) gsum[j] += w * Gi[j];
+      }
+      orc_token_step(g, alpha[t], eta[t], theta[t], gsum, Q + (long)t * dk, M, S, upd,
+                     Y + (long)t * dv);
+    }
+  }
+  free(M0);
+  free(gsum);
+  free(Gi);
+  free(upd);
+}
+
+/* Token recurrence for one head, written separately from the chunked loop:
+ * the gradient of every window term is taken at M_{t-1}
+ * ([ATLAS] §3.3, the b = 1 case; [Titans] Surprise Metric). */
+static void orc_head_recurrent(const orc_cfg* g, const double* K, const double* Q,
+                               const double* V, const double* alpha, const double* eta,
+                               const double* theta, const double* gamma, double* M, double* S,
+                               double* Y) {
+  long n = orc_state_size(g);
+  double* gsum = (double*)malloc(sizeof(double) * n);
+  double* Gi = (double*)malloc(sizeof(double) * n);
+  double* upd = (double*)malloc(sizeof(double) * n);
+  int dk = g->d_k, dv = g->d_v;
+  for (int t = 0; t < g->N; ++t) {
+    for (long j = 0; j < n; ++j) gsum[j] = 0.0;
+    for (int lag = 0; lag < g->c && t - lag >= 0; ++lag) {
+      int i = t - lag;
+      orc_grad(g, M, K + (long)i * dk, V + (long)i * dv, Gi);
+      for (long j = 0; j < n; ++j) gsum[j] += gamma[lag] * Gi[j];
+    }
+    orc_token_step(g, alpha[t], eta[t], theta[t], gsum, Q + (long)t * dk, M, S, upd,
+                   Y + (long)t * dv);
+  }
+  free(gsum);
+  free(Gi);
+  free(upd);
+}
+
+/* ----------------------------------------------------- threads over heads */
+
+typedef struct {
+  const orc_cfg* g;
+  int recurrent;
+  int h0, h1;
+  const double *K, *Q, *V, *alpha, *eta, *theta, *gamma;
+  double *M, *S, *Y;
+} orc_job;
+
+static void* orc_worker(void* p) {
+  orc_job* j = (orc_job*)p;
+  const orc_cfg* g = j->g;
+  long ns = orc_state_size(g);
+  for (int h = j->h0; h < j->h1; ++h) {
+    const double* K = j->K + (long)h * g->N * g->d_k;
+    const double* Q = j->Q + (long)h * g->N * g->d_k;
+    const double* V = j->V + (long)h * g->N * g->d_v;
+    const double* a = j->alpha + (long)h * g->N;
+    const double* e = j->eta + (long)h * g->N;
+    const double* th = j->theta + (long)h * g->N;
+    double* M = j->M + (long)h * ns;
+    double* S = j->S + (long)h * ns;
+    double* Y = j->Y + (long)h * g->N * g->d_v;
+    if (j->recurrent)
+      orc_head_recurrent(g, K, Q, V, a, e, th, j->gamma, M, S, Y);
+    else
+      orc_head_chunked(g, K, Q, V, a, e, th, j->gamma, M, S, Y);
+  }
+  return NULL;
+}
+
+static int orc_check(const orc_cfg* g) {
+  if (g->N < 0 || g->d_k <= 0 || g->d_v <= 0 || g->c < 1 || g->b < 1) return -1;
+  if (g->mem == ORC_MEM_MLP && (g->d_h <= 0 || g->d_k != g->d_v)) return -1;
+  if (g->mem != ORC_MEM_LINEAR && g->mem != ORC_MEM_MLP) return -1;
+  if (g->loss != ORC_LOSS_L2 && g->loss != ORC_LOSS_DOT) return -1;
+  return 0;
+}
+
+static int orc_run(const orc_cfg* g, int recurrent, int n_heads, const double* K,
+                   const double* Q, const double* V, const double* alpha, const double* eta,
+                   const double* theta, const double* gamma, double* M, double* S, double* Y,
+                   int n_threads) {
+  if (orc_check(g) != 0 || n_heads < 0) return -1;
+  if (n_threads <= 0) n_threads = (int)sysconf(_SC_NPROCESSORS_ONLN);
+  if (n_threads > n_heads) n_threads = n_heads;
+  if (n_threads < 1) n_threads = 1;
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * n_threads);
+  orc_job* jobs = (orc_job*)malloc(sizeof(orc_job) * n_threads);
+  for (int w = 0; w < n_threads; ++w) {
+    orc_job j = {g, recurrent, (int)((long)n_heads * w / n_threads),
+                 (int)((long)n_heads * (w + 1) / n_threads), K, Q, V, alpha, eta, theta,
+                 gamma, M, S, Y};
+    jobs[w] = j;
+    pthread_create(&th[w], NULL, orc_worker, &jobs[w]);
+  }
+  for (int w = 0; w < n_threads; ++w) pthread_join(th[w], NULL);
+  free(th);
+  free(jobs);
+  return 0;
+}
+
+/* Chunked forward over n_heads independent heads.  K, Q: [heads, N, d_k];
+ * V: [heads, N, d_v]; alpha, eta, theta: [heads, N]; gamma: [c] by lag;
+ * M, S: [heads, state] in/out (state layout: linear M is d_v x D row-major;
+ * MLP is W1 (d x d_h) then W2 (d_h x d)); Y: [heads, N, d_v] out.
+ * Returns 0, or -1 on an invalid description. */
+int orc_forward_chunked(const orc_cfg* g, int n_heads, const double* K, const double* Q,
+                        const double* V, const double* alpha, const double* eta,
+                        const double* theta, const double* gamma, double* M, double* S,
+                        double* Y, int n_threads) {
+  return orc_run(g, 0, n_heads, K, Q, V, alpha, eta, theta, gamma, M, S, Y, n_threads);
+}
+
+/* Token-recurrent forward, same arguments (b is ignored). */
+int orc_forward_recurrent(const orc_cfg* g, int n_heads, const double* K, const double* Q,
+                          const double* V, const double* alpha, const double* eta,
+                          const double* theta, const double* gamma, double* M, double* S,
+                          double* Y, int n_threads) {
+  return orc_run(g, 1, n_heads, K, Q, V, alpha, eta, theta, gamma, M, S, Y, n_threads);
+}
