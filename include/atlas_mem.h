@@ -1,0 +1,126 @@
+/*
+ * atlas_mem.h -- C ABI of the GB300 test-time memory update library
+ * (libatlasmem.so, built for sm_103a).
+ *
+ * The operation (Titans / Miras / ATLAS family).  For every head, a memory M
+ * (a d_v x D matrix over features Phi(k), or a residual MLP
+ * M(x) = x + W1 GELU(W2 x)) takes, per token t, one momentum step on the
+ * sliding-window ("Omega rule") loss
+ *     l_t(M) = sum_{j=0..c-1} gamma[j] * || M(Phi(k_{t-j})) - v_{t-j} ||^2
+ *   S_t = eta_t S_{t-1} - theta_t grad l_t,      M_t = (1 - alpha_t) M_{t-1} + S_t
+ * (or + NS(S_t), a Newton-Schulz orthogonalised momentum), and is read out as
+ *     y_t = M_t(Phi(q_t)).
+ * In the chunked form every gradient of the tokens of a chunk of b tokens is
+ * taken at the state the previous chunk ended with; b = 1 is the recurrence.
+ *
+ * Sources (page title, section):
+ *   "[Paper Review] Titans 논문 이해하기": Learning Process and Surprise
+ *     Metric (S_t), Objective (l2 loss), Forgetting Mechanism (M_t),
+ *     Retrieving a Memory (y = M*(q), no update while reading), 3.2 (chunked
+ *     mini-batch GD as matmuls).
+ *   "논문 리뷰 Google ATLAS": 3.1 (polynomial feature map Phi_p), 3.2 (Omega
+ *     rule), 3.3 (chunked Omega rule, gradients at the chunk-start state).
+ *   "ATLAS: Learning to Optimally Memorize the Context at Test Time"
+ *     (paperlayer summary): 5 Memory Optimization (Muon / Newton-Schulz),
+ *     App. E (2-layer residual MLP memory, GELU).
+ *   "It's All Connected: ... (Miras)": Associative Memory & Attentional Bias
+ *     (dot-product bias = linear attention), Training (chunk-wise
+ *     parallelisation; the layer outputs M(q_t)).
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor arguments are DEVICE pointers owned by the caller, contiguous,
+ *     head-major: index [b][h][token][feature].  The library never frees them.
+ *   - Calls only enqueue work on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream) and return without synchronising.
+ *   - Argument errors are reported before anything is launched; the output
+ *     buffers are then untouched.
+ *   - The library allocates no device memory: scratch comes from the
+ *     caller's `workspace`.
+ */
+#ifndef ATLAS_MEM_H
+#define ATLAS_MEM_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* memory architecture */
+#define ATLAS_MEM_LINEAR 0 /* M: d_v x D matrix, y = M Phi(x) */
+#define ATLAS_MEM_MLP 1    /* M(x) = x + W1 GELU(W2 x), d_k = d_v = d */
+/* feature map (linear memory only; the MLP takes x itself) */
+#define ATLAS_PHI_IDENTITY 0 /* D = d_k */
+#define ATLAS_PHI_POLY2 1    /* D = d_k + d_k(d_k+1)/2: [x_i] then [x_i x_j, i<=j, i-major] */
+/* attentional bias */
+#define ATLAS_LOSS_L2 0  /* ||M(Phi(k)) - v||^2 (gradient carries the factor 2) */
+#define ATLAS_LOSS_DOT 1 /* -2 <M(Phi(k)), v> (linear memory only: linear attention) */
+/* K, Q, V element type */
+#define ATLAS_F32 0
+#define ATLAS_BF16 1
+
+/* status codes */
+#define ATLAS_OK 0
+#define ATLAS_ERR_INVALID -1     /* null pointer, bad size, bad enum value */
+#define ATLAS_ERR_UNSUPPORTED -2 /* valid description that no kernel here handles */
+#define ATLAS_ERR_WORKSPACE -3   /* workspace missing or smaller than required */
+#define ATLAS_ERR_CUDA -4        /* a CUDA runtime call or launch failed */
+#define ATLAS_ERR_TIMEOUT -5     /* a bounded device-side wait ran out (status word) */
+
+typedef struct atlas_mem_cfg {
+  int B, H, N;        /* batch, heads, tokens per head (N >= 0) */
+  int d_k, d_v, d_h;  /* key width, value width, MLP hidden width (0 for linear) */
+  int mem;            /* ATLAS_MEM_* */
+  int phi;            /* ATLAS_PHI_* */
+  int loss;           /* ATLAS_LOSS_* */
+  int c;              /* Omega window length (>= 1); gamma has c entries */
+  int b;              /* chunk length (>= 1); 1 = token recurrence */
+  int ns_steps;       /* Newton-Schulz iterations on the momentum, 0 = plain momentum */
+  float ns_a, ns_b, ns_c; /* X <- a X + b (X X^T) X + c (X X^T)^2 X */
+  float ns_eps;       /* X_0 = S / (||S||_F + ns_eps) */
+  int in_dtype;       /* ATLAS_F32 or ATLAS_BF16 for K, Q, V */
+  float* S_state;     /* optional device momentum [B,H,state] in/out; NULL = start
+                         from zero and do not return it */
+  void* workspace;    /* device scratch of at least atlas_mem_workspace_bytes() */
+  size_t workspace_bytes;
+  int* status_dev;    /* optional device int; set to ATLAS_ERR_TIMEOUT by a kernel
+                         whose bounded wait ran out (never cleared by the library) */
+} atlas_mem_cfg;
+
+/* Number of fp32 entries in one head's memory state (and momentum):
+ * linear d_v * D; MLP 2 * d * d_h.  0 for an invalid description. */
+size_t atlas_mem_state_size(const atlas_mem_cfg* cfg);
+
+/* Bytes of device workspace atlas_mem_forward needs for this description
+ * (may be 0).  (size_t)-1 for an invalid description. */
+size_t atlas_mem_workspace_bytes(const atlas_mem_cfg* cfg);
+
+/* The chunked memory update over all B*H heads.
+ *   K, Q   [B,H,N,d_k]  keys, queries (fp32 or bf16 per cfg->in_dtype)
+ *   V      [B,H,N,d_v]  values (same type)
+ *   alpha, eta, theta [B,H,N] fp32 per-token decay, momentum and step gates
+ *   gamma  [c] fp32     window weight by lag: gamma[j] weighs token t-j in l_t
+ *   Y      [B,H,N,d_v]  fp32 out: y_t = M_t(Phi(q_t))
+ *   M_final [B,H,state] fp32 in/out: M_0 on entry, M_N on return.  Linear
+ *          layout d_v x D row-major; MLP layout W1 (d x d_h) then W2
+ *          (d_h x d), both row-major.
+ * Returns ATLAS_OK or a negative ATLAS_ERR_* code. */
+int atlas_mem_forward(const void* K, const void* Q, const void* V, const float* alpha,
+                      const float* eta, const float* theta, const float* gamma,
+                      const atlas_mem_cfg* cfg, float* Y, float* M_final, void* stream);
+
+/* Static description of a status code. */
+const char* atlas_mem_strerror(int status);
+
+/* Name of the kernel family atlas_mem_forward would launch for cfg (for
+ * reports): "linear_tc", "linear_simt", "mlp_simt", ... or "" if invalid. */
+const char* atlas_mem_path(const atlas_mem_cfg* cfg);
+
+/* Number of kernel launches atlas_mem_forward makes for cfg (for reports). */
+long atlas_mem_launch_count(const atlas_mem_cfg* cfg);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATLAS_MEM_H */

@@ -1,0 +1,165 @@
+// atlas_mem.cu -- C-ABI entry points: argument validation, path choice,
+// workspace sizing and launch.  Every computation happens in the kernels of
+// linear_simt.cu, linear_tc.cu and mlp_simt.cu; this file only plans.
+#include <string.h>
+
+#include "atlas_mem.h"
+#include "kernels.h"
+
+using namespace atlas;
+
+namespace {
+
+enum Path { PATH_INVALID = 0, PATH_LINEAR_SIMT, PATH_LINEAR_TC, PATH_MLP_SIMT };
+
+int feature_dim(const atlas_mem_cfg* c) {
+  if (c->mem == ATLAS_MEM_LINEAR && c->phi == ATLAS_PHI_POLY2)
+    return c->d_k + c->d_k * (c->d_k + 1) / 2;
+  return c->d_k;
+}
+
+// Structural validation (no pointers).  Returns ATLAS_OK, INVALID or UNSUPPORTED.
+int check_cfg(const atlas_mem_cfg* c) {
+  if (!c) return ATLAS_ERR_INVALID;
+  if (c->B < 0 || c->H < 0 || c->N < 0) return ATLAS_ERR_INVALID;
+  if (c->d_k <= 0 || c->d_v <= 0 || c->c < 1 || c->b < 1) return ATLAS_ERR_INVALID;
+  if (c->mem != ATLAS_MEM_LINEAR && c->mem != ATLAS_MEM_MLP) return ATLAS_ERR_INVALID;
+  if (c->phi != ATLAS_PHI_IDENTITY && c->phi != ATLAS_PHI_POLY2) return ATLAS_ERR_INVALID;
+  if (c->loss != ATLAS_LOSS_L2 && c->loss != ATLAS_LOSS_DOT) return ATLAS_ERR_INVALID;
+  if (c->in_dtype != ATLAS_F32 && c->in_dtype != ATLAS_BF16) return ATLAS_ERR_INVALID;
+  if (c->ns_steps < 0) return ATLAS_ERR_INVALID;
+  if ((long)c->B * c->H > 65535L * 1024) return ATLAS_ERR_UNSUPPORTED;
+  if (c->mem == ATLAS_MEM_MLP) {
+    if (c->d_h <= 0 || c->d_k != c->d_v) return ATLAS_ERR_INVALID;
+    if (c->phi != ATLAS_PHI_IDENTITY) return ATLAS_ERR_INVALID;
+    if (c->loss != ATLAS_LOSS_L2) return ATLAS_ERR_UNSUPPORTED;
+  } else {
+    if (c->ns_steps > 0) return ATLAS_ERR_UNSUPPORTED;
+    if (c->phi == ATLAS_PHI_POLY2 && c->d_k > 64) return ATLAS_ERR_UNSUPPORTED;
+  }
+  return ATLAS_OK;
+}
+
+LinArgs lin_args(const void* K, const void* Q, const void* V, const float* alpha,
+                 const float* eta, const float* theta, const float* gamma,
+                 const atlas_mem_cfg* c, float* Y, float* M) {
+  LinArgs a;
+  a.K = K; a.Q = Q; a.V = V;
+  a.alpha = alpha; a.eta = eta; a.theta = theta; a.gamma = gamma;
+  a.Y = Y; a.M = M; a.S = c->S_state;
+  a.N = c->N; a.d_k = c->d_k; a.d_v = c->d_v; a.D = feature_dim(c);
+  a.c = c->c; a.b = c->b;
+  a.poly = c->phi == ATLAS_PHI_POLY2;
+  a.dot = c->loss == ATLAS_LOSS_DOT;
+  a.bf16 = c->in_dtype == ATLAS_BF16;
+  return a;
+}
+
+MlpArgs mlp_args(const void* K, const void* Q, const void* V, const float* alpha,
+                 const float* eta, const float* theta, const float* gamma,
+                 const atlas_mem_cfg* c, float* Y, float* M) {
+  MlpArgs a;
+  a.K = K; a.Q = Q; a.V = V;
+  a.alpha = alpha; a.eta = eta; a.theta = theta; a.gamma = gamma;
+  a.Y = Y; a.M = M; a.S = c->S_state;
+  a.heads = c->B * c->H; a.N = c->N; a.d = c->d_k; a.dh = c->d_h; a.c = c->c; a.b = c->b;
+  a.bf16 = c->in_dtype == ATLAS_BF16;
+  a.ns_steps = c->ns_steps;
+  a.ns_a = c->ns_a; a.ns_b = c->ns_b; a.ns_c = c->ns_c; a.ns_eps = c->ns_eps;
+  a.s_is_zero = c->S_state == nullptr;
+  return a;
+}
+
+Path choose_path(const atlas_mem_cfg* c) {
+  if (check_cfg(c) != ATLAS_OK) return PATH_INVALID;
+  if (c->mem == ATLAS_MEM_MLP) return PATH_MLP_SIMT;
+  LinArgs a = lin_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, c,
+                       nullptr, nullptr);
+  if (linear_tc_supported(a)) return PATH_LINEAR_TC;
+  int RV;
+  size_t smem;
+  if (linear_simt_plan(a, c->B * c->H, &RV, &smem) != ATLAS_OK) return PATH_INVALID;
+  return PATH_LINEAR_SIMT;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t atlas_mem_state_size(const atlas_mem_cfg* cfg) {
+  if (check_cfg(cfg) != ATLAS_OK) return 0;
+  if (cfg->mem == ATLAS_MEM_MLP) return (size_t)2 * cfg->d_k * cfg->d_h;
+  return (size_t)cfg->d_v * feature_dim(cfg);
+}
+
+size_t atlas_mem_workspace_bytes(const atlas_mem_cfg* cfg) {
+  if (check_cfg(cfg) != ATLAS_OK) return (size_t)-1;
+  if (cfg->mem == ATLAS_MEM_MLP) {
+    MlpArgs a = mlp_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, cfg,
+                         nullptr, nullptr);
+    return mlp_simt_workspace_bytes(a);
+  }
+  return 0;
+}
+
+const char* atlas_mem_path(const atlas_mem_cfg* cfg) {
+  switch (choose_path(cfg)) {
+    case PATH_LINEAR_SIMT: return "linear_simt";
+    case PATH_LINEAR_TC: return "linear_tc";
+    case PATH_MLP_SIMT: return "mlp_simt";
+    default: return "";
+  }
+}
+
+long atlas_mem_launch_count(const atlas_mem_cfg* cfg) {
+  switch (choose_path(cfg)) {
+    case PATH_LINEAR_SIMT:
+    case PATH_LINEAR_TC:
+      return (long)cfg->B * cfg->H > 0 ? 1 : 0;
+    case PATH_MLP_SIMT: {
+      if ((long)cfg->B * cfg->H == 0) return 0;
+      MlpArgs a = mlp_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, cfg,
+                           nullptr, nullptr);
+      return mlp_simt_launch_count(a);
+    }
+    default: return 0;
+  }
+}
+
+int atlas_mem_forward(const void* K, const void* Q, const void* V, const float* alpha,
+                      const float* eta, const float* theta, const float* gamma,
+                      const atlas_mem_cfg* cfg, float* Y, float* M_final, void* stream) {
+  int rc = check_cfg(cfg);
+  if (rc != ATLAS_OK) return rc;
+  const long heads = (long)cfg->B * cfg->H;
+  if (heads == 0) return ATLAS_OK;
+  if (!M_final || !gamma) return ATLAS_ERR_INVALID;
+  if (cfg->N > 0 && (!K || !Q || !V || !alpha || !eta || !theta || !Y)) return ATLAS_ERR_INVALID;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Path path = choose_path(cfg);
+  if (path == PATH_INVALID) return ATLAS_ERR_UNSUPPORTED;
+  if (path == PATH_MLP_SIMT) {
+    MlpArgs a = mlp_args(K, Q, V, alpha, eta, theta, gamma, cfg, Y, M_final);
+    const size_t need = mlp_simt_workspace_bytes(a);
+    if (need > 0 && (!cfg->workspace || cfg->workspace_bytes < need)) return ATLAS_ERR_WORKSPACE;
+    if (cfg->N == 0) return ATLAS_OK;
+    return mlp_simt_forward(a, cfg->workspace, st);
+  }
+  LinArgs a = lin_args(K, Q, V, alpha, eta, theta, gamma, cfg, Y, M_final);
+  if (path == PATH_LINEAR_TC) return linear_tc_launch(a, (int)heads, cfg->status_dev, st);
+  return linear_simt_launch(a, (int)heads, st);
+}
+
+const char* atlas_mem_strerror(int status) {
+  switch (status) {
+    case ATLAS_OK: return "ok";
+    case ATLAS_ERR_INVALID: return "invalid argument";
+    case ATLAS_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATLAS_ERR_WORKSPACE: return "workspace missing or too small";
+    case ATLAS_ERR_CUDA: return "CUDA runtime error";
+    case ATLAS_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,73 @@
+// common.cuh -- small device helpers shared by the memory-update kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "atlas_mem.h"
+
+#define ATLAS_HD __host__ __device__ __forceinline__
+
+// Element t of a K/Q/V tensor stored as fp32 or bf16.
+__device__ __forceinline__ float ld_in(const void* p, long idx, int bf16) {
+  if (bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[idx]);
+  return reinterpret_cast<const float*>(p)[idx];
+}
+
+// Feature j of Phi(x) for x in shared memory.  Degree-2 map (ATLAS review
+// §3.1, constant dropped): j < d -> x_j; otherwise the product x_p x_q of the
+// pair (p <= q) in i-major order, looked up in the pair table.
+__device__ __forceinline__ float phi_at(const float* x, int j, int d, const uint8_t* pp,
+                                        const uint8_t* pq, int poly) {
+  if (!poly || j < d) return x[j];
+  return x[pp[j - d]] * x[pq[j - d]];
+}
+
+// Per-chunk scalar tables of the unrolled momentum / decay recursion.
+// Within a chunk with start state (M0, S0) and window gradients G_i taken at
+// M0 (i over the L window tokens), for the chunk's n-th token:
+//   S_n = eps_n S0 - sum_i U[n,i] G_i,   M_n = a_n M0 + beta_n S0 - sum_i W[n,i] G_i
+// with a_n = prod(1-alpha), eps_n = prod(eta), beta_n = (1-alpha_n) beta_{n-1} + eps_n,
+// U[n,i] = eta_n U[n-1,i] + theta_n gamma[t_n - t_i] (lag inside the window),
+// W[n,i] = (1-alpha_n) W[n-1,i] + U[n,i].
+// One warp builds them; lanes stride over the window tokens.  Urun/Wrun are
+// running rows of length L; Wt (nb x ldw) receives every W row; Ulast / Wlast
+// the last rows.
+__device__ __forceinline__ void chunk_tables_warp(const float* alpha, const float* eta,
+                                                  const float* theta, const float* gamma,
+                                                  int t0, int nb, int i0, int L, int c,
+                                                  float* Urun, float* Wrun, float* Wt, int ldw,
+                                                  float* Ut, float* a_out, float* e_out,
+                                                  float* b_out) {
+  const int lane = threadIdx.x & 31;
+  for (int i = lane; i < L; i += 32) {
+    Urun[i] = 0.f;
+    Wrun[i] = 0.f;
+  }
+  float pa = 1.f, pe = 1.f, pb = 0.f;
+  for (int n = 0; n < nb; ++n) {
+    const int tn = t0 + n;
+    const float keep = 1.f - alpha[tn];
+    const float et = eta[tn];
+    const float th = theta[tn];
+    pa *= keep;
+    pe *= et;
+    pb = keep * pb + pe;
+    for (int i = lane; i < L; i += 32) {
+      const int lag = tn - (i0 + i);
+      const float g = (lag >= 0 && lag < c) ? gamma[lag] : 0.f;
+      const float u = et * Urun[i] + th * g;
+      const float w = keep * Wrun[i] + u;
+      Urun[i] = u;
+      Wrun[i] = w;
+      if (Wt) Wt[n * ldw + i] = w;
+      if (Ut) Ut[n * ldw + i] = u;
+    }
+    if (lane == 0) {
+      a_out[n] = pa;
+      e_out[n] = pe;
+      b_out[n] = pb;
+    }
+  }
+  __syncwarp();
+}

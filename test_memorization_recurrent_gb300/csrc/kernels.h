@@ -1,0 +1,55 @@
+// kernels.h -- internal interface between the C-ABI host layer and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+namespace atlas {
+
+// Arguments of every linear-memory kernel (one head = one [N, .] slice).
+struct LinArgs {
+  const void* K;
+  const void* Q;
+  const void* V;
+  const float* alpha;
+  const float* eta;
+  const float* theta;
+  const float* gamma;
+  float* Y;
+  float* M;  // [heads, d_v, D] in/out
+  float* S;  // [heads, d_v, D] in/out, or nullptr (start at zero, not returned)
+  int N, d_k, d_v, D, c, b;
+  int poly, dot, bf16;
+};
+
+int linear_simt_launch(const LinArgs& a, int heads, cudaStream_t st);
+int linear_simt_plan(const LinArgs& a, int heads, int* RV_out, size_t* smem_out);
+
+// Tensor-core path: linear memory, identity map, d_k = d_v = 128, bf16 inputs,
+// b = 64, c = 1.
+bool linear_tc_supported(const LinArgs& a);
+int linear_tc_launch(const LinArgs& a, int heads, int* status, cudaStream_t st);
+
+// Arguments of the MLP-memory path.
+struct MlpArgs {
+  const void* K;
+  const void* Q;
+  const void* V;
+  const float* alpha;
+  const float* eta;
+  const float* theta;
+  const float* gamma;
+  float* Y;
+  float* M;  // [heads, W1 (d x dh) | W2 (dh x d)] in/out
+  float* S;  // same layout, in/out (caller's or workspace)
+  int heads, N, d, dh, c, b;
+  int bf16;
+  int ns_steps;
+  float ns_a, ns_b, ns_c, ns_eps;
+  int s_is_zero;  // S must be cleared before the first chunk
+};
+
+size_t mlp_simt_workspace_bytes(const MlpArgs& a);
+int mlp_simt_forward(const MlpArgs& a, void* ws, cudaStream_t st);
+long mlp_simt_launch_count(const MlpArgs& a);
+
+}  // namespace atlas

@@ -1,0 +1,113 @@
+"""The C-ABI library builds, loads and exports every entry point its header
+declares; host-side validation rejects bad descriptions before any launch.
+No test here touches a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import workloads as W
+from test_memorization_recurrent_gb300 import build as B
+import test_memorization_recurrent_gb300 as A
+from test_memorization_recurrent_gb300.harness import cfg_for
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "atlas_mem.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return A.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(atlas_mem_\w+)\s*\(", text,
+                                 flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    assert "atlas_mem_forward" in names and "atlas_mem_workspace_bytes" in names
+    assert set(A.EXPORTS) <= set(names) | set()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        ctypes.cast(getattr(lib, name), ctypes.c_void_p)
+
+
+def test_strerror_codes(lib):
+    assert A.atlas_mem_strerror(0) == "ok"
+    for code in (-1, -2, -3, -4, -5):
+        assert A.atlas_mem_strerror(code) not in ("ok", "unknown status")
+    assert A.atlas_mem_strerror(-99) == "unknown status"
+
+
+@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
+def test_state_size_and_path(lib, wid):
+    w = W.workload(wid)
+    cfg = cfg_for(w, w.heads, w.N)
+    assert A.atlas_mem_state_size(cfg) == w.state_size
+    assert A.atlas_mem_path(cfg) in ("linear_simt", "linear_tc", "mlp_simt")
+    assert A.atlas_mem_launch_count(cfg) >= 1
+    nbytes = A.atlas_mem_workspace_bytes(cfg)
+    assert nbytes >= 0
+    if w.mem == W.MEM_MLP:
+        assert nbytes > 0
+
+
+def _bad(**kw):
+    base = dict(B=1, H=2, N=16, d_k=8, d_v=8)
+    base.update(kw)
+    return A.make_cfg(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(N=-1), A.ERR_INVALID),
+    (dict(d_k=0), A.ERR_INVALID),
+    (dict(c=0), A.ERR_INVALID),
+    (dict(b=0), A.ERR_INVALID),
+    (dict(mem=7), A.ERR_INVALID),
+    (dict(phi=3), A.ERR_INVALID),
+    (dict(loss=2), A.ERR_INVALID),
+    (dict(in_dtype=5), A.ERR_INVALID),
+    (dict(mem=A.MEM_MLP, d_h=0), A.ERR_INVALID),
+    (dict(mem=A.MEM_MLP, d_h=16, d_v=4), A.ERR_INVALID),
+    (dict(mem=A.MEM_MLP, d_h=16, loss=A.LOSS_DOT), A.ERR_UNSUPPORTED),
+    (dict(ns_steps=5), A.ERR_UNSUPPORTED),
+    (dict(phi=A.PHI_POLY2, d_k=80), A.ERR_UNSUPPORTED),
+])
+def test_invalid_descriptions_rejected_before_launch(lib, kw, code):
+    cfg = _bad(**kw)
+    rc = lib.atlas_mem_forward(1, 1, 1, 1, 1, 1, 1, ctypes.byref(cfg), 1, 1, None)
+    assert rc == code
+
+
+def test_null_pointers_rejected(lib):
+    cfg = _bad()
+    rc = lib.atlas_mem_forward(None, None, None, None, None, None, None, ctypes.byref(cfg), None,
+                               None, None)
+    assert rc == A.ERR_INVALID
+
+
+def test_missing_workspace_rejected(lib):
+    cfg = _bad(mem=A.MEM_MLP, d_h=16)
+    assert A.atlas_mem_workspace_bytes(cfg) > 0
+    rc = lib.atlas_mem_forward(1, 1, 1, 1, 1, 1, 1, ctypes.byref(cfg), 1, 1, None)
+    assert rc == A.ERR_WORKSPACE
+
+
+def test_zero_heads_is_a_no_op(lib):
+    cfg = _bad(H=0)
+    rc = lib.atlas_mem_forward(None, None, None, None, None, None, None, ctypes.byref(cfg), None,
+                               None, None)
+    assert rc == A.OK
+
+
+def test_invalid_workspace_query():
+    with pytest.raises(A.AtlasError):
+        A.atlas_mem_workspace_bytes(_bad(b=0))

@@ -1,0 +1,161 @@
+"""Parity of the CUDA path (called through the C ABI) with the fp64 oracle on
+the same seeded inputs.
+
+Small cases span several chunks and a ragged tail; full-size cases run every
+head of a workload in the launch configuration the benchmark times and compare
+sampled heads (whole sequences where the oracle is quick, a token prefix
+otherwise -- the update is causal, so a prefix of the outputs is exact).
+Tolerances: fp32 inputs max|x-y|/max|y| <= 1e-4; bf16 inputs max|x-y|/RMS(y)
+<= 2e-2, on Y and on M_final separately.
+"""
+import numpy as np
+import pytest
+
+import workloads as W
+from parity_util import rel_err, run_oracle, tol
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from test_memorization_recurrent_gb300 import build
+    build.build()
+
+
+def gpu_run(w, inp, N=None, S0=None, with_S=False):
+    from test_memorization_recurrent_gb300.harness import Runner, to_device
+    N = inp["K"].shape[1] if N is None else N
+    sub = {k: (v[:, :N] if k in ("K", "Q", "V", "alpha", "eta", "theta") else v)
+           for k, v in inp.items()}
+    d = to_device(w, sub)
+    r = Runner(w, sub["K"].shape[0], N, with_S=with_S or S0 is not None)
+    S0d = None if S0 is None else torch.from_numpy(np.asarray(S0, np.float32)).cuda()
+    Y, M = r(d, S0=S0d)
+    torch.cuda.synchronize()
+    assert int(r.status.item()) == 0
+    S = None if r.S is None else r.S.cpu().numpy()
+    return Y.cpu().numpy(), M.cpu().numpy(), S
+
+
+def check(w, Yg, Mg, Yo, Mo, what=""):
+    ey, em = rel_err(Yg, Yo, w.bf16), rel_err(Mg, Mo, w.bf16)
+    assert np.isfinite(Yg).all() and np.isfinite(Mg).all(), what
+    assert ey <= tol(w), f"{what} Y err {ey:.3e} > {tol(w)}"
+    assert em <= tol(w), f"{what} M err {em:.3e} > {tol(w)}"
+    return ey, em
+
+
+# ------------------------------------------------------------------ small cases
+
+SMALL = {
+    1: dict(heads=[0], N=512),
+    2: dict(heads=[0, 5, 9], N=64 * 3 + 17),
+    3: dict(heads=[0, 3], N=64 * 2 + 37),
+    4: dict(heads=[0, 7], N=64 * 2 + 19),
+    5: dict(heads=[0, 11], N=64 + 21),
+}
+
+
+@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
+def test_small_parity(wid):
+    w = W.workload(wid, bounded=True)
+    s = SMALL[wid]
+    inp = W.generate(w, heads=s["heads"], n_tokens=s["N"])
+    Yo, Mo, _ = run_oracle(w, inp)
+    Yg, Mg, _ = gpu_run(w, inp)
+    check(w, Yg, Mg, Yo, Mo, f"workload {wid}")
+
+
+@pytest.mark.parametrize("wid", [3, 4])
+def test_small_parity_verbatim_gates_finite_prefix(wid):
+    """The literal gates of the poly2 and MLP workloads overflow after a few
+    chunks; parity is checked on the prefix where the oracle stays finite and
+    moderate, with the error taken relative to the RMS of each chunk."""
+    w = W.workload(wid)
+    N = 2 * w.b
+    inp = W.generate(w, heads=[1], n_tokens=N)
+    Yo, Mo, _ = run_oracle(w, inp)
+    Yg, Mg, _ = gpu_run(w, inp)
+    for c0 in range(0, N, w.b):
+        yo, yg = Yo[:, c0:c0 + w.b], Yg[:, c0:c0 + w.b]
+        if not np.isfinite(yo).all() or np.abs(yo).max() > 1e6:
+            break
+        assert rel_err(yg, yo, True) <= tol(w), f"chunk {c0 // w.b}"
+
+
+@pytest.mark.parametrize("b", [1, 5, 64])
+def test_linear_attention_mode(b):
+    """Dot-product bias, alpha = eta = 0, theta = 1/2: the GPU path reproduces
+    causal linear attention for any chunk size (checked against the oracle,
+    itself pinned to (Q K^T * mask) V)."""
+    w = W.workload(2, loss=W.LOSS_DOT, b=b, N=150)
+    inp = W.generate(w, heads=[0, 1])
+    inp["alpha"][:] = 0
+    inp["eta"][:] = 0
+    inp["theta"][:] = 0.5
+    Yo, Mo, _ = run_oracle(w, inp)
+    Yg, Mg, _ = gpu_run(w, inp)
+    check(w, Yg, Mg, Yo, Mo)
+
+
+@pytest.mark.parametrize("wid", [1, 2, 4])
+def test_momentum_state_round_trip(wid):
+    """Two calls over halves of the sequence (split on a chunk boundary, c = 1
+    or handled by the caller) carrying M and S equal one call over all of it."""
+    w = W.workload(wid, bounded=True, c=1)
+    N = 4 * w.b if w.b > 1 else 64
+    inp = W.generate(w, heads=[0, 2], n_tokens=N)
+    Yo, Mo, So = run_oracle(w, inp)
+    half = N // 2
+    first = {k: (v[:, :half] if k in ("K", "Q", "V", "alpha", "eta", "theta") else v)
+             for k, v in inp.items()}
+    second = {k: (v[:, half:] if k in ("K", "Q", "V", "alpha", "eta", "theta") else v)
+              for k, v in inp.items()}
+    Y1, M1, S1 = gpu_run(w, first, with_S=True)
+    second["M0"] = M1
+    Y2, M2, S2 = gpu_run(w, second, S0=S1)
+    check(w, np.concatenate([Y1, Y2], axis=1), M2, Yo, Mo, "split")
+    assert rel_err(S2, So, w.bf16) <= tol(w)
+
+
+@pytest.mark.parametrize("N", [0, 1, 63, 65])
+def test_edge_lengths(N):
+    w = W.workload(3, bounded=True, N=max(N, 1))
+    inp = W.generate(w, heads=[0], n_tokens=N)
+    Yo, Mo, _ = run_oracle(w, inp)
+    Yg, Mg, _ = gpu_run(w, inp)
+    if N:
+        check(w, Yg, Mg, Yo, Mo)
+    else:
+        np.testing.assert_array_equal(Mg, inp["M0"])
+
+
+def test_chunk_longer_than_sequence_and_window_longer_than_chunk():
+    w = W.workload(1, b=16, c=40, N=30)
+    inp = W.generate(w)
+    Yo, Mo, _ = run_oracle(w, inp)
+    Yg, Mg, _ = gpu_run(w, inp)
+    check(w, Yg, Mg, Yo, Mo)
+
+
+# -------------------------------------------------------------- full sizes
+
+@pytest.mark.parametrize("wid,sample,prefix", [
+    (2, [0, 77, 127], None),     # all 128 heads x 4096; sampled heads in full
+    (3, [0, 31], 1024),          # all 32 heads x 8192; sampled heads, first 16 chunks
+    (4, [0, 19], 4096),          # all 32 heads x 16384; sampled heads, first 64 chunks
+])
+def test_full_size_sampled(wid, sample, prefix):
+    w = W.workload(wid, bounded=True)
+    inp = W.generate(w)
+    Yg, Mg, _ = gpu_run(w, inp)
+    sub = {k: (v[sample] if k not in ("gamma",) else v) for k, v in inp.items()}
+    Yo, Mo, _ = run_oracle(w, sub, N=prefix)
+    if prefix is None:
+        check(w, Yg[sample], Mg[sample], Yo, Mo, f"workload {wid}")
+    else:
+        ey = rel_err(Yg[sample, :prefix], Yo, w.bf16)
+        assert ey <= tol(w), f"workload {wid} Y prefix err {ey:.3e}"
+    assert np.isfinite(Yg).all()
