@@ -109,6 +109,32 @@ int atlas_mem_forward(const void* K, const void* Q, const void* V, const float* 
                       const float* eta, const float* theta, const float* gamma,
                       const atlas_mem_cfg* cfg, float* Y, float* M_final, void* stream);
 
+/* Size of the device scratch array that atlas_mem_forward_noalloc uses:
+ * 32 MiB, held by every GPU that loads the library until the process exits. */
+#define ATLAS_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* atlas_mem_forward for callers that cannot allocate device memory.
+ * (No counterpart in the method's description: a library convenience.)
+ * Code that runs where allocation is not allowed -- inside an allocator or
+ * memory-pool callback, or in a process whose device memory is reserved up
+ * front -- cannot create the workspace atlas_mem_forward asks for.  This entry
+ * point takes the same arguments, ignores cfg->workspace and
+ * cfg->workspace_bytes, and uses a fixed scratch array built into the library
+ * instead; it calls no cudaMalloc, cudaFree or allocating routine.
+ * - Limit: a description whose atlas_mem_workspace_bytes() exceeds
+ *   ATLAS_NOALLOC_SCRATCH_BYTES returns ATLAS_ERR_WORKSPACE and launches
+ *   nothing (split the heads over several calls instead).
+ * - The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ * - All calls on a device share the one array and each call overwrites it:
+ *   calls whose work overlaps on the GPU (different streams, or threads)
+ *   race and give wrong results.  Serialise them, e.g. on one stream.
+ * Returns what atlas_mem_forward returns. */
+int atlas_mem_forward_noalloc(const void* K, const void* Q, const void* V, const float* alpha,
+                              const float* eta, const float* theta, const float* gamma,
+                              const atlas_mem_cfg* cfg, float* Y, float* M_final, void* stream);
+
 /* Static description of a status code. */
 const char* atlas_mem_strerror(int status);
 

@@ -23,6 +23,7 @@ F32, BF16 = 0, 1
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
 
 EXPORTS = ("atlas_mem_state_size", "atlas_mem_workspace_bytes", "atlas_mem_forward",
+           "atlas_mem_forward_noalloc",
            "atlas_mem_strerror", "atlas_mem_path", "atlas_mem_launch_count")
 
 
@@ -75,6 +76,9 @@ def load_library(path: str = LIB_PATH):
             lib.atlas_mem_path.restype = ctypes.c_char_p
             lib.atlas_mem_launch_count.argtypes = [cp]
             lib.atlas_mem_launch_count.restype = ctypes.c_long
+            lib.atlas_mem_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, cp, vp, vp,
+                                                      vp]
+            lib.atlas_mem_forward_noalloc.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -132,5 +136,32 @@ def atlas_mem_forward(K, Q, V, alpha, eta, theta, gamma, cfg: AtlasMemCfg, Y, M_
     rc = load_library().atlas_mem_forward(
         _ptr(K), _ptr(Q), _ptr(V), _ptr(alpha), _ptr(eta), _ptr(theta), _ptr(gamma),
         ctypes.byref(cfg), _ptr(Y), _ptr(M_final), ctypes.c_void_p(stream))
+    if rc != OK:
+        raise AtlasError(rc, atlas_mem_strerror(rc))
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20  # ATLAS_NOALLOC_SCRATCH_BYTES in include/atlas_mem.h
+
+
+def atlas_mem_forward_noalloc(K, Q, V, alpha, eta, theta, gamma, cfg: AtlasMemCfg, Y, M_final,
+                              stream=None) -> None:
+    """``atlas_mem_forward`` for callers that cannot allocate device memory: the
+    library's built-in scratch array (NOALLOC_SCRATCH_BYTES per device, shared by
+    all calls on that device) replaces ``cfg.workspace``.  Calls that overlap on
+    the GPU race on that array; make the first call on a device before any
+    stream capture.  Raises AtlasError if the problem needs more scratch than
+    the array holds."""
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream().cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    rc = load_library().atlas_mem_forward_noalloc(
+        _ptr(K), _ptr(Q), _ptr(V), _ptr(alpha), _ptr(eta), _ptr(theta), _ptr(gamma),
+        ctypes.byref(cfg), _ptr(Y), _ptr(M_final), ctypes.c_void_p(stream))
+    if rc == ERR_WORKSPACE:
+        need = atlas_mem_workspace_bytes(cfg)
+        raise AtlasError(rc, f"problem needs {need} bytes of scratch; the built-in array holds "
+                             f"{NOALLOC_SCRATCH_BYTES} (split the heads over several calls)")
     if rc != OK:
         raise AtlasError(rc, atlas_mem_strerror(rc))
