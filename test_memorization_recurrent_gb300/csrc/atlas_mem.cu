@@ -114,8 +114,9 @@ const char* atlas_mem_path(const atlas_mem_cfg* cfg) {
 long atlas_mem_launch_count(const atlas_mem_cfg* cfg) {
   switch (choose_path(cfg)) {
     case PATH_LINEAR_SIMT:
-    case PATH_LINEAR_TC:
       return (long)cfg->B * cfg->H > 0 ? 1 : 0;
+    case PATH_LINEAR_TC:
+      return (long)cfg->B * cfg->H > 0 ? 2 : 0;
     case PATH_MLP_SIMT: {
       if ((long)cfg->B * cfg->H == 0) return 0;
       MlpArgs a = mlp_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, cfg,

@@ -22,10 +22,13 @@ struct LinArgs {
 };
 
 int linear_simt_launch(const LinArgs& a, int heads, cudaStream_t st);
+// Same kernel, restricted to the heads whose eta has a non-zero entry.
+int linear_simt_launch_masked(const LinArgs& a, int heads, cudaStream_t st);
 int linear_simt_plan(const LinArgs& a, int heads, int* RV_out, size_t* smem_out);
 
 // Tensor-core path: linear memory, identity map, d_k = d_v = 128, bf16 inputs,
-// b = 64, c = 1.
+// b = 64, c = 1, N % 4 == 0.  Launches the tensor-core kernel (heads with
+// eta == 0) and the masked CUDA-core kernel (the other heads).
 bool linear_tc_supported(const LinArgs& a);
 int linear_tc_launch(const LinArgs& a, int heads, int* status, cudaStream_t st);
 

@@ -159,3 +159,39 @@ def test_full_size_sampled(wid, sample, prefix):
         ey = rel_err(Yg[sample, :prefix], Yo, w.bf16)
         assert ey <= tol(w), f"workload {wid} Y prefix err {ey:.3e}"
     assert np.isfinite(Yg).all()
+
+
+# ------------------------------------------------- tensor-core linear path
+
+def test_tensor_core_path_selected_for_the_deltanet_workload():
+    import test_memorization_recurrent_gb300 as A
+    from test_memorization_recurrent_gb300.harness import cfg_for
+    w = W.workload(2)
+    assert A.atlas_mem_path(cfg_for(w, w.heads, w.N)) == "linear_tc"
+    assert A.atlas_mem_path(cfg_for(w, 3, 212)) == "linear_tc"
+    assert A.atlas_mem_path(cfg_for(w, 3, 209)) == "linear_simt"  # N % 4 != 0
+
+
+@pytest.mark.parametrize("N", [64, 212, 64 * 5])
+def test_tensor_core_path_small(N):
+    """Several chunks and a ragged tail (N = 212) through the tcgen05 kernel."""
+    w = W.workload(2, N=N)
+    inp = W.generate(w, heads=[0, 3, 8, 13])
+    inp["M0"] = (np.random.default_rng(N).standard_normal(inp["M0"].shape) * 0.1).astype(np.float32)
+    Yo, Mo, _ = run_oracle(w, inp)
+    Yg, Mg, _ = gpu_run(w, inp)
+    check(w, Yg, Mg, Yo, Mo, f"N={N}")
+
+
+def test_tensor_core_path_mixed_momentum_heads_and_state_out():
+    """Heads with a non-zero eta go to the CUDA-core kernel in the same call;
+    the momentum returned through S_state matches for both kinds of head."""
+    w = W.workload(2, N=256)
+    inp = W.generate(w, heads=[0, 1, 2, 3])
+    rng = np.random.default_rng(7)
+    inp["eta"][1] = rng.uniform(0.5, 0.9, w.N).astype(np.float32)
+    inp["eta"][3, 100] = 0.25
+    Yo, Mo, So = run_oracle(w, inp)
+    Yg, Mg, Sg = gpu_run(w, inp, with_S=True)
+    check(w, Yg, Mg, Yo, Mo, "mixed")
+    assert rel_err(Sg, So, True) <= tol(w)
