@@ -94,56 +94,88 @@ def profile_traffic(kernel_src: str, profile_name: str, units_per_launch: float)
 
 
 class Clocks:
-    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampling of SM clocks and throttle reasons.  The sampler starts
+    before the warm-up; only samples stamped inside the timed region count."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, interval_ms: int = 20):
         self.gpu = gpu_index
+        self.interval = interval_ms
         self.proc = None
-        self.out = None
+        self.path = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval), "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
         except (FileNotFoundError, OSError):
             self.proc = None
         return self
+
+    def wait_ready(self, timeout_s: float = 5.0):
+        """Block until the sampler has written its first line (or timeout)."""
+        t = time.time()
+        while self.proc is not None and time.time() - t < timeout_s:
+            if os.path.getsize(self.path) > 0:
+                return
+            time.sleep(0.02)
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+        time.sleep(2.5 * self.interval / 1e3)
 
     def __exit__(self, *exc):
         if self.proc is not None:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                self.out, _ = self.proc.communicate()
 
     def summary(self):
-        if not self.out:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm, mx, reasons = [], [], set()
+        import datetime
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.out.strip().splitlines():
+        rows = []
+        try:
+            text = open(self.path).read()
+            os.unlink(self.path)
+        except OSError:
+            text = ""
+        for line in text.strip().splitlines():
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[2]), float(f[3]), f[6:10]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.01 <= r[0] <= self.t1 + 0.01]
+        window = "timed region"
+        if not inside:  # region shorter than the sampling interval: nearest samples
+            inside = sorted(rows, key=lambda r: abs(r[0] - (self.t0 or 0)))[:3]
+            window = "nearest to the timed region"
+        reasons = set()
+        for r in inside:
+            for n, v in zip(names, r[3]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "samples": len(inside),
+                "window": window, "reasons": sorted(reasons)}
 
 
 # ------------------------------------------------------------------ oracle leg
@@ -237,16 +269,18 @@ def run_atlas(args, w):
     stream = torch.cuda.current_stream()
 
     # -- device-resident timing
-    for _ in range(args.warmup):
-        run(d)
-    torch.cuda.synchronize()
     k_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     k_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     with Clocks(torch.cuda.current_device()) as clk:
+        for _ in range(args.warmup):
+            run(d)
+        torch.cuda.synchronize()
+        clk.wait_ready()
         barrier(world)
         torch.cuda.synchronize()
+        clk.mark_start()
         t_start.record(stream)
         for i in range(args.steps):
             run.M.copy_(d["M0"])
@@ -256,6 +290,7 @@ def run_atlas(args, w):
             k_end[i].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
+        clk.mark_end()
         barrier(world)
     elapsed = t_start.elapsed_time(t_end) / 1e3
     kernel_s = sum(a.elapsed_time(b) for a, b in zip(k_start, k_end)) / 1e3 / args.steps
@@ -355,7 +390,7 @@ def run_atlas(args, w):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="atlas", choices=["atlas", "reference"])

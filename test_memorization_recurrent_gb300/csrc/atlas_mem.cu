@@ -99,6 +99,7 @@ size_t atlas_mem_workspace_bytes(const atlas_mem_cfg* cfg) {
                          nullptr, nullptr);
     return mlp_simt_workspace_bytes(a);
   }
+  if (choose_path(cfg) == PATH_LINEAR_TC) return linear_tc_workspace_bytes(cfg->B * cfg->H);
   return 0;
 }
 
@@ -147,7 +148,11 @@ int atlas_mem_forward(const void* K, const void* Q, const void* V, const float* 
     return mlp_simt_forward(a, cfg->workspace, st);
   }
   LinArgs a = lin_args(K, Q, V, alpha, eta, theta, gamma, cfg, Y, M_final);
-  if (path == PATH_LINEAR_TC) return linear_tc_launch(a, (int)heads, cfg->status_dev, st);
+  if (path == PATH_LINEAR_TC) {
+    const size_t need = linear_tc_workspace_bytes((int)heads);
+    if (!cfg->workspace || cfg->workspace_bytes < need) return ATLAS_ERR_WORKSPACE;
+    return linear_tc_launch(a, (int)heads, cfg->status_dev, cfg->workspace, st);
+  }
   return linear_simt_launch(a, (int)heads, st);
 }
 

@@ -22,15 +22,17 @@ struct LinArgs {
 };
 
 int linear_simt_launch(const LinArgs& a, int heads, cudaStream_t st);
-// Same kernel, restricted to the heads whose eta has a non-zero entry.
-int linear_simt_launch_masked(const LinArgs& a, int heads, cudaStream_t st);
+// Same kernel, restricted to the heads whose flag (device int per head) is set.
+int linear_simt_launch_flagged(const LinArgs& a, int heads, const int* flags, cudaStream_t st);
 int linear_simt_plan(const LinArgs& a, int heads, int* RV_out, size_t* smem_out);
 
 // Tensor-core path: linear memory, identity map, d_k = d_v = 128, bf16 inputs,
 // b = 64, c = 1, N % 4 == 0.  Launches the tensor-core kernel (heads with
-// eta == 0) and the masked CUDA-core kernel (the other heads).
+// eta == 0; it flags the others in the workspace) and the CUDA-core kernel on
+// the flagged heads.  Workspace: one int per head.
 bool linear_tc_supported(const LinArgs& a);
-int linear_tc_launch(const LinArgs& a, int heads, int* status, cudaStream_t st);
+size_t linear_tc_workspace_bytes(int heads);
+int linear_tc_launch(const LinArgs& a, int heads, int* status, void* workspace, cudaStream_t st);
 
 // Arguments of the MLP-memory path.
 struct MlpArgs {

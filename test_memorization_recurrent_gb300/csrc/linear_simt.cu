@@ -53,9 +53,10 @@ static LinSimtSmem lin_simt_layout(int RV, int D, int Lmax, int b, int d_k) {
   return s;
 }
 
-// masked = 1: only heads whose eta has a non-zero entry (the heads the
-// tensor-core kernel leaves); every other head returns at once.
-__global__ void __launch_bounds__(256) linear_simt_kernel(LinArgs p, LinSimtSmem L, int masked) {
+// flags != nullptr: only the heads whose flag is set (the heads the tensor-core
+// kernel leaves, which it marks); every other head returns at once.
+__global__ void __launch_bounds__(256) linear_simt_kernel(LinArgs p, LinSimtSmem L,
+                                                          const int* flags) {
   extern __shared__ float sm[];
   float* Ms = sm + L.Ms;
   float* Ss = sm + L.Ss;
@@ -73,12 +74,7 @@ __global__ void __launch_bounds__(256) linear_simt_kernel(LinArgs p, LinSimtSmem
   uint8_t* pq = pp + (L.D - p.d_k > 0 ? L.D - p.d_k : 0);
 
   const int head = blockIdx.x;
-  if (masked) {
-    const float* e = p.eta + (long)head * p.N;
-    int nz = 0;
-    for (int x = threadIdx.x; x < p.N; x += blockDim.x) nz |= e[x] != 0.f;
-    if (!__syncthreads_or(nz)) return;
-  }
+  if (flags && flags[head] == 0) return;
   const int r0 = blockIdx.y * L.RV;
   const int rv = min(L.RV, p.d_v - r0);
   const int D = L.D, dk = p.d_k, dv = p.d_v;
@@ -212,7 +208,7 @@ int linear_simt_plan(const LinArgs& a, int heads, int* RV_out, size_t* smem_out)
   return ATLAS_OK;
 }
 
-static int launch(const LinArgs& a, int heads, int masked, cudaStream_t st) {
+static int launch(const LinArgs& a, int heads, const int* flags, cudaStream_t st) {
   int RV;
   size_t smem;
   int rc = linear_simt_plan(a, heads, &RV, &smem);
@@ -222,16 +218,16 @@ static int launch(const LinArgs& a, int heads, int masked, cudaStream_t st) {
                            (int)smem) != cudaSuccess)
     return ATLAS_ERR_CUDA;
   dim3 grid(heads, (a.d_v + RV - 1) / RV);
-  linear_simt_kernel<<<grid, 256, smem, st>>>(a, s, masked);
+  linear_simt_kernel<<<grid, 256, smem, st>>>(a, s, flags);
   return cudaGetLastError() == cudaSuccess ? ATLAS_OK : ATLAS_ERR_CUDA;
 }
 
 int linear_simt_launch(const LinArgs& a, int heads, cudaStream_t st) {
-  return launch(a, heads, 0, st);
+  return launch(a, heads, nullptr, st);
 }
 
-int linear_simt_launch_masked(const LinArgs& a, int heads, cudaStream_t st) {
-  return launch(a, heads, 1, st);
+int linear_simt_launch_flagged(const LinArgs& a, int heads, const int* flags, cudaStream_t st) {
+  return launch(a, heads, flags, st);
 }
 
 }  // namespace atlas

@@ -12,28 +12,28 @@
 // prod_{l=i+1..n} (1 - alpha_l) ("[Paper Review] Titans 논문 이해하기":
 // S_t = -theta_t grad, M_t = (1 - alpha_t) M_{t-1} + S_t, y_t = M_t q_t).
 //
-// Four tensor-core products per chunk (M = 128 rows, fp32 accumulators in TMEM):
-//   D_QP = [Phi; Q] Phi^T          (rows 64..127: q_n . k_i)
-//   D1   = [Phi; Q] M0^T           (rows 0..63: Phi M0^T; rows 64..127: Q M0^T)
-//   dM   = Ew^T Phi                (Ew = W[63,:] * E, the rank-64 state update)
-//   D1  += [* ; P'] E              (P' = -2 W * (Q Phi^T), added onto the rows
-//                                   64..127 of D1 once they are scaled by a_n:
-//                                   they become y_n)
-// K, Q, V are bf16 and exact; the state-derived operands (M0, E, Ew, P) are
-// split into bf16 hi + lo parts (x = hi + lo to ~2^-17), so every product keeps
-// fp32-level accuracy.  The fp32 master state M lives in the registers of the
-// eight epilogue warps (thread = row of M, 64 columns each).
+// Everything is computed transposed, with the value index v (128) on the TMEM
+// lanes, so that each of the eight epilogue warps owns 32 rows v and 32 of the
+// chunk's tokens.  Per chunk (fp32 accumulators in TMEM):
+//   [T | Qy] = M0 [Phi; Q]^T   (128 x 128): T -> E^T = T - V^T,
+//                                 Qy = M0 Q^T scaled by a_n per query column
+//   QP  = [Phi; Q] Phi^T  (rows 64..127: q_n . k_i) -> P' = -2 W * (Q Phi^T)
+//   dM  = Ew^T Phi        (128 x 128) with Ew = W[63,:] * E   (state update)
+//   Qy += E^T P'^T        (128 x 64)  -> y^T, the readout of the chunk
+// M0 and Ew are A operands held in TMEM (bf16 hi + lo halves, x = hi + lo to
+// ~2^-16); Phi, Q (bf16, exact) come from shared memory by TMA, E and P' are
+// split the same way into shared memory.  The fp32 master state M lives in the
+// registers of the epilogue warps (thread = row v, 64 columns).
 //
-// Warp roles (320 threads): warp 0 issues TMA loads of chunk j+1 while chunk j
-// runs (two stages); warp 1 builds the per-chunk gate tables and issues the
-// MMAs from one thread; warps 2..9 are the epilogue (TMEM -> registers ->
-// shared memory / global), two warps per 32-lane TMEM quadrant.
+// Warp roles (320 threads): warp 0 issues TMA loads three chunks deep; warp 1
+// builds the gate tables (warp-wide scans) and issues every MMA from one
+// thread; warps 2..9 are the epilogue, two per 32-lane TMEM quadrant.
 //
-// Heads whose eta has any non-zero entry are left to the CUDA-core kernel,
-// which is launched right after this one and takes exactly those heads (both
-// kernels read eta and decide the same way).  Every wait on an mbarrier is
-// bounded; on expiry the kernel records ATLAS_ERR_TIMEOUT in the status word,
-// drains its in-flight copies and MMAs, frees TMEM and returns.
+// Heads whose eta has any non-zero entry are left to the CUDA-core kernel
+// launched right after this one: this kernel writes one flag per head to the
+// workspace and that kernel takes exactly the flagged heads.  Every mbarrier
+// wait is bounded; on expiry the kernel records ATLAS_ERR_TIMEOUT in the status
+// word, drains its in-flight copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <string.h>
@@ -55,60 +55,123 @@ constexpr int kDim = 128;
 constexpr long long kWaitLimit = 2000000000LL;  // clock cycles (~1 s)
 
 // shared-memory map (bytes from a 1024-aligned base)
-constexpr uint32_t STAGE_BYTES = 33792;  // Phi/Q (4 x 8 KB) + gates (3 x 256 B), padded
+//   stage: Phi kb0 | Q kb0 | Phi kb1 | Q kb1 (8 KB each, 128B-swizzled) | V (64 x 128
+//   bf16, row-major) | alpha | eta | theta
+constexpr uint32_t ST_V = 32768;
+constexpr uint32_t ST_GATES = ST_V + 16384;
+constexpr uint32_t STAGE_BYTES = ST_GATES + 1024;  // 50176 = 49 x 1024
+constexpr int kStages = 3;
 constexpr uint32_t OFF_STAGE0 = 0;
-constexpr uint32_t OFF_MHI = 2 * STAGE_BYTES;       // 67584
-constexpr uint32_t OFF_MLO = OFF_MHI + 32768;
-constexpr uint32_t OFF_EHI = OFF_MLO + 32768;
+constexpr uint32_t OFF_EHI = kStages * STAGE_BYTES;   // E^T as [v][i], K-major, 16 KB
 constexpr uint32_t OFF_ELO = OFF_EHI + 16384;
-constexpr uint32_t OFF_EWHI = OFF_ELO + 16384;
-constexpr uint32_t OFF_EWLO = OFF_EWHI + 16384;
-constexpr uint32_t OFF_PHI = OFF_EWLO + 16384;      // preceded by 8 KB of EWLO (A-tile rows 0..63)
+constexpr uint32_t OFF_PHI = OFF_ELO + 16384;         // P' as [n][i], K-major, 8 KB
 constexpr uint32_t OFF_PLO = OFF_PHI + 8192;
 constexpr uint32_t OFF_TAB = OFF_PLO + 8192;
-constexpr uint32_t TAB_FLOATS = 5 * kChunk;          // a, pb, wb, keep, th
+constexpr uint32_t TAB_FLOATS = 5 * kChunk;           // a, pb, wb, keep, th
 constexpr uint32_t OFF_ELAST = OFF_TAB + 2 * TAB_FLOATS * 4;
 constexpr uint32_t OFF_BARS = OFF_ELAST + kDim * 4;
 constexpr uint32_t SMEM_USED = OFF_BARS + 256;
-constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;   // alignment slack
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;    // alignment slack
 
-constexpr uint32_t STAGE_TX = 4 * 8192 + 3 * 256;
+constexpr uint32_t STAGE_TX = 4 * 8192 + 16384 + 3 * 256;
 
-// TMEM columns: D1 is double-buffered so that the readout of chunk j can
-// leave TMEM while chunk j+1's products already run.
-constexpr uint32_t TM_QP = 0, TM_D1 = 64, TM_DM = 320, TM_COLS = 512;
-__device__ __forceinline__ uint32_t tm_d1(int j) { return TM_D1 + 128u * (uint32_t)(j & 1); }
+// TMEM columns.  Two 128-column buffers hold [T | Qy] of consecutive chunks;
+// chunk j's QP goes into the T half of the other buffer (free by then), so
+// chunk j's readout can leave TMEM while chunk j+1 already runs.
+constexpr uint32_t TM_D1 = 0;      // [T | Qy], two buffers (2 x 128)
+constexpr uint32_t TM_DM = 256;    // state update        (128)
+constexpr uint32_t TM_MHI = 384;   // A operand M0: hi (64 cols = 128 bf16), lo
+constexpr uint32_t TM_MLO = 448;
+constexpr uint32_t TM_EWHI = 384;  // A operand Ew (reuses the M0 columns once T is done)
+constexpr uint32_t TM_EWLO = 416;
+constexpr uint32_t TM_COLS = 512;
+__device__ __forceinline__ uint32_t tm_t(int j) { return TM_D1 + 128u * (uint32_t)(j & 1); }
+__device__ __forceinline__ uint32_t tm_q(int j) { return tm_t(j) + 64u; }
+__device__ __forceinline__ uint32_t tm_qp(int j) { return tm_t(j + 1); }
 
 enum Bar {
-  B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_QP, B_D1, B_DM, B_Y, B_E, B_P, B_M, B_TAB0, B_TAB1,
-  B_S, B_DRAIN, B_COUNT
+  B_FULL0 = 0, B_FULL1, B_FULL2, B_EMPTY0, B_EMPTY1, B_EMPTY2, B_QP, B_D1, B_DM, B_Y, B_E, B_P,
+  B_M, B_TAB0, B_TAB1, B_S, B_DRAIN, B_COUNT
 };
 
 struct TcParams {
   const __nv_bfloat16* K;
-  const __nv_bfloat16* V;
   const float* eta;
   const float* theta;
   const float* gamma;
   float* Y;
   float* M;
-  float* S;  // optional
-  int* status;
+  float* S;     // optional
+  int* status;  // optional
+  int* flags;   // [heads]: 1 = left to the CUDA-core kernel
   int N;
 };
 
 struct TcMaps {
-  CUtensorMap k, q, alpha, eta, theta;
+  CUtensorMap k, q, v, alpha, eta, theta;
 };
 
-__device__ __forceinline__ void table_ptrs(unsigned char* sm, int buf, float*& a, float*& pb,
-                                           float*& wb, float*& keep, float*& th) {
-  float* t = reinterpret_cast<float*>(sm + OFF_TAB) + buf * TAB_FLOATS;
-  a = t;
-  pb = t + kChunk;
-  wb = t + 2 * kChunk;
-  keep = t + 3 * kChunk;
-  th = t + 4 * kChunk;
+__device__ __forceinline__ float* table(unsigned char* sm, int buf) {
+  return reinterpret_cast<float*>(sm + OFF_TAB) + buf * TAB_FLOATS;
+}
+
+// Split 8 fp32 values x = hi + lo into two bf16x8 chunks: hi keeps the top 16
+// bits (truncation), lo = rn(x - hi), so |x - hi - lo| <= 2^-16 |x|.
+__device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const uint32_t a = __float_as_uint(x[2 * p]), b = __float_as_uint(x[2 * p + 1]);
+    h[p] = __byte_perm(a, b, 0x7632);  // top halves of a (low) and b (high)
+    const float ra = x[2 * p] - __uint_as_float(a & 0xFFFF0000u);
+    const float rb = x[2 * p + 1] - __uint_as_float(b & 0xFFFF0000u);
+    const __nv_bfloat162 r = __floats2bfloat162_rn(ra, rb);
+    l[p] = *reinterpret_cast<const uint32_t*>(&r);
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+__device__ __forceinline__ void st_shared_u4(uint32_t addr, const uint4& v) {
+  st_shared_v4(addr, v.x, v.y, v.z, v.w);
+}
+
+// 16 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Pack 32 fp32 values into hi / lo bf16 pairs (element 2c in the low half of
+// column c), the TMEM A-operand layout.
+__device__ __forceinline__ void pack_split32(const float* x, uint32_t* hi, uint32_t* lo) {
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    const uint32_t a = __float_as_uint(x[2 * c]), b = __float_as_uint(x[2 * c + 1]);
+    hi[c] = __byte_perm(a, b, 0x7632);
+    const __nv_bfloat162 r = __floats2bfloat162_rn(x[2 * c] - __uint_as_float(a & 0xFFFF0000u),
+                                                   x[2 * c + 1] - __uint_as_float(b & 0xFFFF0000u));
+    lo[c] = *reinterpret_cast<const uint32_t*>(&r);
+  }
 }
 
 }  // namespace
@@ -135,21 +198,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float4 v = e4[x];
       nz |= (v.x != 0.f) | (v.y != 0.f) | (v.z != 0.f) | (v.w != 0.f);
     }
-    if (__syncthreads_or(nz)) return;
+    nz = __syncthreads_or(nz);
+    if (tid == 0) p.flags[head] = nz ? 1 : 0;
+    if (nz) return;
   }
   if (nchunks == 0) return;
 
   if (tid == 0) {
     for (int b = 0; b < B_COUNT; ++b) {
       uint32_t cnt = 1;
-      if (b == B_E || b == B_P) cnt = 4;
-      if (b == B_M || b == B_S) cnt = 8;
+      if (b == B_P) cnt = 4;
+      if (b == B_E || b == B_M || b == B_S) cnt = 8;
       mbar_init(&bars[b], cnt);
     }
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&maps.k);
     prefetch_tmap(&maps.q);
+    prefetch_tmap(&maps.v);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TM_COLS);
@@ -171,8 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int issued = 0;
       for (int j = 0; j < nchunks; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && !mbar_wait(&bars[B_EMPTY0 + s], ((j - 2) >> 1) & 1, abort_flag, kWaitLimit)) {
+        const int s = j % kStages;
+        if (j >= kStages &&
+            !mbar_wait(&bars[B_EMPTY0 + s], ((j - kStages) / kStages) & 1, abort_flag, kWaitLimit)) {
           fail();
           break;
         }
@@ -184,15 +251,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(st + 8192, &maps.q, fb, 0, t0, head);
         tma_load_3d(st + 16384, &maps.k, fb, 64, t0, head);
         tma_load_3d(st + 24576, &maps.q, fb, 64, t0, head);
-        tma_load_2d(st + 32768, &maps.alpha, fb, t0, head);
-        tma_load_2d(st + 32768 + 256, &maps.eta, fb, t0, head);
-        tma_load_2d(st + 32768 + 512, &maps.theta, fb, t0, head);
+        tma_load_3d(st + ST_V, &maps.v, fb, 0, t0, head);
+        tma_load_2d(st + ST_GATES, &maps.alpha, fb, t0, head);
+        tma_load_2d(st + ST_GATES + 256, &maps.eta, fb, t0, head);
+        tma_load_2d(st + ST_GATES + 512, &maps.theta, fb, t0, head);
         issued = j + 1;
       }
       // drain: every issued load must land before shared memory is released
-      for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j) {
+      for (int j = issued - kStages < 0 ? 0 : issued - kStages; j < issued; ++j) {
         volatile int zero = 0;
-        mbar_wait(&bars[B_FULL0 + (j & 1)], (j >> 1) & 1, &zero, kWaitLimit);
+        mbar_wait(&bars[B_FULL0 + j % kStages], (j / kStages) & 1, &zero, kWaitLimit);
       }
     }
     __syncwarp();
@@ -200,90 +268,98 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------- tables + MMA issuer
     const float g0 = p.gamma[0];
     auto tables = [&](int j) -> bool {
-      const int s = j & 1;
-      if (!mbar_wait(&bars[B_FULL0 + s], (j >> 1) & 1, abort_flag, kWaitLimit)) return false;
-      if (lane == 0) {
-        const float* ga = reinterpret_cast<const float*>(sm + OFF_STAGE0 + s * STAGE_BYTES + 32768);
-        const float* gt = ga + 128;
-        float *a, *pb, *wb, *keep, *th;
-        table_ptrs(sm, s, a, pb, wb, keep, th);
-        float pa = 1.f, pbv = 1.f;
-        for (int n = 0; n < kChunk; ++n) {
-          const float k = 1.f - ga[n];
-          keep[n] = k;
-          th[n] = gt[n] * g0;
-          pa *= k;
-          a[n] = pa;
-          if (n >= 32) pbv *= k;
-          pb[n] = n >= 32 ? pbv : 1.f;
-        }
-        float suf = 1.f;  // prod_{l=i+1..63} keep_l
-        for (int i = kChunk - 1; i >= 0; --i) {
-          wb[i] = th[i] * suf;
-          suf *= keep[i];
-        }
-        mbar_arrive(&bars[B_TAB0 + s]);
+      const int s = j % kStages;
+      if (!mbar_wait(&bars[B_FULL0 + s], (j / kStages) & 1, abort_flag, kWaitLimit)) return false;
+      // warp-parallel scans: lane l owns tokens 2l and 2l+1
+      const float* ga = reinterpret_cast<const float*>(sm + OFF_STAGE0 + s * STAGE_BYTES + ST_GATES);
+      const float* gt = ga + 128;
+      float* tb = table(sm, j & 1);
+      float *a = tb, *pb = tb + kChunk, *wb = tb + 2 * kChunk, *keep = tb + 3 * kChunk,
+            *th = tb + 4 * kChunk;
+      const unsigned full = 0xFFFFFFFFu;
+      const int n0 = 2 * lane, n1 = n0 + 1;
+      const float k0 = 1.f - ga[n0], k1 = 1.f - ga[n1];
+      const float t0v = gt[n0] * g0, t1v = gt[n1] * g0;
+      float pa = k0 * k1;
+      float pp = lane >= 16 ? pa : 1.f;
+      float sf = pa;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float ua = __shfl_up_sync(full, pa, o);
+        const float up = __shfl_up_sync(full, pp, o);
+        const float ds = __shfl_down_sync(full, sf, o);
+        if (lane >= o) { pa *= ua; pp *= up; }
+        if (lane + o < 32) sf *= ds;
       }
+      float ea = __shfl_up_sync(full, pa, 1);    // product over tokens < n0
+      float ep = __shfl_up_sync(full, pp, 1);
+      float es = __shfl_down_sync(full, sf, 1);  // product over tokens > n1
+      if (lane == 0) { ea = 1.f; ep = 1.f; }
+      if (lane == 31) es = 1.f;
+      keep[n0] = k0; keep[n1] = k1;
+      th[n0] = t0v; th[n1] = t1v;
+      a[n0] = ea * k0;
+      a[n1] = ea * k0 * k1;
+      pb[n0] = lane >= 16 ? ep * k0 : 1.f;
+      pb[n1] = lane >= 16 ? ep * k0 * k1 : 1.f;
+      wb[n1] = t1v * es;
+      wb[n0] = t0v * es * k1;
       __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_TAB0 + (j & 1)]);
       return true;
     };
     bool ok = tables(0);
-    if (!ok) fail();
     for (int j = 0; ok && j < nchunks; ++j) {
-      const int s = j & 1;
+      const int s = j % kStages;
       const uint32_t st = sbase + OFF_STAGE0 + s * STAGE_BYTES;
-      // stage j is loaded (waited in tables(j))
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t id = idesc_bf16(128, 64, false, false);
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_bf16(tmem + TM_QP, sdesc_sw128(st + off, 16, 1024), sdesc_sw128(st + off, 16, 1024),
-                   id, k > 0);
-        }
-        mma_commit(&bars[B_QP]);
-      }
-      __syncwarp();
+      // M0 in TMEM (written by the epilogue), stage j loaded (waited in tables(j))
       if (!mbar_wait(&bars[B_M], j & 1, abort_flag, kWaitLimit)) { ok = false; break; }
       tc_fence_after();
       if (lane == 0) {
         const uint32_t id = idesc_bf16(128, 128, false, false);
-        for (int k = 0; k < 16; ++k) {
+        for (int k = 0; k < 16; ++k) {  // [T | Qy] = M0 [Phi; Q]^T; hi then lo halves of M0
+          const uint32_t am = tmem + (k < 8 ? TM_MHI : TM_MLO) + 8 * (k & 7);
           const uint32_t off = ((k & 7) >> 2) * 16384 + (k & 3) * 32;
-          const uint32_t mb = sbase + (k < 8 ? OFF_MHI : OFF_MLO);
-          mma_bf16(tmem + tm_d1(j), sdesc_sw128(st + off, 16, 1024),
-                   sdesc_sw128(mb + off, 16, 1024), id, k > 0);
+          mma_bf16_ta(tmem + tm_t(j), am, sdesc_sw128(st + off, 16, 1024), id, k > 0);
         }
         mma_commit(&bars[B_D1]);
+        const uint32_t id64 = idesc_bf16(128, 64, false, false);
+        for (int k = 0; k < 8; ++k) {  // QP = [Phi; Q] Phi^T
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          mma_bf16(tmem + tm_qp(j), sdesc_sw128(st + off, 16, 1024),
+                   sdesc_sw128(st + off, 16, 1024), id64, k > 0);
+        }
+        mma_commit(&bars[B_QP]);
       }
       __syncwarp();
+      // next chunk's gate tables while this chunk's products run (the buffer's
+      // previous readers, chunk j-1's epilogue, are done: B_M was complete)
+      if (j + 1 < nchunks && !tables(j + 1)) { ok = false; break; }
       if (!mbar_wait(&bars[B_E], j & 1, abort_flag, kWaitLimit)) { ok = false; break; }
       tc_fence_after();
-      if (lane == 0) {
-        const uint32_t id = idesc_bf16(128, 128, true, true);
+      if (lane == 0) {  // dM = Ew^T Phi (Ew in TMEM, Phi MN-major in the stage)
+        const uint32_t id = idesc_bf16(128, 128, false, true);
         for (int k = 0; k < 8; ++k) {
-          const uint32_t ew = sbase + ((k < 4) ? OFF_EWHI : OFF_EWLO) + (k & 3) * 2048;
-          mma_bf16(tmem + TM_DM, sdesc_sw128(ew, 8192, 1024),
-                   sdesc_sw128(st + (k & 3) * 2048, 16384, 1024), id, k > 0);
+          const uint32_t ae = tmem + (k < 4 ? TM_EWHI : TM_EWLO) + 8 * (k & 3);
+          mma_bf16_ta(tmem + TM_DM, ae, sdesc_sw128(st + (k & 3) * 2048, 16384, 1024), id, k > 0);
         }
         mma_commit(&bars[B_DM]);
       }
       __syncwarp();
       if (!mbar_wait(&bars[B_P], j & 1, abort_flag, kWaitLimit)) { ok = false; break; }
       tc_fence_after();
-      if (lane == 0) {
-        const uint32_t id = idesc_bf16(128, 128, false, true);
+      if (lane == 0) {  // Qy += E^T P'^T: Ehi*Phi, Elo*Phi, Ehi*Plo
+        const uint32_t id = idesc_bf16(128, 64, false, false);
         for (int k = 0; k < 12; ++k) {
-          const int part = k >> 2;  // 0: Phi*Ehi, 1: Phi*Elo, 2: Plo*Ehi
-          const uint32_t pa = sbase + (part < 2 ? OFF_PHI : OFF_PLO) - 8192 + (k & 3) * 32;
-          const uint32_t eb = sbase + (part == 1 ? OFF_ELO : OFF_EHI) + (k & 3) * 2048;
-          mma_bf16(tmem + tm_d1(j), sdesc_sw128(pa, 16, 1024), sdesc_sw128(eb, 8192, 1024), id, 1);
+          const int part = k >> 2;
+          const uint32_t ea = sbase + (part == 1 ? OFF_ELO : OFF_EHI) + (k & 3) * 32;
+          const uint32_t pb = sbase + (part == 2 ? OFF_PLO : OFF_PHI) + (k & 3) * 32;
+          mma_bf16(tmem + tm_q(j), sdesc_sw128(ea, 16, 1024), sdesc_sw128(pb, 16, 1024), id, 1);
         }
         mma_commit(&bars[B_Y]);
         mma_commit(&bars[B_EMPTY0 + s]);
       }
       __syncwarp();
-      if (j + 1 < nchunks && !tables(j + 1)) { ok = false; break; }
     }
     if (!ok) fail();
     if (lane == 0) {
@@ -296,86 +372,97 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;             // TMEM lane quadrant
-    const int h = (warp - 2) >> 2;      // column half
-    const int r = 32 * q + lane;        // TMEM lane = row of the 128-row tiles
+    const int h = (warp - 2) >> 2;      // half: columns / tokens / queries
+    const int v = 32 * q + lane;        // TMEM lane = value index v
     const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
-    const bool low = q < 2;
-    float m[64];
+    const bool high = q >= 2;
+    float m[64];                        // M0[v][64h .. 64h+63]
     {
-      const float4* src = reinterpret_cast<const float4*>(p.M + ((long)head * kDim + r) * kDim + 64 * h);
+      const float4* src = reinterpret_cast<const float4*>(p.M + ((long)head * kDim + v) * kDim + 64 * h);
 #pragma unroll
       for (int x = 0; x < 16; ++x) {
-        const float4 v = src[x];
-        m[4 * x] = v.x; m[4 * x + 1] = v.y; m[4 * x + 2] = v.z; m[4 * x + 3] = v.w;
+        const float4 t = src[x];
+        m[4 * x] = t.x; m[4 * x + 1] = t.y; m[4 * x + 2] = t.z; m[4 * x + 3] = t.w;
       }
-      const uint32_t mh = sbase + OFF_MHI + h * 16384, ml = sbase + OFF_MLO + h * 16384;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) store_split8(mh + sw128_offset(r, c), ml + sw128_offset(r, c), m + 8 * c);
-      fence_proxy_async_smem();
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t hi[16], lo[16];
+        pack_split32(m + 32 * cc, hi, lo);
+        tmem_st16(tl + TM_MHI + 32 * h + 16 * cc, hi);
+        tmem_st16(tl + TM_MLO + 32 * h + 16 * cc, lo);
+      }
+      tmem_wait_st();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_M]);
     }
-    const __nv_bfloat16* Vh = p.V + (long)head * N * kDim;
     float* Yh = p.Y + (long)head * N * kDim;
     bool ok = true;
     for (int j = 0; j < nchunks; ++j) {
-      const int s = j & 1, t0 = j * kChunk;
+      const int t0 = j * kChunk;
       const uint32_t par = j & 1;
-      if (!mbar_wait(&bars[B_TAB0 + s], (j >> 1) & 1, abort_flag, kWaitLimit)) { ok = false; break; }
-      float *ta, *tpb, *twb, *tkeep, *tth;
-      table_ptrs(sm, s, ta, tpb, twb, tkeep, tth);
-      if (low) {
-        // ---- errors E = Phi M0^T - V of token i = r
-        const int i = r;
-        uint32_t vv[32];  // 64 bf16 values of v_i, packed in pairs
-        const bool valid = t0 + i < N;
-        const uint4* vsrc = reinterpret_cast<const uint4*>(Vh + (long)(t0 + i) * kDim + 64 * h);
+      const unsigned char* stg = sm + OFF_STAGE0 + (j % kStages) * STAGE_BYTES;
+      if (!mbar_wait(&bars[B_TAB0 + (j & 1)], (j >> 1) & 1, abort_flag, kWaitLimit)) { ok = false; break; }
+      const float* tb = table(sm, j & 1);
+      const float *ta = tb, *tpb = tb + kChunk, *twb = tb + 2 * kChunk, *tkeep = tb + 3 * kChunk,
+                  *tth = tb + 4 * kChunk;
+      // V^T[v][i] of this thread's tokens, read before the products are done
+      float vt[32];
+      {
+        const __nv_bfloat16* Vs = reinterpret_cast<const __nv_bfloat16*>(stg + ST_V);
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
-          const uint4 v = valid ? vsrc[x] : make_uint4(0, 0, 0, 0);
-          vv[4 * x] = v.x; vv[4 * x + 1] = v.y; vv[4 * x + 2] = v.z; vv[4 * x + 3] = v.w;
+        for (int x = 0; x < 32; ++x) vt[x] = __bfloat162float(Vs[(32 * h + x) * kDim + v]);
+      }
+      if (!mbar_wait(&bars[B_D1], par, abort_flag, kWaitLimit)) { ok = false; break; }
+      tc_fence_after();
+      {
+        // ---- E^T[v][i] = T[v][i] - V[i][v] for tokens i in [32h, 32h+32)
+        float e[32];
+        tmem_ld32(tl + tm_t(j) + 32 * h, e);
+#pragma unroll
+        for (int x = 0; x < 32; ++x) e[x] -= vt[x];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4 hi, lo;
+          split8(e + 8 * c, hi, lo);
+          const uint32_t o = sw128_offset(v, 4 * h + c);
+          st_shared_u4(sbase + OFF_EHI + o, hi);
+          st_shared_u4(sbase + OFF_ELO + o, lo);
         }
-        if (!mbar_wait(&bars[B_D1], par, abort_flag, kWaitLimit)) { ok = false; break; }
-        tc_fence_after();
-        const float w_i = twb[i];
-        const bool last_tok = p.S && j == nchunks - 1 && t0 + i == N - 1;
+        if (p.S && j == nchunks - 1) {
+          const int il = N - 1 - t0 - 32 * h;
+          if (il >= 0 && il < 32) {
+            float* el = reinterpret_cast<float*>(sm + OFF_ELAST);
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          float d[32];
-          tmem_ld32(tl + tm_d1(j) + 64 * h + 32 * cc, d);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float e[8], ew[8];
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              const uint32_t pk = vv[16 * cc + 4 * c + x];
-              e[2 * x] = d[8 * c + 2 * x] - __uint_as_float(pk << 16);
-              e[2 * x + 1] = d[8 * c + 2 * x + 1] - __uint_as_float(pk & 0xFFFF0000u);
-            }
-#pragma unroll
-            for (int x = 0; x < 8; ++x) ew[x] = w_i * e[x];
-            const uint32_t o = h * 8192 + sw128_offset(i, 4 * cc + c);
-            store_split8(sbase + OFF_EHI + o, sbase + OFF_ELO + o, e);
-            store_split8(sbase + OFF_EWHI + o, sbase + OFF_EWLO + o, ew);
-            if (last_tok) {
-              float* el = reinterpret_cast<float*>(sm + OFF_ELAST) + 64 * h + 32 * cc + 8 * c;
-#pragma unroll
-              for (int x = 0; x < 8; ++x) el[x] = e[x];
-            }
+            for (int x = 0; x < 32; ++x)
+              if (x == il) el[v] = e[x];
           }
         }
+        // Ew = W[63, i] E into TMEM (A operand of the state update)
+#pragma unroll
+        for (int x = 0; x < 32; ++x) e[x] *= twb[32 * h + x];
+        uint32_t hi[16], lo[16];
+        pack_split32(e, hi, lo);
+        tmem_st16(tl + TM_EWHI + 16 * h, hi);
+        tmem_st16(tl + TM_EWLO + 16 * h, lo);
+        // queries n in [32h, 32h+32): scale M0 q_n by a_n in place
+        float t[32];
+        tmem_ld32(tl + tm_q(j) + 32 * h, t);
+#pragma unroll
+        for (int x = 0; x < 32; ++x) t[x] *= ta[32 * h + x];
+        tmem_st32(tl + tm_q(j) + 32 * h, t);  // waits for all stores of this thread
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_E]);
-      } else {
-        // ---- P = W * (Q Phi^T) of query n = r - 64, keys i in [32h, 32h+32)
-        const int n = r - 64;
+      }
+      if (high) {
+        // ---- P'[n][i] = -2 W[n,i] (q_n . k_i), query n = v - 64, keys i in [32h, 32h+32)
+        const int n = v - 64;
         if (!mbar_wait(&bars[B_QP], par, abort_flag, kWaitLimit)) { ok = false; break; }
         tc_fence_after();
-        float pv[32];  // q_n . k_i, then P[n,i]
-        tmem_ld32(tl + TM_QP + 32 * h, pv);
-        // W[n,i] = th_i prod_{l=i+1..n} keep_l, walked from i = 32h+31 down to 32h
+        float pv[32];
+        tmem_ld32(tl + tm_qp(j) + 32 * h, pv);
         float da = (h == 0 && n >= 32) ? tpb[n] : 1.f;
 #pragma unroll
         for (int x = 31; x >= 0; --x) {
@@ -386,75 +473,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
+          uint4 hi, lo;
+          split8(pv + 8 * c, hi, lo);
           const uint32_t o = sw128_offset(n, 4 * h + c);
-          store_split8(sbase + OFF_PHI + o, sbase + OFF_PLO + o, pv + 8 * c);
+          st_shared_u4(sbase + OFF_PHI + o, hi);
+          st_shared_u4(sbase + OFF_PLO + o, lo);
         }
         fence_proxy_async_smem();
-        // ---- scale this query row of Q M0^T by a_n in place; the readout MMA
-        //      then adds -2 (P E)_n onto it
-        if (!mbar_wait(&bars[B_D1], par, abort_flag, kWaitLimit)) { ok = false; break; }
-        tc_fence_after();
-        {
-          const float an = ta[n];
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            float t[32];
-            const uint32_t ad = tl + tm_d1(j) + 64 * h + 32 * cc;
-            tmem_ld32(ad, t);
-#pragma unroll
-            for (int x = 0; x < 32; ++x) t[x] *= an;
-            tmem_st32(ad, t);
-          }
-        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_P]);
       }
-      // ---- state update M = a_63 M - 2 dM; write the next chunk's M operand
+      // ---- state update M = a_63 M - 2 dM; the next chunk's A operand into TMEM
       if (!mbar_wait(&bars[B_DM], par, abort_flag, kWaitLimit)) { ok = false; break; }
       tc_fence_after();
       {
         const float ab = ta[kChunk - 1];
-        const uint32_t mh = sbase + OFF_MHI + h * 16384, ml = sbase + OFF_MLO + h * 16384;
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           float dm[32];
           tmem_ld32(tl + TM_DM + 64 * h + 32 * cc, dm);
 #pragma unroll
           for (int x = 0; x < 32; ++x) m[32 * cc + x] = ab * m[32 * cc + x] - 2.f * dm[x];
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            store_split8(mh + sw128_offset(r, 4 * cc + c), ml + sw128_offset(r, 4 * cc + c),
-                         m + 32 * cc + 8 * c);
+          uint32_t hi[16], lo[16];
+          pack_split32(m + 32 * cc, hi, lo);
+          tmem_st16(tl + TM_MHI + 32 * h + 16 * cc, hi);
+          tmem_st16(tl + TM_MLO + 32 * h + 16 * cc, lo);
         }
-        fence_proxy_async_smem();
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_M]);
       }
-      if (!low) {
-        // ---- readout: rows 64..127 of D1 now hold y_n = a_n (M0 q_n) - 2 (P E)_n
-        const int n = r - 64;
-        if (!mbar_wait(&bars[B_Y], par, abort_flag, kWaitLimit)) { ok = false; break; }
-        tc_fence_after();
-        const bool valid = t0 + n < N;
+      // ---- readout: Qy now holds y^T for the queries n in [32h, 32h+32)
+      if (!mbar_wait(&bars[B_Y], par, abort_flag, kWaitLimit)) { ok = false; break; }
+      tc_fence_after();
+      {
+        float y[32];
+        tmem_ld32(tl + tm_q(j) + 32 * h, y);
+        const int nv = N - t0 - 32 * h;  // valid queries in this half
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          float y[32];
-          tmem_ld32(tl + tm_d1(j) + 64 * h + 32 * cc, y);
-          if (valid) {
-            float4* dst = reinterpret_cast<float4*>(Yh + (long)(t0 + n) * kDim + 64 * h + 32 * cc);
-#pragma unroll
-            for (int x = 0; x < 8; ++x)
-              dst[x] = make_float4(y[4 * x], y[4 * x + 1], y[4 * x + 2], y[4 * x + 3]);
-          }
-        }
+        for (int x = 0; x < 32; ++x)
+          if (x < nv) Yh[(long)(t0 + 32 * h + x) * kDim + v] = y[x];
         tc_fence_before();
       }
     }
     if (!ok) fail();
     if (ok) {
-      float4* dst = reinterpret_cast<float4*>(p.M + ((long)head * kDim + r) * kDim + 64 * h);
+      float4* dst = reinterpret_cast<float4*>(p.M + ((long)head * kDim + v) * kDim + 64 * h);
 #pragma unroll
       for (int x = 0; x < 16; ++x) dst[x] = make_float4(m[4 * x], m[4 * x + 1], m[4 * x + 2], m[4 * x + 3]);
     }
@@ -464,9 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars[B_S]);
       if (mbar_wait(&bars[B_S], 0, abort_flag, kWaitLimit) && ok) {
         const float* el = reinterpret_cast<const float*>(sm + OFF_ELAST);
-        const float coef = -2.f * p.gamma[0] * p.theta[(long)head * N + N - 1] * el[r];
+        const float coef = -2.f * p.gamma[0] * p.theta[(long)head * N + N - 1] * el[v];
         const __nv_bfloat16* kl = p.K + ((long)head * N + N - 1) * kDim + 64 * h;
-        float* dst = p.S + ((long)head * kDim + r) * kDim + 64 * h;
+        float* dst = p.S + ((long)head * kDim + v) * kDim + 64 * h;
         for (int x = 0; x < 64; ++x) dst[x] = coef * __bfloat162float(kl[x]);
       }
     }
@@ -500,13 +566,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return g_encode;
 }
 
-bool make_map_kq(CUtensorMap* m, const void* base, int N, int heads) {
+// [heads, N, 128] bf16, boxes of 64 tokens x `cols` features.
+bool make_map_tokens(CUtensorMap* m, const void* base, int N, int heads, int cols, bool swz) {
   cuuint64_t dims[3] = {(cuuint64_t)kDim, (cuuint64_t)N, (cuuint64_t)heads};
   cuuint64_t strides[2] = {(cuuint64_t)kDim * 2, (cuuint64_t)N * kDim * 2};
-  cuuint32_t box[3] = {64, 64, 1};
+  cuuint32_t box[3] = {(cuuint32_t)cols, 64, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -531,22 +599,26 @@ bool linear_tc_supported(const LinArgs& a) {
          !a.dot && a.bf16 && a.N > 0 && (a.N % 4) == 0;
 }
 
-int linear_tc_launch(const LinArgs& a, int heads, int* status, cudaStream_t st) {
+size_t linear_tc_workspace_bytes(int heads) { return (size_t)heads * sizeof(int); }
+
+int linear_tc_launch(const LinArgs& a, int heads, int* status, void* workspace, cudaStream_t st) {
   if (!linear_tc_supported(a)) return ATLAS_ERR_UNSUPPORTED;
   if (!aligned16(a.K) || !aligned16(a.Q) || !aligned16(a.V) || !aligned16(a.alpha) ||
       !aligned16(a.eta) || !aligned16(a.theta) || !aligned16(a.Y) || !aligned16(a.M) ||
       (a.S && !aligned16(a.S)))
     return ATLAS_ERR_UNSUPPORTED;
+  if (!workspace) return ATLAS_ERR_WORKSPACE;
   if (!encoder()) return ATLAS_ERR_CUDA;
   TcMaps maps;
-  if (!make_map_kq(&maps.k, a.K, a.N, heads) || !make_map_kq(&maps.q, a.Q, a.N, heads) ||
+  if (!make_map_tokens(&maps.k, a.K, a.N, heads, 64, true) ||
+      !make_map_tokens(&maps.q, a.Q, a.N, heads, 64, true) ||
+      !make_map_tokens(&maps.v, a.V, a.N, heads, 128, false) ||
       !make_map_gate(&maps.alpha, a.alpha, a.N, heads) ||
       !make_map_gate(&maps.eta, a.eta, a.N, heads) ||
       !make_map_gate(&maps.theta, a.theta, a.N, heads))
     return ATLAS_ERR_CUDA;
   TcParams p;
   p.K = reinterpret_cast<const __nv_bfloat16*>(a.K);
-  p.V = reinterpret_cast<const __nv_bfloat16*>(a.V);
   p.eta = a.eta;
   p.theta = a.theta;
   p.gamma = a.gamma;
@@ -554,14 +626,15 @@ int linear_tc_launch(const LinArgs& a, int heads, int* status, cudaStream_t st) 
   p.M = a.M;
   p.S = a.S;
   p.status = status;
+  p.flags = reinterpret_cast<int*>(workspace);
   p.N = a.N;
   if (cudaFuncSetAttribute(linear_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)SMEM_ALLOC) != cudaSuccess)
     return ATLAS_ERR_CUDA;
   linear_tc_kernel<<<heads, kThreads, SMEM_ALLOC, st>>>(maps, p);
   if (cudaGetLastError() != cudaSuccess) return ATLAS_ERR_CUDA;
-  // heads with a non-zero eta: the CUDA-core kernel takes exactly those
-  return linear_simt_launch_masked(a, heads, st);
+  // heads with a non-zero eta: the CUDA-core kernel takes exactly the flagged ones
+  return linear_simt_launch_flagged(a, heads, p.flags, st);
 }
 
 }  // namespace atlas
