@@ -23,9 +23,10 @@
 // M0 and Ew are A operands held in TMEM (bf16 hi + lo halves, x = hi + lo to
 // ~2^-16); Phi, Q (bf16, exact) come from shared memory by TMA, E and P' are
 // split the same way into shared memory.  The fp32 master state M lives in the
-// registers of the epilogue warps (thread = row v, 64 columns).
+// registers of the epilogue warps (thread = row v, 64 columns).  Y leaves
+// through a shared-memory tile and one TMA store per chunk.
 //
-// Warp roles (320 threads): warp 0 issues TMA loads three chunks deep; warp 1
+// Warp roles (320 threads): warp 0 issues TMA loads two chunks deep; warp 1
 // builds the gate tables (warp-wide scans) and issues every MMA from one
 // thread; warps 2..9 are the epilogue, two per 32-lane TMEM quadrant.
 //
@@ -60,13 +61,14 @@ constexpr long long kWaitLimit = 2000000000LL;  // clock cycles (~1 s)
 constexpr uint32_t ST_V = 32768;
 constexpr uint32_t ST_GATES = ST_V + 16384;
 constexpr uint32_t STAGE_BYTES = ST_GATES + 1024;  // 50176 = 49 x 1024
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 constexpr uint32_t OFF_STAGE0 = 0;
 constexpr uint32_t OFF_EHI = kStages * STAGE_BYTES;   // E^T as [v][i], K-major, 16 KB
 constexpr uint32_t OFF_ELO = OFF_EHI + 16384;
 constexpr uint32_t OFF_PHI = OFF_ELO + 16384;         // P' as [n][i], K-major, 8 KB
 constexpr uint32_t OFF_PLO = OFF_PHI + 8192;
-constexpr uint32_t OFF_TAB = OFF_PLO + 8192;
+constexpr uint32_t OFF_Y = OFF_PLO + 8192;            // y tile [64 n][128 v] fp32, 32 KB
+constexpr uint32_t OFF_TAB = OFF_Y + 32768;
 constexpr uint32_t TAB_FLOATS = 5 * kChunk;           // a, pb, wb, keep, th
 constexpr uint32_t OFF_ELAST = OFF_TAB + 2 * TAB_FLOATS * 4;
 constexpr uint32_t OFF_BARS = OFF_ELAST + kDim * 4;
@@ -90,8 +92,8 @@ __device__ __forceinline__ uint32_t tm_q(int j) { return tm_t(j) + 64u; }
 __device__ __forceinline__ uint32_t tm_qp(int j) { return tm_t(j + 1); }
 
 enum Bar {
-  B_FULL0 = 0, B_FULL1, B_FULL2, B_EMPTY0, B_EMPTY1, B_EMPTY2, B_QP, B_D1, B_DM, B_Y, B_E, B_P,
-  B_M, B_TAB0, B_TAB1, B_S, B_DRAIN, B_COUNT
+  B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_QP, B_D1, B_DM, B_Y, B_E, B_P, B_M, B_TAB0,
+  B_TAB1, B_S, B_DRAIN, B_YS, B_YF, B_COUNT
 };
 
 struct TcParams {
@@ -108,7 +110,7 @@ struct TcParams {
 };
 
 struct TcMaps {
-  CUtensorMap k, q, v, alpha, eta, theta;
+  CUtensorMap k, q, v, alpha, eta, theta, y;
 };
 
 __device__ __forceinline__ float* table(unsigned char* sm, int buf) {
@@ -208,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < B_COUNT; ++b) {
       uint32_t cnt = 1;
       if (b == B_P) cnt = 4;
-      if (b == B_E || b == B_M || b == B_S) cnt = 8;
+      if (b == B_E || b == B_M || b == B_S || b == B_YS) cnt = 8;
       mbar_init(&bars[b], cnt);
     }
     *abort_flag = 0;
@@ -308,6 +310,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars[B_TAB0 + (j & 1)]);
       return true;
     };
+    // descriptor constants: address bits added per use
+    const uint64_t dK = sdesc_sw128(0, 16, 1024);       // K-major, 128-byte rows
+    const uint64_t dMN = sdesc_sw128(0, 16384, 1024);   // Phi as an MN-major operand
+    const uint64_t dsb = dK | (uint64_t)((sbase >> 4) & 0x3FFFu);
+    constexpr uint32_t kId128 = idesc_bf16(128, 128, false, false);
+    constexpr uint32_t kId64 = idesc_bf16(128, 64, false, false);
+    constexpr uint32_t kIdDM = idesc_bf16(128, 128, false, true);
     bool ok = tables(0);
     for (int j = 0; ok && j < nchunks; ++j) {
       const int s = j % kStages;
@@ -316,18 +325,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&bars[B_M], j & 1, abort_flag, kWaitLimit)) { ok = false; break; }
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t id = idesc_bf16(128, 128, false, false);
+        const uint64_t dst = dK | (uint64_t)((st >> 4) & 0x3FFFu);
+        const uint32_t dt = tmem + tm_t(j);
+#pragma unroll
         for (int k = 0; k < 16; ++k) {  // [T | Qy] = M0 [Phi; Q]^T; hi then lo halves of M0
           const uint32_t am = tmem + (k < 8 ? TM_MHI : TM_MLO) + 8 * (k & 7);
           const uint32_t off = ((k & 7) >> 2) * 16384 + (k & 3) * 32;
-          mma_bf16_ta(tmem + tm_t(j), am, sdesc_sw128(st + off, 16, 1024), id, k > 0);
+          mma_bf16_ta(dt, am, dst + (off >> 4), kId128, k > 0);
         }
         mma_commit(&bars[B_D1]);
-        const uint32_t id64 = idesc_bf16(128, 64, false, false);
+        const uint32_t dqp = tmem + tm_qp(j);
+#pragma unroll
         for (int k = 0; k < 8; ++k) {  // QP = [Phi; Q] Phi^T
           const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_bf16(tmem + tm_qp(j), sdesc_sw128(st + off, 16, 1024),
-                   sdesc_sw128(st + off, 16, 1024), id64, k > 0);
+          mma_bf16(dqp, dst + (off >> 4), dst + (off >> 4), kId64, k > 0);
         }
         mma_commit(&bars[B_QP]);
       }
@@ -338,10 +349,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&bars[B_E], j & 1, abort_flag, kWaitLimit)) { ok = false; break; }
       tc_fence_after();
       if (lane == 0) {  // dM = Ew^T Phi (Ew in TMEM, Phi MN-major in the stage)
-        const uint32_t id = idesc_bf16(128, 128, false, true);
+        const uint64_t dph = dMN | (uint64_t)((st >> 4) & 0x3FFFu);
+#pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t ae = tmem + (k < 4 ? TM_EWHI : TM_EWLO) + 8 * (k & 3);
-          mma_bf16_ta(tmem + TM_DM, ae, sdesc_sw128(st + (k & 3) * 2048, 16384, 1024), id, k > 0);
+          mma_bf16_ta(tmem + TM_DM, ae, dph + (((k & 3) * 2048) >> 4), kIdDM, k > 0);
         }
         mma_commit(&bars[B_DM]);
       }
@@ -349,12 +361,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&bars[B_P], j & 1, abort_flag, kWaitLimit)) { ok = false; break; }
       tc_fence_after();
       if (lane == 0) {  // Qy += E^T P'^T: Ehi*Phi, Elo*Phi, Ehi*Plo
-        const uint32_t id = idesc_bf16(128, 64, false, false);
+        const uint32_t dq = tmem + tm_q(j);
+#pragma unroll
         for (int k = 0; k < 12; ++k) {
           const int part = k >> 2;
-          const uint32_t ea = sbase + (part == 1 ? OFF_ELO : OFF_EHI) + (k & 3) * 32;
-          const uint32_t pb = sbase + (part == 2 ? OFF_PLO : OFF_PHI) + (k & 3) * 32;
-          mma_bf16(tmem + tm_q(j), sdesc_sw128(ea, 16, 1024), sdesc_sw128(pb, 16, 1024), id, 1);
+          const uint32_t ea = (part == 1 ? OFF_ELO : OFF_EHI) + (k & 3) * 32;
+          const uint32_t pb = (part == 2 ? OFF_PLO : OFF_PHI) + (k & 3) * 32;
+          mma_bf16(dq, dsb + (ea >> 4), dsb + (pb >> 4), kId64, 1);
         }
         mma_commit(&bars[B_Y]);
         mma_commit(&bars[B_EMPTY0 + s]);
@@ -396,7 +409,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_M]);
     }
-    float* Yh = p.Y + (long)head * N * kDim;
     bool ok = true;
     for (int j = 0; j < nchunks; ++j) {
       const int t0 = j * kChunk;
@@ -440,7 +452,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // Ew = W[63, i] E into TMEM (A operand of the state update)
 #pragma unroll
-        for (int x = 0; x < 32; ++x) e[x] *= twb[32 * h + x];
+        for (int x = 0; x < 8; ++x) {
+          const float4 w4 = reinterpret_cast<const float4*>(twb + 32 * h)[x];
+          e[4 * x] *= w4.x; e[4 * x + 1] *= w4.y; e[4 * x + 2] *= w4.z; e[4 * x + 3] *= w4.w;
+        }
         uint32_t hi[16], lo[16];
         pack_split32(e, hi, lo);
         tmem_st16(tl + TM_EWHI + 16 * h, hi);
@@ -449,7 +464,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         float t[32];
         tmem_ld32(tl + tm_q(j) + 32 * h, t);
 #pragma unroll
-        for (int x = 0; x < 32; ++x) t[x] *= ta[32 * h + x];
+        for (int x = 0; x < 8; ++x) {
+          const float4 a4 = reinterpret_cast<const float4*>(ta + 32 * h)[x];
+          t[4 * x] *= a4.x; t[4 * x + 1] *= a4.y; t[4 * x + 2] *= a4.z; t[4 * x + 3] *= a4.w;
+        }
         tmem_st32(tl + tm_q(j) + 32 * h, t);  // waits for all stores of this thread
         fence_proxy_async_smem();
         tc_fence_before();
@@ -509,16 +527,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&bars[B_Y], par, abort_flag, kWaitLimit)) { ok = false; break; }
       tc_fence_after();
       {
+        const bool elected = warp == 2 && lane == 0;
+        if (elected) {  // the previous chunk's store has finished reading the tile
+          bulk_wait_read0();
+          mbar_arrive(&bars[B_YF]);
+        }
         float y[32];
         tmem_ld32(tl + tm_q(j) + 32 * h, y);
-        const int nv = N - t0 - 32 * h;  // valid queries in this half
-#pragma unroll
-        for (int x = 0; x < 32; ++x)
-          if (x < nv) Yh[(long)(t0 + 32 * h + x) * kDim + v] = y[x];
         tc_fence_before();
+        if (!mbar_wait(&bars[B_YF], par, abort_flag, kWaitLimit)) { ok = false; break; }
+        float* yt = reinterpret_cast<float*>(sm + OFF_Y) + 32 * h * kDim + v;
+#pragma unroll
+        for (int x = 0; x < 32; ++x) yt[x * kDim] = y[x];
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[B_YS]);
+        if (elected) {
+          if (!mbar_wait(&bars[B_YS], par, abort_flag, kWaitLimit)) { ok = false; break; }
+          tma_store_3d(&maps.y, sm + OFF_Y, 0, t0, head);  // rows past N are clipped
+          bulk_commit();
+        }
       }
     }
     if (!ok) fail();
+    if (warp == 2 && lane == 0) bulk_wait0();  // Y stores complete before exit
     if (ok) {
       float4* dst = reinterpret_cast<float4*>(p.M + ((long)head * kDim + v) * kDim + 64 * h);
 #pragma unroll
@@ -590,6 +622,18 @@ bool make_map_gate(CUtensorMap* m, const float* base, int N, int heads) {
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [heads, N, 128] fp32 outputs, boxes of 64 tokens x 128 values.
+bool make_map_y(CUtensorMap* m, float* base, int N, int heads) {
+  cuuint64_t dims[3] = {(cuuint64_t)kDim, (cuuint64_t)N, (cuuint64_t)heads};
+  cuuint64_t strides[2] = {(cuuint64_t)kDim * 4, (cuuint64_t)N * kDim * 4};
+  cuuint32_t box[3] = {(cuuint32_t)kDim, 64, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 }  // namespace
@@ -615,7 +659,7 @@ int linear_tc_launch(const LinArgs& a, int heads, int* status, void* workspace, 
       !make_map_tokens(&maps.v, a.V, a.N, heads, 128, false) ||
       !make_map_gate(&maps.alpha, a.alpha, a.N, heads) ||
       !make_map_gate(&maps.eta, a.eta, a.N, heads) ||
-      !make_map_gate(&maps.theta, a.theta, a.N, heads))
+      !make_map_gate(&maps.theta, a.theta, a.N, heads) || !make_map_y(&maps.y, a.Y, a.N, heads))
     return ATLAS_ERR_CUDA;
   TcParams p;
   p.K = reinterpret_cast<const __nv_bfloat16*>(a.K);
