@@ -53,10 +53,29 @@ static LinSimtSmem lin_simt_layout(int RV, int D, int Lmax, int b, int d_k) {
   return s;
 }
 
+// One CTA: rows [r0, r0 + RV) of one head, the whole sequence.
+__device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimtSmem& L, int head,
+                                                 int r0);
+
 // flags != nullptr: only the heads whose flag is set (the heads the tensor-core
-// kernel leaves, which it marks); every other head returns at once.
+// kernel leaves, which it marks); every other head returns at once, and each
+// CTA walks all row blocks of its head so that the grid stays one CTA per head.
 __global__ void __launch_bounds__(256) linear_simt_kernel(LinArgs p, LinSimtSmem L,
                                                           const int* flags) {
+  const int head = blockIdx.x;
+  if (flags) {
+    if (flags[head] == 0) return;
+    for (int r0 = 0; r0 < p.d_v; r0 += L.RV) {
+      linear_simt_rows(p, L, head, r0);
+      __syncthreads();
+    }
+    return;
+  }
+  linear_simt_rows(p, L, head, blockIdx.y * L.RV);
+}
+
+__device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimtSmem& L, int head,
+                                                 int r0) {
   extern __shared__ float sm[];
   float* Ms = sm + L.Ms;
   float* Ss = sm + L.Ss;
@@ -73,9 +92,7 @@ __global__ void __launch_bounds__(256) linear_simt_kernel(LinArgs p, LinSimtSmem
   uint8_t* pp = reinterpret_cast<uint8_t*>(sm + L.total_floats);
   uint8_t* pq = pp + (L.D - p.d_k > 0 ? L.D - p.d_k : 0);
 
-  const int head = blockIdx.x;
-  if (flags && flags[head] == 0) return;
-  const int r0 = blockIdx.y * L.RV;
+
   const int rv = min(L.RV, p.d_v - r0);
   const int D = L.D, dk = p.d_k, dv = p.d_v;
   const int tid = threadIdx.x, nt = blockDim.x;
@@ -217,7 +234,7 @@ static int launch(const LinArgs& a, int heads, const int* flags, cudaStream_t st
   if (cudaFuncSetAttribute(linear_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return ATLAS_ERR_CUDA;
-  dim3 grid(heads, (a.d_v + RV - 1) / RV);
+  dim3 grid(heads, flags ? 1 : (a.d_v + RV - 1) / RV);
   linear_simt_kernel<<<grid, 256, smem, st>>>(a, s, flags);
   return cudaGetLastError() == cudaSuccess ? ATLAS_OK : ATLAS_ERR_CUDA;
 }

@@ -11,18 +11,21 @@
 // with a_n = prod_{l<=n} (1 - alpha_l) and W[n,i] = gamma_0 theta_i
 // prod_{l=i+1..n} (1 - alpha_l) ("[Paper Review] Titans 논문 이해하기":
 // S_t = -theta_t grad, M_t = (1 - alpha_t) M_{t-1} + S_t, y_t = M_t q_t).
+// With s_n = prod_{l=n+1..63} (1 - alpha_l), W[n,i] = gamma_0 theta_i s_i / s_n for
+// i <= n (s_i / s_n is the product over l = i+1..n), so both the state update and the
+// intra-chunk readout use the same weighted errors Ew_i = gamma_0 theta_i s_i e_i:
+//   M_end = a_63 M0 - 2 Ew^T Phi,   y_n = a_n (M0 q_n) + sum_{i<=n} (-2 q_n.k_i / s_n) Ew_i.
+// A chunk whose s_0 falls below 1e-30 (a decay gate at or near 1) is not
+// handled here: the head is flagged and recomputed by the CUDA-core kernel.
 //
-// Everything is computed transposed, with the value index v (128) on the TMEM
-// lanes, so that each of the eight epilogue warps owns 32 rows v and 32 of the
-// chunk's tokens.  Per chunk (fp32 accumulators in TMEM):
-//   [T | Qy] = M0 [Phi; Q]^T   (128 x 128): T -> E^T = T - V^T,
-//                                 Qy = M0 Q^T scaled by a_n per query column
-//   QP  = [Phi; Q] Phi^T  (rows 64..127: q_n . k_i) -> P' = -2 W * (Q Phi^T)
-//   dM  = Ew^T Phi        (128 x 128) with Ew = W[63,:] * E   (state update)
-//   Qy += E^T P'^T        (128 x 64)  -> y^T, the readout of the chunk
+// Products per chunk, with the value index v on the TMEM lanes (fp32 accumulators):
+//   [T | Qy]   = M0 [Phi; Q]^T           (128 x 128)  T -> Ew^T = s.theta.(T - V^T)
+//   QP         = [Phi; Q] Q^T, rows 0..63: k_i . q_n    -> P'' = -2 [i<=n] k_i.q_n / s_n
+//   [dM | Yi]  = Ew^T [Phi | P'']        (128 x 192)  one MMA chain for both
+//   y^T        = a_n Qy + Yi,            M_end = a_63 M0 - 2 dM
 // M0 and Ew are A operands held in TMEM (bf16 hi + lo halves, x = hi + lo to
-// ~2^-16); Phi, Q (bf16, exact) come from shared memory by TMA, E and P' are
-// split the same way into shared memory.  The fp32 master state M lives in the
+// ~2^-16); Phi, Q (bf16, exact) come from shared memory by TMA; P'' is split
+// the same way into shared memory.  The fp32 master state M lives in the
 // registers of the epilogue warps (thread = row v, 64 columns).  Y leaves
 // through a shared-memory tile and one TMA store per chunk.
 //
@@ -30,11 +33,11 @@
 // builds the gate tables (warp-wide scans) and issues every MMA from one
 // thread; warps 2..9 are the epilogue, two per 32-lane TMEM quadrant.
 //
-// Heads whose eta has any non-zero entry are left to the CUDA-core kernel
-// launched right after this one: this kernel writes one flag per head to the
-// workspace and that kernel takes exactly the flagged heads.  Every mbarrier
-// wait is bounded; on expiry the kernel records ATLAS_ERR_TIMEOUT in the status
-// word, drains its in-flight copies and MMAs, frees TMEM and returns.
+// Heads whose eta has any non-zero entry are also left to the CUDA-core
+// kernel launched right after this one: this kernel writes one flag per head
+// to the workspace and that kernel takes exactly the flagged heads.  Every
+// mbarrier wait is bounded; on expiry the kernel records ATLAS_ERR_TIMEOUT in
+// the status word, drains its in-flight copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <string.h>
@@ -54,22 +57,22 @@ constexpr int kThreads = 320;
 constexpr int kChunk = 64;
 constexpr int kDim = 128;
 constexpr long long kWaitLimit = 2000000000LL;  // clock cycles (~1 s)
+constexpr float kMinSuffix = 1e-30f;            // smallest s_0 handled here
 
 // shared-memory map (bytes from a 1024-aligned base)
-//   stage: Phi kb0 | Q kb0 | Phi kb1 | Q kb1 (8 KB each, 128B-swizzled) | V (64 x 128
-//   bf16, row-major) | alpha | eta | theta
-constexpr uint32_t ST_V = 32768;
+//   stage: Phi kb0 | Q kb0 | Phi kb1 | Q kb1 (8 KB each, 128B-swizzled, loaded by
+//   TMA) | P''hi | P''lo ([i][n], 128B-swizzled, written by the epilogue) |
+//   V (64 x 128 bf16, row-major) | alpha | eta | theta
+constexpr uint32_t ST_PHI = 32768;
+constexpr uint32_t ST_PLO = ST_PHI + 8192;
+constexpr uint32_t ST_V = ST_PLO + 8192;
 constexpr uint32_t ST_GATES = ST_V + 16384;
-constexpr uint32_t STAGE_BYTES = ST_GATES + 1024;  // 50176 = 49 x 1024
+constexpr uint32_t STAGE_BYTES = ST_GATES + 1024;  // 66560 = 65 x 1024
 constexpr int kStages = 2;
 constexpr uint32_t OFF_STAGE0 = 0;
-constexpr uint32_t OFF_EHI = kStages * STAGE_BYTES;   // E^T as [v][i], K-major, 16 KB
-constexpr uint32_t OFF_ELO = OFF_EHI + 16384;
-constexpr uint32_t OFF_PHI = OFF_ELO + 16384;         // P' as [n][i], K-major, 8 KB
-constexpr uint32_t OFF_PLO = OFF_PHI + 8192;
-constexpr uint32_t OFF_Y = OFF_PLO + 8192;            // y tile [64 n][128 v] fp32, 32 KB
+constexpr uint32_t OFF_Y = kStages * STAGE_BYTES;     // y tile [64 n][128 v] fp32, 32 KB
 constexpr uint32_t OFF_TAB = OFF_Y + 32768;
-constexpr uint32_t TAB_FLOATS = 5 * kChunk;           // a, pb, wb, keep, th
+constexpr uint32_t TAB_FLOATS = 3 * kChunk;           // a, wb, cn
 constexpr uint32_t OFF_ELAST = OFF_TAB + 2 * TAB_FLOATS * 4;
 constexpr uint32_t OFF_BARS = OFF_ELAST + kDim * 4;
 constexpr uint32_t SMEM_USED = OFF_BARS + 256;
@@ -77,24 +80,25 @@ constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;    // alignment slack
 
 constexpr uint32_t STAGE_TX = 4 * 8192 + 16384 + 3 * 256;
 
-// TMEM columns.  Two 128-column buffers hold [T | Qy] of consecutive chunks;
-// chunk j's QP goes into the T half of the other buffer (free by then), so
-// chunk j's readout can leave TMEM while chunk j+1 already runs.
-constexpr uint32_t TM_D1 = 0;      // [T | Qy], two buffers (2 x 128)
-constexpr uint32_t TM_DM = 256;    // state update        (128)
+// TMEM columns
+constexpr uint32_t TM_T = 0;       // [T | Qy]            (128)
+constexpr uint32_t TM_QY = 64;
+constexpr uint32_t TM_QP = 128;    // k_i . q_n           (64)
+constexpr uint32_t TM_DM = 192;    // [dM | Yi]           (192)
+constexpr uint32_t TM_YI = 320;
 constexpr uint32_t TM_MHI = 384;   // A operand M0: hi (64 cols = 128 bf16), lo
 constexpr uint32_t TM_MLO = 448;
 constexpr uint32_t TM_EWHI = 384;  // A operand Ew (reuses the M0 columns once T is done)
 constexpr uint32_t TM_EWLO = 416;
 constexpr uint32_t TM_COLS = 512;
-__device__ __forceinline__ uint32_t tm_t(int j) { return TM_D1 + 128u * (uint32_t)(j & 1); }
-__device__ __forceinline__ uint32_t tm_q(int j) { return tm_t(j) + 64u; }
-__device__ __forceinline__ uint32_t tm_qp(int j) { return tm_t(j + 1); }
 
 enum Bar {
-  B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_QP, B_D1, B_DM, B_Y, B_E, B_P, B_M, B_TAB0,
-  B_TAB1, B_S, B_DRAIN, B_YS, B_YF, B_COUNT
+  B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_QP, B_D1, B_DM, B_E, B_P, B_M, B_TAB0, B_TAB1,
+  B_S, B_DRAIN, B_YS, B_YF, B_COUNT
 };
+
+// abort_flag values
+constexpr int kRun = 0, kTimeout = 1, kHandOff = 2;
 
 struct TcParams {
   const __nv_bfloat16* K;
@@ -176,6 +180,7 @@ __device__ __forceinline__ void pack_split32(const float* x, uint32_t* hi, uint3
   }
 }
 
+
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -213,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (b == B_E || b == B_M || b == B_S || b == B_YS) cnt = 8;
       mbar_init(&bars[b], cnt);
     }
-    *abort_flag = 0;
+    *abort_flag = kRun;
     fence_barrier_init();
     prefetch_tmap(&maps.k);
     prefetch_tmap(&maps.q);
@@ -229,9 +234,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t sbase = smem_u32(sm);
 
-  auto fail = [&]() {
-    *abort_flag = 1;
-    if (p.status) atomicExch(p.status, ATLAS_ERR_TIMEOUT);
+  auto timeout = [&]() {
+    if (*abort_flag == kRun) {
+      *abort_flag = kTimeout;
+      if (p.status) atomicExch(p.status, ATLAS_ERR_TIMEOUT);
+    }
   };
 
   if (warp == 0) {
@@ -242,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = j % kStages;
         if (j >= kStages &&
             !mbar_wait(&bars[B_EMPTY0 + s], ((j - kStages) / kStages) & 1, abort_flag, kWaitLimit)) {
-          fail();
+          timeout();
           break;
         }
         unsigned char* st = sm + OFF_STAGE0 + s * STAGE_BYTES;
@@ -269,112 +276,117 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------- tables + MMA issuer
     const float g0 = p.gamma[0];
+    // Gate tables of chunk j (warp-wide scans, lane l owns tokens 2l, 2l+1):
+    // a_n = prod_{l<=n}(1-alpha_l), wb_i = gamma_0 theta_i s_i, cn_n = -2 / s_n.
+    // Returns false on a timeout, or if s_0 is too small (hand the head off).
     auto tables = [&](int j) -> bool {
       const int s = j % kStages;
-      if (!mbar_wait(&bars[B_FULL0 + s], (j / kStages) & 1, abort_flag, kWaitLimit)) return false;
-      // warp-parallel scans: lane l owns tokens 2l and 2l+1
+      if (!mbar_wait(&bars[B_FULL0 + s], (j / kStages) & 1, abort_flag, kWaitLimit)) {
+        timeout();
+        return false;
+      }
       const float* ga = reinterpret_cast<const float*>(sm + OFF_STAGE0 + s * STAGE_BYTES + ST_GATES);
       const float* gt = ga + 128;
       float* tb = table(sm, j & 1);
-      float *a = tb, *pb = tb + kChunk, *wb = tb + 2 * kChunk, *keep = tb + 3 * kChunk,
-            *th = tb + 4 * kChunk;
+      float *a = tb, *wb = tb + kChunk, *cn = tb + 2 * kChunk;
       const unsigned full = 0xFFFFFFFFu;
       const int n0 = 2 * lane, n1 = n0 + 1;
       const float k0 = 1.f - ga[n0], k1 = 1.f - ga[n1];
-      const float t0v = gt[n0] * g0, t1v = gt[n1] * g0;
-      float pa = k0 * k1;
-      float pp = lane >= 16 ? pa : 1.f;
-      float sf = pa;
+      float pa = k0 * k1;  // inclusive prefix product over lanes
+      float sf = pa;       // inclusive suffix product over lanes
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const float ua = __shfl_up_sync(full, pa, o);
-        const float up = __shfl_up_sync(full, pp, o);
         const float ds = __shfl_down_sync(full, sf, o);
-        if (lane >= o) { pa *= ua; pp *= up; }
+        if (lane >= o) pa *= ua;
         if (lane + o < 32) sf *= ds;
       }
       float ea = __shfl_up_sync(full, pa, 1);    // product over tokens < n0
-      float ep = __shfl_up_sync(full, pp, 1);
-      float es = __shfl_down_sync(full, sf, 1);  // product over tokens > n1
-      if (lane == 0) { ea = 1.f; ep = 1.f; }
+      float es = __shfl_down_sync(full, sf, 1);  // product over tokens > n1 (= s_{n1})
+      if (lane == 0) ea = 1.f;
       if (lane == 31) es = 1.f;
-      keep[n0] = k0; keep[n1] = k1;
-      th[n0] = t0v; th[n1] = t1v;
+      const float s1 = es, s0 = es * k1;          // s_{n1}, s_{n0}
       a[n0] = ea * k0;
       a[n1] = ea * k0 * k1;
-      pb[n0] = lane >= 16 ? ep * k0 : 1.f;
-      pb[n1] = lane >= 16 ? ep * k0 * k1 : 1.f;
-      wb[n1] = t1v * es;
-      wb[n0] = t0v * es * k1;
+      wb[n0] = gt[n0] * g0 * s0;
+      wb[n1] = gt[n1] * g0 * s1;
+      cn[n0] = -2.f / s0;
+      cn[n1] = -2.f / s1;
+      const bool handled = __shfl_sync(full, s0, 0) >= kMinSuffix;  // s_0 is the smallest
       __syncwarp();
+      if (!handled) {
+        if (lane == 0 && *abort_flag == kRun) {
+          *abort_flag = kHandOff;
+          p.flags[head] = 1;
+        }
+        return false;
+      }
       if (lane == 0) mbar_arrive(&bars[B_TAB0 + (j & 1)]);
       return true;
     };
-    // descriptor constants: address bits added per use
+    // descriptor constants: address bits are added per use
     const uint64_t dK = sdesc_sw128(0, 16, 1024);       // K-major, 128-byte rows
-    const uint64_t dMN = sdesc_sw128(0, 16384, 1024);   // Phi as an MN-major operand
-    const uint64_t dsb = dK | (uint64_t)((sbase >> 4) & 0x3FFFu);
+    const uint64_t dMN = sdesc_sw128(0, 16384, 1024);   // MN-major, atoms 16 KB apart
     constexpr uint32_t kId128 = idesc_bf16(128, 128, false, false);
     constexpr uint32_t kId64 = idesc_bf16(128, 64, false, false);
-    constexpr uint32_t kIdDM = idesc_bf16(128, 128, false, true);
+    constexpr uint32_t kId192mn = idesc_bf16(128, 192, false, true);
+    constexpr uint32_t kId64mn = idesc_bf16(128, 64, false, true);
+    auto issue_qp = [&](int j) {  // QP = [Phi; Q] Q^T (rows 0..63: k_i . q_n)
+      const uint32_t st = sbase + OFF_STAGE0 + (j % kStages) * STAGE_BYTES;
+      const uint64_t dst = dK | (uint64_t)((st >> 4) & 0x3FFFu);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+        mma_bf16(tmem + TM_QP, dst + (off >> 4), dst + ((off + 8192) >> 4), kId64, k > 0);
+      }
+      mma_commit(&bars[B_QP]);
+    };
     bool ok = tables(0);
+    if (ok && lane == 0) issue_qp(0);
+    __syncwarp();
     for (int j = 0; ok && j < nchunks; ++j) {
       const int s = j % kStages;
       const uint32_t st = sbase + OFF_STAGE0 + s * STAGE_BYTES;
-      // M0 in TMEM (written by the epilogue), stage j loaded (waited in tables(j))
+      // M0 in TMEM and the previous chunk's [T | Qy] read out
       if (!mbar_wait(&bars[B_M], j & 1, abort_flag, kWaitLimit)) { ok = false; break; }
       tc_fence_after();
-      if (lane == 0) {
+      if (lane == 0) {  // [T | Qy] = M0 [Phi; Q]^T; hi then lo halves of M0
         const uint64_t dst = dK | (uint64_t)((st >> 4) & 0x3FFFu);
-        const uint32_t dt = tmem + tm_t(j);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {  // [T | Qy] = M0 [Phi; Q]^T; hi then lo halves of M0
+        for (int k = 0; k < 16; ++k) {
           const uint32_t am = tmem + (k < 8 ? TM_MHI : TM_MLO) + 8 * (k & 7);
           const uint32_t off = ((k & 7) >> 2) * 16384 + (k & 3) * 32;
-          mma_bf16_ta(dt, am, dst + (off >> 4), kId128, k > 0);
+          mma_bf16_ta(tmem + TM_T, am, dst + (off >> 4), kId128, k > 0);
         }
         mma_commit(&bars[B_D1]);
-        const uint32_t dqp = tmem + tm_qp(j);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {  // QP = [Phi; Q] Phi^T
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_bf16(dqp, dst + (off >> 4), dst + (off >> 4), kId64, k > 0);
-        }
-        mma_commit(&bars[B_QP]);
       }
       __syncwarp();
-      // next chunk's gate tables while this chunk's products run (the buffer's
-      // previous readers, chunk j-1's epilogue, are done: B_M was complete)
+      // the next chunk's gate tables while this chunk's products run (the
+      // buffer's previous readers, chunk j-1's epilogue, are done: B_M was complete)
       if (j + 1 < nchunks && !tables(j + 1)) { ok = false; break; }
       if (!mbar_wait(&bars[B_E], j & 1, abort_flag, kWaitLimit)) { ok = false; break; }
-      tc_fence_after();
-      if (lane == 0) {  // dM = Ew^T Phi (Ew in TMEM, Phi MN-major in the stage)
-        const uint64_t dph = dMN | (uint64_t)((st >> 4) & 0x3FFFu);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t ae = tmem + (k < 4 ? TM_EWHI : TM_EWLO) + 8 * (k & 3);
-          mma_bf16_ta(tmem + TM_DM, ae, dph + (((k & 3) * 2048) >> 4), kIdDM, k > 0);
-        }
-        mma_commit(&bars[B_DM]);
-      }
-      __syncwarp();
       if (!mbar_wait(&bars[B_P], j & 1, abort_flag, kWaitLimit)) { ok = false; break; }
       tc_fence_after();
-      if (lane == 0) {  // Qy += E^T P'^T: Ehi*Phi, Elo*Phi, Ehi*Plo
-        const uint32_t dq = tmem + tm_q(j);
+      if (lane == 0) {
+        // [dM | Yi] = Ew^T [Phi | P''hi] (Ew hi, then lo), then Yi += Ew_hi^T P''lo
+        const uint64_t dph = dMN | (uint64_t)((st >> 4) & 0x3FFFu);
+        const uint64_t dpl = dMN | (uint64_t)(((st + ST_PLO) >> 4) & 0x3FFFu);
 #pragma unroll
         for (int k = 0; k < 12; ++k) {
-          const int part = k >> 2;
-          const uint32_t ea = (part == 1 ? OFF_ELO : OFF_EHI) + (k & 3) * 32;
-          const uint32_t pb = (part == 2 ? OFF_PLO : OFF_PHI) + (k & 3) * 32;
-          mma_bf16(dq, dsb + (ea >> 4), dsb + (pb >> 4), kId64, 1);
+          const uint32_t ae = tmem + ((k >> 2) == 1 ? TM_EWLO : TM_EWHI) + 8 * (k & 3);
+          const uint64_t b = ((k >> 2) == 2 ? dpl : dph) + (((k & 3) * 2048) >> 4);
+          if (k < 8)
+            mma_bf16_ta(tmem + TM_DM, ae, b, kId192mn, k > 0);
+          else
+            mma_bf16_ta(tmem + TM_YI, ae, b, kId64mn, 1);
         }
-        mma_commit(&bars[B_Y]);
+        mma_commit(&bars[B_DM]);
         mma_commit(&bars[B_EMPTY0 + s]);
+        if (j + 1 < nchunks) issue_qp(j + 1);  // P-epilogue of j done: its QP was read
       }
       __syncwarp();
     }
-    if (!ok) fail();
+    if (!ok) timeout();
     if (lane == 0) {
       // no MMA may outlive the TMEM: wait for everything this thread issued
       volatile int zero = 0;
@@ -386,9 +398,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;             // TMEM lane quadrant
     const int h = (warp - 2) >> 2;      // half: columns / tokens / queries
-    const int v = 32 * q + lane;        // TMEM lane = value index v
+    const int v = 32 * q + lane;        // TMEM lane = value index v (or token i)
     const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
-    const bool high = q >= 2;
+    const bool low = q < 2;
+    const bool elected = warp == 2 && lane == 0;
     float m[64];                        // M0[v][64h .. 64h+63]
     {
       const float4* src = reinterpret_cast<const float4*>(p.M + ((long)head * kDim + v) * kDim + 64 * h);
@@ -413,11 +426,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < nchunks; ++j) {
       const int t0 = j * kChunk;
       const uint32_t par = j & 1;
-      const unsigned char* stg = sm + OFF_STAGE0 + (j % kStages) * STAGE_BYTES;
+      unsigned char* stg = sm + OFF_STAGE0 + (j % kStages) * STAGE_BYTES;
       if (!mbar_wait(&bars[B_TAB0 + (j & 1)], (j >> 1) & 1, abort_flag, kWaitLimit)) { ok = false; break; }
       const float* tb = table(sm, j & 1);
-      const float *ta = tb, *tpb = tb + kChunk, *twb = tb + 2 * kChunk, *tkeep = tb + 3 * kChunk,
-                  *tth = tb + 4 * kChunk;
+      const float *ta = tb, *twb = tb + kChunk, *tcn = tb + 2 * kChunk;
       // V^T[v][i] of this thread's tokens, read before the products are done
       float vt[32];
       {
@@ -425,22 +437,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int x = 0; x < 32; ++x) vt[x] = __bfloat162float(Vs[(32 * h + x) * kDim + v]);
       }
-      if (!mbar_wait(&bars[B_D1], par, abort_flag, kWaitLimit)) { ok = false; break; }
-      tc_fence_after();
-      {
-        // ---- E^T[v][i] = T[v][i] - V[i][v] for tokens i in [32h, 32h+32)
-        float e[32];
-        tmem_ld32(tl + tm_t(j) + 32 * h, e);
+      if (low) {
+        // ---- P''[n][i] = -2 [i <= n] (k_i . q_n) / s_n, token i = v, queries n in [32h, 32h+32)
+        const int i = v;
+        if (!mbar_wait(&bars[B_QP], par, abort_flag, kWaitLimit)) { ok = false; break; }
+        tc_fence_after();
+        float pv[32];
+        tmem_ld32(tl + TM_QP + 32 * h, pv);
 #pragma unroll
-        for (int x = 0; x < 32; ++x) e[x] -= vt[x];
+        for (int x = 0; x < 8; ++x) {
+          const float4 c4 = reinterpret_cast<const float4*>(tcn + 32 * h)[x];
+          const int n = 32 * h + 4 * x;
+          pv[4 * x] = n >= i ? c4.x * pv[4 * x] : 0.f;
+          pv[4 * x + 1] = n + 1 >= i ? c4.y * pv[4 * x + 1] : 0.f;
+          pv[4 * x + 2] = n + 2 >= i ? c4.z * pv[4 * x + 2] : 0.f;
+          pv[4 * x + 3] = n + 3 >= i ? c4.w * pv[4 * x + 3] : 0.f;
+        }
+        const uint32_t ph = smem_u32(stg + ST_PHI), pl = smem_u32(stg + ST_PLO);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint4 hi, lo;
-          split8(e + 8 * c, hi, lo);
-          const uint32_t o = sw128_offset(v, 4 * h + c);
-          st_shared_u4(sbase + OFF_EHI + o, hi);
-          st_shared_u4(sbase + OFF_ELO + o, lo);
+          split8(pv + 8 * c, hi, lo);
+          const uint32_t o = sw128_offset(i, 4 * h + c);
+          st_shared_u4(ph + o, hi);
+          st_shared_u4(pl + o, lo);
         }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[B_P]);
+      }
+      if (!mbar_wait(&bars[B_D1], par, abort_flag, kWaitLimit)) { ok = false; break; }
+      tc_fence_after();
+      {
+        // ---- Ew^T[v][i] = wb_i (T[v][i] - V[i][v]) for tokens i in [32h, 32h+32)
+        float e[32];
+        tmem_ld32(tl + TM_T + 32 * h, e);
+#pragma unroll
+        for (int x = 0; x < 32; ++x) e[x] -= vt[x];
         if (p.S && j == nchunks - 1) {
           const int il = N - 1 - t0 - 32 * h;
           if (il >= 0 && il < 32) {
@@ -450,7 +484,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (x == il) el[v] = e[x];
           }
         }
-        // Ew = W[63, i] E into TMEM (A operand of the state update)
 #pragma unroll
         for (int x = 0; x < 8; ++x) {
           const float4 w4 = reinterpret_cast<const float4*>(twb + 32 * h)[x];
@@ -460,51 +493,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         pack_split32(e, hi, lo);
         tmem_st16(tl + TM_EWHI + 16 * h, hi);
         tmem_st16(tl + TM_EWLO + 16 * h, lo);
-        // queries n in [32h, 32h+32): scale M0 q_n by a_n in place
-        float t[32];
-        tmem_ld32(tl + tm_q(j) + 32 * h, t);
-#pragma unroll
-        for (int x = 0; x < 8; ++x) {
-          const float4 a4 = reinterpret_cast<const float4*>(ta + 32 * h)[x];
-          t[4 * x] *= a4.x; t[4 * x + 1] *= a4.y; t[4 * x + 2] *= a4.z; t[4 * x + 3] *= a4.w;
-        }
-        tmem_st32(tl + tm_q(j) + 32 * h, t);  // waits for all stores of this thread
-        fence_proxy_async_smem();
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_E]);
       }
-      if (high) {
-        // ---- P'[n][i] = -2 W[n,i] (q_n . k_i), query n = v - 64, keys i in [32h, 32h+32)
-        const int n = v - 64;
-        if (!mbar_wait(&bars[B_QP], par, abort_flag, kWaitLimit)) { ok = false; break; }
-        tc_fence_after();
-        float pv[32];
-        tmem_ld32(tl + tm_qp(j) + 32 * h, pv);
-        float da = (h == 0 && n >= 32) ? tpb[n] : 1.f;
-#pragma unroll
-        for (int x = 31; x >= 0; --x) {
-          const int i = 32 * h + x;
-          const bool in = i <= n;
-          pv[x] = in ? -2.f * tth[i] * da * pv[x] : 0.f;
-          da = in ? da * tkeep[i] : da;
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint4 hi, lo;
-          split8(pv + 8 * c, hi, lo);
-          const uint32_t o = sw128_offset(n, 4 * h + c);
-          st_shared_u4(sbase + OFF_PHI + o, hi);
-          st_shared_u4(sbase + OFF_PLO + o, lo);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[B_P]);
-      }
-      // ---- state update M = a_63 M - 2 dM; the next chunk's A operand into TMEM
+      // ---- [dM | Yi] done: readout first (frees [T | Qy]), then the state update
       if (!mbar_wait(&bars[B_DM], par, abort_flag, kWaitLimit)) { ok = false; break; }
       tc_fence_after();
+      {
+        if (elected) {  // the previous chunk's store has finished reading the tile
+          bulk_wait_read0();
+          mbar_arrive(&bars[B_YF]);
+        }
+        float y[32], yi[32];
+        tmem_ld32(tl + TM_QY + 32 * h, y);
+        tmem_ld32(tl + TM_YI + 32 * h, yi);
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+          const float4 a4 = reinterpret_cast<const float4*>(ta + 32 * h)[x];
+          y[4 * x] = a4.x * y[4 * x] + yi[4 * x];
+          y[4 * x + 1] = a4.y * y[4 * x + 1] + yi[4 * x + 1];
+          y[4 * x + 2] = a4.z * y[4 * x + 2] + yi[4 * x + 2];
+          y[4 * x + 3] = a4.w * y[4 * x + 3] + yi[4 * x + 3];
+        }
+        if (!mbar_wait(&bars[B_YF], par, abort_flag, kWaitLimit)) { ok = false; break; }
+        float* yt = reinterpret_cast<float*>(sm + OFF_Y) + 32 * h * kDim + v;
+#pragma unroll
+        for (int x = 0; x < 32; ++x) yt[x * kDim] = y[x];
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[B_YS]);
+      }
       {
         const float ab = ta[kChunk - 1];
 #pragma unroll
@@ -523,44 +543,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_M]);
       }
-      // ---- readout: Qy now holds y^T for the queries n in [32h, 32h+32)
-      if (!mbar_wait(&bars[B_Y], par, abort_flag, kWaitLimit)) { ok = false; break; }
-      tc_fence_after();
-      {
-        const bool elected = warp == 2 && lane == 0;
-        if (elected) {  // the previous chunk's store has finished reading the tile
-          bulk_wait_read0();
-          mbar_arrive(&bars[B_YF]);
-        }
-        float y[32];
-        tmem_ld32(tl + tm_q(j) + 32 * h, y);
-        tc_fence_before();
-        if (!mbar_wait(&bars[B_YF], par, abort_flag, kWaitLimit)) { ok = false; break; }
-        float* yt = reinterpret_cast<float*>(sm + OFF_Y) + 32 * h * kDim + v;
-#pragma unroll
-        for (int x = 0; x < 32; ++x) yt[x * kDim] = y[x];
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[B_YS]);
-        if (elected) {
-          if (!mbar_wait(&bars[B_YS], par, abort_flag, kWaitLimit)) { ok = false; break; }
-          tma_store_3d(&maps.y, sm + OFF_Y, 0, t0, head);  // rows past N are clipped
-          bulk_commit();
-        }
+      if (elected) {
+        if (!mbar_wait(&bars[B_YS], par, abort_flag, kWaitLimit)) { ok = false; break; }
+        tma_store_3d(&maps.y, sm + OFF_Y, 0, t0, head);  // rows past N are clipped
+        bulk_commit();
       }
     }
-    if (!ok) fail();
-    if (warp == 2 && lane == 0) bulk_wait0();  // Y stores complete before exit
-    if (ok) {
+    if (!ok && *abort_flag != kHandOff) timeout();
+    if (elected) bulk_wait0();  // Y stores complete before exit
+    const bool done = *abort_flag == kRun;
+    if (done) {
       float4* dst = reinterpret_cast<float4*>(p.M + ((long)head * kDim + v) * kDim + 64 * h);
 #pragma unroll
       for (int x = 0; x < 16; ++x) dst[x] = make_float4(m[4 * x], m[4 * x + 1], m[4 * x + 2], m[4 * x + 3]);
     }
-    if (p.S) {
+    if (p.S && done) {
       // eta = 0: the final momentum is S_N = -gamma_0 theta_{N-1} 2 e_{N-1} k_{N-1}^T
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_S]);
-      if (mbar_wait(&bars[B_S], 0, abort_flag, kWaitLimit) && ok) {
+      if (mbar_wait(&bars[B_S], 0, abort_flag, kWaitLimit)) {
         const float* el = reinterpret_cast<const float*>(sm + OFF_ELAST);
         const float coef = -2.f * p.gamma[0] * p.theta[(long)head * N + N - 1] * el[v];
         const __nv_bfloat16* kl = p.K + ((long)head * N + N - 1) * kDim + 64 * h;

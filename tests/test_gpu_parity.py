@@ -195,3 +195,16 @@ def test_tensor_core_path_mixed_momentum_heads_and_state_out():
     Yg, Mg, Sg = gpu_run(w, inp, with_S=True)
     check(w, Yg, Mg, Yo, Mo, "mixed")
     assert rel_err(Sg, So, True) <= tol(w)
+
+
+def test_tensor_core_path_hands_off_a_full_reset_gate():
+    """alpha = 1 (a full reset) makes the tensor-core kernel's rescaled readout
+    weights undefined; that head is recomputed by the CUDA-core kernel in the
+    same call and still matches the oracle."""
+    w = W.workload(2, N=256)
+    inp = W.generate(w, heads=[0, 1, 2])
+    inp["alpha"][1, 70] = 1.0
+    inp["alpha"][2, 130:140] = 0.9999
+    Yo, Mo, _ = run_oracle(w, inp)
+    Yg, Mg, _ = gpu_run(w, inp)
+    check(w, Yg, Mg, Yo, Mo, "reset gate")
