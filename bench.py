@@ -34,6 +34,7 @@ import workloads as W  # noqa: E402
 
 METRIC = "memory-update tokens/sec on 1 GB300 per config; % of bf16 tensor/HBM roofline"
 UNIT = "tokens/s"
+L2_BYTES = 129 * 1024 * 1024  # L2 of one GB300
 
 
 # ----------------------------------------------------------------- helpers
@@ -268,7 +269,15 @@ def run_atlas(args, w):
     launches_per_step = A.atlas_mem_launch_count(run.cfg)
     stream = torch.cuda.current_stream()
 
-    # -- device-resident timing
+    # -- device-resident timing.  A step whose data fits in L2 is preceded by a
+    # write of a buffer twice the L2 size, outside its events, and the step
+    # time is the sum of the per-step events; otherwise the steps run back to
+    # back and the step time is the whole loop's.
+    bytes_launch = w.tokens * W.bytes_per_token(w) + 2 * 4 * w.heads * w.state_size
+    flush = bytes_launch < 2 * L2_BYTES
+    scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    s_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    s_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     k_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     k_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
@@ -283,16 +292,23 @@ def run_atlas(args, w):
         clk.mark_start()
         t_start.record(stream)
         for i in range(args.steps):
+            if flush:
+                scrub.fill_(float(i))
+            s_start[i].record(stream)
             run.M.copy_(d["M0"])
             k_start[i].record(stream)
             A.atlas_mem_forward(d["K"], d["Q"], d["V"], d["alpha"], d["eta"], d["theta"],
                                 d["gamma"], run.cfg, run.Y, run.M, stream)
             k_end[i].record(stream)
+            s_end[i].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
         clk.mark_end()
         barrier(world)
-    elapsed = t_start.elapsed_time(t_end) / 1e3
+    if flush:
+        elapsed = sum(a.elapsed_time(b) for a, b in zip(s_start, s_end)) / 1e3
+    else:
+        elapsed = t_start.elapsed_time(t_end) / 1e3
     kernel_s = sum(a.elapsed_time(b) for a, b in zip(k_start, k_end)) / 1e3 / args.steps
     elapsed_max = max_over_ranks(elapsed, world, dev)
     status = int(run.status.item())
@@ -335,7 +351,6 @@ def run_atlas(args, w):
     tokens = w.tokens
     value = aggregate(tokens, world, elapsed_max, args.steps)
     hbm, tf, tf_sus, peak_kind = load_peaks()
-    bytes_launch = tokens * W.bytes_per_token(w) + 2 * 4 * w.heads * w.state_size
     flops_launch = tokens * W.flop_per_token(w)
     ai = flops_launch / bytes_launch
     ridge = tf * 1e12 / (hbm * 1e9)
@@ -372,7 +387,8 @@ def run_atlas(args, w):
         "dtype": "bf16" if w.bf16 else "f32", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d_k": w.d_k, "d_v": w.d_v,
                    "d_h": w.d_h, "c": w.c, "b": w.b, "path": path,
-                   "l2": "inputs larger than L2 (K,Q,V,Y %.0f MB per step)"
+                   "l2": ("L2 flushed before every step (%.2f MB per step)" if flush else
+                          "inputs larger than L2 (K,Q,V,Y %.0f MB per step)")
                          % (bytes_launch / 1e6)},
         "roofline": roof,
         "cpu_baseline": cpu,
@@ -395,8 +411,12 @@ def main(argv=None):
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="atlas", choices=["atlas", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="run only the first TOKENS tokens of every head (0 = the whole workload)")
     args = ap.parse_args(argv)
     w = W.workload(args.workload, bounded=True)
+    if args.tokens:
+        w = w.with_(N=min(args.tokens, w.N))
     if args.impl == "reference":
         run_reference(args, w)
     else:

@@ -10,7 +10,7 @@ using namespace atlas;
 
 namespace {
 
-enum Path { PATH_INVALID = 0, PATH_LINEAR_SIMT, PATH_LINEAR_TC, PATH_MLP_SIMT };
+enum Path { PATH_INVALID = 0, PATH_LINEAR_SIMT, PATH_LINEAR_TC, PATH_LINEAR_SEQ, PATH_MLP_SIMT };
 
 int feature_dim(const atlas_mem_cfg* c) {
   if (c->mem == ATLAS_MEM_LINEAR && c->phi == ATLAS_PHI_POLY2)
@@ -76,6 +76,7 @@ Path choose_path(const atlas_mem_cfg* c) {
   LinArgs a = lin_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, c,
                        nullptr, nullptr);
   if (linear_tc_supported(a)) return PATH_LINEAR_TC;
+  if (linear_seq_supported(a)) return PATH_LINEAR_SEQ;
   int RV;
   size_t smem;
   if (linear_simt_plan(a, c->B * c->H, &RV, &smem) != ATLAS_OK) return PATH_INVALID;
@@ -107,6 +108,7 @@ const char* atlas_mem_path(const atlas_mem_cfg* cfg) {
   switch (choose_path(cfg)) {
     case PATH_LINEAR_SIMT: return "linear_simt";
     case PATH_LINEAR_TC: return "linear_tc";
+    case PATH_LINEAR_SEQ: return "linear_seq";
     case PATH_MLP_SIMT: return "mlp_simt";
     default: return "";
   }
@@ -115,6 +117,7 @@ const char* atlas_mem_path(const atlas_mem_cfg* cfg) {
 long atlas_mem_launch_count(const atlas_mem_cfg* cfg) {
   switch (choose_path(cfg)) {
     case PATH_LINEAR_SIMT:
+    case PATH_LINEAR_SEQ:
       return (long)cfg->B * cfg->H > 0 ? 1 : 0;
     case PATH_LINEAR_TC:
       return (long)cfg->B * cfg->H > 0 ? 2 : 0;
@@ -153,6 +156,7 @@ int atlas_mem_forward(const void* K, const void* Q, const void* V, const float* 
     if (!cfg->workspace || cfg->workspace_bytes < need) return ATLAS_ERR_WORKSPACE;
     return linear_tc_launch(a, (int)heads, cfg->status_dev, cfg->workspace, st);
   }
+  if (path == PATH_LINEAR_SEQ) return linear_seq_launch(a, (int)heads, st);
   return linear_simt_launch(a, (int)heads, st);
 }
 

@@ -26,6 +26,11 @@ int linear_simt_launch(const LinArgs& a, int heads, cudaStream_t st);
 int linear_simt_launch_flagged(const LinArgs& a, int heads, const int* flags, cudaStream_t st);
 int linear_simt_plan(const LinArgs& a, int heads, int* RV_out, size_t* smem_out);
 
+// Token-serial path for small linear memories (identity map, d_k = 32,
+// window c <= 8, any chunk length): state in registers, rows split over CTAs.
+bool linear_seq_supported(const LinArgs& a);
+int linear_seq_launch(const LinArgs& a, int heads, cudaStream_t st);
+
 // Tensor-core path: linear memory, identity map, d_k = d_v = 128, bf16 inputs,
 // b = 64, c = 1, N % 4 == 0.  Launches the tensor-core kernel (heads with
 // eta == 0; it flags the others in the workspace) and the CUDA-core kernel on

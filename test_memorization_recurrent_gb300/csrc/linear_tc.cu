@@ -15,8 +15,9 @@
 // i <= n (s_i / s_n is the product over l = i+1..n), so both the state update and the
 // intra-chunk readout use the same weighted errors Ew_i = gamma_0 theta_i s_i e_i:
 //   M_end = a_63 M0 - 2 Ew^T Phi,   y_n = a_n (M0 q_n) + sum_{i<=n} (-2 q_n.k_i / s_n) Ew_i.
-// A chunk whose s_0 falls below 1e-30 (a decay gate at or near 1) is not
-// handled here: the head is flagged and recomputed by the CUDA-core kernel.
+// A chunk whose s_0 falls below 1e-30 (a decay gate at or near 1), or whose
+// eta has a non-zero entry (momentum), is not handled here: the head is flagged
+// and recomputed from scratch by the CUDA-core kernel.
 //
 // Products per chunk, with the value index v on the TMEM lanes (fp32 accumulators):
 //   [T | Qy]   = M0 [Phi; Q]^T           (128 x 128)  T -> Ew^T = s.theta.(T - V^T)
@@ -33,9 +34,9 @@
 // builds the gate tables (warp-wide scans) and issues every MMA from one
 // thread; warps 2..9 are the epilogue, two per 32-lane TMEM quadrant.
 //
-// Heads whose eta has any non-zero entry are also left to the CUDA-core
-// kernel launched right after this one: this kernel writes one flag per head
-// to the workspace and that kernel takes exactly the flagged heads.  Every
+// The CUDA-core kernel is launched right after this one: this kernel writes
+// one flag per head to the workspace and that kernel takes exactly the flagged
+// heads.  Every
 // mbarrier wait is bounded; on expiry the kernel records ATLAS_ERR_TIMEOUT in
 // the status word, drains its in-flight copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -197,18 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int N = p.N;
   const int nchunks = (N + kChunk - 1) / kChunk;
 
-  // ---- heads with momentum belong to the CUDA-core kernel
-  {
-    const float4* e4 = reinterpret_cast<const float4*>(p.eta + (long)head * N);
-    int nz = 0;
-    for (int x = tid; x < N / 4; x += kThreads) {
-      const float4 v = e4[x];
-      nz |= (v.x != 0.f) | (v.y != 0.f) | (v.z != 0.f) | (v.w != 0.f);
-    }
-    nz = __syncthreads_or(nz);
-    if (tid == 0) p.flags[head] = nz ? 1 : 0;
-    if (nz) return;
-  }
+  // the head is this kernel's unless a chunk hands it off (momentum, reset gate)
+  if (tid == 0) p.flags[head] = 0;
   if (nchunks == 0) return;
 
   if (tid == 0) {
@@ -286,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return false;
       }
       const float* ga = reinterpret_cast<const float*>(sm + OFF_STAGE0 + s * STAGE_BYTES + ST_GATES);
+      const float* ge = ga + 64;
       const float* gt = ga + 128;
       float* tb = table(sm, j & 1);
       float *a = tb, *wb = tb + kChunk, *cn = tb + 2 * kChunk;
@@ -312,7 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       wb[n1] = gt[n1] * g0 * s1;
       cn[n0] = -2.f / s0;
       cn[n1] = -2.f / s1;
-      const bool handled = __shfl_sync(full, s0, 0) >= kMinSuffix;  // s_0 is the smallest
+      const bool handled = __shfl_sync(full, s0, 0) >= kMinSuffix &&  // s_0 is the smallest
+                           !__any_sync(full, ge[n0] != 0.f || ge[n1] != 0.f);
       __syncwarp();
       if (!handled) {
         if (lane == 0 && *abort_flag == kRun) {

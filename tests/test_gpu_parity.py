@@ -140,6 +140,35 @@ def test_chunk_longer_than_sequence_and_window_longer_than_chunk():
     check(w, Yg, Mg, Yo, Mo)
 
 
+# ------------------------------------------------- token-serial linear path
+
+def test_token_serial_path_selected_for_the_exact_recurrence_workload():
+    from test_memorization_recurrent_gb300.harness import cfg_for
+    import test_memorization_recurrent_gb300 as A
+    w = W.workload(1)
+    assert A.atlas_mem_path(cfg_for(w, w.heads, w.N)) == "linear_seq"
+    assert A.atlas_mem_path(cfg_for(w.with_(c=9), 1, 64)) == "linear_simt"
+    assert A.atlas_mem_path(cfg_for(w.with_(d_k=16, d_v=16), 1, 64)) == "linear_simt"
+
+
+@pytest.mark.parametrize("c,b,d_v,H,N,loss,bf16", [
+    (1, 1, 32, 1, 64, W.LOSS_L2, False),
+    (4, 1, 32, 2, 513, W.LOSS_L2, False),     # several tiles, ragged tail
+    (8, 16, 32, 1, 200, W.LOSS_L2, False),    # widest window, chunked
+    (3, 5, 20, 3, 131, W.LOSS_L2, False),     # ragged rows, chunk not a power of 2
+    (2, 64, 48, 1, 300, W.LOSS_L2, True),     # two CTAs of rows, bf16 inputs
+    (5, 1, 7, 2, 66, W.LOSS_DOT, False),      # dot loss
+    (4, 8, 32, 1, 1, W.LOSS_L2, False),       # one token
+])
+def test_token_serial_path(c, b, d_v, H, N, loss, bf16):
+    w = W.workload(1, c=c, b=b, d_v=d_v, H=H, N=N, loss=loss, bf16=bf16)
+    inp = W.generate(w)
+    Yo, Mo, So = run_oracle(w, inp)
+    Yg, Mg, Sg = gpu_run(w, inp, with_S=True)
+    check(w, Yg, Mg, Yo, Mo, f"c={c} b={b} d_v={d_v}")
+    assert rel_err(Sg, So, w.bf16) <= tol(w)
+
+
 # -------------------------------------------------------------- full sizes
 
 @pytest.mark.parametrize("wid,sample,prefix", [
