@@ -243,6 +243,7 @@ def run_reference(args, w):
 KERNEL_OF_PATH = {
     "linear_tc": ("linear_tc.cu", "linear_tc_{wname}.md"),
     "linear_simt": ("linear_simt.cu", "linear_simt_{wname}.md"),
+    "linear_seq": ("linear_seq.cu", "linear_seq_{wname}.md"),
     "mlp_simt": ("mlp_simt.cu", "mlp_simt_{wname}.md"),
 }
 
