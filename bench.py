@@ -245,6 +245,7 @@ KERNEL_OF_PATH = {
     "linear_simt": ("linear_simt.cu", "linear_simt_{wname}.md"),
     "linear_seq": ("linear_seq.cu", "linear_seq_{wname}.md"),
     "mlp_simt": ("mlp_simt.cu", "mlp_simt_{wname}.md"),
+    "mlp_tc": ("mlp_tc.cu", "mlp_tc_{wname}.md"),
 }
 
 

@@ -1,6 +1,6 @@
 // atlas_mem.cu -- C-ABI entry points: argument validation, path choice,
 // workspace sizing and launch.  Every computation happens in the kernels of
-// linear_simt.cu, linear_tc.cu and mlp_simt.cu; this file only plans.
+// linear_*.cu and mlp_*.cu; this file only plans.
 #include <string.h>
 
 #include "atlas_mem.h"
@@ -10,7 +10,9 @@ using namespace atlas;
 
 namespace {
 
-enum Path { PATH_INVALID = 0, PATH_LINEAR_SIMT, PATH_LINEAR_TC, PATH_LINEAR_SEQ, PATH_MLP_SIMT };
+enum Path {
+  PATH_INVALID = 0, PATH_LINEAR_SIMT, PATH_LINEAR_TC, PATH_LINEAR_SEQ, PATH_MLP_SIMT, PATH_MLP_TC
+};
 
 int feature_dim(const atlas_mem_cfg* c) {
   if (c->mem == ATLAS_MEM_LINEAR && c->phi == ATLAS_PHI_POLY2)
@@ -67,12 +69,17 @@ MlpArgs mlp_args(const void* K, const void* Q, const void* V, const float* alpha
   a.ns_steps = c->ns_steps;
   a.ns_a = c->ns_a; a.ns_b = c->ns_b; a.ns_c = c->ns_c; a.ns_eps = c->ns_eps;
   a.s_is_zero = c->S_state == nullptr;
+  a.status = c->status_dev;
   return a;
 }
 
 Path choose_path(const atlas_mem_cfg* c) {
   if (check_cfg(c) != ATLAS_OK) return PATH_INVALID;
-  if (c->mem == ATLAS_MEM_MLP) return PATH_MLP_SIMT;
+  if (c->mem == ATLAS_MEM_MLP) {
+    MlpArgs m = mlp_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, c,
+                         nullptr, nullptr);
+    return mlp_tc_supported(m) ? PATH_MLP_TC : PATH_MLP_SIMT;
+  }
   LinArgs a = lin_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, c,
                        nullptr, nullptr);
   if (linear_tc_supported(a)) return PATH_LINEAR_TC;
@@ -98,7 +105,8 @@ size_t atlas_mem_workspace_bytes(const atlas_mem_cfg* cfg) {
   if (cfg->mem == ATLAS_MEM_MLP) {
     MlpArgs a = mlp_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, cfg,
                          nullptr, nullptr);
-    return mlp_simt_workspace_bytes(a);
+    return choose_path(cfg) == PATH_MLP_TC ? mlp_tc_workspace_bytes(a)
+                                           : mlp_simt_workspace_bytes(a);
   }
   if (choose_path(cfg) == PATH_LINEAR_TC) return linear_tc_workspace_bytes(cfg->B * cfg->H);
   return 0;
@@ -110,6 +118,7 @@ const char* atlas_mem_path(const atlas_mem_cfg* cfg) {
     case PATH_LINEAR_TC: return "linear_tc";
     case PATH_LINEAR_SEQ: return "linear_seq";
     case PATH_MLP_SIMT: return "mlp_simt";
+    case PATH_MLP_TC: return "mlp_tc";
     default: return "";
   }
 }
@@ -118,6 +127,7 @@ long atlas_mem_launch_count(const atlas_mem_cfg* cfg) {
   switch (choose_path(cfg)) {
     case PATH_LINEAR_SIMT:
     case PATH_LINEAR_SEQ:
+    case PATH_MLP_TC:
       return (long)cfg->B * cfg->H > 0 ? 1 : 0;
     case PATH_LINEAR_TC:
       return (long)cfg->B * cfg->H > 0 ? 2 : 0;
@@ -143,6 +153,13 @@ int atlas_mem_forward(const void* K, const void* Q, const void* V, const float* 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   Path path = choose_path(cfg);
   if (path == PATH_INVALID) return ATLAS_ERR_UNSUPPORTED;
+  if (path == PATH_MLP_TC) {
+    MlpArgs a = mlp_args(K, Q, V, alpha, eta, theta, gamma, cfg, Y, M_final);
+    const size_t need = mlp_tc_workspace_bytes(a);
+    if (!cfg->workspace || cfg->workspace_bytes < need) return ATLAS_ERR_WORKSPACE;
+    if (cfg->N == 0) return ATLAS_OK;
+    return mlp_tc_launch(a, cfg->workspace, st);
+  }
   if (path == PATH_MLP_SIMT) {
     MlpArgs a = mlp_args(K, Q, V, alpha, eta, theta, gamma, cfg, Y, M_final);
     const size_t need = mlp_simt_workspace_bytes(a);

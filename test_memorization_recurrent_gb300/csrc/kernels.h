@@ -56,9 +56,17 @@ struct MlpArgs {
   int ns_steps;
   float ns_a, ns_b, ns_c, ns_eps;
   int s_is_zero;  // S must be cleared before the first chunk
+  int* status;    // optional device status word (timeouts)
 };
 
 size_t mlp_simt_workspace_bytes(const MlpArgs& a);
+
+// Tensor-core path (mlp_tc.cu): d = 128, d_h = 512, c = 1, b = 64, bf16 inputs,
+// no Newton-Schulz.  One 4-CTA cluster per head; the workspace holds the W2,
+// S2, S1 slices of every head as bf16 hi/lo pairs.
+bool mlp_tc_supported(const MlpArgs& a);
+size_t mlp_tc_workspace_bytes(const MlpArgs& a);
+int mlp_tc_launch(const MlpArgs& a, void* ws, cudaStream_t st);
 int mlp_simt_forward(const MlpArgs& a, void* ws, cudaStream_t st);
 long mlp_simt_launch_count(const MlpArgs& a);
 

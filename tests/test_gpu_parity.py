@@ -169,6 +169,42 @@ def test_token_serial_path(c, b, d_v, H, N, loss, bf16):
     assert rel_err(Sg, So, w.bf16) <= tol(w)
 
 
+# ------------------------------------------------------ tensor-core MLP path
+
+def test_mlp_tensor_core_path_selected():
+    from test_memorization_recurrent_gb300.harness import cfg_for
+    import test_memorization_recurrent_gb300 as A
+    w = W.workload(4)
+    assert A.atlas_mem_path(cfg_for(w, w.heads, w.N)) == "mlp_tc"
+    assert A.atlas_mem_path(cfg_for(w.with_(c=2), 2, 64)) == "mlp_simt"
+    assert A.atlas_mem_path(cfg_for(w.with_(d_h=256), 2, 64)) == "mlp_simt"
+    assert A.atlas_mem_path(cfg_for(W.workload(5), 16, 64)) == "mlp_simt"  # Newton-Schulz
+
+
+@pytest.mark.parametrize("N,heads", [(1, [5]), (64, [0, 1, 2]), (200, [3, 30]), (517, [9])])
+def test_mlp_tensor_core_path(N, heads):
+    """Chunk-aligned, ragged and single-token lengths; momentum S in and out."""
+    w = W.workload(4, bounded=True, N=N)
+    inp = W.generate(w, heads=heads, n_tokens=N)
+    Yo, Mo, So = run_oracle(w, inp)
+    Yg, Mg, Sg = gpu_run(w, inp, with_S=True)
+    check(w, Yg, Mg, Yo, Mo, f"N={N}")
+    assert rel_err(Sg, So, w.bf16) <= tol(w)
+
+
+def test_mlp_tensor_core_path_with_initial_momentum():
+    """A non-zero S_0 (state handed over from a previous call) enters both the
+    decay of M and the momentum; compared with the oracle started from the same S_0."""
+    w = W.workload(4, bounded=True, N=130)
+    inp = W.generate(w, heads=[4, 11], n_tokens=130)
+    rng = np.random.default_rng(7)
+    S0 = (rng.standard_normal(inp["M0"].shape) * 0.01).astype(np.float32)
+    Yo, Mo, So = run_oracle(w, inp, S0=S0)
+    Yg, Mg, Sg = gpu_run(w, inp, S0=S0)
+    check(w, Yg, Mg, Yo, Mo, "S0")
+    assert rel_err(Sg, So, w.bf16) <= tol(w)
+
+
 # -------------------------------------------------------------- full sizes
 
 @pytest.mark.parametrize("wid,sample,prefix", [

@@ -26,7 +26,7 @@ def lib():
 
 
 def test_oversized_problem_is_rejected_before_launch(lib):
-    w = W.workload(4)  # 32 heads x 16384 tokens: far more scratch than the array holds
+    w = W.workload(5)  # Newton-Schulz MLP workload: far more scratch than the array holds
     from test_memorization_recurrent_gb300.harness import cfg_for
     cfg = cfg_for(w, w.heads, w.N)
     assert lib.atlas_mem_workspace_bytes(cfg) > lib.NOALLOC_SCRATCH_BYTES
