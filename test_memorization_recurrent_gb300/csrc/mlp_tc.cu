@@ -97,10 +97,10 @@ constexpr uint32_t TM_S2 = 384;   // S2 slice [j][d], fp32 state (128 columns)
 constexpr uint32_t TM_COLS = 512;
 
 enum Bar {
-  B_KFULL = 0, B_QFULL, B_TR, B_VQFULL, B_S1FULL, B_TAB,
+  B_KFULL = 0, B_QFULL, B_TR, B_VQFULL, B_S1FULL, B_TAB0, B_TAB1,
   B_T1, B_F2, B_F3, B_U2A, B_R2C, B_U2B, B_R3, B_R4, B_U1A, B_U1B,
   B_H, B_EFULL, B_D, B_HQ, B_DU, B_P2, B_EW, B_EU, B_VQFREE,
-  B_RFREE, B_RED, B_OWN, B_SREAD, B_DRAIN, B_COUNT
+  B_RFREE, B_RED, B_OWN, B_SREAD, B_S1OLDH, B_S1OLDL, B_S1NEW, B_S1READ, B_DRAIN, B_COUNT
 };
 
 // state planes of the workspace: [head][c][plane][128][128] bf16 (S1 slice [d][j])
@@ -395,8 +395,8 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 1)
   float* Sh = p.S ? p.S + (long)head * 2 * kD * kHid : nullptr;
 
   if (tid == 0) {
-    const uint32_t counts[B_COUNT] = {1, 1, 8, 1, 1, 1,  1, 1, 1, 1, 1, 1, 1, 1, 1, 1,
-                                      8, 1, 8, 8, 8, 4, 8, 8, 2,  3, 1, 2, 2, 1};
+    const uint32_t counts[B_COUNT] = {1, 1, 8, 1, 1, 1, 1,  1, 1, 1, 1, 1, 1, 1, 1, 1, 1,
+                                      8, 1, 8, 8, 8, 4, 8, 8, 2,  3, 1, 2, 2,  1, 1, 8, 1,  1};
     for (int b = 0; b < B_COUNT; ++b) mbar_init(&bars[b], counts[b]);
     *abort_flag = 0;
     fence_barrier_init();
@@ -437,60 +437,62 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 1)
   };
 
   if (warp == 0) {
-    // =========================== producer: chunk tables (whole warp), TMA loads (lane 0)
+    // =========================== producer: chunk tables (whole warp), TMA (lane 0)
+    // Per chunk: K, Q, the V / Q slices; the tables of the next chunk; S1 hi for the
+    // readout; the S1 slice (hi into the K / Q regions, lo into the E region once
+    // those are free) for the carry at the chunk end, and its store back.
     bool ok = true;
-    int last = -1, s1last = -1;  // last chunk whose loads were issued
     const int pw = (int)plane0;
     auto W = [&](int b, int ch) { return mbar_wait(&bars[b], ch & 1, abort_flag, kWait); };
     const float g0 = p.gamma[0];
+    auto tables = [&](int ch) {  // whole warp; buffer ch % 3, barrier B_TAB0 + (ch & 1)
+      float* G = reinterpret_cast<float*>(sm + R_G + (ch % kGBufs) * G_BYTES);
+      const int t0 = ch * kL;
+      const int nb = min(kL, N - t0), L = nb - 1;
+      const long gb = (long)head * N + t0;
+      auto gate = [&](const float* g, int n) { return n < nb ? g[gb + n] : 0.f; };
+      const int n0 = 2 * lane, n1 = n0 + 1;
+      const float al0 = gate(p.alpha, n0), al1 = gate(p.alpha, n1);
+      const float et0 = gate(p.eta, n0), et1 = gate(p.eta, n1);
+      const float th0 = gate(p.theta, n0), th1 = gate(p.theta, n1);
+      G[G_AL + n0] = al0; G[G_AL + n1] = al1;
+      G[G_ET + n0] = et0; G[G_ET + n1] = et1;
+      G[G_TH + n0] = th0; G[G_TH + n1] = th1;
+      float a0, a1, e0, e1, b0, b1;
+      lin_scan64(1.f - al0, 0.f, 1.f - al1, 0.f, 1.f, a0, a1);  // a_n = prod (1 - alpha)
+      lin_scan64(et0, 0.f, et1, 0.f, 1.f, e0, e1);              // eps_n = prod eta
+      lin_scan64(1.f - al0, e0, 1.f - al1, e1, 0.f, b0, b1);    // beta_n
+      G[G_A + n0] = a0; G[G_A + n1] = a1;
+      G[G_BE + n0] = b0; G[G_BE + n1] = b1;
+      if (n0 == L) { G[G_SC + 0] = a0; G[G_SC + 1] = b0; G[G_SC + 2] = e0; }
+      if (n1 == L) { G[G_SC + 0] = a1; G[G_SC + 1] = b1; G[G_SC + 2] = e1; }
+      // backward, r = 63 - i: A_i = prod_{l=i+1..L} (1 - alpha_l),
+      // E_i = prod_{l=i+1..L} eta_l, R_i = A_i + eta_{i+1} R_{i+1} (R_L = 1)
+      const int i0 = 63 - n0, i1 = 63 - n1;  // i0 = i1 + 1
+      const float k0 = 1.f - gate(p.alpha, i0 + 1), k1 = 1.f - gate(p.alpha, i1 + 1);
+      const float h0 = gate(p.eta, i0 + 1), h1 = gate(p.eta, i1 + 1);
+      const float c0 = i0 + 1 <= L ? h0 : 0.f, c1 = i1 + 1 <= L ? h1 : 0.f;
+      float A0, A1, E0, E1, R0, R1;
+      lin_scan64(k0, 0.f, k1, 0.f, 1.f, A0, A1);
+      lin_scan64(i0 + 1 <= L ? h0 : 1.f, 0.f, i1 + 1 <= L ? h1 : 1.f, 0.f, 1.f, E0, E1);
+      lin_scan64(c0, A0, c1, A1, 0.f, R0, R1);
+      const float ti0 = gate(p.theta, i0), ti1 = gate(p.theta, i1);
+      G[G_WL + i0] = g0 * ti0 * R0; G[G_WL + i1] = g0 * ti1 * R1;
+      G[G_UL + i0] = g0 * ti0 * E0; G[G_UL + i1] = g0 * ti1 * E1;
+      if (lane == 0) G[G_SC + 3] = g0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_TAB0 + (ch & 1)]);
+    };
+    tables(0);
     for (int ch = 0; ch < nch; ++ch) {
       const int t0 = ch * kL;
-      // -- tables of chunk ch, a chunk ahead of its use (buffer ch % 3 was last read by
-      //    chunk ch - 3, finished: this warp has seen chunk ch - 2's B_VQFREE)
-      {
-        float* G = reinterpret_cast<float*>(sm + R_G + (ch % kGBufs) * G_BYTES);
-        const int nb = min(kL, N - t0), L = nb - 1;
-        const long gb = (long)head * N + t0;
-        auto gate = [&](const float* g, int n) { return n < nb ? g[gb + n] : 0.f; };
-        const int n0 = 2 * lane, n1 = n0 + 1;
-        const float al0 = gate(p.alpha, n0), al1 = gate(p.alpha, n1);
-        const float et0 = gate(p.eta, n0), et1 = gate(p.eta, n1);
-        const float th0 = gate(p.theta, n0), th1 = gate(p.theta, n1);
-        G[G_AL + n0] = al0; G[G_AL + n1] = al1;
-        G[G_ET + n0] = et0; G[G_ET + n1] = et1;
-        G[G_TH + n0] = th0; G[G_TH + n1] = th1;
-        float a0, a1, e0, e1, b0, b1;
-        lin_scan64(1.f - al0, 0.f, 1.f - al1, 0.f, 1.f, a0, a1);  // a_n = prod (1 - alpha)
-        lin_scan64(et0, 0.f, et1, 0.f, 1.f, e0, e1);              // eps_n = prod eta
-        lin_scan64(1.f - al0, e0, 1.f - al1, e1, 0.f, b0, b1);    // beta_n
-        G[G_A + n0] = a0; G[G_A + n1] = a1;
-        G[G_BE + n0] = b0; G[G_BE + n1] = b1;
-        if (n0 == L) { G[G_SC + 0] = a0; G[G_SC + 1] = b0; G[G_SC + 2] = e0; }
-        if (n1 == L) { G[G_SC + 0] = a1; G[G_SC + 1] = b1; G[G_SC + 2] = e1; }
-        // backward, r = 63 - i: A_i = prod_{l=i+1..L} (1 - alpha_l),
-        // E_i = prod_{l=i+1..L} eta_l, R_i = A_i + eta_{i+1} R_{i+1} (R_L = 1)
-        const int i0 = 63 - n0, i1 = 63 - n1;  // i0 = i1 + 1
-        const float k0 = 1.f - gate(p.alpha, i0 + 1), k1 = 1.f - gate(p.alpha, i1 + 1);
-        const float h0 = gate(p.eta, i0 + 1), h1 = gate(p.eta, i1 + 1);
-        const float c0 = i0 + 1 <= L ? h0 : 0.f, c1 = i1 + 1 <= L ? h1 : 0.f;
-        float A0, A1, E0, E1, R0, R1;
-        lin_scan64(k0, 0.f, k1, 0.f, 1.f, A0, A1);
-        lin_scan64(i0 + 1 <= L ? h0 : 1.f, 0.f, i1 + 1 <= L ? h1 : 1.f, 0.f, 1.f, E0, E1);
-        lin_scan64(c0, A0, c1, A1, 0.f, R0, R1);
-        const float ti0 = gate(p.theta, i0), ti1 = gate(p.theta, i1);
-        G[G_WL + i0] = g0 * ti0 * R0; G[G_WL + i1] = g0 * ti1 * R1;
-        G[G_UL + i0] = g0 * ti0 * E0; G[G_UL + i1] = g0 * ti1 * E1;
-        if (lane == 0) G[G_SC + 3] = g0;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[B_TAB]);
-      }
       if (lane == 0) {
         do {
-          if (ch > 0 && !(ok = W(B_U2B, ch - 1))) break;
+          // the previous chunk's S1 store has read the K / Q regions
+          if (ch > 0 && !(ok = W(B_S1READ, ch - 1))) break;
           mbar_arrive_expect_tx(&bars[B_KFULL], 16384);
           tma_load_3d(sm + R_K, &maps.k, &bars[B_KFULL], 0, t0, head);
           tma_load_3d(sm + R_K + 8192, &maps.k, &bars[B_KFULL], 64, t0, head);
-          if (ch > 0 && !(ok = W(B_R4, ch - 1))) break;
           mbar_arrive_expect_tx(&bars[B_QFULL], 16384);
           tma_load_3d(sm + R_Q, &maps.q, &bars[B_QFULL], 0, t0, head);
           tma_load_3d(sm + R_Q + 8192, &maps.q, &bars[B_QFULL], 64, t0, head);
@@ -498,27 +500,43 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 1)
           mbar_arrive_expect_tx(&bars[B_VQFULL], 4096 + 4096);
           tma_load_3d(sm + X_V, &maps.vs, &bars[B_VQFULL], 32 * c, t0, head);
           tma_load_3d(sm + X_QS, &maps.qs, &bars[B_VQFULL], 32 * c, t0, head);
-          last = ch;
-          if (!(ok = W(B_U2B, ch))) break;
+        } while (false);
+      }
+      if (!__shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0)) break;
+      if (ch + 1 < nch) tables(ch + 1);  // buffer (ch + 1) % 3: chunk ch - 2 is done
+      if (lane == 0) {
+        do {
+          if (!(ok = W(B_U2B, ch))) break;  // Du read: the scratch takes S1 hi
+          bulk_wait0();                     // the previous chunk's S1 is in global memory
+          fence_proxy_async_global();
           mbar_arrive_expect_tx(&bars[B_S1FULL], 32768);
           tma_load_3d(sm + T_SC, &maps.st, &bars[B_S1FULL], 0, 0, pw + P_S1HI);
           tma_load_3d(sm + T_SC + 16384, &maps.st, &bars[B_S1FULL], 64, 0, pw + P_S1HI);
-          s1last = ch;
+          if (!(ok = W(B_R4, ch))) break;  // K and Hq read: S1 hi (old) into those regions
+          mbar_arrive_expect_tx(&bars[B_S1OLDH], 32768);
+          tma_load_3d(sm + R_K, &maps.st, &bars[B_S1OLDH], 0, 0, pw + P_S1HI);
+          tma_load_3d(sm + R_K + 16384, &maps.st, &bars[B_S1OLDH], 64, 0, pw + P_S1HI);
+          if (!(ok = W(B_EU, ch))) break;  // E read: S1 lo (old) into its region
+          mbar_arrive_expect_tx(&bars[B_S1OLDL], 32768);
+          tma_load_3d(sm + T_E, &maps.st, &bars[B_S1OLDL], 0, 0, pw + P_S1LO);
+          tma_load_3d(sm + T_E + 16384, &maps.st, &bars[B_S1OLDL], 64, 0, pw + P_S1LO);
+          if (!(ok = W(B_S1NEW, ch))) break;  // carried S1 in place: store it back
+          tma_store_3d(&maps.st, sm + R_K, 0, 0, pw + P_S1HI);
+          tma_store_3d(&maps.st, sm + R_K + 16384, 64, 0, pw + P_S1HI);
+          tma_store_3d(&maps.st, sm + T_E, 0, 0, pw + P_S1LO);
+          tma_store_3d(&maps.st, sm + T_E + 16384, 64, 0, pw + P_S1LO);
+          bulk_commit();
+          bulk_wait_read0();
+          mbar_arrive(&bars[B_S1READ]);
         } while (false);
       }
       if (!__shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0)) break;
     }
-    if (lane == 0 && !ok) {
-      fail();
-      // no copy may land after this CTA is gone: wait for the last issued loads
-      volatile int zero = 0;
-      if (last >= 0) {
-        const uint32_t pl = last & 1;
-        mbar_wait(&bars[B_KFULL], pl, &zero, kWait);
-        mbar_wait(&bars[B_QFULL], pl, &zero, kWait);
-        mbar_wait(&bars[B_VQFULL], pl, &zero, kWait);
-      }
-      if (s1last >= 0) mbar_wait(&bars[B_S1FULL], s1last & 1, &zero, kWait);
+    if (lane == 0) {
+      if (!ok) fail();
+      bulk_wait0();  // S1 complete in global memory before the state goes out
+      // (on a failure the loads in flight land in a CTA that waits for its peers at
+      // the final cluster barrier; every barrier wait here is bounded)
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -736,7 +754,10 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 1)
       const int t0 = ch * kL;
       const float* G = reinterpret_cast<const float*>(sm + R_G + (ch % kGBufs) * G_BYTES);
       float v[32], w[32];
-      if (!(ok = W(B_TAB, ch))) break;
+      if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bars[B_TAB0 + (ch & 1)], (ch >> 1) & 1,
+                                                   abort_flag, kWait)) != 0))
+        break;
+      if (ch > 0 && !(ok = W(B_S1READ, ch - 1))) break;  // the S1 store has read T_E
       const float aL = G[G_SC + 0], bL = G[G_SC + 1], eL = G[G_SC + 2];
       // ---- e0: chunk-start operand copies of W2 (hi/lo) and S2 (hi) into shared
       // memory (the previous chunk's products are done: B_U1B), then the decay of
@@ -977,17 +998,10 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 1)
         }
         fence_proxy_async_smem();
         arrive_warp(B_EU);
-        if (!(ok = W(B_U1B, ch))) break;
+        if (!(ok = W(B_U1B, ch) && W(B_S1OLDH, ch) && W(B_S1OLDL, ch))) break;
         tc_fence_after();
         for (int u = 0; u < 2; ++u) {
           const int j0 = 64 * h + 32 * u;
-          const long o = (long)d * kHs + j0;
-          uint4 old[8];  // S hi, S lo for 4 chunks of 8: issued together
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            old[2 * k + 0] = *reinterpret_cast<const uint4*>(plane(P_S1HI) + o + 8 * k);
-            old[2 * k + 1] = *reinterpret_cast<const uint4*>(plane(P_S1LO) + o + 8 * k);
-          }
           tmem_ld32(tl + TM_U1A + j0, v);  // W1 update product
           tmem_ld32(tl + TM_U1B + j0, w);  // S1 update product
 #pragma unroll
@@ -995,19 +1009,19 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 1)
             const uint32_t off = tile_chunk(d, j0 + 8 * k, 16384);
             float wv[8], sv[8];
             ld_pair8_smem(sb + R_W1 + off, sb + R_W1 + 32768 + off, wv);
-            unpack_pair8(old[2 * k + 0], old[2 * k + 1], sv);
+            ld_pair8_smem(sb + R_K + off, sb + T_E + off, sv);
 #pragma unroll
             for (int x = 0; x < 8; ++x) {
               wv[x] = aL * wv[x] + bL * sv[x] - 2.f * v[8 * k + x];
               sv[x] = eL * sv[x] - 2.f * w[8 * k + x];
             }
             store_split8(sb + R_W1 + off, sb + R_W1 + 32768 + off, wv);
-            st_pair8_global(plane(P_S1HI) + o + 8 * k, plane(P_S1LO) + o + 8 * k, sv);
+            store_split8(sb + R_K + off, sb + T_E + off, sv);
           }
         }
-        fence_proxy_async_global();
         fence_proxy_async_smem();
         tc_fence_before();
+        arrive_warp(B_S1NEW);
       }
     }
     if (!ok) fail();
