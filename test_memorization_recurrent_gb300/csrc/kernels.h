@@ -39,6 +39,32 @@ bool linear_tc_supported(const LinArgs& a);
 size_t linear_tc_workspace_bytes(int heads);
 int linear_tc_launch(const LinArgs& a, int heads, int* status, void* workspace, cudaStream_t st);
 
+// Batched strided GEMM on fp32 operands (tc_gemm.cu, tensor cores with bf16
+// hi/lo operand splitting), used by the MLP-memory path:
+//   C[b](m,n) = alpha rowscale[b](m) sum_k A[b](m,k) kscale[b](k) B[b](k,n) + beta D[b](m,n)
+//               (+ C[b](m,n) when accumulate is set)
+// Batch index b splits as (b / bdiv, b % bdiv) when bdiv > 0; every batched
+// pointer then moves by s?b per outer and s?b2 per inner step (bdiv = 0: only
+// the outer strides, over b).  symmetric: B(k, n) = A(n, k) and M = N = 128
+// (a Gram tile): the operand is staged once and serves both sides.
+struct TcGemm {
+  int M, N, K, batch, bdiv;
+  const float* A; long sAb, sAb2, sAm, sAk;
+  const float* B; long sBb, sBb2, sBk, sBn;
+  float* C; long sCb, sCb2, sCm, sCn;
+  float alpha;
+  const float* rowscale; long sRb, sRb2;    // optional per-row factor of the product
+  const float* kscale; long sKb, sKb2;      // optional per-k factor of A
+  const float* D; long sDb, sDb2, sDm, sDn; // optional addend beta * D
+  float beta;
+  int accumulate;                           // C += term (else C = term)
+  int symmetric;
+  int* status;                              // optional device status word (timeouts)
+  int modeA, modeB;                         // set by tc_gemm_launch (operand load paths)
+};
+
+int tc_gemm_launch(const TcGemm& g, cudaStream_t st);
+
 // Arguments of the MLP-memory path.
 struct MlpArgs {
   const void* K;

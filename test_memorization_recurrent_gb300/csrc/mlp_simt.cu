@@ -15,10 +15,16 @@
 //   W1  = a_b W1_0 + beta_b S1_0 - 2 sum_i W[b,i] e_i h_i^T,  S1 = eps_b S1_0 - 2 sum_i U[b,i] e_i h_i^T
 //   (W2, S2 likewise with delta_i k_i^T).
 // With Newton-Schulz ("ATLAS ... (paperlayer)" §5) the update of M is not
-// linear in S, so every token of the chunk is stepped in turn:
-//   S = eta S - theta g_n, g_n = 2 sum_j gamma_j [e h^T | delta k^T]_{n-j};
-//   W = (1 - alpha) W + NS(S) per weight matrix; y = q + W1 GELU(W2 q).
-// NS uses the Gram matrix of the short side: (X X^T) X = X (X^T X).
+// linear in S, but S itself still is: within a chunk
+//   S_n = eps_n S0 - sum_i U[n,i] G_i,   G_i = 2 [e_i h_i^T | delta_i k_i^T] at M0,
+// so every S_n of the chunk is built at once (one product per head and weight
+// block, batched over n), N_n = NS(S_n) runs for all (head, n) instances
+// together, and with r[n,m] = prod_{l=m+1..n} (1 - alpha_l)
+//   M_n = a_n M0 + sum_{m<=n} r[n,m] N_m,
+//   zq_n = a_n W2_0 q_n + sum_{m<=n} r[n,m] N2_m q_n,   hq_n = GELU(zq_n),
+//   y_n  = q_n + a_n W1_0 hq_n + sum_{m<=n} r[n,m] N1_m hq_n.
+// NS uses the Gram matrix of the short side: (X X^T) X = X (X^T X).  These
+// batched products run on the tensor cores (tc_gemm.cu, bf16 hi/lo operands).
 #include <math.h>
 
 #include "common.cuh"
@@ -115,6 +121,13 @@ static Gemm gemm0() {
   return g;
 }
 
+static TcGemm tc0() {
+  TcGemm g;
+  memset(&g, 0, sizeof(g));
+  g.alpha = 1.f;
+  return g;
+}
+
 static int run_gemm(const Gemm& g, cudaStream_t st) {
   if (g.M <= 0 || g.N <= 0 || g.batch <= 0) return ATLAS_OK;
   dim3 grid((g.N + GT - 1) / GT, (g.M + GT - 1) / GT, g.batch);
@@ -128,6 +141,9 @@ struct MlpWs {
   long Kw, Vw, E, Qc, H, Gp, Dl, ta, te, tb, U, W, P1, P2, Zq, Gq, Ew, Eu, Dw, Du, X, T1, T2,
       A, nrm, per_head;
   long S;  // S buffer (all heads), when the caller gives none
+  // Newton-Schulz, all (head, token) instances of a chunk: S_n / NS iterate,
+  // the second iterate, Gram and its square, and the readout products.
+  long nsX, nsT, nsA, nsA2, nsP, nsR;
   size_t bytes;
 };
 
@@ -165,6 +181,16 @@ static MlpWs mlp_layout(const MlpArgs& a) {
   w.per_head = o;
   w.S = o * a.heads;
   long total = w.S + (a.S ? 0 : (long)a.heads * 2 * d * dh);
+  w.nsX = w.nsT = w.nsA = w.nsA2 = w.nsP = w.nsR = 0;
+  if (a.ns_steps > 0) {
+    const long inst = (long)a.heads * b, state = 2 * d * dh;
+    w.nsX = total; total += inst * state;
+    w.nsT = total; total += inst * state;
+    w.nsA = total; total += inst * 2 * small * small;
+    w.nsA2 = total; total += inst * 2 * small * small;
+    w.nsP = total; total += inst * dh * b;
+    w.nsR = total; total += inst * d * b;
+  }
   w.bytes = (size_t)total * sizeof(float);
   return w;
 }
@@ -297,6 +323,84 @@ __global__ void ns_apply_kernel(float* M, long state, long off, long n, const fl
     m[x] = keep * m[x] + xs[x];
 }
 
+// X[inst][block] = S[inst][block] / (||S[inst][block]||_F + eps), in place; one
+// CTA per (instance, block).
+__global__ void ns_normalize_kernel(float* X, long state, long half, float eps) {
+  float* x = X + (long)blockIdx.x * state + (long)blockIdx.y * half;
+  __shared__ float red[256];
+  float acc = 0.f;
+  for (long i = threadIdx.x; i < half; i += blockDim.x) acc += x[i] * x[i];
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int o = 128; o > 0; o >>= 1) {
+    if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
+    __syncthreads();
+  }
+  const float inv = 1.f / (sqrtf(red[0]) + eps);
+  for (long i = threadIdx.x; i < half; i += blockDim.x) x[i] *= inv;
+}
+
+// S_n = eps_n S0 for the nb instances of every head (the window term is added
+// by the batched product).
+__global__ void ns_fill_kernel(float* Sn, const float* S0, long state, const float* ws,
+                               long per_head, long te, int nb) {
+  const int inst = blockIdx.y, h = inst / nb, n = inst % nb;
+  const float e = ws[h * per_head + te + n];
+  const float* s0 = S0 + h * state;
+  float* out = Sn + (long)inst * state;
+  for (long x = blockIdx.x * blockDim.x + threadIdx.x; x < state;
+       x += (long)gridDim.x * blockDim.x)
+    out[x] = e * s0[x];
+}
+
+// out[h][row][col] = S_{nb-1} of head h (the momentum carried to the next chunk).
+__global__ void ns_copy_last_kernel(float* S, const float* Sn, long state, int nb) {
+  const int h = blockIdx.y;
+  const float* src = Sn + ((long)h * nb + nb - 1) * state;
+  for (long x = blockIdx.x * blockDim.x + threadIdx.x; x < state;
+       x += (long)gridDim.x * blockDim.x)
+    S[h * state + x] = src[x];
+}
+
+// out[h][n][j] (row stride ld) += sum_{m<=n} r[n,m] Pm[h][m][j][n] with
+// r[n,m] = prod_{l=m+1..n} (1 - alpha_l); then optionally GELU.
+__global__ void ns_readout_add_kernel(float* out, long out_head, long ld, const float* P,
+                                      int rows, int nb, const float* alpha, long N, int t0,
+                                      int gelu) {
+  const int h = blockIdx.y;
+  const long per = (long)rows * nb;
+  for (long x = blockIdx.x * blockDim.x + threadIdx.x; x < per;
+       x += (long)gridDim.x * blockDim.x) {
+    const int n = (int)(x / rows), j = (int)(x % rows);
+    const float* ph = P + (long)h * nb * per;
+    float acc = 0.f, r = 1.f;
+    for (int m = n; m >= 0; --m) {
+      acc += r * ph[(long)m * per + (long)j * nb + n];
+      r *= 1.f - alpha[(long)h * N + t0 + m];
+    }
+    float* o = out + h * out_head + (long)n * ld + j;
+    float v = *o + acc;
+    if (gelu) v = 0.5f * v * (1.f + erff(v * 0.70710678118654752f));
+    *o = v;
+  }
+}
+
+// M[h] = a_L M[h] + sum_m r[L,m] N_m (L = nb - 1), both weight blocks.
+__global__ void ns_state_kernel(float* M, long state, const float* X, int nb, const float* ws,
+                                long per_head, long ta, const float* alpha, long N, int t0) {
+  const int h = blockIdx.y;
+  const float aL = ws[h * per_head + ta + nb - 1];
+  for (long x = blockIdx.x * blockDim.x + threadIdx.x; x < state;
+       x += (long)gridDim.x * blockDim.x) {
+    float acc = 0.f, r = 1.f;
+    for (int m = nb - 1; m >= 0; --m) {
+      acc += r * X[((long)h * nb + m) * state + x];
+      r *= 1.f - alpha[(long)h * N + t0 + m];
+    }
+    M[h * state + x] = aL * M[h * state + x] + acc;
+  }
+}
+
 // ------------------------------------------------------------- host driver
 
 static dim3 ew_grid(long n, int heads) {
@@ -317,10 +421,7 @@ static dim3 ew_grid(long n, int heads) {
 
 long mlp_simt_launch_count(const MlpArgs& a) {
   const long chunks = (a.N + a.b - 1) / a.b;
-  if (a.ns_steps > 0) {
-    const long per_tok = 1 + 2 * (1 + 3L * a.ns_steps + a.ns_steps + 1) + 1 + 1 + 1;
-    return 1 + chunks * 4 + (long)a.N * per_tok;
-  }
+  if (a.ns_steps > 0) return 1 + chunks * (17 + 6L * a.ns_steps);
   return 1 + chunks * (4 + 1 + 3 + 1 + 4 + 4 + 1 + 4);
 }
 
@@ -459,71 +560,126 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
       continue;
     }
 
-    // Newton-Schulz momentum: token by token inside the chunk
-    for (int n = 0; n < nb; ++n) {
-      const int t = t0 + n;
-      ns_momentum_kernel<<<ew_grid(state, H), 256, 0, st>>>(p, w, ws, t, i0);
+    // Newton-Schulz momentum: every S_n of the chunk, then NS on all of them
+    {
+      const long sq = d < dh ? (long)d * d : (long)dh * dh;  // Gram of the short side
+      const long inst = (long)H * nb;
+      float* X = ws + w.nsX;
+      float* T = ws + w.nsT;
+      float* Ag = ws + w.nsA;
+      float* A2 = ws + w.nsA2;
+      // S_n = eps_n S0 - 2 sum_i U[n,i] [e_i h_i^T | delta_i k_i^T]
+      ns_fill_kernel<<<dim3(64, (unsigned)inst), 256, 0, st>>>(X, p.S, state, ws, PH, w.te, nb);
       CL();
-      for (int blk = 0; blk < 2; ++blk) {
-        const int rows = blk == 0 ? (int)d : (int)dh;
-        const int cols = blk == 0 ? (int)dh : (int)d;
-        const long off = blk == 0 ? 0 : half;
-        const long nel = (long)rows * cols;
-        ns_init_kernel<<<H, 256, 0, st>>>(p.S, state, off, nel, p.ns_eps, ws, PH, w.X);
-        CL();
-        for (int it = 0; it < p.ns_steps; ++it) {
-          const bool wide = rows <= cols;
-          const int sm = wide ? rows : cols;
-          // Gram of the short side
-          g = gemm0();
-          g.batch = H; g.M = sm; g.N = sm; g.K = wide ? cols : rows;
-          g.A = ws + w.X; g.sAb = PH;
-          g.B = ws + w.X; g.sBb = PH;
-          if (wide) { g.sAm = cols; g.sAk = 1; g.sBk = 1; g.sBn = cols; }
-          else { g.sAm = 1; g.sAk = cols; g.sBk = cols; g.sBn = 1; }
-          g.C = ws + w.A; g.sCb = PH; g.sCm = sm; g.sCn = 1;
-          CK(run_gemm(g, st));
-          // T1 = A X (wide) or X A (tall); T2 = A T1 or T1 A
-          for (int pass = 0; pass < 2; ++pass) {
-            const long src = pass == 0 ? w.X : w.T1;
-            const long dst = pass == 0 ? w.T1 : w.T2;
-            g = gemm0();
-            g.batch = H; g.M = rows; g.N = cols; g.K = sm;
-            if (wide) {
-              g.A = ws + w.A; g.sAb = PH; g.sAm = sm; g.sAk = 1;
-              g.B = ws + src; g.sBb = PH; g.sBk = cols; g.sBn = 1;
-            } else {
-              g.A = ws + src; g.sAb = PH; g.sAm = cols; g.sAk = 1;
-              g.B = ws + w.A; g.sBb = PH; g.sBk = sm; g.sBn = 1;
-            }
-            g.C = ws + dst; g.sCb = PH; g.sCm = cols; g.sCn = 1;
-            CK(run_gemm(g, st));
-          }
-          ns_combine_kernel<<<ew_grid(nel, H), 256, 0, st>>>(ws, PH, w.X, w.T1, w.T2, nel,
-                                                              p.ns_a, p.ns_b, p.ns_c);
-          CL();
-        }
-        ns_apply_kernel<<<ew_grid(nel, H), 256, 0, st>>>(p.M, state, off, nel, p.alpha, p.N, t,
-                                                           ws, PH, w.X);
-        CL();
+      {  // instances (h, n): batch h * nb + n, per-head operands shared over n
+        TcGemm t = tc0();
+        t.batch = (int)inst; t.bdiv = nb; t.M = (int)d; t.N = (int)dh; t.K = L;
+        t.A = ws + w.E; t.sAb = PH; t.sAm = 1; t.sAk = d;
+        t.B = ws + w.H; t.sBb = PH; t.sBk = dh; t.sBn = 1;
+        t.kscale = ws + w.U; t.sKb = PH; t.sKb2 = L;
+        t.C = X; t.sCb = (long)nb * state; t.sCb2 = state; t.sCm = dh; t.sCn = 1;
+        t.alpha = -2.f; t.accumulate = 1;
+        CK(tc_gemm_launch(t, st));
+        t.M = (int)dh; t.N = (int)d;
+        t.A = ws + w.Dl; t.sAm = 1; t.sAk = dh;
+        t.B = ws + w.Kw; t.sBk = d; t.sBn = 1;
+        t.C = X + half; t.sCm = d;
+        CK(tc_gemm_launch(t, st));
       }
-      // y_t = q_t + W1 GELU(W2 q_t)
+      ns_copy_last_kernel<<<ew_grid(state, H), 256, 0, st>>>(p.S, X, state, nb);
+      CL();
+      // N_n = NS(S_n), per weight block; X0 = S / (||S|| + eps)
+      ns_normalize_kernel<<<dim3((unsigned)inst, 2), 256, 0, st>>>(X, state, half, p.ns_eps);
+      CL();
+      for (int it = 0; it < p.ns_steps; ++it) {
+        for (int blk = 0; blk < 2; ++blk) {
+          // block 0: W1 (d x dh); block 1: W2 (dh x d); Gram of the short side
+          const long rows = blk == 0 ? d : dh, cols = blk == 0 ? dh : d;
+          const bool wide = rows <= cols;
+          const long sm = wide ? rows : cols;
+          const long off = blk == 0 ? 0 : half, aoff = blk * sq;
+          TcGemm g1 = tc0();  // G = X X^T (wide) or X^T X (tall)
+          g1.batch = (int)inst; g1.M = (int)sm; g1.N = (int)sm; g1.K = (int)(wide ? cols : rows);
+          g1.A = X + off; g1.sAb = state;
+          g1.B = X + off; g1.sBb = state;
+          if (wide) { g1.sAm = cols; g1.sAk = 1; g1.sBk = 1; g1.sBn = cols; }
+          else { g1.sAm = 1; g1.sAk = cols; g1.sBk = cols; g1.sBn = 1; }
+          g1.C = Ag + aoff; g1.sCb = 2 * sq; g1.sCm = sm; g1.sCn = 1;
+          g1.symmetric = sm == 128;  // both operands are the same tile of X
+          CK(tc_gemm_launch(g1, st));
+          TcGemm g2 = tc0();  // b G + c G^2
+          g2.batch = (int)inst; g2.M = (int)sm; g2.N = (int)sm; g2.K = (int)sm;  // G^2
+          g2.A = Ag + aoff; g2.sAb = 2 * sq; g2.sAm = sm; g2.sAk = 1;
+          g2.B = Ag + aoff; g2.sBb = 2 * sq; g2.sBk = sm; g2.sBn = 1;
+          g2.C = A2 + aoff; g2.sCb = 2 * sq; g2.sCm = sm; g2.sCn = 1;
+          g2.alpha = p.ns_c;  // b G + c G^2
+          g2.D = Ag + aoff; g2.sDb = 2 * sq; g2.sDm = sm; g2.sDn = 1; g2.beta = p.ns_b;
+          CK(tc_gemm_launch(g2, st));
+          // T = a X + (b G + c G^2) X  (wide)  or  a X + X (b G + c G^2)  (tall)
+          TcGemm g3 = tc0();
+          g3.batch = (int)inst; g3.M = (int)rows; g3.N = (int)cols;
+          g3.C = T + off; g3.sCb = state; g3.sCm = cols; g3.sCn = 1;
+          g3.D = X + off; g3.sDb = state; g3.sDm = cols; g3.sDn = 1; g3.beta = p.ns_a;
+          if (wide) {
+            g3.K = (int)rows;
+            g3.A = A2 + aoff; g3.sAb = 2 * sq; g3.sAm = sm; g3.sAk = 1;
+            g3.B = X + off; g3.sBb = state; g3.sBk = cols; g3.sBn = 1;
+          } else {
+            g3.K = (int)cols;
+            g3.A = X + off; g3.sAb = state; g3.sAm = cols; g3.sAk = 1;
+            g3.B = A2 + aoff; g3.sBb = 2 * sq; g3.sBk = sm; g3.sBn = 1;
+          }
+          CK(tc_gemm_launch(g3, st));
+        }
+        float* tmp = X; X = T; T = tmp;
+      }
+      // readout: zq_n = a_n W2_0 q_n + sum_{m<=n} r[n,m] N2_m q_n -> GELU
       g = gemm0();
-      g.batch = H; g.M = 1; g.N = (int)dh; g.K = (int)d;
-      g.A = ws + w.Qc + (long)n * d; g.sAb = PH; g.sAm = d; g.sAk = 1;
+      g.batch = H; g.M = nb; g.N = (int)dh; g.K = (int)d;
+      g.A = ws + w.Qc; g.sAb = PH; g.sAm = d; g.sAk = 1;
       g.B = W2; g.sBb = state; g.sBk = 1; g.sBn = d;
+      g.rowscale = ws + w.ta; g.sRb = PH;
       g.C = ws + w.Zq; g.sCb = PH; g.sCm = dh; g.sCn = 1;
-      g.epi = 1;
       CK(run_gemm(g, st));
-      copy_q_kernel<<<H, 256, 0, st>>>(ws, PH, w.Qc, p.Y, p.N, (int)d, t0, n, n + 1);
+      float* P = ws + w.nsP;
+      float* R = ws + w.nsR;
+      {
+        TcGemm t = tc0();
+        t.batch = (int)inst; t.bdiv = nb; t.M = (int)dh; t.N = nb; t.K = (int)d;
+        t.A = X + half; t.sAb = (long)nb * state; t.sAb2 = state; t.sAm = d; t.sAk = 1;
+        t.B = ws + w.Qc; t.sBb = PH; t.sBk = 1; t.sBn = d;
+        t.C = P; t.sCb = (long)nb * dh * nb; t.sCb2 = dh * nb; t.sCm = nb; t.sCn = 1;
+        CK(tc_gemm_launch(t, st));
+      }
+      ns_readout_add_kernel<<<ew_grid((long)nb * dh, H), 256, 0, st>>>(
+          ws + w.Zq, PH, dh, P, (int)dh, nb, p.alpha, p.N, t0, 1);
+      CL();
+      // y_n = q_n + a_n W1_0 hq_n + sum_{m<=n} r[n,m] N1_m hq_n
+      copy_q_kernel<<<H, 256, 0, st>>>(ws, PH, w.Qc, p.Y, p.N, (int)d, t0, 0, nb);
       CL();
       g = gemm0();
-      g.batch = H; g.M = 1; g.N = (int)d; g.K = (int)dh;
+      g.batch = H; g.M = nb; g.N = (int)d; g.K = (int)dh;
       g.A = ws + w.Zq; g.sAb = PH; g.sAm = dh; g.sAk = 1;
       g.B = W1; g.sBb = state; g.sBk = 1; g.sBn = dh;
-      g.C = p.Y + (long)t * d; g.sCb = (long)p.N * d; g.sCm = d; g.sCn = 1;
+      g.rowscale = ws + w.ta; g.sRb = PH;
+      g.C = p.Y + (long)t0 * d; g.sCb = (long)p.N * d; g.sCm = d; g.sCn = 1;
       g.accumulate = 1;
       CK(run_gemm(g, st));
+      {
+        TcGemm t = tc0();
+        t.batch = (int)inst; t.bdiv = nb; t.M = (int)d; t.N = nb; t.K = (int)dh;
+        t.A = X; t.sAb = (long)nb * state; t.sAb2 = state; t.sAm = dh; t.sAk = 1;
+        t.B = ws + w.Zq; t.sBb = PH; t.sBk = 1; t.sBn = dh;
+        t.C = R; t.sCb = (long)nb * d * nb; t.sCb2 = d * nb; t.sCm = nb; t.sCn = 1;
+        CK(tc_gemm_launch(t, st));
+      }
+      ns_readout_add_kernel<<<ew_grid((long)nb * d, H), 256, 0, st>>>(
+          p.Y + (long)t0 * d, (long)p.N * d, d, R, (int)d, nb, p.alpha, p.N, t0, 0);
+      CL();
+      // M = a_L M0 + sum_m r[L,m] N_m (after the readout, which used M0)
+      ns_state_kernel<<<ew_grid(state, H), 256, 0, st>>>(p.M, state, X, nb, ws, PH, w.ta,
+                                                          p.alpha, p.N, t0);
+      CL();
     }
   }
   return ATLAS_OK;
