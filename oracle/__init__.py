@@ -36,7 +36,7 @@ class OrcCfg(ctypes.Structure):
         ("loss", ctypes.c_int), ("c", ctypes.c_int), ("b", ctypes.c_int),
         ("ns_steps", ctypes.c_int), ("ns_a", ctypes.c_double),
         ("ns_b", ctypes.c_double), ("ns_c", ctypes.c_double),
-        ("ns_eps", ctypes.c_double),
+        ("ns_eps", ctypes.c_double), ("n_history", ctypes.c_int),
     ]
 
 
@@ -96,10 +96,10 @@ def _f64(a) -> np.ndarray:
 
 
 def make_cfg(N, d_k, d_v, d_h=0, mem=MEM_LINEAR, phi=PHI_IDENTITY, loss=LOSS_L2, c=1, b=1,
-             ns_steps=0, ns_a=0.0, ns_b=0.0, ns_c=0.0, ns_eps=0.0) -> OrcCfg:
+             ns_steps=0, ns_a=0.0, ns_b=0.0, ns_c=0.0, ns_eps=0.0, n_history=0) -> OrcCfg:
     return OrcCfg(int(N), int(d_k), int(d_v), int(d_h), int(mem), int(phi), int(loss),
                   int(c), int(b), int(ns_steps), float(ns_a), float(ns_b), float(ns_c),
-                  float(ns_eps))
+                  float(ns_eps), int(n_history))
 
 
 def feature_dim(cfg: OrcCfg) -> int:
@@ -152,14 +152,16 @@ def forward(cfg: OrcCfg, K, Q, V, alpha, eta, theta, gamma, M0=None, S0=None,
             recurrent: bool = False, n_threads: int = 0):
     """Run the oracle over H independent heads.
 
-    K, Q: [H, N, d_k]; V: [H, N, d_v]; alpha, eta, theta: [H, N]; gamma: [c];
-    M0, S0: [H, state] or None (zeros).  Returns (Y [H, N, d_v], M [H, state],
-    S [H, state]), all fp64.
+    K: [H, n_history + N, d_k] and V: [H, n_history + N, d_v] (the history rows
+    first: they only enter windows); Q: [H, N, d_k]; alpha, eta, theta: [H, N];
+    gamma: [c]; M0, S0: [H, state] or None (zeros).  Returns (Y [H, N, d_v],
+    M [H, state], S [H, state]), all fp64.
     """
     K, Q, V = _f64(K), _f64(Q), _f64(V)
     H = K.shape[0]
-    assert K.shape == (H, cfg.N, cfg.d_k) and Q.shape == K.shape
-    assert V.shape == (H, cfg.N, cfg.d_v)
+    nkv = cfg.N + cfg.n_history
+    assert K.shape == (H, nkv, cfg.d_k) and Q.shape == (H, cfg.N, cfg.d_k)
+    assert V.shape == (H, nkv, cfg.d_v)
     alpha, eta, theta = _f64(alpha), _f64(eta), _f64(theta)
     assert alpha.shape == (H, cfg.N) and eta.shape == alpha.shape and theta.shape == alpha.shape
     gamma = _f64(gamma)

@@ -72,6 +72,8 @@ typedef struct {
   int b;        /* chunk length, >= 1 (1 = token recurrence) */
   int ns_steps; /* Newton-Schulz iterations on the momentum, 0 = none */
   double ns_a, ns_b, ns_c, ns_eps;
+  int n_history; /* tokens before the first processed one: K, V rows that only
+                    enter the windows of processed tokens (they update nothing) */
 } orc_cfg;
 
 /* ------------------------------------------------------------------ sizes */
@@ -306,15 +308,16 @@ static void orc_head_chunked(const orc_cfg* g, const double* K, const double* Q,
   double* gsum = (double*)malloc(sizeof(double) * n);
   double* Gi = (double*)malloc(sizeof(double) * n);
   double* upd = (double*)malloc(sizeof(double) * n);
-  int dk = g->d_k, dv = g->d_v;
+  int dk = g->d_k, dv = g->d_v, nh = g->n_history;
+  /* K, V rows: token i (from -nh) is row i + nh */
   for (int t0 = 0; t0 < g->N; t0 += g->b) {
     memcpy(M0, M, sizeof(double) * n);
     int t1 = t0 + g->b < g->N ? t0 + g->b : g->N;
     for (int t = t0; t < t1; ++t) {
       for (long j = 0; j < n; ++j) gsum[j] = 0.0;
-      int i0 = t - g->c + 1 < 0 ? 0 : t - g->c + 1;
+      int i0 = t - g->c + 1 < -nh ? -nh : t - g->c + 1;
       for (int i = i0; i <= t; ++i) {
-        orc_grad(g, M0, K + (long)i * dk, V + (long)i * dv, Gi);
+        orc_grad(g, M0, K + (long)(i + nh) * dk, V + (long)(i + nh) * dv, Gi);
         double w = gamma[t - i];
         for (long j = 0; j < n; ++j) gsum[j] += w * Gi[j];
       }
@@ -339,12 +342,12 @@ static void orc_head_recurrent(const orc_cfg* g, const double* K, const double* 
   double* gsum = (double*)malloc(sizeof(double) * n);
   double* Gi = (double*)malloc(sizeof(double) * n);
   double* upd = (double*)malloc(sizeof(double) * n);
-  int dk = g->d_k, dv = g->d_v;
+  int dk = g->d_k, dv = g->d_v, nh = g->n_history;
   for (int t = 0; t < g->N; ++t) {
     for (long j = 0; j < n; ++j) gsum[j] = 0.0;
-    for (int lag = 0; lag < g->c && t - lag >= 0; ++lag) {
+    for (int lag = 0; lag < g->c && t - lag >= -nh; ++lag) {
       int i = t - lag;
-      orc_grad(g, M, K + (long)i * dk, V + (long)i * dv, Gi);
+      orc_grad(g, M, K + (long)(i + nh) * dk, V + (long)(i + nh) * dv, Gi);
       for (long j = 0; j < n; ++j) gsum[j] += gamma[lag] * Gi[j];
     }
     orc_token_step(g, alpha[t], eta[t], theta[t], gsum, Q + (long)t * dk, M, S, upd,
@@ -370,9 +373,10 @@ static void* orc_worker(void* p) {
   const orc_cfg* g = j->g;
   long ns = orc_state_size(g);
   for (int h = j->h0; h < j->h1; ++h) {
-    const double* K = j->K + (long)h * g->N * g->d_k;
+    const long nkv = (long)g->N + g->n_history;
+    const double* K = j->K + (long)h * nkv * g->d_k;
     const double* Q = j->Q + (long)h * g->N * g->d_k;
-    const double* V = j->V + (long)h * g->N * g->d_v;
+    const double* V = j->V + (long)h * nkv * g->d_v;
     const double* a = j->alpha + (long)h * g->N;
     const double* e = j->eta + (long)h * g->N;
     const double* th = j->theta + (long)h * g->N;
@@ -389,6 +393,7 @@ static void* orc_worker(void* p) {
 
 static int orc_check(const orc_cfg* g) {
   if (g->N < 0 || g->d_k <= 0 || g->d_v <= 0 || g->c < 1 || g->b < 1) return -1;
+  if (g->n_history < 0) return -1;
   if (g->mem == ORC_MEM_MLP && (g->d_h <= 0 || g->d_k != g->d_v)) return -1;
   if (g->mem != ORC_MEM_LINEAR && g->mem != ORC_MEM_MLP) return -1;
   if (g->loss != ORC_LOSS_L2 && g->loss != ORC_LOSS_DOT) return -1;
@@ -418,8 +423,9 @@ static int orc_run(const orc_cfg* g, int recurrent, int n_heads, const double* K
   return 0;
 }
 
-/* Chunked forward over n_heads independent heads.  K, Q: [heads, N, d_k];
- * V: [heads, N, d_v]; alpha, eta, theta: [heads, N]; gamma: [c] by lag;
+/* Chunked forward over n_heads independent heads.  K: [heads, n_history + N, d_k]
+ * and V: [heads, n_history + N, d_v] (history rows first); Q: [heads, N, d_k];
+ * alpha, eta, theta: [heads, N]; gamma: [c] by lag;
  * M, S: [heads, state] in/out (state layout: linear M is d_v x D row-major;
  * MLP is W1 (d x d_h) then W2 (d_h x d)); Y: [heads, N, d_v] out.
  * Returns 0, or -1 on an invalid description. */

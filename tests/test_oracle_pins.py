@@ -462,3 +462,68 @@ def test_empty_sequence():
     Y, M, S = run(cfg, z3, z3, z3, z, z, z, np.ones(2), M0=M0)
     assert Y.shape == (2, 0, 3)
     np.testing.assert_array_equal(M, M0)
+
+
+# ---------------------------------------------------------------- history rows
+
+def _split_run(cfg_kw, K, Q, V, a, e, t, gamma, T, M0=None):
+    """One call over tokens [0, T) and a second over [T, N) whose K, V carry the
+    last c - 1 tokens of the first part as history, M and S handed over."""
+    N, c = K.shape[1], cfg_kw["c"]
+    d_k, d_v = K.shape[2], V.shape[2]
+    c1 = oracle.make_cfg(T, d_k, d_v, **cfg_kw)
+    Y1, M1, S1 = oracle.forward(c1, K[:, :T], Q[:, :T], V[:, :T], a[:, :T], e[:, :T], t[:, :T],
+                                gamma, M0=M0)
+    nh = min(c - 1, T)
+    c2 = oracle.make_cfg(N - T, d_k, d_v, n_history=nh, **cfg_kw)
+    Y2, M2, S2 = oracle.forward(c2, K[:, T - nh:], Q[:, T:], V[:, T - nh:], a[:, T:], e[:, T:],
+                                t[:, T:], gamma, M0=M1, S0=S1)
+    return np.concatenate([Y1, Y2], axis=1), M2, S2
+
+
+@pytest.mark.parametrize("kw,T", [
+    (dict(c=4, b=1), 7),                                          # exact recurrence
+    (dict(c=5, b=8), 16),                                         # chunked, split on a chunk edge
+    (dict(c=12, b=4, phi=oracle.PHI_POLY2), 8),                   # window longer than both parts' chunk
+    (dict(c=3, b=4, mem=oracle.MEM_MLP, d_h=6), 8),               # MLP memory
+    (dict(c=3, b=2, mem=oracle.MEM_MLP, d_h=6, ns_steps=3, ns_a=3.4445, ns_b=-4.775,
+          ns_c=2.0315, ns_eps=1e-7), 6),                          # Newton-Schulz momentum
+])
+def test_history_rows_make_a_split_call_exact(kw, T):
+    """Tokens only enter later windows through history rows: a sequence split on a
+    chunk boundary into two calls, the second carrying the first part's last c - 1
+    keys and values as history and its state, reproduces one call over all of it."""
+    rng = np.random.default_rng(3)
+    d_k = 3 if kw.get("phi") == oracle.PHI_POLY2 else 4
+    d_v = d_k if kw.get("mem") == oracle.MEM_MLP else 3
+    N = T + 9
+    K, Q, V, a, e, t = rand_inputs(rng, 2, N, d_k, d_v)
+    gamma = np.exp(-np.arange(kw["c"]) / 3.0)
+    M0 = None
+    if kw.get("mem") == oracle.MEM_MLP:
+        M0 = rng.standard_normal((2, 2 * d_k * kw["d_h"])) * 0.3
+    Yf, Mf, Sf = oracle.forward(oracle.make_cfg(N, d_k, d_v, **kw), K, Q, V, a, e, t, gamma, M0=M0)
+    Ys, Ms, Ss = _split_run(kw, K, Q, V, a, e, t, gamma, T, M0=M0)
+    np.testing.assert_allclose(Ys, Yf, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(Ms, Mf, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(Ss, Sf, rtol=1e-10, atol=1e-12)
+
+
+def test_history_beyond_the_window_is_ignored():
+    rng = np.random.default_rng(4)
+    K, Q, V, a, e, t = rand_inputs(rng, 1, 20, 4, 3)
+    gamma = np.ones(4)
+    kw = dict(c=4, b=2)
+    c3 = oracle.make_cfg(10, 4, 3, n_history=3, **kw)
+    c9 = oracle.make_cfg(10, 4, 3, n_history=9, **kw)
+    Y3, M3, S3 = oracle.forward(c3, K[:, 7:], Q[:, 10:], V[:, 7:], a[:, 10:], e[:, 10:], t[:, 10:],
+                                gamma)
+    Y9, M9, S9 = oracle.forward(c9, K[:, 1:], Q[:, 10:], V[:, 1:], a[:, 10:], e[:, 10:], t[:, 10:],
+                                gamma)
+    np.testing.assert_array_equal(Y3, Y9)
+    np.testing.assert_array_equal(M3, M9)
+    # and a history row inside the window does change the result
+    c0 = oracle.make_cfg(10, 4, 3, **kw)
+    Y0, _, _ = oracle.forward(c0, K[:, 10:], Q[:, 10:], V[:, 10:], a[:, 10:], e[:, 10:], t[:, 10:],
+                              gamma)
+    assert np.abs(Y0 - Y3).max() > 1e-3
