@@ -81,6 +81,12 @@ typedef struct atlas_mem_cfg {
   int in_dtype;       /* ATLAS_F32 or ATLAS_BF16 for K, Q, V */
   float* S_state;     /* optional device momentum [B,H,state] in/out; NULL = start
                          from zero and do not return it */
+  int n_history;      /* >= 0: K and V hold n_history + N rows per head, history
+                         first.  History rows only enter the windows of the N
+                         processed tokens (they update nothing and have no output),
+                         so a sequence split on a chunk boundary into two calls --
+                         the second given the first part's last c - 1 keys and
+                         values as history, and its M and S -- equals one call. */
   void* workspace;    /* device scratch of at least atlas_mem_workspace_bytes() */
   size_t workspace_bytes;
   int* status_dev;    /* optional device int; set to ATLAS_ERR_TIMEOUT by a kernel
@@ -95,9 +101,10 @@ size_t atlas_mem_state_size(const atlas_mem_cfg* cfg);
  * (may be 0).  (size_t)-1 for an invalid description. */
 size_t atlas_mem_workspace_bytes(const atlas_mem_cfg* cfg);
 
-/* The chunked memory update over all B*H heads.
- *   K, Q   [B,H,N,d_k]  keys, queries (fp32 or bf16 per cfg->in_dtype)
- *   V      [B,H,N,d_v]  values (same type)
+/* The chunked memory update over all B*H heads (nh = cfg->n_history).
+ *   K      [B,H,nh+N,d_k] keys (fp32 or bf16 per cfg->in_dtype), history rows first
+ *   Q      [B,H,N,d_k]  queries (same type)
+ *   V      [B,H,nh+N,d_v] values (same type), history rows first
  *   alpha, eta, theta [B,H,N] fp32 per-token decay, momentum and step gates
  *   gamma  [c] fp32     window weight by lag: gamma[j] weighs token t-j in l_t
  *   Y      [B,H,N,d_v]  fp32 out: y_t = M_t(Phi(q_t))

@@ -37,7 +37,7 @@ class AtlasMemCfg(ctypes.Structure):
         ("ns_steps", ctypes.c_int), ("ns_a", ctypes.c_float), ("ns_b", ctypes.c_float),
         ("ns_c", ctypes.c_float), ("ns_eps", ctypes.c_float),
         ("in_dtype", ctypes.c_int),
-        ("S_state", ctypes.c_void_p),
+        ("S_state", ctypes.c_void_p), ("n_history", ctypes.c_int),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("status_dev", ctypes.c_void_p),
     ]
@@ -85,11 +85,12 @@ def load_library(path: str = LIB_PATH):
 
 def make_cfg(B, H, N, d_k, d_v, d_h=0, mem=MEM_LINEAR, phi=PHI_IDENTITY, loss=LOSS_L2, c=1,
              b=1, ns_steps=0, ns_a=0.0, ns_b=0.0, ns_c=0.0, ns_eps=0.0, in_dtype=BF16,
-             S_state=None, workspace=None, workspace_bytes=0, status_dev=None) -> AtlasMemCfg:
+             S_state=None, workspace=None, workspace_bytes=0, status_dev=None,
+             n_history=0) -> AtlasMemCfg:
     return AtlasMemCfg(int(B), int(H), int(N), int(d_k), int(d_v), int(d_h), int(mem), int(phi),
                        int(loss), int(c), int(b), int(ns_steps), float(ns_a), float(ns_b),
-                       float(ns_c), float(ns_eps), int(in_dtype), _ptr(S_state), _ptr(workspace),
-                       int(workspace_bytes), _ptr(status_dev))
+                       float(ns_c), float(ns_eps), int(in_dtype), _ptr(S_state), int(n_history),
+                       _ptr(workspace), int(workspace_bytes), _ptr(status_dev))
 
 
 def _ptr(t):

@@ -29,7 +29,7 @@ int check_cfg(const atlas_mem_cfg* c) {
   if (c->phi != ATLAS_PHI_IDENTITY && c->phi != ATLAS_PHI_POLY2) return ATLAS_ERR_INVALID;
   if (c->loss != ATLAS_LOSS_L2 && c->loss != ATLAS_LOSS_DOT) return ATLAS_ERR_INVALID;
   if (c->in_dtype != ATLAS_F32 && c->in_dtype != ATLAS_BF16) return ATLAS_ERR_INVALID;
-  if (c->ns_steps < 0) return ATLAS_ERR_INVALID;
+  if (c->ns_steps < 0 || c->n_history < 0) return ATLAS_ERR_INVALID;
   if ((long)c->B * c->H > 65535L * 1024) return ATLAS_ERR_UNSUPPORTED;
   if (c->mem == ATLAS_MEM_MLP) {
     if (c->d_h <= 0 || c->d_k != c->d_v) return ATLAS_ERR_INVALID;
@@ -54,6 +54,7 @@ LinArgs lin_args(const void* K, const void* Q, const void* V, const float* alpha
   a.poly = c->phi == ATLAS_PHI_POLY2;
   a.dot = c->loss == ATLAS_LOSS_DOT;
   a.bf16 = c->in_dtype == ATLAS_BF16;
+  a.nh = c->n_history;
   return a;
 }
 
@@ -65,6 +66,7 @@ MlpArgs mlp_args(const void* K, const void* Q, const void* V, const float* alpha
   a.alpha = alpha; a.eta = eta; a.theta = theta; a.gamma = gamma;
   a.Y = Y; a.M = M; a.S = c->S_state;
   a.heads = c->B * c->H; a.N = c->N; a.d = c->d_k; a.dh = c->d_h; a.c = c->c; a.b = c->b;
+  a.nh = c->n_history;
   a.bf16 = c->in_dtype == ATLAS_BF16;
   a.ns_steps = c->ns_steps;
   a.ns_a = c->ns_a; a.ns_b = c->ns_b; a.ns_c = c->ns_c; a.ns_eps = c->ns_eps;
@@ -78,11 +80,13 @@ Path choose_path(const atlas_mem_cfg* c) {
   if (c->mem == ATLAS_MEM_MLP) {
     MlpArgs m = mlp_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, c,
                          nullptr, nullptr);
-    return mlp_tc_supported(m) ? PATH_MLP_TC : PATH_MLP_SIMT;
+    // the tensor-core kernels take no history rows (with c = 1 they would not matter,
+    // but the K / V strides would): such calls go to the CUDA-core path
+    return (m.nh == 0 && mlp_tc_supported(m)) ? PATH_MLP_TC : PATH_MLP_SIMT;
   }
   LinArgs a = lin_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, c,
                        nullptr, nullptr);
-  if (linear_tc_supported(a)) return PATH_LINEAR_TC;
+  if (a.nh == 0 && linear_tc_supported(a)) return PATH_LINEAR_TC;
   if (linear_seq_supported(a)) return PATH_LINEAR_SEQ;
   int RV;
   size_t smem;

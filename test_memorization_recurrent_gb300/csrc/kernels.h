@@ -19,6 +19,7 @@ struct LinArgs {
   float* S;  // [heads, d_v, D] in/out, or nullptr (start at zero, not returned)
   int N, d_k, d_v, D, c, b;
   int poly, dot, bf16;
+  int nh;  // history rows ahead of token 0 in K and V (head stride (nh + N) rows)
 };
 
 int linear_simt_launch(const LinArgs& a, int heads, cudaStream_t st);
@@ -78,6 +79,7 @@ struct MlpArgs {
   float* M;  // [heads, W1 (d x dh) | W2 (dh x d)] in/out
   float* S;  // same layout, in/out (caller's or workspace)
   int heads, N, d, dh, c, b;
+  int nh;  // history rows ahead of token 0 in K and V
   int bf16;
   int ns_steps;
   float ns_a, ns_b, ns_c, ns_eps;

@@ -13,7 +13,7 @@
 //   S[r,:] = eta_t S[r,:] - 2 theta_t sum_j gamma_j e_j[r] k_{t-j}
 //   M[r,:] = (1 - alpha_t) M[r,:] + S[r,:],      y_t[r] = M[r,:] . q_t
 // where M0 is the state at the start of t's chunk (M itself when b = 1) and
-// window tokens before 0 are absent.  The window's row dot products are a
+// window tokens before the history rows (token -n_history) are absent.  The window's row dot products are a
 // four-term in-register sum plus three shuffle levels; the readout's eight
 // per-lane shares go to shared memory and are summed once per tile, off the
 // token-to-token dependency chain.  K, Q, the CTA's V rows and the
@@ -82,7 +82,10 @@ __global__ void __launch_bounds__(kThr) linear_seq_kernel(LinArgs p) {
   const int r = r0 + rl, cg = lane & 7;   // columns 4cg .. 4cg+3
   const int dv = p.d_v, N = p.N;
   const bool row_ok = r < dv;
-  const long kb = (long)head * N * 32, vb = (long)head * N * dv, gb = (long)head * N;
+  // K, V: head stride (nh + N) rows with token 0 at row nh; Q, Y, gates: N rows
+  const int nh = p.nh;
+  const long kb = ((long)head * (N + nh) + nh) * 32, vb = ((long)head * (N + nh) + nh) * dv;
+  const long qb = (long)head * N * 32, yb = (long)head * N * dv, gb = (long)head * N;
   float* Mrow = p.M + ((long)head * dv + r) * 32 + 4 * cg;
   float* Srow = p.S ? p.S + ((long)head * dv + r) * 32 + 4 * cg : nullptr;
   // the dot loss has no state term in its error: fold that into the copy of M0
@@ -105,7 +108,7 @@ __global__ void __launch_bounds__(kThr) linear_seq_kernel(LinArgs p) {
     for (int x = 0; x < kKPer; ++x) {
       const int e = x * kThr + tid, t = t0 + e / 32;
       pk[x] = t < N ? ld_in(p.K, kb + (long)t * 32 + (e & 31), p.bf16) : 0.f;
-      pq[x] = t < N ? ld_in(p.Q, kb + (long)t * 32 + (e & 31), p.bf16) : 0.f;
+      pq[x] = t < N ? ld_in(p.Q, qb + (long)t * 32 + (e & 31), p.bf16) : 0.f;
     }
 #pragma unroll
     for (int x = 0; x < kVPer; ++x) {
@@ -138,9 +141,16 @@ __global__ void __launch_bounds__(kThr) linear_seq_kernel(LinArgs p) {
     }
   };
 
-  // window history of the first tile: no tokens before 0
-  for (int e = tid; e < (C - 1) * 32; e += kThr) sm.K[e / 32][e & 31] = 0.f;
-  for (int e = tid; e < (C - 1) * kRows; e += kThr) sm.V[e / kRows][e % kRows] = 0.f;
+  // window history of the first tile: the history rows, absent before -nh
+  for (int e = tid; e < (C - 1) * 32; e += kThr) {
+    const int t = e / 32 - (C - 1);
+    sm.K[e / 32][e & 31] = t >= -nh ? ld_in(p.K, kb + (long)t * 32 + (e & 31), p.bf16) : 0.f;
+  }
+  for (int e = tid; e < (C - 1) * kRows; e += kThr) {
+    const int t = e / kRows - (C - 1), rr = r0 + e % kRows;
+    sm.V[e / kRows][e % kRows] =
+        (t >= -nh && rr < dv) ? ld_in(p.V, vb + (long)t * dv + rr, p.bf16) : 0.f;
+  }
   fetch(0);
   deposit();
   __syncthreads();
@@ -198,7 +208,7 @@ __global__ void __launch_bounds__(kThr) linear_seq_kernel(LinArgs p) {
       if (r0 + rr < dv) {
         const float4 a = *reinterpret_cast<const float4*>(&sm.Yp[u][rr][0]);
         const float4 b = *reinterpret_cast<const float4*>(&sm.Yp[u][rr][4]);
-        p.Y[vb + (long)(t0 + u) * dv + r0 + rr] = ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
+        p.Y[yb + (long)(t0 + u) * dv + r0 + rr] = ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
       }
     }
     __syncthreads();

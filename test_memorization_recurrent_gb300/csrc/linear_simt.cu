@@ -8,7 +8,7 @@
 // the chunks in order; no CTA ever waits on another.
 //
 // Per chunk of nb tokens starting at t0, with window tokens i0..t1-1 (L of them,
-// i0 = max(0, t0-c+1)) -- "논문 리뷰 Google ATLAS" §3.3 (gradients at the
+// i0 = max(-n_history, t0-c+1): history rows of K, V enter windows too) -- "논문 리뷰 Google ATLAS" §3.3 (gradients at the
 // chunk-start state), "[Paper Review] Titans 논문 이해하기" (momentum, decay,
 // readout after the write):
 //   E[i,r]  = M0[r,:] . Phi(k_i) - v_i[r]              (dot bias: -v_i[r])
@@ -115,17 +115,20 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
   const float* alpha = p.alpha + (long)head * p.N;
   const float* eta = p.eta + (long)head * p.N;
   const float* theta = p.theta + (long)head * p.N;
-  const long kbase = (long)head * p.N * dk;
-  const long vbase = (long)head * p.N * dv;
+  // K, V: head stride (nh + N) rows, token 0 at row nh; Q, Y: head stride N rows
+  const long kbase = ((long)head * (p.N + p.nh) + p.nh) * dk;
+  const long vbase = ((long)head * (p.N + p.nh) + p.nh) * dv;
+  const long qbase = (long)head * p.N * dk;
+  const long ybase = (long)head * p.N * dv;
 
   for (int t0 = 0; t0 < p.N; t0 += p.b) {
     const int t1 = min(p.N, t0 + p.b);
     const int nb = t1 - t0;
-    const int i0 = max(0, t0 - p.c + 1);
+    const int i0 = max(-p.nh, t0 - p.c + 1);
     const int Lw = t1 - i0;
     __syncthreads();
     for (int x = tid; x < Lw * dk; x += nt) Kw[x] = ld_in(p.K, kbase + (long)i0 * dk + x, p.bf16);
-    for (int x = tid; x < nb * dk; x += nt) Qc[x] = ld_in(p.Q, kbase + (long)t0 * dk + x, p.bf16);
+    for (int x = tid; x < nb * dk; x += nt) Qc[x] = ld_in(p.Q, qbase + (long)t0 * dk + x, p.bf16);
     for (int x = tid; x < Lw * rv; x += nt) {
       const int i = x / rv, r = x % rv;
       Vw[x] = ld_in(p.V, vbase + (long)(i0 + i) * dv + r0 + r, p.bf16);
@@ -183,7 +186,7 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
       }
       float acc = 0.f;
       for (int i = 0; i < Lw; ++i) acc += P[n * L.Lmax + i] * E[i * rv + r];
-      p.Y[vbase + (long)(t0 + n) * dv + r0 + r] = sa[n] * ym + sb[n] * ys - 2.f * acc;
+      p.Y[ybase + (long)(t0 + n) * dv + r0 + r] = sa[n] * ym + sb[n] * ys - 2.f * acc;
     }
     __syncthreads();
     // carry the state to the end of the chunk

@@ -204,7 +204,9 @@ __global__ void mlp_gather_kernel(MlpArgs p, MlpWs w, float* ws, int t0, int nb,
   const int h = blockIdx.x;
   float* base = ws + h * w.per_head;
   const int d = p.d;
-  const long kb = (long)h * p.N * d;
+  // K, V: head stride (nh + N) rows, token 0 at row nh (i0 may be negative)
+  const long kb = ((long)h * (p.N + p.nh) + p.nh) * d;
+  const long qb = (long)h * p.N * d;
   for (int x = threadIdx.x; x < L * d; x += blockDim.x) {
     const float k = ld_in(p.K, kb + (long)i0 * d + x, p.bf16);
     const float v = ld_in(p.V, kb + (long)i0 * d + x, p.bf16);
@@ -213,7 +215,7 @@ __global__ void mlp_gather_kernel(MlpArgs p, MlpWs w, float* ws, int t0, int nb,
     base[w.E + x] = k - v;
   }
   for (int x = threadIdx.x; x < nb * d; x += blockDim.x)
-    base[w.Qc + x] = ld_in(p.Q, kb + (long)t0 * d + x, p.bf16);
+    base[w.Qc + x] = ld_in(p.Q, qb + (long)t0 * d + x, p.bf16);
   if (threadIdx.x < 32) {
     const long gb = (long)h * p.N;
     // U and W rows go to their tables; the running rows reuse P1/P2 scratch.
@@ -257,70 +259,6 @@ __global__ void copy_q_kernel(const float* ws, long per_head, long Qc, float* Y,
   const float* q = ws + h * per_head + Qc;
   for (int x = threadIdx.x; x < (n_hi - n_lo) * d; x += blockDim.x)
     Y[(long)h * N * d + (long)(t0 + n_lo) * d + x] = q[n_lo * d + x];
-}
-
-// S = eta_t S - theta_t g_t with g_t = 2 sum_j gamma_j grad_{t-j} at the
-// chunk-start state: [e h^T] on the W1 block, [delta k^T] on the W2 block.
-__global__ void ns_momentum_kernel(MlpArgs p, MlpWs w, const float* ws, int t, int i0) {
-  const int h = blockIdx.y;
-  const float* base = ws + h * w.per_head;
-  const long d = p.d, dh = p.dh, half = d * dh;
-  const float et = p.eta[(long)h * p.N + t], th = p.theta[(long)h * p.N + t];
-  float* S = p.S + h * 2 * half;
-  const int j_lo = max(i0, t - p.c + 1);
-  for (long x = blockIdx.x * blockDim.x + threadIdx.x; x < 2 * half;
-       x += (long)gridDim.x * blockDim.x) {
-    float g = 0.f;
-    if (x < half) {
-      const int r = (int)(x / dh), col = (int)(x % dh);
-      for (int i = j_lo; i <= t; ++i)
-        g += p.gamma[t - i] * base[w.E + (i - i0) * d + r] * base[w.H + (i - i0) * dh + col];
-    } else {
-      const long y = x - half;
-      const int row = (int)(y / d), col = (int)(y % d);
-      for (int i = j_lo; i <= t; ++i)
-        g += p.gamma[t - i] * base[w.Dl + (i - i0) * dh + row] * base[w.Kw + (i - i0) * d + col];
-    }
-    S[x] = et * S[x] - th * 2.f * g;
-  }
-}
-
-// X = S / (||S||_F + eps) for one weight block of every head.
-__global__ void ns_init_kernel(const float* S, long state, long off, long n, float eps, float* ws,
-                               long per_head, long X) {
-  const int h = blockIdx.x;
-  const float* s = S + h * state + off;
-  __shared__ float red[256];
-  float acc = 0.f;
-  for (long x = threadIdx.x; x < n; x += blockDim.x) acc += s[x] * s[x];
-  red[threadIdx.x] = acc;
-  __syncthreads();
-  for (int o = 128; o > 0; o >>= 1) {
-    if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
-    __syncthreads();
-  }
-  const float inv = 1.f / (sqrtf(red[0]) + eps);
-  float* xo = ws + h * per_head + X;
-  for (long x = threadIdx.x; x < n; x += blockDim.x) xo[x] = s[x] * inv;
-}
-
-// X = a X + b T1 + c T2.
-__global__ void ns_combine_kernel(float* ws, long per_head, long X, long T1, long T2, long n,
-                                  float a, float b, float c) {
-  float* base = ws + blockIdx.y * per_head;
-  for (long x = blockIdx.x * blockDim.x + threadIdx.x; x < n; x += (long)gridDim.x * blockDim.x)
-    base[X + x] = a * base[X + x] + b * base[T1 + x] + c * base[T2 + x];
-}
-
-// W_block = (1 - alpha_t) W_block + X.
-__global__ void ns_apply_kernel(float* M, long state, long off, long n, const float* alpha,
-                                long N, int t, const float* ws, long per_head, long X) {
-  const int h = blockIdx.y;
-  const float keep = 1.f - alpha[(long)h * N + t];
-  float* m = M + h * state + off;
-  const float* xs = ws + h * per_head + X;
-  for (long x = blockIdx.x * blockDim.x + threadIdx.x; x < n; x += (long)gridDim.x * blockDim.x)
-    m[x] = keep * m[x] + xs[x];
 }
 
 // X[inst][block] = S[inst][block] / (||S[inst][block]||_F + eps), in place; one
@@ -443,7 +381,7 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
   const long PH = w.per_head;
   for (int t0 = 0; t0 < p.N; t0 += p.b) {
     const int t1 = min(p.N, t0 + p.b), nb = t1 - t0;
-    const int i0 = max(0, t0 - p.c + 1), L = t1 - i0;
+    const int i0 = max(-p.nh, t0 - p.c + 1), L = t1 - i0;  // history rows enter windows
     mlp_gather_kernel<<<H, 256, 0, st>>>(p, w, ws, t0, nb, i0, L);
     CL();
     // Z = K_w W2^T ; H = GELU(Z), Gp = GELU'(Z)

@@ -14,13 +14,13 @@ from . import (BF16, F32, AtlasMemCfg, atlas_mem_forward, atlas_mem_workspace_by
 
 
 def cfg_for(w, heads: int, N: int, S_state=None, workspace=None, workspace_bytes=0,
-            status_dev=None) -> AtlasMemCfg:
+            status_dev=None, n_history: int = 0) -> AtlasMemCfg:
     """Config of workload ``w`` with ``heads`` heads (as B = 1, H = heads) and N tokens."""
     a, b_, c_ = w.ns_coef
     return make_cfg(1, heads, N, w.d_k, w.d_v, w.d_h, mem=w.mem, phi=w.phi, loss=w.loss, c=w.c,
                     b=w.b, ns_steps=w.ns_steps, ns_a=a, ns_b=b_, ns_c=c_, ns_eps=w.ns_eps,
                     in_dtype=BF16 if w.bf16 else F32, S_state=S_state, workspace=workspace,
-                    workspace_bytes=workspace_bytes, status_dev=status_dev)
+                    workspace_bytes=workspace_bytes, status_dev=status_dev, n_history=n_history)
 
 
 def to_device(w, inp: dict, device="cuda") -> dict:
@@ -37,7 +37,8 @@ def to_device(w, inp: dict, device="cuda") -> dict:
 class Runner:
     """Owns the output, state and workspace buffers for repeated calls."""
 
-    def __init__(self, w, heads: int, N: int, device="cuda", with_S: bool = False):
+    def __init__(self, w, heads: int, N: int, device="cuda", with_S: bool = False,
+                 n_history: int = 0):
         self.w, self.heads, self.N = w, heads, N
         self.device = device
         self.Y = torch.empty((heads, N, w.d_v), device=device, dtype=torch.float32)
@@ -45,12 +46,12 @@ class Runner:
         self.S = (torch.zeros((heads, w.state_size), device=device, dtype=torch.float32)
                   if with_S else None)
         self.status = torch.zeros(1, device=device, dtype=torch.int32)
-        probe = cfg_for(w, heads, N, S_state=self.S)
+        probe = cfg_for(w, heads, N, S_state=self.S, n_history=n_history)
         nbytes = atlas_mem_workspace_bytes(probe)
         self.ws = (torch.empty(max(nbytes, 1), device=device, dtype=torch.uint8)
                    if nbytes else None)
         self.cfg = cfg_for(w, heads, N, S_state=self.S, workspace=self.ws,
-                           workspace_bytes=nbytes, status_dev=self.status)
+                           workspace_bytes=nbytes, status_dev=self.status, n_history=n_history)
 
     def __call__(self, d: dict, M0=None, S0=None, stream=None):
         """One forward over device inputs ``d``; M0/S0 (device) reset the state first."""

@@ -23,10 +23,10 @@ def tol(w) -> float:
     return TOL_BF16 if w.bf16 else TOL_F32
 
 
-def oracle_cfg(w, N):
+def oracle_cfg(w, N, n_history=0):
     a, b, c = w.ns_coef
     return oracle.make_cfg(N, w.d_k, w.d_v, w.d_h, w.mem, w.phi, w.loss, w.c, w.b,
-                           w.ns_steps, a, b, c, w.ns_eps)
+                           w.ns_steps, a, b, c, w.ns_eps, n_history=n_history)
 
 
 def run_oracle(w, inp, N=None, recurrent=False, S0=None, n_threads=0):

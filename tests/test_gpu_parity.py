@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 import workloads as W
-from parity_util import rel_err, run_oracle, tol
+from parity_util import oracle_cfg, rel_err, run_oracle, tol
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -203,6 +203,38 @@ def test_mlp_tensor_core_path_with_initial_momentum():
     Yg, Mg, Sg = gpu_run(w, inp, S0=S0)
     check(w, Yg, Mg, Yo, Mo, "S0")
     assert rel_err(Sg, So, w.bf16) <= tol(w)
+
+
+# ------------------------------------------------------------- history rows
+
+@pytest.mark.parametrize("wid,kw,N,nh,heads", [
+    (1, dict(), 100, 3, [0]),                 # token-serial kernel, window 4, b = 1
+    (1, dict(b=16, c=6, H=2), 70, 9, [0, 1]),  # token-serial, chunked; history > window
+    (1, dict(c=12), 50, 11, [0]),             # linear CUDA-core kernel (window > 8)
+    (3, {}, 80, 63, [0, 5]),                  # poly2, window 64
+    (4, dict(c=3), 100, 2, [0, 3]),           # MLP CUDA-core path
+    (5, {}, 70, 255, [2]),                    # Newton-Schulz, window 256
+])
+def test_history_rows(wid, kw, N, nh, heads):
+    """K and V carry n_history rows ahead of the processed tokens; they enter the
+    windows of the first tokens only.  Same history given to the oracle."""
+    from test_memorization_recurrent_gb300.harness import Runner, to_device
+    import oracle
+    w = W.workload(wid, bounded=True, **kw)
+    full = W.generate(w.with_(N=N + nh), heads=heads, n_tokens=N + nh)
+    inp = dict(full)
+    for k in ("Q", "alpha", "eta", "theta"):
+        inp[k] = full[k][:, nh:]
+    ho = {k: inp[k] for k in ("K", "Q", "V", "alpha", "eta", "theta")}
+    Yo, Mo, So = oracle.forward(oracle_cfg(w, N, nh), ho["K"], ho["Q"], ho["V"], ho["alpha"],
+                                ho["eta"], ho["theta"], inp["gamma"], inp["M0"])
+    d = to_device(w, inp)
+    r = Runner(w, len(heads), N, with_S=True, n_history=nh)
+    Yg, Mg = r(d)
+    torch.cuda.synchronize()
+    assert int(r.status.item()) == 0
+    check(w, Yg.cpu().numpy(), Mg.cpu().numpy(), Yo, Mo, f"history {nh}")
+    assert rel_err(r.S.cpu().numpy(), So, w.bf16) <= tol(w)
 
 
 # -------------------------------------------------------------- full sizes
