@@ -244,6 +244,7 @@ KERNEL_OF_PATH = {
     "linear_tc": ("linear_tc.cu", "linear_tc_{wname}.md"),
     "linear_simt": ("linear_simt.cu", "linear_simt_{wname}.md"),
     "linear_seq": ("linear_seq.cu", "linear_seq_{wname}.md"),
+    "linear_chunk": ("tc_gemm.cu", "linear_chunk_{wname}.md"),
     "mlp_simt": ("mlp_simt.cu", "mlp_simt_{wname}.md"),
     "mlp_tc": ("mlp_tc.cu", "mlp_tc_{wname}.md"),
 }

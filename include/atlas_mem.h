@@ -146,8 +146,8 @@ int atlas_mem_forward_noalloc(const void* K, const void* Q, const void* V, const
 const char* atlas_mem_strerror(int status);
 
 /* Name of the kernel family atlas_mem_forward would launch for cfg (for
- * reports): "linear_tc", "linear_seq", "linear_simt", "mlp_simt", or "" if
- * invalid. */
+ * reports): "linear_tc", "linear_seq", "linear_chunk", "linear_simt", "mlp_tc",
+ * "mlp_simt", or "" if invalid. */
 const char* atlas_mem_path(const atlas_mem_cfg* cfg);
 
 /* Number of kernel launches atlas_mem_forward makes for cfg (for reports). */

@@ -11,7 +11,8 @@ using namespace atlas;
 namespace {
 
 enum Path {
-  PATH_INVALID = 0, PATH_LINEAR_SIMT, PATH_LINEAR_TC, PATH_LINEAR_SEQ, PATH_MLP_SIMT, PATH_MLP_TC
+  PATH_INVALID = 0, PATH_LINEAR_SIMT, PATH_LINEAR_TC, PATH_LINEAR_SEQ, PATH_LINEAR_CHUNK,
+  PATH_MLP_SIMT, PATH_MLP_TC
 };
 
 int feature_dim(const atlas_mem_cfg* c) {
@@ -88,6 +89,7 @@ Path choose_path(const atlas_mem_cfg* c) {
                        nullptr, nullptr);
   if (a.nh == 0 && linear_tc_supported(a)) return PATH_LINEAR_TC;
   if (linear_seq_supported(a)) return PATH_LINEAR_SEQ;
+  if (linear_chunk_supported(a)) return PATH_LINEAR_CHUNK;
   int RV;
   size_t smem;
   if (linear_simt_plan(a, c->B * c->H, &RV, &smem) != ATLAS_OK) return PATH_INVALID;
@@ -113,6 +115,11 @@ size_t atlas_mem_workspace_bytes(const atlas_mem_cfg* cfg) {
                                            : mlp_simt_workspace_bytes(a);
   }
   if (choose_path(cfg) == PATH_LINEAR_TC) return linear_tc_workspace_bytes(cfg->B * cfg->H);
+  if (choose_path(cfg) == PATH_LINEAR_CHUNK) {
+    LinArgs a = lin_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, cfg,
+                         nullptr, nullptr);
+    return linear_chunk_workspace_bytes(a, cfg->B * cfg->H);
+  }
   return 0;
 }
 
@@ -121,6 +128,7 @@ const char* atlas_mem_path(const atlas_mem_cfg* cfg) {
     case PATH_LINEAR_SIMT: return "linear_simt";
     case PATH_LINEAR_TC: return "linear_tc";
     case PATH_LINEAR_SEQ: return "linear_seq";
+    case PATH_LINEAR_CHUNK: return "linear_chunk";
     case PATH_MLP_SIMT: return "mlp_simt";
     case PATH_MLP_TC: return "mlp_tc";
     default: return "";
@@ -135,6 +143,11 @@ long atlas_mem_launch_count(const atlas_mem_cfg* cfg) {
       return (long)cfg->B * cfg->H > 0 ? 1 : 0;
     case PATH_LINEAR_TC:
       return (long)cfg->B * cfg->H > 0 ? 2 : 0;
+    case PATH_LINEAR_CHUNK: {
+      LinArgs a = lin_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, cfg,
+                           nullptr, nullptr);
+      return linear_chunk_launch_count(a, cfg->B * cfg->H);
+    }
     case PATH_MLP_SIMT: {
       if ((long)cfg->B * cfg->H == 0) return 0;
       MlpArgs a = mlp_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, cfg,
@@ -178,6 +191,11 @@ int atlas_mem_forward(const void* K, const void* Q, const void* V, const float* 
     return linear_tc_launch(a, (int)heads, cfg->status_dev, cfg->workspace, st);
   }
   if (path == PATH_LINEAR_SEQ) return linear_seq_launch(a, (int)heads, st);
+  if (path == PATH_LINEAR_CHUNK) {
+    const size_t need = linear_chunk_workspace_bytes(a, (int)heads);
+    if (!cfg->workspace || cfg->workspace_bytes < need) return ATLAS_ERR_WORKSPACE;
+    return linear_chunk_forward(a, (int)heads, cfg->workspace, st);
+  }
   return linear_simt_launch(a, (int)heads, st);
 }
 

@@ -32,6 +32,13 @@ int linear_simt_plan(const LinArgs& a, int heads, int* RV_out, size_t* smem_out)
 bool linear_seq_supported(const LinArgs& a);
 int linear_seq_launch(const LinArgs& a, int heads, cudaStream_t st);
 
+// Host-driven path for linear memories with a wide feature map (D >= 256, the
+// degree-2 map): per chunk, batched tensor-core GEMMs over all heads.
+bool linear_chunk_supported(const LinArgs& a);
+size_t linear_chunk_workspace_bytes(const LinArgs& a, int heads);
+long linear_chunk_launch_count(const LinArgs& a, int heads);
+int linear_chunk_forward(const LinArgs& a, int heads, void* ws, cudaStream_t st);
+
 // Tensor-core path: linear memory, identity map, d_k = d_v = 128, bf16 inputs,
 // b = 64, c = 1, N % 4 == 0.  Launches the tensor-core kernel (heads with
 // eta == 0; it flags the others in the workspace) and the CUDA-core kernel on
@@ -59,6 +66,8 @@ struct TcGemm {
   const float* D; long sDb, sDb2, sDm, sDn; // optional addend beta * D
   float beta;
   int accumulate;                           // C += term (else C = term)
+  int ksplit;                               // > 1: K split over that many CTAs, their
+                                            // terms added to C atomically (no D)
   int symmetric;
   int* status;                              // optional device status word (timeouts)
   int modeA, modeB;                         // set by tc_gemm_launch (operand load paths)

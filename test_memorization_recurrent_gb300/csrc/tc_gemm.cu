@@ -129,14 +129,18 @@ __global__ void __launch_bounds__(kThr) tc_gemm_kernel(TcGemm g) {
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + 4 * TILE + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + 4 * TILE + 16);
 
-  const int bz = blockIdx.z;
+  const int nsplit = g.ksplit > 1 ? g.ksplit : 1;
+  const int bz = blockIdx.z / nsplit, split = blockIdx.z % nsplit;
   const long bo = g.bdiv > 0 ? bz / g.bdiv : bz, bi = g.bdiv > 0 ? bz % g.bdiv : 0;
+  // this CTA's K range (whole blocks of TK)
+  const int kchunk = ((g.K + nsplit - 1) / nsplit + TK - 1) / TK * TK;
+  const int kbeg = split * kchunk, kend = min(g.K, kbeg + kchunk);
   const int m0 = blockIdx.y * TB, n0 = blockIdx.x * TB;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // A(m, k) and B(k, n) seen as rows m / n over k
-  Operand oa{g.A + bo * g.sAb + bi * g.sAb2, g.sAm, g.sAk, g.M, g.K, g.modeA,
+  Operand oa{g.A + bo * g.sAb + bi * g.sAb2, g.sAm, g.sAk, g.M, kend, g.modeA,
              g.kscale ? g.kscale + bo * g.sKb + bi * g.sKb2 : nullptr};
-  Operand ob{g.B + bo * g.sBb + bi * g.sBb2, g.sBn, g.sBk, g.N, g.K, g.modeB, nullptr};
+  Operand ob{g.B + bo * g.sBb + bi * g.sBb2, g.sBn, g.sBk, g.N, kend, g.modeB, nullptr};
   const bool sym = g.symmetric != 0;
 
   if (tid == 0) {
@@ -158,11 +162,11 @@ __global__ void __launch_bounds__(kThr) tc_gemm_kernel(TcGemm g) {
 
   bool ok = true;
   int commits = 0;
-  const int nkb = (g.K + TK - 1) / TK;
+  const int nkb = kend > kbeg ? (kend - kbeg + TK - 1) / TK : 0;
   float va[32], vb[32];
   if (nkb > 0) {
-    load_block(oa, m0, 0, va);
-    if (!sym) load_block(ob, n0, 0, vb);
+    load_block(oa, m0, kbeg, va);
+    if (!sym) load_block(ob, n0, kbeg, vb);
   }
   for (int kb = 0; kb < nkb && ok; ++kb) {
     if (kb > 0) {  // the tiles are read by the previous block's MMAs until they complete
@@ -190,8 +194,8 @@ __global__ void __launch_bounds__(kThr) tc_gemm_kernel(TcGemm g) {
     }
     __syncwarp();
     if (kb + 1 < nkb) {  // next block into registers while the MMAs run
-      load_block(oa, m0, (kb + 1) * TK, va);
-      if (!sym) load_block(ob, n0, (kb + 1) * TK, vb);
+      load_block(oa, m0, kbeg + (kb + 1) * TK, va);
+      if (!sym) load_block(ob, n0, kbeg + (kb + 1) * TK, vb);
     }
   }
   if (ok && nkb > 0) {
@@ -233,6 +237,10 @@ __global__ void __launch_bounds__(kThr) tc_gemm_kernel(TcGemm g) {
         const int nl = 32 * j + lane, n = n0 + nl;
         if (n >= g.N) continue;
         float t = rs * tile[ml * TB + (nl ^ (ml & 31))];
+        if (nsplit > 1) {
+          atomicAdd(crow + n, t);
+          continue;
+        }
         if (drow) t += g.beta * drow[n];
         crow[n] = g.accumulate ? crow[n] + t : t;
       }
@@ -295,6 +303,8 @@ int tc_gemm_launch(const TcGemm& g0, cudaStream_t st) {
   if (g0.M <= 0 || g0.N <= 0 || g0.batch <= 0) return ATLAS_OK;
   TcGemm g = g0;
   if (g.symmetric && (g.M != TB || g.N != TB)) return ATLAS_ERR_UNSUPPORTED;
+  const int nsplit = g.ksplit > 1 ? g.ksplit : 1;
+  if (nsplit > 1 && (g.D || g.sCn != 1)) return ATLAS_ERR_UNSUPPORTED;
   g.modeA = pick_mode(g.A, g.sAm, g.sAk, g.sAb, g.sAb2, g.batch);
   g.modeB = pick_mode(g.B, g.sBn, g.sBk, g.sBb, g.sBb2, g.batch);
   // a per-k factor is applied elementwise: the vector paths handle it too
@@ -305,7 +315,7 @@ int tc_gemm_launch(const TcGemm& g0, cudaStream_t st) {
       return ATLAS_ERR_CUDA;
     attr_set = true;
   }
-  dim3 grid((g.N + TB - 1) / TB, (g.M + TB - 1) / TB, g.batch);
+  dim3 grid((g.N + TB - 1) / TB, (g.M + TB - 1) / TB, g.batch * nsplit);
   tc_gemm_kernel<<<grid, kThr, SMEM_G, st>>>(g);
   return cudaGetLastError() == cudaSuccess ? ATLAS_OK : ATLAS_ERR_CUDA;
 }

@@ -52,7 +52,8 @@ def test_state_size_and_path(lib, wid):
     w = W.workload(wid)
     cfg = cfg_for(w, w.heads, w.N)
     assert A.atlas_mem_state_size(cfg) == w.state_size
-    assert A.atlas_mem_path(cfg) in ("linear_simt", "linear_seq", "linear_tc", "mlp_simt", "mlp_tc")
+    assert A.atlas_mem_path(cfg) in ("linear_simt", "linear_seq", "linear_chunk", "linear_tc", "mlp_simt",
+                                      "mlp_tc")
     assert A.atlas_mem_launch_count(cfg) >= 1
     nbytes = A.atlas_mem_workspace_bytes(cfg)
     assert nbytes >= 0
