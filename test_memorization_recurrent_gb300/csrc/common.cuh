@@ -45,11 +45,20 @@ __device__ __forceinline__ void chunk_tables_warp(const float* alpha, const floa
     Wrun[i] = 0.f;
   }
   float pa = 1.f, pe = 1.f, pb = 0.f;
+  // the gates of 32 tokens at a time come in one load per lane (ahead of the
+  // sequential loop) and are broadcast from lane to lane
+  float g_keep = 1.f, g_eta = 0.f, g_theta = 0.f;
   for (int n = 0; n < nb; ++n) {
     const int tn = t0 + n;
-    const float keep = 1.f - alpha[tn];
-    const float et = eta[tn];
-    const float th = theta[tn];
+    if ((n & 31) == 0) {
+      const int mine = tn + lane;
+      g_keep = mine < t0 + nb ? 1.f - alpha[mine] : 1.f;
+      g_eta = mine < t0 + nb ? eta[mine] : 0.f;
+      g_theta = mine < t0 + nb ? theta[mine] : 0.f;
+    }
+    const float keep = __shfl_sync(0xFFFFFFFFu, g_keep, n & 31);
+    const float et = __shfl_sync(0xFFFFFFFFu, g_eta, n & 31);
+    const float th = __shfl_sync(0xFFFFFFFFu, g_theta, n & 31);
     pa *= keep;
     pe *= et;
     pb = keep * pb + pe;

@@ -75,6 +75,7 @@ __global__ void lc_gather_kernel(LinArgs p, LcWs w, float* ws, int t0, int nb, i
   const long qb = (long)h * p.N * dk;
   float* Ks = lc_sm;
   float* Qs = Ks + L * dk;
+  float* run = Qs + nb * dk;  // running U and W rows of the table recursion [2][L]
   for (int x = threadIdx.x; x < L * dk; x += blockDim.x)
     Ks[x] = ld_in(p.K, kb + (long)i0 * dk + x, p.bf16);
   for (int x = threadIdx.x; x < nb * dk; x += blockDim.x)
@@ -88,11 +89,15 @@ __global__ void lc_gather_kernel(LinArgs p, LcWs w, float* ws, int t0, int nb, i
         ++o;
       }
   }
-  if (blockIdx.x == 0 && threadIdx.x < 32) {
+  if (blockIdx.x == 0 && threadIdx.x < 32) {  // running rows in shared memory
     const long gb = (long)h * p.N;
     chunk_tables_warp(p.alpha + gb, p.eta + gb, p.theta + gb, p.gamma, t0, nb, i0, L, p.c,
-                      base + w.Urun, base + w.Wrun, base + w.W, L, base + w.U, base + w.ta,
-                      base + w.te, base + w.tb);
+                      run, run + L, base + w.W, L, base + w.U, base + w.ta, base + w.te,
+                      base + w.tb);
+    for (int i = threadIdx.x; i < L; i += 32) {  // the last rows (for the state update)
+      base[w.Urun + i] = run[i];
+      base[w.Wrun + i] = run[L + i];
+    }
   }
   __syncthreads();
   const long tid = (long)blockIdx.x * blockDim.x + threadIdx.x, nt = (long)gridDim.x * blockDim.x;
@@ -219,7 +224,7 @@ int linear_chunk_forward(const LinArgs& a0, int heads, void* wsv, cudaStream_t s
   for (int t0 = 0; t0 < p.N; t0 += p.b) {
     const int t1 = min(p.N, t0 + p.b), nb = t1 - t0;
     const int i0 = max(-p.nh, t0 - p.c + 1), L = t1 - i0;
-    const size_t gsm = sizeof(float) * (size_t)(L + nb) * dk;
+    const size_t gsm = sizeof(float) * ((size_t)(L + nb) * dk + 2 * L);
     if (gsm > 96 * 1024) return ATLAS_ERR_UNSUPPORTED;
     lc_gather_kernel<<<dim3(8, H), 256, gsm, st>>>(p, w, ws, t0, nb, i0, L);
     LC_CL();

@@ -199,6 +199,9 @@ size_t mlp_simt_workspace_bytes(const MlpArgs& a) { return mlp_layout(a).bytes; 
 
 // ---------------------------------------------------------- small kernels
 
+// Window lengths whose two running table rows fit in 48 KB of shared memory.
+constexpr int kRunSmem = 6144;
+
 // Window and chunk inputs as fp32, E preset to K - V, and the scalar tables.
 __global__ void mlp_gather_kernel(MlpArgs p, MlpWs w, float* ws, int t0, int nb, int i0, int L) {
   const int h = blockIdx.x;
@@ -218,10 +221,14 @@ __global__ void mlp_gather_kernel(MlpArgs p, MlpWs w, float* ws, int t0, int nb,
     base[w.Qc + x] = ld_in(p.Q, qb + (long)t0 * d + x, p.bf16);
   if (threadIdx.x < 32) {
     const long gb = (long)h * p.N;
-    // U and W rows go to their tables; the running rows reuse P1/P2 scratch.
+    // U and W rows go to their tables; the running rows live in shared memory
+    // when they fit (dynamic size 2 L floats), else in the P1/P2 scratch
+    extern __shared__ float run_sm[];
+    float* run_u = L <= kRunSmem ? run_sm : base + w.P1;
+    float* run_w = L <= kRunSmem ? run_sm + L : base + w.P2;
     chunk_tables_warp(p.alpha + gb, p.eta + gb, p.theta + gb, p.gamma, t0, nb, i0, L, p.c,
-                      base + w.P1, base + w.P2, base + w.W, L, base + w.U, base + w.ta,
-                      base + w.te, base + w.tb);
+                      run_u, run_w, base + w.W, L, base + w.U, base + w.ta, base + w.te,
+                      base + w.tb);
   }
 }
 
@@ -382,7 +389,7 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
   for (int t0 = 0; t0 < p.N; t0 += p.b) {
     const int t1 = min(p.N, t0 + p.b), nb = t1 - t0;
     const int i0 = max(-p.nh, t0 - p.c + 1), L = t1 - i0;  // history rows enter windows
-    mlp_gather_kernel<<<H, 256, 0, st>>>(p, w, ws, t0, nb, i0, L);
+    mlp_gather_kernel<<<H, 256, L <= kRunSmem ? 2 * L * sizeof(float) : 0, st>>>(p, w, ws, t0, nb, i0, L);
     CL();
     // Z = K_w W2^T ; H = GELU(Z), Gp = GELU'(Z)
     Gemm g = gemm0();
