@@ -121,7 +121,7 @@ __device__ __forceinline__ void store_block(const Operand& o, const float* v, ui
 
 }  // namespace
 
-__global__ void __launch_bounds__(kThr) tc_gemm_kernel(TcGemm g) {
+__global__ void __launch_bounds__(kThr, 3) tc_gemm_kernel(TcGemm g) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
