@@ -107,4 +107,18 @@ int mlp_tc_launch(const MlpArgs& a, void* ws, cudaStream_t st);
 int mlp_simt_forward(const MlpArgs& a, void* ws, cudaStream_t st);
 long mlp_simt_launch_count(const MlpArgs& a);
 
+// Fused Newton-Schulz (ns_fused.cu): n_inst instances, each two blocks of one
+// MLP state (W1 part d x dh at X + i * inst_stride, W2 part dh x d at + half),
+// every block normalised by its own Frobenius norm and iterated `steps` times
+// in place.  Supported for d = 128, dh = 512; X 16-byte aligned.
+struct NsArgs {
+  float* X;
+  long inst_stride, half;
+  int n_inst, steps;
+  float a, b, c, eps;
+  int* status;  // optional device status word (timeouts)
+};
+bool ns_fused_supported(int d, int dh);
+int ns_fused_launch(const NsArgs& a, cudaStream_t st);
+
 }  // namespace atlas

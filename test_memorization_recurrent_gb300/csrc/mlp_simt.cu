@@ -366,7 +366,8 @@ static dim3 ew_grid(long n, int heads) {
 
 long mlp_simt_launch_count(const MlpArgs& a) {
   const long chunks = (a.N + a.b - 1) / a.b;
-  if (a.ns_steps > 0) return 1 + chunks * (17 + 6L * a.ns_steps);
+  if (a.ns_steps > 0)
+    return 1 + chunks * (ns_fused_supported(a.d, a.dh) ? 17 : 17 + 6L * a.ns_steps);
   return 1 + chunks * (4 + 1 + 3 + 1 + 4 + 4 + 1 + 4);
 }
 
@@ -534,6 +535,13 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
       ns_copy_last_kernel<<<ew_grid(state, H), 256, 0, st>>>(p.S, X, state, nb);
       CL();
       // N_n = NS(S_n), per weight block; X0 = S / (||S|| + eps)
+      if (ns_fused_supported((int)d, (int)dh)) {  // every instance on chip for all steps
+        NsArgs n;
+        n.X = X; n.inst_stride = state; n.half = half; n.n_inst = (int)inst;
+        n.steps = p.ns_steps; n.a = p.ns_a; n.b = p.ns_b; n.c = p.ns_c; n.eps = p.ns_eps;
+        n.status = p.status;
+        CK(ns_fused_launch(n, st));
+      } else {
       ns_normalize_kernel<<<dim3((unsigned)inst, 2), 256, 0, st>>>(X, state, half, p.ns_eps);
       CL();
       for (int it = 0; it < p.ns_steps; ++it) {
@@ -577,6 +585,7 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
           CK(tc_gemm_launch(g3, st));
         }
         float* tmp = X; X = T; T = tmp;
+      }
       }
       // readout: zq_n = a_n W2_0 q_n + sum_{m<=n} r[n,m] N2_m q_n -> GELU
       g = gemm0();
