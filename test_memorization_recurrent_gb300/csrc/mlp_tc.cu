@@ -86,7 +86,8 @@ constexpr int G_AL = 0, G_ET = 64, G_TH = 128, G_A = 192, G_BE = 256, G_WL = 320
               G_SC = 448;  // aL, betaL, epsL, gamma0
 
 // TMEM columns
-constexpr uint32_t TM_A0 = 0;     // Z, GELU'(Z), Delta (bf16 hi | lo, the A of Delta P1^T), W1 Hq^T
+constexpr uint32_t TM_A0 = 0;     // Z, GELU'(Z), Delta (per 32 tokens: 16 columns of bf16 pairs hi,
+                                  // 16 lo; the A of Delta P1^T), W1 Hq^T
 constexpr uint32_t TM_A1 = 64;    // W2 Q^T, then S1 Hq^T
 constexpr uint32_t TM_A2 = 128;   // S2 Q^T, then E P2^T
 constexpr uint32_t TM_A3 = 192;   // P1, E partial, Delta raw, Delta P1^T, P2
@@ -225,15 +226,10 @@ __device__ __forceinline__ float gelu_f(float z) {
   return g;
 }
 
-__device__ __forceinline__ uint32_t bf16_bits(float x) {
-  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
-}
-
 // 8 values -> one 16-byte chunk of bf16 (round to nearest).
 __device__ __forceinline__ void st_hi8(uint32_t addr, const float* x) {
-  st_shared_v4(addr, bf16_bits(x[0]) | (bf16_bits(x[1]) << 16),
-               bf16_bits(x[2]) | (bf16_bits(x[3]) << 16), bf16_bits(x[4]) | (bf16_bits(x[5]) << 16),
-               bf16_bits(x[6]) | (bf16_bits(x[7]) << 16));
+  st_shared_v4(addr, pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
+               pack_bf16(x[6], x[7]));
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -276,12 +272,7 @@ __device__ __forceinline__ void st_pair8_global(__nv_bfloat16* hi, __nv_bfloat16
                                                 const float* x) {
   uint32_t hh[4], ll[4];
 #pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    const float h0 = __bfloat162float(__float2bfloat16_rn(x[2 * p]));
-    const float h1 = __bfloat162float(__float2bfloat16_rn(x[2 * p + 1]));
-    hh[p] = bf16_bits(h0) | (bf16_bits(h1) << 16);
-    ll[p] = bf16_bits(x[2 * p] - h0) | (bf16_bits(x[2 * p + 1] - h1) << 16);
-  }
+  for (int p = 0; p < 4; ++p) split_pair(x[2 * p], x[2 * p + 1], hh[p], ll[p]);
   *reinterpret_cast<uint4*>(hi) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
   *reinterpret_cast<uint4*>(lo) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
 }
@@ -307,12 +298,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* v) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
       : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
         "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
         "=r"(v[14]), "=r"(v[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      : "r"(taddr)
+      : "memory");
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]^T (A: bf16 pairs packed two to a column).
@@ -611,7 +603,8 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 1)
         for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
           for (int s = 0; s < 3; ++s)
-            mma_bf16_ta(tmem + TM_A3, tmem + TM_A0 + (s == 2 ? 32 : 0) + 8 * kk,
+            mma_bf16_ta(tmem + TM_A3,
+                        tmem + TM_A0 + 32 * (kk >> 1) + 8 * (kk & 1) + (s == 2 ? 16 : 0),
                         dk((s == 1 ? R_PL : X_P) + kk * 32), id64, (kk | s) ? 1u : 0u);
         mma_commit(&bars[B_R2C]);
         ++commits;
@@ -860,17 +853,13 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 1)
       tmem_ld32(tl + TM_A0 + 32 * h, w);
 #pragma unroll
       for (int x = 0; x < 32; ++x) v[x] *= w[x];
-      {  // GELU' is done with: Delta takes its place as bf16 hi | lo pairs (tokens 32h..)
+      {  // GELU' is done with: Delta takes its columns as bf16 pairs, hi then lo
+        // (tokens 32h.. in columns [32h, 32h + 32): each warp writes only what it read)
         uint32_t dh[16], dl[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float h0 = __bfloat162float(__float2bfloat16_rn(v[2 * e]));
-          const float h1 = __bfloat162float(__float2bfloat16_rn(v[2 * e + 1]));
-          dh[e] = bf16_bits(h0) | (bf16_bits(h1) << 16);
-          dl[e] = bf16_bits(v[2 * e] - h0) | (bf16_bits(v[2 * e + 1] - h1) << 16);
-        }
-        tmem_st16(tl + TM_A0 + 16 * h, dh);
-        tmem_st16(tl + TM_A0 + 32 + 16 * h, dl);
+        for (int e = 0; e < 16; ++e) split_pair(v[2 * e], v[2 * e + 1], dh[e], dl[e]);
+        tmem_st16(tl + TM_A0 + 32 * h, dh);
+        tmem_st16(tl + TM_A0 + 32 * h + 16, dl);
       }
 #pragma unroll
       for (int x = 0; x < 32; ++x) w[x] = -2.f * v[x] * G[G_WL + 32 * h + x];
@@ -902,8 +891,8 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 1)
       tc_fence_after();
       {
         uint32_t dh[16], dl[16];
-        tmem_ld16(tl + TM_A0 + 16 * h, dh);
-        tmem_ld16(tl + TM_A0 + 32 + 16 * h, dl);
+        tmem_ld16(tl + TM_A0 + 32 * h, dh);
+        tmem_ld16(tl + TM_A0 + 32 * h + 16, dl);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           v[2 * e] = bf16_lo(dh[e]) + bf16_lo(dl[e]);

@@ -192,6 +192,20 @@ def test_mlp_tensor_core_path(N, heads):
     assert rel_err(Sg, So, w.bf16) <= tol(w)
 
 
+@pytest.mark.parametrize("wid,N,heads", [(4, 147, [0, 7]), (5, 85, [0, 11])])
+def test_repeated_runs_are_bit_identical(wid, N, heads):
+    """The cluster kernels (MLP tensor-core path, fused Newton-Schulz) hand data
+    between warps and CTAs through TMEM and shared memory; a missing ordering
+    shows up as run-to-run differences long before it breaks a tolerance.  Eight
+    runs of the same inputs must agree to the bit."""
+    w = W.workload(wid, bounded=True)
+    inp = W.generate(w, heads=heads, n_tokens=N)
+    Y0, M0, S0 = gpu_run(w, inp, with_S=True)
+    for _ in range(7):
+        Y, M, S = gpu_run(w, inp, with_S=True)
+        assert np.array_equal(Y, Y0) and np.array_equal(M, M0) and np.array_equal(S, S0)
+
+
 def test_mlp_tensor_core_path_with_initial_momentum():
     """A non-zero S_0 (state handed over from a previous call) enters both the
     decay of M and the momentum; compared with the oracle started from the same S_0."""
