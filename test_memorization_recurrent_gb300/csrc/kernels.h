@@ -64,6 +64,7 @@ struct TcGemm {
   const float* rowscale; long sRb, sRb2;    // optional per-row factor of the product
   const float* kscale; long sKb, sKb2;      // optional per-k factor of A
   const float* D; long sDb, sDb2, sDm, sDn; // optional addend beta * D
+  const float* dscale; long sEb, sEb2;      // optional per-batch factor of the addend
   float beta;
   int accumulate;                           // C += term (else C = term)
   int ksplit;                               // > 1: K split over that many CTAs, their

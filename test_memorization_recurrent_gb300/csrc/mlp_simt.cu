@@ -285,19 +285,6 @@ __global__ void ns_normalize_kernel(float* X, long state, long half, float eps) 
   for (long i = threadIdx.x; i < half; i += blockDim.x) x[i] *= inv;
 }
 
-// S_n = eps_n S0 for the nb instances of every head (the window term is added
-// by the batched product).
-__global__ void ns_fill_kernel(float* Sn, const float* S0, long state, const float* ws,
-                               long per_head, long te, int nb) {
-  const int inst = blockIdx.y, h = inst / nb, n = inst % nb;
-  const float e = ws[h * per_head + te + n];
-  const float* s0 = S0 + h * state;
-  float* out = Sn + (long)inst * state;
-  for (long x = blockIdx.x * blockDim.x + threadIdx.x; x < state;
-       x += (long)gridDim.x * blockDim.x)
-    out[x] = e * s0[x];
-}
-
 // out[h][row][col] = S_{nb-1} of head h (the momentum carried to the next chunk).
 __global__ void ns_copy_last_kernel(float* S, const float* Sn, long state, int nb) {
   const int h = blockIdx.y;
@@ -367,7 +354,7 @@ static dim3 ew_grid(long n, int heads) {
 long mlp_simt_launch_count(const MlpArgs& a) {
   const long chunks = (a.N + a.b - 1) / a.b;
   if (a.ns_steps > 0)
-    return 1 + chunks * (ns_fused_supported(a.d, a.dh) ? 17 : 17 + 6L * a.ns_steps);
+    return 1 + chunks * (ns_fused_supported(a.d, a.dh) ? 16 : 16 + 6L * a.ns_steps);
   return 1 + chunks * (4 + 1 + 3 + 1 + 4 + 4 + 1 + 4);
 }
 
@@ -514,9 +501,8 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
       float* T = ws + w.nsT;
       float* Ag = ws + w.nsA;
       float* A2 = ws + w.nsA2;
-      // S_n = eps_n S0 - 2 sum_i U[n,i] [e_i h_i^T | delta_i k_i^T]
-      ns_fill_kernel<<<dim3(64, (unsigned)inst), 256, 0, st>>>(X, p.S, state, ws, PH, w.te, nb);
-      CL();
+      // S_n = eps_n S0 - 2 sum_i U[n,i] [e_i h_i^T | delta_i k_i^T]: eps_n S0 enters as
+      // the products' addend (per-instance factor eps_n of the head's S0)
       {  // instances (h, n): batch h * nb + n, per-head operands shared over n
         TcGemm t = tc0();
         t.batch = (int)inst; t.bdiv = nb; t.M = (int)d; t.N = (int)dh; t.K = L;
@@ -524,12 +510,15 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
         t.B = ws + w.H; t.sBb = PH; t.sBk = dh; t.sBn = 1;
         t.kscale = ws + w.U; t.sKb = PH; t.sKb2 = L;
         t.C = X; t.sCb = (long)nb * state; t.sCb2 = state; t.sCm = dh; t.sCn = 1;
-        t.alpha = -2.f; t.accumulate = 1;
+        t.alpha = -2.f;
+        t.D = p.S; t.sDb = state; t.sDb2 = 0; t.sDm = dh; t.sDn = 1; t.beta = 1.f;
+        t.dscale = ws + w.te; t.sEb = PH; t.sEb2 = 1;
         CK(tc_gemm_launch(t, st));
         t.M = (int)dh; t.N = (int)d;
         t.A = ws + w.Dl; t.sAm = 1; t.sAk = dh;
         t.B = ws + w.Kw; t.sBk = d; t.sBn = 1;
         t.C = X + half; t.sCm = d;
+        t.D = p.S + half; t.sDm = d;
         CK(tc_gemm_launch(t, st));
       }
       ns_copy_last_kernel<<<ew_grid(state, H), 256, 0, st>>>(p.S, X, state, nb);

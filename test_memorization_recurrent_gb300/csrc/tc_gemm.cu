@@ -3,7 +3,7 @@
 // the window products of the MLP-memory path.
 //
 //   C[b](m, n) = alpha * rowscale[b](m) * sum_k A[b](m, k) kscale[b](k) B[b](k, n)
-//                + beta * D[b](m, n)  (+ C[b](m, n) when accumulating)
+//                + beta * dscale[b] * D[b](m, n)  (+ C[b](m, n) when accumulating)
 //
 // Each operand element is split into bf16 hi + lo (hi = rn(x), lo = rn(x - hi));
 // the product is accumulated in fp32 from hi*hi + hi*lo + lo*hi, which keeps
@@ -225,6 +225,7 @@ __global__ void __launch_bounds__(kThr, 3) tc_gemm_kernel(TcGemm g) {
     __syncthreads();
     float* C = g.C + bo * g.sCb + bi * g.sCb2;
     const float* D = g.D ? g.D + bo * g.sDb + bi * g.sDb2 : nullptr;
+    const float db = g.beta * (g.dscale ? g.dscale[bo * g.sEb + bi * g.sEb2] : 1.f);
     const float* RS = g.rowscale ? g.rowscale + bo * g.sRb + bi * g.sRb2 : nullptr;
     for (int ml = warp; ml < TB; ml += kThr / 32) {
       const int m = m0 + ml;
@@ -241,7 +242,7 @@ __global__ void __launch_bounds__(kThr, 3) tc_gemm_kernel(TcGemm g) {
           atomicAdd(crow + n, t);
           continue;
         }
-        if (drow) t += g.beta * drow[n];
+        if (drow) t += db * drow[n];
         crow[n] = g.accumulate ? crow[n] + t : t;
       }
     }
@@ -254,6 +255,7 @@ __global__ void __launch_bounds__(kThr, 3) tc_gemm_kernel(TcGemm g) {
         (g.rowscale && m < g.M) ? g.rowscale[bo * g.sRb + bi * g.sRb2 + m] : 1.f;
     float* C = g.C + bo * g.sCb + bi * g.sCb2;
     const float* D = g.D ? g.D + bo * g.sDb + bi * g.sDb2 : nullptr;
+    const float db = g.beta * (g.dscale ? g.dscale[bo * g.sEb + bi * g.sEb2] : 1.f);
 #pragma unroll 1
     for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
       float acc[32];
@@ -264,7 +266,7 @@ __global__ void __launch_bounds__(kThr, 3) tc_gemm_kernel(TcGemm g) {
           const int n = n0 + c0 + x;
           if (n >= g.N) continue;
           float t = g.alpha * rs * acc[x];
-          if (D) t += g.beta * D[(long)m * g.sDm + (long)n * g.sDn];
+          if (D) t += db * D[(long)m * g.sDm + (long)n * g.sDn];
           float* c = C + (long)m * g.sCm + (long)n * g.sCn;
           *c = g.accumulate ? *c + t : t;
         }
