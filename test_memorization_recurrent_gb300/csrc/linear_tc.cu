@@ -79,7 +79,8 @@ constexpr uint32_t OFF_BARS = OFF_ELAST + kDim * 4;
 constexpr uint32_t SMEM_USED = OFF_BARS + 256;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;    // alignment slack
 
-constexpr uint32_t STAGE_TX = 4 * 8192 + 16384 + 3 * 256;
+constexpr uint32_t STAGE_TX = 4 * 8192 + 16384 + 3 * 256;  // with the gates (N % 4 == 0)
+constexpr uint32_t STAGE_TX_NOGATES = 4 * 8192 + 16384;
 
 // TMEM columns
 constexpr uint32_t TM_T = 0;       // [T | Qy]            (128)
@@ -103,6 +104,7 @@ constexpr int kRun = 0, kTimeout = 1, kHandOff = 2;
 
 struct TcParams {
   const __nv_bfloat16* K;
+  const float* alpha;
   const float* eta;
   const float* theta;
   const float* gamma;
@@ -112,6 +114,7 @@ struct TcParams {
   int* status;  // optional
   int* flags;   // [heads]: 1 = left to the CUDA-core kernel
   int N;
+  int gate_tma;  // gates loaded by TMA (N % 4 == 0, aligned rows), else with plain loads
 };
 
 struct TcMaps {
@@ -245,16 +248,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         unsigned char* st = sm + OFF_STAGE0 + s * STAGE_BYTES;
         uint64_t* fb = &bars[B_FULL0 + s];
-        mbar_arrive_expect_tx(fb, STAGE_TX);
+        mbar_arrive_expect_tx(fb, p.gate_tma ? STAGE_TX : STAGE_TX_NOGATES);
         const int t0 = j * kChunk;
         tma_load_3d(st + 0, &maps.k, fb, 0, t0, head);
         tma_load_3d(st + 8192, &maps.q, fb, 0, t0, head);
         tma_load_3d(st + 16384, &maps.k, fb, 64, t0, head);
         tma_load_3d(st + 24576, &maps.q, fb, 64, t0, head);
         tma_load_3d(st + ST_V, &maps.v, fb, 0, t0, head);
-        tma_load_2d(st + ST_GATES, &maps.alpha, fb, t0, head);
-        tma_load_2d(st + ST_GATES + 256, &maps.eta, fb, t0, head);
-        tma_load_2d(st + ST_GATES + 512, &maps.theta, fb, t0, head);
+        if (p.gate_tma) {  // gate rows of N floats start 16-byte aligned
+          tma_load_2d(st + ST_GATES, &maps.alpha, fb, t0, head);
+          tma_load_2d(st + ST_GATES + 256, &maps.eta, fb, t0, head);
+          tma_load_2d(st + ST_GATES + 512, &maps.theta, fb, t0, head);
+        }
         issued = j + 1;
       }
       // drain: every issued load must land before shared memory is released
@@ -276,9 +281,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         timeout();
         return false;
       }
-      const float* ga = reinterpret_cast<const float*>(sm + OFF_STAGE0 + s * STAGE_BYTES + ST_GATES);
-      const float* ge = ga + 64;
-      const float* gt = ga + 128;
+      float* ga = reinterpret_cast<float*>(sm + OFF_STAGE0 + s * STAGE_BYTES + ST_GATES);
+      float* ge = ga + 64;
+      float* gt = ga + 128;
+      if (!p.gate_tma) {  // plain loads into the stage (zero past the end, as TMA fills)
+        const long gb = (long)head * N + (long)j * kChunk;
+        const int nb = min(kChunk, N - j * kChunk);
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          const int n = 2 * lane + x;
+          ga[n] = n < nb ? p.alpha[gb + n] : 0.f;
+          ge[n] = n < nb ? p.eta[gb + n] : 0.f;
+          gt[n] = n < nb ? p.theta[gb + n] : 0.f;
+        }
+        __syncwarp();
+      }
       float* tb = table(sm, j & 1);
       float *a = tb, *wb = tb + kChunk, *cn = tb + 2 * kChunk;
       const unsigned full = 0xFFFFFFFFu;
@@ -634,16 +651,15 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 bool linear_tc_supported(const LinArgs& a) {
   return a.d_k == kDim && a.d_v == kDim && a.D == kDim && a.b == kChunk && a.c == 1 && !a.poly &&
-         !a.dot && a.bf16 && a.N > 0 && (a.N % 4) == 0;
+         !a.dot && a.bf16 && a.N > 0;
 }
 
 size_t linear_tc_workspace_bytes(int heads) { return (size_t)heads * sizeof(int); }
 
 int linear_tc_launch(const LinArgs& a, int heads, int* status, void* workspace, cudaStream_t st) {
   if (!linear_tc_supported(a)) return ATLAS_ERR_UNSUPPORTED;
-  if (!aligned16(a.K) || !aligned16(a.Q) || !aligned16(a.V) || !aligned16(a.alpha) ||
-      !aligned16(a.eta) || !aligned16(a.theta) || !aligned16(a.Y) || !aligned16(a.M) ||
-      (a.S && !aligned16(a.S)))
+  if (!aligned16(a.K) || !aligned16(a.Q) || !aligned16(a.V) || !aligned16(a.Y) ||
+      !aligned16(a.M) || (a.S && !aligned16(a.S)))
     return ATLAS_ERR_UNSUPPORTED;
   if (!workspace) return ATLAS_ERR_WORKSPACE;
   if (!encoder()) return ATLAS_ERR_CUDA;
@@ -651,12 +667,20 @@ int linear_tc_launch(const LinArgs& a, int heads, int* status, void* workspace, 
   if (!make_map_tokens(&maps.k, a.K, a.N, heads, 64, true) ||
       !make_map_tokens(&maps.q, a.Q, a.N, heads, 64, true) ||
       !make_map_tokens(&maps.v, a.V, a.N, heads, 128, false) ||
-      !make_map_gate(&maps.alpha, a.alpha, a.N, heads) ||
-      !make_map_gate(&maps.eta, a.eta, a.N, heads) ||
-      !make_map_gate(&maps.theta, a.theta, a.N, heads) || !make_map_y(&maps.y, a.Y, a.N, heads))
+      !make_map_y(&maps.y, a.Y, a.N, heads))
+    return ATLAS_ERR_CUDA;
+  const bool gate_tma =
+      (a.N % 4) == 0 && aligned16(a.alpha) && aligned16(a.eta) && aligned16(a.theta);
+  memset(&maps.alpha, 0, sizeof(maps.alpha));
+  memset(&maps.eta, 0, sizeof(maps.eta));
+  memset(&maps.theta, 0, sizeof(maps.theta));
+  if (gate_tma && (!make_map_gate(&maps.alpha, a.alpha, a.N, heads) ||
+                   !make_map_gate(&maps.eta, a.eta, a.N, heads) ||
+                   !make_map_gate(&maps.theta, a.theta, a.N, heads)))
     return ATLAS_ERR_CUDA;
   TcParams p;
   p.K = reinterpret_cast<const __nv_bfloat16*>(a.K);
+  p.alpha = a.alpha;
   p.eta = a.eta;
   p.theta = a.theta;
   p.gamma = a.gamma;
@@ -666,6 +690,7 @@ int linear_tc_launch(const LinArgs& a, int heads, int* status, void* workspace, 
   p.status = status;
   p.flags = reinterpret_cast<int*>(workspace);
   p.N = a.N;
+  p.gate_tma = gate_tma ? 1 : 0;
   if (cudaFuncSetAttribute(linear_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)SMEM_ALLOC) != cudaSuccess)
     return ATLAS_ERR_CUDA;

@@ -280,12 +280,13 @@ def test_tensor_core_path_selected_for_the_deltanet_workload():
     w = W.workload(2)
     assert A.atlas_mem_path(cfg_for(w, w.heads, w.N)) == "linear_tc"
     assert A.atlas_mem_path(cfg_for(w, 3, 212)) == "linear_tc"
-    assert A.atlas_mem_path(cfg_for(w, 3, 209)) == "linear_simt"  # N % 4 != 0
+    assert A.atlas_mem_path(cfg_for(w, 3, 209)) == "linear_tc"  # gates by plain loads
 
 
-@pytest.mark.parametrize("N", [64, 212, 64 * 5])
+@pytest.mark.parametrize("N", [64, 212, 64 * 5, 209, 1, 63])
 def test_tensor_core_path_small(N):
-    """Several chunks and a ragged tail (N = 212) through the tcgen05 kernel."""
+    """Several chunks and a ragged tail (N = 212) through the tcgen05 kernel; lengths
+    that are not a multiple of 4 (gate rows not 16-byte aligned: plain gate loads)."""
     w = W.workload(2, N=N)
     inp = W.generate(w, heads=[0, 3, 8, 13])
     inp["M0"] = (np.random.default_rng(N).standard_normal(inp["M0"].shape) * 0.1).astype(np.float32)
