@@ -26,7 +26,7 @@ _LIB = os.path.join(_HERE, "_build", "libatlas_oracle.so")
 
 MEM_LINEAR, MEM_MLP = 0, 1
 PHI_IDENTITY, PHI_POLY2 = 0, 1
-LOSS_L2, LOSS_DOT = 0, 1
+LOSS_L2, LOSS_DOT, LOSS_LP, LOSS_HUBER = 0, 1, 2, 3
 
 
 class OrcCfg(ctypes.Structure):
@@ -37,6 +37,7 @@ class OrcCfg(ctypes.Structure):
         ("ns_steps", ctypes.c_int), ("ns_a", ctypes.c_double),
         ("ns_b", ctypes.c_double), ("ns_c", ctypes.c_double),
         ("ns_eps", ctypes.c_double), ("n_history", ctypes.c_int),
+        ("loss_param", ctypes.c_double),
     ]
 
 
@@ -96,10 +97,12 @@ def _f64(a) -> np.ndarray:
 
 
 def make_cfg(N, d_k, d_v, d_h=0, mem=MEM_LINEAR, phi=PHI_IDENTITY, loss=LOSS_L2, c=1, b=1,
-             ns_steps=0, ns_a=0.0, ns_b=0.0, ns_c=0.0, ns_eps=0.0, n_history=0) -> OrcCfg:
+             ns_steps=0, ns_a=0.0, ns_b=0.0, ns_c=0.0, ns_eps=0.0, n_history=0,
+             loss_param=0.0) -> OrcCfg:
+    """loss_param: p of the l_p bias, delta of the Huber bias (unused otherwise)."""
     return OrcCfg(int(N), int(d_k), int(d_v), int(d_h), int(mem), int(phi), int(loss),
                   int(c), int(b), int(ns_steps), float(ns_a), float(ns_b), float(ns_c),
-                  float(ns_eps), int(n_history))
+                  float(ns_eps), int(n_history), float(loss_param))
 
 
 def feature_dim(cfg: OrcCfg) -> int:

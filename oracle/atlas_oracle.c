@@ -24,9 +24,10 @@
  *             MLP memory, expansion 4, GELU).
  *   [Miras]   "It's All Connected: A Journey Through Test-Time Memorization,
  *             ..." (still-with-you.github.io), Associative Memory & Attentional
- *             Bias (linear attention = GD on -2<Mk, v>), Training (chunk-wise
- *             parallelisation at the chunk-start state, Miras layer outputs
- *             M(q_t)).
+ *             Bias (linear attention = GD on -2<Mk, v>), #1 Alternative
+ *             Attentional Biases (l_p loss ||M(k) - v||_p^p, Huber loss),
+ *             Training (chunk-wise parallelisation at the chunk-start state,
+ *             Miras layer outputs M(q_t)).
  *
  * Readings taken where the pages are silent or disagree (each one is listed
  * in the design notes of the repository):
@@ -43,7 +44,11 @@
  *   - MLP memory M(x) = x + W1 GELU(W2 x) without LayerNorm, exact (erf) GELU;
  *   - Newton-Schulz (when enabled) acts on the momentum of each weight matrix
  *     separately, per token: M_t = (1 - alpha_t) M_{t-1} + NS(S_t), with
- *     X_0 = S / (||S||_F + eps) and the literal X X^T Gram.
+ *     X_0 = S / (||S||_F + eps) and the literal X X^T Gram;
+ *   - the Huber bias is taken per coordinate with one threshold delta for all
+ *     tokens, scaled to agree with the l2 bias inside the threshold:
+ *     h(e) = e^2 for |e| <= delta, 2 delta |e| - delta^2 beyond (the pages let
+ *     delta vary per token and channel; a constant is the plainest case).
  */
 #include <math.h>
 #include <pthread.h>
@@ -57,6 +62,8 @@
 #define ORC_PHI_POLY2 1
 #define ORC_LOSS_L2 0
 #define ORC_LOSS_DOT 1
+#define ORC_LOSS_LP 2
+#define ORC_LOSS_HUBER 3
 
 /* Per-head problem description.  All tensors handed to the oracle are fp64,
  * one head after another. */
@@ -67,13 +74,14 @@ typedef struct {
   int d_h;      /* MLP hidden width (MLP memory only) */
   int mem;      /* ORC_MEM_LINEAR or ORC_MEM_MLP */
   int phi;      /* ORC_PHI_IDENTITY or ORC_PHI_POLY2 (linear memory only) */
-  int loss;     /* ORC_LOSS_L2 or ORC_LOSS_DOT */
+  int loss;     /* ORC_LOSS_L2, _DOT, _LP or _HUBER */
   int c;        /* Omega window length, >= 1 */
   int b;        /* chunk length, >= 1 (1 = token recurrence) */
   int ns_steps; /* Newton-Schulz iterations on the momentum, 0 = none */
   double ns_a, ns_b, ns_c, ns_eps;
   int n_history; /* tokens before the first processed one: K, V rows that only
                     enter the windows of processed tokens (they update nothing) */
+  double loss_param; /* p of the l_p bias (>= 1), delta of the Huber bias (> 0) */
 } orc_cfg;
 
 /* ------------------------------------------------------------------ sizes */
@@ -152,10 +160,30 @@ void orc_memory_apply(const orc_cfg* g, const double* state, const double* x, do
 
 /* ------------------------------------------------------- loss gradient */
 
+/* Derivative of the bias with respect to one output coordinate y, with
+ * e = y - v.  [Titans] Objective: l2, sum e^2 -> 2 e.  [Miras] #1 Alternative
+ * Attentional Biases: l_p, sum |e|^p -> p |e|^(p-1) sign(e); Huber (per
+ * coordinate, see the readings above) -> 2 e inside the threshold,
+ * 2 delta sign(e) beyond. */
+static double orc_bias_dy(const orc_cfg* g, double e) {
+  if (g->loss == ORC_LOSS_LP) {
+    if (e == 0.0) return 0.0;
+    const double s = e > 0.0 ? 1.0 : -1.0;
+    return g->loss_param * pow(fabs(e), g->loss_param - 1.0) * s;
+  }
+  if (g->loss == ORC_LOSS_HUBER) {
+    const double d = g->loss_param;
+    if (fabs(e) <= d) return 2.0 * e;
+    return e > 0.0 ? 2.0 * d : -2.0 * d;
+  }
+  return 2.0 * e;
+}
+
 /* Gradient of the attentional bias with respect to the memory state, written
  * into G (state layout).
  *   l2  ([Titans] Objective; [ATLAS] §3.1):  l = ||M(Phi(k)) - v||^2.
  *   dot ([Miras] Associative Memory & Attentional Bias): l = -2 <M(Phi(k)), v>.
+ *   l_p, Huber ([Miras] #1 Alternative Attentional Biases): orc_bias_dy.
  * For the MLP the gradient is plain backpropagation through
  * y = k + W1 h, h = GELU(z), z = W2 k. */
 void orc_grad(const orc_cfg* g, const double* state, const double* k, const double* v, double* G) {
@@ -166,15 +194,15 @@ void orc_grad(const orc_cfg* g, const double* state, const double* k, const doub
     orc_phi(g, k, f);
     for (int r = 0; r < dv; ++r) {
       if (g->loss == ORC_LOSS_DOT) {
-        e[r] = -v[r];               /* dl/d(M Phi) = -2 v */
+        e[r] = -2.0 * v[r];         /* dl/d(M Phi) = -2 v */
       } else {
         double s = 0.0;
         for (int j = 0; j < D; ++j) s += state[(long)r * D + j] * f[j];
-        e[r] = s - v[r];            /* dl/d(M Phi) = 2 (M Phi - v) */
+        e[r] = orc_bias_dy(g, s - v[r]);  /* l2: dl/d(M Phi) = 2 (M Phi - v) */
       }
     }
     for (int r = 0; r < dv; ++r)
-      for (int j = 0; j < D; ++j) G[(long)r * D + j] = 2.0 * e[r] * f[j];
+      for (int j = 0; j < D; ++j) G[(long)r * D + j] = e[r] * f[j];
     free(f);
     free(e);
     return;
@@ -200,7 +228,7 @@ void orc_grad(const orc_cfg* g, const double* state, const double* k, const doub
     } else {
       double y = k[r];
       for (int j = 0; j < dh; ++j) y += W1[(long)r * dh + j] * h[j];
-      dy[r] = 2.0 * (y - v[r]);
+      dy[r] = orc_bias_dy(g, y - v[r]);
     }
   }
   /* dl/dW1 = dy h^T */
@@ -396,7 +424,9 @@ static int orc_check(const orc_cfg* g) {
   if (g->n_history < 0) return -1;
   if (g->mem == ORC_MEM_MLP && (g->d_h <= 0 || g->d_k != g->d_v)) return -1;
   if (g->mem != ORC_MEM_LINEAR && g->mem != ORC_MEM_MLP) return -1;
-  if (g->loss != ORC_LOSS_L2 && g->loss != ORC_LOSS_DOT) return -1;
+  if (g->loss < ORC_LOSS_L2 || g->loss > ORC_LOSS_HUBER) return -1;
+  if (g->loss == ORC_LOSS_LP && !(g->loss_param >= 1.0 && g->loss_param < 1e6)) return -1;
+  if (g->loss == ORC_LOSS_HUBER && !(g->loss_param > 0.0)) return -1;
   return 0;
 }
 

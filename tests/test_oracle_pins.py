@@ -91,10 +91,20 @@ def test_gelu_prime_by_finite_differences(x):
 
 
 def _loss(cfg, state, k, v):
+    """The attentional biases written out: l2 and dot (Titans Objective, Miras
+    Associative Memory), l_p and Huber (Miras #1 Alternative Attentional Biases;
+    Huber per coordinate, equal to e^2 inside the threshold)."""
     y = oracle.memory_apply(cfg, state, k)
+    e = y - v
     if cfg.loss == oracle.LOSS_DOT:
         return -2.0 * float(np.dot(y, v))
-    return float(np.sum((y - v) ** 2))
+    if cfg.loss == oracle.LOSS_LP:
+        return float(np.sum(np.abs(e) ** cfg.loss_param))
+    if cfg.loss == oracle.LOSS_HUBER:
+        d = cfg.loss_param
+        a = np.abs(e)
+        return float(np.sum(np.where(a <= d, e ** 2, 2 * d * a - d * d)))
+    return float(np.sum(e ** 2))
 
 
 def _fd_grad(cfg, state, k, v, h=1e-6):
@@ -107,10 +117,14 @@ def _fd_grad(cfg, state, k, v, h=1e-6):
     return g
 
 
-@pytest.mark.parametrize("loss", [oracle.LOSS_L2, oracle.LOSS_DOT])
-def test_mlp_gradient_by_finite_differences(loss):
+BIASES = [(oracle.LOSS_L2, 0.0), (oracle.LOSS_DOT, 0.0), (oracle.LOSS_LP, 3.0),
+          (oracle.LOSS_LP, 1.5), (oracle.LOSS_HUBER, 0.4)]
+
+
+@pytest.mark.parametrize("loss,prm", BIASES)
+def test_mlp_gradient_by_finite_differences(loss, prm):
     d, dh = 4, 6
-    cfg = oracle.make_cfg(1, d, d, dh, mem=oracle.MEM_MLP, loss=loss)
+    cfg = oracle.make_cfg(1, d, d, dh, mem=oracle.MEM_MLP, loss=loss, loss_param=prm)
     state = RNG.standard_normal(2 * d * dh) * 0.7
     k, v = RNG.standard_normal(d), RNG.standard_normal(d)
     np.testing.assert_allclose(oracle.grad(cfg, state, k, v), _fd_grad(cfg, state, k, v),
@@ -118,15 +132,65 @@ def test_mlp_gradient_by_finite_differences(loss):
 
 
 @pytest.mark.parametrize("phi", [oracle.PHI_IDENTITY, oracle.PHI_POLY2])
-@pytest.mark.parametrize("loss", [oracle.LOSS_L2, oracle.LOSS_DOT])
-def test_linear_gradient_by_finite_differences(phi, loss):
-    d_k, d_v = 3, 2
-    cfg = oracle.make_cfg(1, d_k, d_v, phi=phi, loss=loss)
+@pytest.mark.parametrize("loss,prm", BIASES)
+def test_linear_gradient_by_finite_differences(phi, loss, prm):
+    d_k, d_v = 3, 4
+    cfg = oracle.make_cfg(1, d_k, d_v, phi=phi, loss=loss, loss_param=prm)
     D = oracle.feature_dim(cfg)
     state = RNG.standard_normal(d_v * D)
     k, v = RNG.standard_normal(d_k), RNG.standard_normal(d_v)
     np.testing.assert_allclose(oracle.grad(cfg, state, k, v), _fd_grad(cfg, state, k, v),
                                rtol=1e-7, atol=1e-8)
+
+
+@pytest.mark.parametrize("mem", [oracle.MEM_LINEAR, oracle.MEM_MLP])
+def test_lp_with_p2_and_huber_with_a_huge_threshold_are_the_l2_bias(mem):
+    """|e|^2 is e^2, and a Huber threshold above every error never clips: both
+    runs must equal the l2 run to the last bit (the gradient 2 |e| sign(e) and
+    2 e are the same number)."""
+    H, N, d, dh = 2, 37, 4, 8
+    rng = np.random.default_rng(5)
+    K, Q, V, a, e, t = rand_inputs(rng, H, N, d, d, theta=(0.005, 0.03))  # bounded trajectory
+    kw = dict(c=3, b=4, d_h=dh if mem == oracle.MEM_MLP else 0, mem=mem)
+    M0 = None if mem == oracle.MEM_LINEAR else rng.standard_normal((H, 2 * d * dh)) * 0.1
+    base = run(oracle.make_cfg(N, d, d, **kw), K, Q, V, a, e, t, np.ones(3), M0)
+    for loss, prm in ((oracle.LOSS_LP, 2.0), (oracle.LOSS_HUBER, 1e300)):
+        out = run(oracle.make_cfg(N, d, d, loss=loss, loss_param=prm, **kw), K, Q, V, a, e, t,
+                  np.ones(3), M0)
+        for x, y in zip(out, base):
+            assert np.isfinite(y).all() and np.array_equal(x, y)
+
+
+@pytest.mark.parametrize("loss,prm,step", [
+    (oracle.LOSS_HUBER, 0.05, lambda v, prm: 2 * prm * np.sign(v)),  # every |v| > delta: clipped
+    (oracle.LOSS_LP, 1.0, lambda v, prm: np.sign(v)),                # sign of the error only
+    (oracle.LOSS_LP, 3.0, lambda v, prm: 3 * v * np.abs(v)),
+])
+def test_first_token_under_the_alternative_biases(loss, prm, step):
+    """From M_0 = 0, S_0 = 0 the first error is e = -v, so
+    S_1 = -theta_1 dl/dM = theta_1 psi(v) k^T with psi the bias derivative, and
+    y_1 = (1 - alpha_1) 0 + S_1 q = theta_1 (k . q) psi(v): Huber's
+    2 delta sign(v) beyond the threshold, l_1's sign(v) (the pages' value-less
+    +-1 memory), l_3's 3 v |v|."""
+    H, N, d = 3, 1, 5
+    rng = np.random.default_rng(9)
+    K, Q, _, a, e, t = rand_inputs(rng, H, N, d, d)
+    V = np.sign(rng.standard_normal((H, N, d))) * rng.uniform(0.2, 1.5, (H, N, d))
+    cfg = oracle.make_cfg(N, d, d, loss=loss, loss_param=prm)
+    Y, M, S = run(cfg, K, Q, V, a, e, t, np.ones(1))
+    for h in range(H):
+        k, q, v = K[h, 0], Q[h, 0], V[h, 0]
+        ref = t[h, 0] * np.dot(k, q) * step(v, prm)
+        np.testing.assert_allclose(Y[h, 0], ref, rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(M[h].reshape(d, d), t[h, 0] * np.outer(step(v, prm), k),
+                                   rtol=1e-13, atol=1e-15)
+
+
+def test_invalid_bias_parameters_are_rejected():
+    K, Q, V, a, e, t = rand_inputs(RNG, 1, 4, 3, 3)
+    for loss, prm in ((oracle.LOSS_LP, 0.5), (oracle.LOSS_HUBER, 0.0), (7, 1.0)):
+        with pytest.raises(Exception):
+            run(oracle.make_cfg(4, 3, 3, loss=loss, loss_param=prm), K, Q, V, a, e, t, np.ones(1))
 
 
 def test_mlp_memory_apply_residual_form():
