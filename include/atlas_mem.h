@@ -55,6 +55,11 @@ extern "C" {
 /* attentional bias */
 #define ATLAS_LOSS_L2 0  /* ||M(Phi(k)) - v||^2 (gradient carries the factor 2) */
 #define ATLAS_LOSS_DOT 1 /* -2 <M(Phi(k)), v> (linear memory only: linear attention) */
+/* Miras alternative attentional biases ("It's All Connected: ...", #1 Alternative
+ * Attentional Biases), e = M(Phi(k)) - v per output coordinate: */
+#define ATLAS_LOSS_LP 2    /* sum |e|^p, p = loss_param >= 1 (gradient p |e|^(p-1) sign e) */
+#define ATLAS_LOSS_HUBER 3 /* sum e^2 for |e| <= delta, 2 delta |e| - delta^2 beyond, with
+                              delta = loss_param > 0 (gradient 2 clamp(e, -delta, delta)) */
 /* K, Q, V element type */
 #define ATLAS_F32 0
 #define ATLAS_BF16 1
@@ -73,6 +78,7 @@ typedef struct atlas_mem_cfg {
   int mem;            /* ATLAS_MEM_* */
   int phi;            /* ATLAS_PHI_* */
   int loss;           /* ATLAS_LOSS_* */
+  float loss_param;   /* p of ATLAS_LOSS_LP, delta of ATLAS_LOSS_HUBER; unused otherwise */
   int c;              /* Omega window length (>= 1); gamma has c entries */
   int b;              /* chunk length (>= 1); 1 = token recurrence */
   int ns_steps;       /* Newton-Schulz iterations on the momentum, 0 = plain momentum */

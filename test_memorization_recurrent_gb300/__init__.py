@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(HERE, "_build", "libatlasmem.so")
 
 MEM_LINEAR, MEM_MLP = 0, 1
 PHI_IDENTITY, PHI_POLY2 = 0, 1
-LOSS_L2, LOSS_DOT = 0, 1
+LOSS_L2, LOSS_DOT, LOSS_LP, LOSS_HUBER = 0, 1, 2, 3
 F32, BF16 = 0, 1
 
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
@@ -33,7 +33,7 @@ class AtlasMemCfg(ctypes.Structure):
         ("B", ctypes.c_int), ("H", ctypes.c_int), ("N", ctypes.c_int),
         ("d_k", ctypes.c_int), ("d_v", ctypes.c_int), ("d_h", ctypes.c_int),
         ("mem", ctypes.c_int), ("phi", ctypes.c_int), ("loss", ctypes.c_int),
-        ("c", ctypes.c_int), ("b", ctypes.c_int),
+        ("loss_param", ctypes.c_float), ("c", ctypes.c_int), ("b", ctypes.c_int),
         ("ns_steps", ctypes.c_int), ("ns_a", ctypes.c_float), ("ns_b", ctypes.c_float),
         ("ns_c", ctypes.c_float), ("ns_eps", ctypes.c_float),
         ("in_dtype", ctypes.c_int),
@@ -86,9 +86,11 @@ def load_library(path: str = LIB_PATH):
 def make_cfg(B, H, N, d_k, d_v, d_h=0, mem=MEM_LINEAR, phi=PHI_IDENTITY, loss=LOSS_L2, c=1,
              b=1, ns_steps=0, ns_a=0.0, ns_b=0.0, ns_c=0.0, ns_eps=0.0, in_dtype=BF16,
              S_state=None, workspace=None, workspace_bytes=0, status_dev=None,
-             n_history=0) -> AtlasMemCfg:
+             n_history=0, loss_param=0.0) -> AtlasMemCfg:
+    """loss_param: p of LOSS_LP, delta of LOSS_HUBER (unused otherwise)."""
     return AtlasMemCfg(int(B), int(H), int(N), int(d_k), int(d_v), int(d_h), int(mem), int(phi),
-                       int(loss), int(c), int(b), int(ns_steps), float(ns_a), float(ns_b),
+                       int(loss), float(loss_param), int(c), int(b), int(ns_steps), float(ns_a),
+                       float(ns_b),
                        float(ns_c), float(ns_eps), int(in_dtype), _ptr(S_state), int(n_history),
                        _ptr(workspace), int(workspace_bytes), _ptr(status_dev))
 

@@ -28,14 +28,18 @@ int check_cfg(const atlas_mem_cfg* c) {
   if (c->d_k <= 0 || c->d_v <= 0 || c->c < 1 || c->b < 1) return ATLAS_ERR_INVALID;
   if (c->mem != ATLAS_MEM_LINEAR && c->mem != ATLAS_MEM_MLP) return ATLAS_ERR_INVALID;
   if (c->phi != ATLAS_PHI_IDENTITY && c->phi != ATLAS_PHI_POLY2) return ATLAS_ERR_INVALID;
-  if (c->loss != ATLAS_LOSS_L2 && c->loss != ATLAS_LOSS_DOT) return ATLAS_ERR_INVALID;
+  if (c->loss < ATLAS_LOSS_L2 || c->loss > ATLAS_LOSS_HUBER) return ATLAS_ERR_INVALID;
+  if (c->loss == ATLAS_LOSS_LP && !(c->loss_param >= 1.f && c->loss_param < 1e6f))
+    return ATLAS_ERR_INVALID;
+  if (c->loss == ATLAS_LOSS_HUBER && !(c->loss_param > 0.f && c->loss_param < 3e38f))
+    return ATLAS_ERR_INVALID;
   if (c->in_dtype != ATLAS_F32 && c->in_dtype != ATLAS_BF16) return ATLAS_ERR_INVALID;
   if (c->ns_steps < 0 || c->n_history < 0) return ATLAS_ERR_INVALID;
   if ((long)c->B * c->H > 65535L * 1024) return ATLAS_ERR_UNSUPPORTED;
   if (c->mem == ATLAS_MEM_MLP) {
     if (c->d_h <= 0 || c->d_k != c->d_v) return ATLAS_ERR_INVALID;
     if (c->phi != ATLAS_PHI_IDENTITY) return ATLAS_ERR_INVALID;
-    if (c->loss != ATLAS_LOSS_L2) return ATLAS_ERR_UNSUPPORTED;
+    if (c->loss == ATLAS_LOSS_DOT) return ATLAS_ERR_UNSUPPORTED;
   } else {
     if (c->ns_steps > 0) return ATLAS_ERR_UNSUPPORTED;
     if (c->phi == ATLAS_PHI_POLY2 && c->d_k > 64) return ATLAS_ERR_UNSUPPORTED;
@@ -54,6 +58,8 @@ LinArgs lin_args(const void* K, const void* Q, const void* V, const float* alpha
   a.c = c->c; a.b = c->b;
   a.poly = c->phi == ATLAS_PHI_POLY2;
   a.dot = c->loss == ATLAS_LOSS_DOT;
+  a.lk = c->loss;
+  a.lp = c->loss_param;
   a.bf16 = c->in_dtype == ATLAS_BF16;
   a.nh = c->n_history;
   return a;
@@ -69,6 +75,8 @@ MlpArgs mlp_args(const void* K, const void* Q, const void* V, const float* alpha
   a.heads = c->B * c->H; a.N = c->N; a.d = c->d_k; a.dh = c->d_h; a.c = c->c; a.b = c->b;
   a.nh = c->n_history;
   a.bf16 = c->in_dtype == ATLAS_BF16;
+  a.lk = c->loss;
+  a.lp = c->loss_param;
   a.ns_steps = c->ns_steps;
   a.ns_a = c->ns_a; a.ns_b = c->ns_b; a.ns_c = c->ns_c; a.ns_eps = c->ns_eps;
   a.s_is_zero = c->S_state == nullptr;

@@ -14,6 +14,22 @@ __device__ __forceinline__ float ld_in(const void* p, long idx, int bf16) {
   return reinterpret_cast<const float*>(p)[idx];
 }
 
+// Attentional bias, per output coordinate with error e = y - v, in units of the
+// l2 bias's derivative 2e ("It's All Connected: ...", #1 Alternative Attentional
+// Biases): l2 (and the dot product, whose "error" is already -v): e; l_p,
+// sum |e|^p: (p/2) |e|^(p-1) sign(e); Huber with threshold delta (per
+// coordinate, e^2 inside): e clamped to [-delta, delta].
+__device__ __forceinline__ float bias_grad(float e, int kind, float prm) {
+  if (kind == ATLAS_LOSS_LP) {
+    const float a = fabsf(e);
+    if (a == 0.f) return 0.f;
+    const float m = prm == 3.f ? a * a : prm == 2.f ? a : powf(a, prm - 1.f);
+    return copysignf(0.5f * prm * m, e);
+  }
+  if (kind == ATLAS_LOSS_HUBER) return fminf(fmaxf(e, -prm), prm);
+  return e;
+}
+
 // Feature j of Phi(x) for x in shared memory.  Degree-2 map (ATLAS review
 // §3.1, constant dropped): j < d -> x_j; otherwise the product x_p x_q of the
 // pair (p <= q) in i-major order, looked up in the pair table.

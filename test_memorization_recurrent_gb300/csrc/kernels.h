@@ -19,6 +19,8 @@ struct LinArgs {
   float* S;  // [heads, d_v, D] in/out, or nullptr (start at zero, not returned)
   int N, d_k, d_v, D, c, b;
   int poly, dot, bf16;
+  int lk;    // attentional bias: 0 l2, 1 dot, 2 l_p, 3 Huber (ATLAS_LOSS_*)
+  float lp;  // its parameter (p, delta)
   int nh;  // history rows ahead of token 0 in K and V (head stride (nh + N) rows)
 };
 
@@ -91,6 +93,8 @@ struct MlpArgs {
   int heads, N, d, dh, c, b;
   int nh;  // history rows ahead of token 0 in K and V
   int bf16;
+  int lk;    // attentional bias: 0 l2, 2 l_p, 3 Huber (ATLAS_LOSS_*)
+  float lp;  // its parameter (p, delta)
   int ns_steps;
   float ns_a, ns_b, ns_c, ns_eps;
   int s_is_zero;  // S must be cleared before the first chunk

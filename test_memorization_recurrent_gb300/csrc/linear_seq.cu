@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kThr) linear_seq_kernel(LinArgs p) {
       float g[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < C; ++j) {
-        const float w = gam[j] * (e[j] - cur.v[j]);
+        const float w = gam[j] * bias_grad(e[j] - cur.v[j], p.lk, p.lp);
         g[0] += w * cur.k[j].x;
         g[1] += w * cur.k[j].y;
         g[2] += w * cur.k[j].z;

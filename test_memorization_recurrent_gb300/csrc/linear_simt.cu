@@ -148,7 +148,7 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
         const float* k = Kw + i * dk;
         float s = 0.f;
         for (int j = 0; j < D; ++j) s += m[j] * phi_at(k, j, dk, pp, pq, p.poly);
-        e = s - Vw[x];
+        e = bias_grad(s - Vw[x], p.lk, p.lp);
       }
       E[x] = e;
     }

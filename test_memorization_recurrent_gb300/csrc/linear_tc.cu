@@ -115,6 +115,8 @@ struct TcParams {
   int* flags;   // [heads]: 1 = left to the CUDA-core kernel
   int N;
   int gate_tma;  // gates loaded by TMA (N % 4 == 0, aligned rows), else with plain loads
+  int lk;        // attentional bias (ATLAS_LOSS_L2, _LP or _HUBER)
+  float lp;      // its parameter
 };
 
 struct TcMaps {
@@ -485,6 +487,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tl + TM_T + 32 * h, e);
 #pragma unroll
         for (int x = 0; x < 32; ++x) e[x] -= vt[x];
+        if (p.lk != ATLAS_LOSS_L2) {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) e[x] = bias_grad(e[x], p.lk, p.lp);
+        }
         if (p.S && j == nchunks - 1) {
           const int il = N - 1 - t0 - 32 * h;
           if (il >= 0 && il < 32) {
@@ -691,6 +697,8 @@ int linear_tc_launch(const LinArgs& a, int heads, int* status, void* workspace, 
   p.flags = reinterpret_cast<int*>(workspace);
   p.N = a.N;
   p.gate_tma = gate_tma ? 1 : 0;
+  p.lk = a.lk;
+  p.lp = a.lp;
   if (cudaFuncSetAttribute(linear_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)SMEM_ALLOC) != cudaSuccess)
     return ATLAS_ERR_CUDA;

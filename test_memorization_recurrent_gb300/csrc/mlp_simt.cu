@@ -268,6 +268,14 @@ __global__ void copy_q_kernel(const float* ws, long per_head, long Qc, float* Y,
     Y[(long)h * N * d + (long)(t0 + n_lo) * d + x] = q[n_lo * d + x];
 }
 
+// E <- the attentional bias's derivative of E (in units of the l2 bias's 2e),
+// rows of every head.
+__global__ void bias_rows_kernel(float* ws, long per_head, long n, int kind, float prm) {
+  float* e = ws + (long)blockIdx.y * per_head;
+  for (long x = blockIdx.x * (long)blockDim.x + threadIdx.x; x < n; x += (long)gridDim.x * blockDim.x)
+    e[x] = bias_grad(e[x], kind, prm);
+}
+
 // X[inst][block] = S[inst][block] / (||S[inst][block]||_F + eps), in place; one
 // CTA per (instance, block).
 __global__ void ns_normalize_kernel(float* X, long state, long half, float eps) {
@@ -353,9 +361,10 @@ static dim3 ew_grid(long n, int heads) {
 
 long mlp_simt_launch_count(const MlpArgs& a) {
   const long chunks = (a.N + a.b - 1) / a.b;
+  const long bias = a.lk != ATLAS_LOSS_L2 ? 1 : 0;  // the bias kernel on E
   if (a.ns_steps > 0)
-    return 1 + chunks * (ns_fused_supported(a.d, a.dh) ? 16 : 16 + 6L * a.ns_steps);
-  return 1 + chunks * (4 + 1 + 3 + 1 + 4 + 4 + 1 + 4);
+    return 1 + chunks * (bias + (ns_fused_supported(a.d, a.dh) ? 16 : 16 + 6L * a.ns_steps));
+  return 1 + chunks * (bias + 4 + 1 + 3 + 1 + 4 + 4 + 1 + 4);
 }
 
 int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
@@ -395,6 +404,11 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
     g.C = ws + w.E; g.sCb = PH; g.sCm = d; g.sCn = 1;
     g.accumulate = 1;
     CK(run_gemm(g, st));
+    if (p.lk != ATLAS_LOSS_L2) {  // the attentional bias acts on E elementwise
+      bias_rows_kernel<<<ew_grid((long)L * d, H), 256, 0, st>>>(ws + w.E, PH, (long)L * d, p.lk,
+                                                               p.lp);
+      CL();
+    }
     // Delta = (E W1) * GELU'(Z)
     g = gemm0();
     g.batch = H; g.M = L; g.N = (int)dh; g.K = (int)d;

@@ -17,7 +17,8 @@ def cfg_for(w, heads: int, N: int, S_state=None, workspace=None, workspace_bytes
             status_dev=None, n_history: int = 0) -> AtlasMemCfg:
     """Config of workload ``w`` with ``heads`` heads (as B = 1, H = heads) and N tokens."""
     a, b_, c_ = w.ns_coef
-    return make_cfg(1, heads, N, w.d_k, w.d_v, w.d_h, mem=w.mem, phi=w.phi, loss=w.loss, c=w.c,
+    return make_cfg(1, heads, N, w.d_k, w.d_v, w.d_h, mem=w.mem, phi=w.phi, loss=w.loss,
+                    loss_param=w.loss_param, c=w.c,
                     b=w.b, ns_steps=w.ns_steps, ns_a=a, ns_b=b_, ns_c=c_, ns_eps=w.ns_eps,
                     in_dtype=BF16 if w.bf16 else F32, S_state=S_state, workspace=workspace,
                     workspace_bytes=workspace_bytes, status_dev=status_dev, n_history=n_history)

@@ -74,7 +74,9 @@ def _bad(**kw):
     (dict(b=0), A.ERR_INVALID),
     (dict(mem=7), A.ERR_INVALID),
     (dict(phi=3), A.ERR_INVALID),
-    (dict(loss=2), A.ERR_INVALID),
+    (dict(loss=4), A.ERR_INVALID),
+    (dict(loss=A.LOSS_LP, loss_param=0.5), A.ERR_INVALID),      # p < 1
+    (dict(loss=A.LOSS_HUBER, loss_param=0.0), A.ERR_INVALID),   # delta must be > 0
     (dict(in_dtype=5), A.ERR_INVALID),
     (dict(mem=A.MEM_MLP, d_h=0), A.ERR_INVALID),
     (dict(mem=A.MEM_MLP, d_h=16, d_v=4), A.ERR_INVALID),
@@ -112,3 +114,17 @@ def test_zero_heads_is_a_no_op(lib):
 def test_invalid_workspace_query():
     with pytest.raises(A.AtlasError):
         A.atlas_mem_workspace_bytes(_bad(b=0))
+
+
+def test_alternative_biases_choose_paths_that_apply_them(lib):
+    """l_p and Huber act on the error elementwise in the token-serial, CUDA-core and
+    tensor-core linear kernels and in the CUDA-core MLP path; the wide-feature
+    linear path and the tensor-core MLP kernel take only l2 (and dot)."""
+    from test_memorization_recurrent_gb300.harness import cfg_for
+    for loss, prm in ((A.LOSS_LP, 3.0), (A.LOSS_HUBER, 0.5)):
+        for wid, path in ((1, "linear_seq"), (2, "linear_tc"), (3, "linear_simt"),
+                          (4, "mlp_simt"), (5, "mlp_simt")):
+            w = W.workload(wid)
+            w = w.__class__(**{**w.__dict__, "loss": loss, "loss_param": prm})
+            cfg = cfg_for(w, 2, 256)
+            assert A.atlas_mem_path(cfg) == path, (wid, loss)

@@ -320,3 +320,23 @@ def test_tensor_core_path_hands_off_a_full_reset_gate():
     Yo, Mo, _ = run_oracle(w, inp)
     Yg, Mg, _ = gpu_run(w, inp)
     check(w, Yg, Mg, Yo, Mo, "reset gate")
+
+
+# ------------------------------------------------- alternative attentional biases
+
+@pytest.mark.parametrize("loss,prm", [(W.LOSS_LP, 3.0), (W.LOSS_LP, 1.5), (W.LOSS_HUBER, 0.3)])
+@pytest.mark.parametrize("wid,N,heads", [
+    (1, 100, [0]),          # token-serial kernel
+    (2, 64 + 13, [0, 5]),   # tensor-core linear kernel (ragged tail)
+    (3, 64 + 9, [0]),       # CUDA-core linear kernel (the wide-feature path takes l2 only)
+    (4, 64 + 19, [0, 7]),   # CUDA-core MLP path
+    (5, 12, [0]),           # CUDA-core MLP path with Newton-Schulz
+])
+def test_alternative_biases(wid, N, heads, loss, prm):
+    """l_p and Huber biases (Miras alternative attentional biases) through every
+    path that applies them, against the oracle on the same inputs."""
+    w = W.workload(wid, bounded=True, loss=loss, loss_param=prm)
+    inp = W.generate(w, heads=heads, n_tokens=N)
+    Yo, Mo, _ = run_oracle(w, inp)
+    Yg, Mg, _ = gpu_run(w, inp)
+    check(w, Yg, Mg, Yo, Mo, f"workload {wid} loss {loss} ({prm})")

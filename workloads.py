@@ -25,7 +25,7 @@ BLOCK = 256  # tokens per independently seeded block
 
 MEM_LINEAR, MEM_MLP = 0, 1
 PHI_IDENTITY, PHI_POLY2 = 0, 1
-LOSS_L2, LOSS_DOT = 0, 1
+LOSS_L2, LOSS_DOT, LOSS_LP, LOSS_HUBER = 0, 1, 2, 3
 
 
 @dataclasses.dataclass(frozen=True)
@@ -41,6 +41,7 @@ class Workload:
     mem: int = MEM_LINEAR
     phi: int = PHI_IDENTITY
     loss: int = LOSS_L2
+    loss_param: float = 0.0        # p of LOSS_LP, delta of LOSS_HUBER
     c: int = 1
     b: int = 1
     gamma: str = "ones"            # "ones" or "exp32": gamma_j = exp(-j/32)
