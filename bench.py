@@ -188,7 +188,7 @@ def oracle_rate(w, heads, n_tokens, seed=0):
     inp = W.generate(w, seed=seed, heads=heads, n_tokens=n_tokens)
     a, b_, c_ = w.ns_coef
     cfg = oracle.make_cfg(n_tokens, w.d_k, w.d_v, w.d_h, w.mem, w.phi, w.loss, w.c, w.b,
-                          w.ns_steps, a, b_, c_, w.ns_eps)
+                          w.ns_steps, a, b_, c_, w.ns_eps, loss_param=w.loss_param)
     t = time.perf_counter()
     oracle.forward(cfg, inp["K"], inp["Q"], inp["V"], inp["alpha"], inp["eta"], inp["theta"],
                    inp["gamma"], inp["M0"])
@@ -416,10 +416,18 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0,
                     help="run only the first TOKENS tokens of every head (0 = the whole workload)")
+    ap.add_argument("--loss", default="l2", choices=["l2", "lp", "huber"],
+                    help="attentional bias: l2 (the workloads'), or the Miras l_p / Huber variants")
+    ap.add_argument("--loss-param", type=float, default=0.0,
+                    help="p of the l_p bias (default 3), delta of the Huber bias (default 0.3)")
     args = ap.parse_args(argv)
     w = W.workload(args.workload, bounded=True)
     if args.tokens:
         w = w.with_(N=min(args.tokens, w.N))
+    if args.loss != "l2":
+        kind = W.LOSS_LP if args.loss == "lp" else W.LOSS_HUBER
+        prm = args.loss_param or (3.0 if args.loss == "lp" else 0.3)
+        w = w.with_(loss=kind, loss_param=prm, name=f"{w.name}-{args.loss}{prm:g}")
     if args.impl == "reference":
         run_reference(args, w)
     else:

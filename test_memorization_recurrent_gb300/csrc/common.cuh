@@ -19,14 +19,17 @@ __device__ __forceinline__ float ld_in(const void* p, long idx, int bf16) {
 // Biases): l2 (and the dot product, whose "error" is already -v): e; l_p,
 // sum |e|^p: (p/2) |e|^(p-1) sign(e); Huber with threshold delta (per
 // coordinate, e^2 inside): e clamped to [-delta, delta].
+__device__ __forceinline__ float lp_grad(float e, float p) {
+  const float a = fabsf(e);
+  const float m = p == 3.f ? a * a : p == 2.f ? a : exp2f((p - 1.f) * log2f(a));
+  return a == 0.f ? 0.f : copysignf(0.5f * p * m, e);
+}
+__device__ __forceinline__ float huber_grad(float e, float delta) {
+  return fminf(fmaxf(e, -delta), delta);
+}
 __device__ __forceinline__ float bias_grad(float e, int kind, float prm) {
-  if (kind == ATLAS_LOSS_LP) {
-    const float a = fabsf(e);
-    if (a == 0.f) return 0.f;
-    const float m = prm == 3.f ? a * a : prm == 2.f ? a : powf(a, prm - 1.f);
-    return copysignf(0.5f * prm * m, e);
-  }
-  if (kind == ATLAS_LOSS_HUBER) return fminf(fmaxf(e, -prm), prm);
+  if (kind == ATLAS_LOSS_LP) return lp_grad(e, prm);
+  if (kind == ATLAS_LOSS_HUBER) return huber_grad(e, prm);
   return e;
 }
 

@@ -487,9 +487,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tl + TM_T + 32 * h, e);
 #pragma unroll
         for (int x = 0; x < 32; ++x) e[x] -= vt[x];
-        if (p.lk != ATLAS_LOSS_L2) {
+        if (p.lk == ATLAS_LOSS_HUBER) {  // attentional bias, one loop per kind
 #pragma unroll
-          for (int x = 0; x < 32; ++x) e[x] = bias_grad(e[x], p.lk, p.lp);
+          for (int x = 0; x < 32; ++x) e[x] = huber_grad(e[x], p.lp);
+        } else if (p.lk == ATLAS_LOSS_LP) {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) e[x] = lp_grad(e[x], p.lp);
         }
         if (p.S && j == nchunks - 1) {
           const int il = N - 1 - t0 - 32 * h;
