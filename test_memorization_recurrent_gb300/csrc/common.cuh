@@ -21,7 +21,13 @@ __device__ __forceinline__ float ld_in(const void* p, long idx, int bf16) {
 // coordinate, e^2 inside): e clamped to [-delta, delta].
 __device__ __forceinline__ float lp_grad(float e, float p) {
   const float a = fabsf(e);
-  const float m = p == 3.f ? a * a : p == 2.f ? a : exp2f((p - 1.f) * log2f(a));
+  float m;  // |e|^(p-1); p is uniform, so the branches cost nothing
+  if (p == 3.f)
+    m = a * a;
+  else if (p == 2.f)
+    m = a;
+  else
+    m = exp2f((p - 1.f) * log2f(a));
   return a == 0.f ? 0.f : copysignf(0.5f * p * m, e);
 }
 __device__ __forceinline__ float huber_grad(float e, float delta) {
