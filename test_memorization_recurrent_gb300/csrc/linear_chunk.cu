@@ -152,6 +152,13 @@ __global__ void lc_neg_kernel(float* ws, long per_head, long E, long Vw, long n)
     base[E + x] = -base[Vw + x];
 }
 
+// E <- the attentional bias's derivative of E (l_p, Huber), elementwise.
+__global__ void lc_bias_kernel(float* ws, long per_head, long E, long n, int kind, float prm) {
+  float* e = ws + blockIdx.y * per_head + E;
+  for (long x = blockIdx.x * blockDim.x + threadIdx.x; x < n; x += (long)gridDim.x * blockDim.x)
+    e[x] = bias_grad(e[x], kind, prm);
+}
+
 // M = a_b M + beta_b S, S = eps_b S (the S0 terms of the chunk's last token).
 __global__ void lc_carry_kernel(float* M, float* S, long state, const float* ws, long per_head,
                                 long ta, long te, long tb, int last) {
@@ -181,9 +188,7 @@ dim3 ew_grid(long n, int heads) {
 
 }  // namespace
 
-bool linear_chunk_supported(const LinArgs& a) {
-  return a.D >= 256 && a.d_v <= 512 && (a.lk == ATLAS_LOSS_L2 || a.lk == ATLAS_LOSS_DOT);
-}
+bool linear_chunk_supported(const LinArgs& a) { return a.D >= 256 && a.d_v <= 512; }
 
 size_t linear_chunk_workspace_bytes(const LinArgs& a, int heads) {
   const size_t s = (size_t)heads * a.d_v * a.D * sizeof(float);  // S when none is given
@@ -193,7 +198,8 @@ size_t linear_chunk_workspace_bytes(const LinArgs& a, int heads) {
 long linear_chunk_launch_count(const LinArgs& a, int heads) {
   if (heads <= 0 || a.N <= 0) return 0;
   const long chunks = (a.N + a.b - 1) / a.b;
-  return (a.S ? 0 : 1) + chunks * 11;
+  const long bias = (a.lk == ATLAS_LOSS_LP || a.lk == ATLAS_LOSS_HUBER) ? 1 : 0;
+  return (a.S ? 0 : 1) + chunks * (11 + bias);
 }
 
 int linear_chunk_forward(const LinArgs& a0, int heads, void* wsv, cudaStream_t st) {
@@ -243,6 +249,11 @@ int linear_chunk_forward(const LinArgs& a0, int heads, void* wsv, cudaStream_t s
       g.B = p.M; g.sBb = state; g.sBk = 1; g.sBn = D;
       g.C = ws + w.E; g.sCb = PH; g.sCm = dv; g.sCn = 1;
       LC_CK(tc_gemm_launch(g, st));
+    }
+    if (p.lk == ATLAS_LOSS_LP || p.lk == ATLAS_LOSS_HUBER) {
+      lc_bias_kernel<<<ew_grid((long)L * dv, H), 256, 0, st>>>(ws, PH, w.E, (long)L * dv, p.lk,
+                                                               p.lp);
+      LC_CL();
     }
     // y = a (PhiQ M0^T) + beta (PhiQ S0^T) - 2 P E (split K, added onto zeros)
     float* Y = p.Y + (long)t0 * dv;

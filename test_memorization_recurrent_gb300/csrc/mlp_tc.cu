@@ -122,6 +122,8 @@ struct MtParams {
   __nv_bfloat16* ws;
   int* status;
   int N;
+  int lk;    // attentional bias (ATLAS_LOSS_L2, _LP or _HUBER)
+  float lp;  // its parameter
 };
 
 // ------------------------------------------------------------ device helpers
@@ -365,6 +367,9 @@ __device__ __forceinline__ void lin_scan64(float A0, float B0, float A1, float B
 
 }  // namespace
 
+// kBias: the attentional bias is l_p or Huber (a separate instantiation, so the l2
+// kernel's code is not touched by it)
+template <bool kBias>
 __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 1)
     mlp_tc_kernel(const __grid_constant__ MtMaps maps, MtParams p) {
   extern __shared__ unsigned char smem_raw[];
@@ -825,6 +830,15 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThr, 1)
               *reinterpret_cast<const __nv_bfloat16*>(sm + X_V + (i * 32 + lane) * 2);
           v[x] += __bfloat162float(kv) - __bfloat162float(vv);
         }
+        if constexpr (kBias) {  // the attentional bias on the finished E rows
+          if (p.lk == ATLAS_LOSS_HUBER) {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) v[x] = huber_grad(v[x], p.lp);
+          } else {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) v[x] = lp_grad(v[x], p.lp);
+          }
+        }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint32_t off = sw128_offset(d, 4 * h + k);
@@ -1096,7 +1110,7 @@ bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 bool mlp_tc_supported(const MlpArgs& a) {
   return a.d == kD && a.dh == kHid && a.c == 1 && a.b == kL && a.bf16 && a.ns_steps == 0 &&
-         a.lk == ATLAS_LOSS_L2 && a.N > 0 && a.heads > 0 && a.heads <= 65535;
+         a.N > 0 && a.heads > 0 && a.heads <= 65535;
 }
 
 size_t mlp_tc_workspace_bytes(const MlpArgs& a) {
@@ -1130,10 +1144,19 @@ int mlp_tc_launch(const MlpArgs& a, void* ws, cudaStream_t st) {
   p.ws = reinterpret_cast<__nv_bfloat16*>(ws);
   p.status = a.status;
   p.N = a.N;
-  if (cudaFuncSetAttribute(mlp_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)SMEM_ALLOC) != cudaSuccess)
-    return ATLAS_ERR_CUDA;
-  mlp_tc_kernel<<<dim3(kCl, H), kThr, SMEM_ALLOC, st>>>(m, p);
+  p.lk = a.lk;
+  p.lp = a.lp;
+  if (a.lk == ATLAS_LOSS_LP || a.lk == ATLAS_LOSS_HUBER) {
+    if (cudaFuncSetAttribute(mlp_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_ALLOC) != cudaSuccess)
+      return ATLAS_ERR_CUDA;
+    mlp_tc_kernel<true><<<dim3(kCl, H), kThr, SMEM_ALLOC, st>>>(m, p);
+  } else {
+    if (cudaFuncSetAttribute(mlp_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_ALLOC) != cudaSuccess)
+      return ATLAS_ERR_CUDA;
+    mlp_tc_kernel<false><<<dim3(kCl, H), kThr, SMEM_ALLOC, st>>>(m, p);
+  }
   return cudaGetLastError() == cudaSuccess ? ATLAS_OK : ATLAS_ERR_CUDA;
 }
 

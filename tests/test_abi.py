@@ -117,13 +117,12 @@ def test_invalid_workspace_query():
 
 
 def test_alternative_biases_choose_paths_that_apply_them(lib):
-    """l_p and Huber act on the error elementwise in the token-serial, CUDA-core and
-    tensor-core linear kernels and in the CUDA-core MLP path; the wide-feature
-    linear path and the tensor-core MLP kernel take only l2 (and dot)."""
+    """l_p and Huber act on the error elementwise in every path: the workloads keep
+    their l2 paths."""
     from test_memorization_recurrent_gb300.harness import cfg_for
     for loss, prm in ((A.LOSS_LP, 3.0), (A.LOSS_HUBER, 0.5)):
-        for wid, path in ((1, "linear_seq"), (2, "linear_tc"), (3, "linear_simt"),
-                          (4, "mlp_simt"), (5, "mlp_simt")):
+        for wid, path in ((1, "linear_seq"), (2, "linear_tc"), (3, "linear_chunk"),
+                          (4, "mlp_tc"), (5, "mlp_simt")):
             w = W.workload(wid)
             w = w.__class__(**{**w.__dict__, "loss": loss, "loss_param": prm})
             cfg = cfg_for(w, 2, 256)

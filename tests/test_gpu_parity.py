@@ -328,8 +328,8 @@ def test_tensor_core_path_hands_off_a_full_reset_gate():
 @pytest.mark.parametrize("wid,N,heads", [
     (1, 100, [0]),          # token-serial kernel
     (2, 64 + 13, [0, 5]),   # tensor-core linear kernel (ragged tail)
-    (3, 64 + 9, [0]),       # CUDA-core linear kernel (the wide-feature path takes l2 only)
-    (4, 64 + 19, [0, 7]),   # CUDA-core MLP path
+    (3, 64 + 9, [0]),       # wide-feature path (batched tensor-core GEMMs)
+    (4, 64 + 19, [0, 7]),   # tensor-core MLP kernel
     (5, 12, [0]),           # CUDA-core MLP path with Newton-Schulz
 ])
 def test_alternative_biases(wid, N, heads, loss, prm):
