@@ -127,3 +127,15 @@ def test_alternative_biases_choose_paths_that_apply_them(lib):
             w = w.__class__(**{**w.__dict__, "loss": loss, "loss_param": prm})
             cfg = cfg_for(w, 2, 256)
             assert A.atlas_mem_path(cfg) == path, (wid, loss)
+
+
+def test_bias_launches_are_counted():
+    """The wide-feature and CUDA-core MLP paths add one elementwise launch per chunk for
+    an l_p or Huber bias; the other paths apply it inside their kernels."""
+    from test_memorization_recurrent_gb300.harness import cfg_for
+    N = 64 * 3 + 5  # four chunks
+    for wid, extra in ((1, 0), (2, 0), (3, 4), (4, 0), (5, 4)):
+        w = W.workload(wid)
+        base = A.atlas_mem_launch_count(cfg_for(w, 2, N))
+        wb = w.__class__(**{**w.__dict__, "loss": A.LOSS_HUBER, "loss_param": 0.3})
+        assert A.atlas_mem_launch_count(cfg_for(wb, 2, N)) == base + extra, wid
