@@ -49,6 +49,10 @@ extern "C" {
 /* memory architecture */
 #define ATLAS_MEM_LINEAR 0 /* M: d_v x D matrix, y = M Phi(x) */
 #define ATLAS_MEM_MLP 1    /* M(x) = x + W1 GELU(W2 x), d_k = d_v = d */
+/* Memory variants defined (and pinned) in the oracle, with no kernel here yet:
+ * atlas_mem_forward returns ATLAS_ERR_UNSUPPORTED for them. */
+#define ATLAS_MEM_MLP_LN 2    /* x + LN(W1 GELU(W2 x)), plain LN over the d outputs */
+#define ATLAS_MEM_MLP_GATED 3 /* x + W1 (GELU(W2 x) * (W3 x)), W3 d_h x d after W2 */
 /* feature map (linear memory only; the MLP takes x itself) */
 #define ATLAS_PHI_IDENTITY 0 /* D = d_k */
 #define ATLAS_PHI_POLY2 1    /* D = d_k + d_k(d_k+1)/2: [x_i] then [x_i x_j, i<=j, i-major] */

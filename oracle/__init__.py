@@ -24,7 +24,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "atlas_oracle.c")
 _LIB = os.path.join(_HERE, "_build", "libatlas_oracle.so")
 
-MEM_LINEAR, MEM_MLP = 0, 1
+MEM_LINEAR, MEM_MLP, MEM_MLP_LN, MEM_MLP_GATED = 0, 1, 2, 3
 PHI_IDENTITY, PHI_POLY2 = 0, 1
 LOSS_L2, LOSS_DOT, LOSS_LP, LOSS_HUBER = 0, 1, 2, 3
 

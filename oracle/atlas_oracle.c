@@ -20,14 +20,16 @@
  *             the previous chunk ended with).
  *   [ATLAS-s] "ATLAS: Learning to Optimally Memorize the Context at Test
  *             Time" (paperlayer.ai summary), §5 Memory Optimization (Muon /
- *             Newton-Schulz in place of plain GD), App. E (2-layer residual
- *             MLP memory, expansion 4, GELU).
+ *             Newton-Schulz in place of plain GD; Atlas++: a gated MLP memory
+ *             with three linear maps), App. E (2-layer residual MLP memory,
+ *             expansion 4, GELU), §6 (residual connections and layer
+ *             normalisation in the memory).
  *   [Miras]   "It's All Connected: A Journey Through Test-Time Memorization,
  *             ..." (still-with-you.github.io), Associative Memory & Attentional
  *             Bias (linear attention = GD on -2<Mk, v>), #1 Alternative
  *             Attentional Biases (l_p loss ||M(k) - v||_p^p, Huber loss),
  *             Training (chunk-wise parallelisation at the chunk-start state,
- *             Miras layer outputs M(q_t)).
+ *             Miras layer outputs M(q_t); the memory x + LN(W1 sigma(W2 x))).
  *
  * Readings taken where the pages are silent or disagree (each one is listed
  * in the design notes of the repository):
@@ -45,6 +47,11 @@
  *   - Newton-Schulz (when enabled) acts on the momentum of each weight matrix
  *     separately, per token: M_t = (1 - alpha_t) M_{t-1} + NS(S_t), with
  *     X_0 = S / (||S||_F + eps) and the literal X X^T Gram;
+ *   - the layer-normalised MLP memory is x + LN(W1 GELU(W2 x)) with a plain
+ *     LN (no learned scale or shift; variance over the d outputs, divided by
+ *     d, plus 1e-5 under the square root);
+ *   - the gated (Atlas++) memory is x + W1 (GELU(W2 x) * (W3 x)), with W2 and
+ *     W3 both d_h x d, and Newton-Schulz (when enabled) applied to W3 as to W2;
  *   - the Huber bias is taken per coordinate with one threshold delta for all
  *     tokens, scaled to agree with the l2 bias inside the threshold:
  *     h(e) = e^2 for |e| <= delta, 2 delta |e| - delta^2 beyond (the pages let
@@ -58,6 +65,9 @@
 
 #define ORC_MEM_LINEAR 0
 #define ORC_MEM_MLP 1
+#define ORC_MEM_MLP_LN 2     /* x + LN(W1 GELU(W2 x)) */
+#define ORC_MEM_MLP_GATED 3  /* x + W1 (GELU(W2 x) * (W3 x)) */
+#define ORC_LN_EPS 1e-5
 #define ORC_PHI_IDENTITY 0
 #define ORC_PHI_POLY2 1
 #define ORC_LOSS_L2 0
@@ -72,7 +82,7 @@ typedef struct {
   int d_k;      /* key / query width before the feature map */
   int d_v;      /* value width */
   int d_h;      /* MLP hidden width (MLP memory only) */
-  int mem;      /* ORC_MEM_LINEAR or ORC_MEM_MLP */
+  int mem;      /* ORC_MEM_LINEAR, ORC_MEM_MLP, ORC_MEM_MLP_LN or ORC_MEM_MLP_GATED */
   int phi;      /* ORC_PHI_IDENTITY or ORC_PHI_POLY2 (linear memory only) */
   int loss;     /* ORC_LOSS_L2, _DOT, _LP or _HUBER */
   int c;        /* Omega window length, >= 1 */
@@ -89,14 +99,15 @@ typedef struct {
 /* Width of Phi(x).  [ATLAS] §3.1: Phi_p(x) = [x^beta]_{|beta| <= p}; with the
  * constant dropped and p = 2 that is d linear terms and d(d+1)/2 products. */
 int orc_feature_dim(const orc_cfg* g) {
-  if (g->mem == ORC_MEM_MLP) return g->d_k;
+  if (g->mem != ORC_MEM_LINEAR) return g->d_k;
   if (g->phi == ORC_PHI_POLY2) return g->d_k + g->d_k * (g->d_k + 1) / 2;
   return g->d_k;
 }
 
 /* Number of fp64 entries in one head's memory state (and in its momentum). */
 long orc_state_size(const orc_cfg* g) {
-  if (g->mem == ORC_MEM_MLP) return 2L * g->d_k * g->d_h;
+  if (g->mem == ORC_MEM_MLP || g->mem == ORC_MEM_MLP_LN) return 2L * g->d_k * g->d_h;
+  if (g->mem == ORC_MEM_MLP_GATED) return 3L * g->d_k * g->d_h;
   return (long)g->d_v * orc_feature_dim(g);
 }
 
@@ -106,7 +117,7 @@ long orc_state_size(const orc_cfg* g) {
 void orc_phi(const orc_cfg* g, const double* x, double* out) {
   int d = g->d_k;
   for (int i = 0; i < d; ++i) out[i] = x[i];
-  if (g->mem == ORC_MEM_MLP || g->phi == ORC_PHI_IDENTITY) return;
+  if (g->mem != ORC_MEM_LINEAR || g->phi == ORC_PHI_IDENTITY) return;
   int p = d;
   for (int i = 0; i < d; ++i)
     for (int j = i; j < d; ++j) out[p++] = x[i] * x[j];
@@ -125,9 +136,56 @@ double orc_gelu_prime(double x) {
 
 /* ------------------------------------------------------- memory forward */
 
+/* The MLP memories' branch, M(x) = x + out:
+ *   plain:  z = W2 x, h = GELU(z),                 out = W1 h
+ *   LN:     the same, then out = LN(W1 h) = (u - mean u) / sqrt(var u + 1e-5)
+ *   gated:  z = W2 x, w = W3 x, h = GELU(z) * w,   out = W1 h
+ * Intermediates (each may be NULL): z, w [d_h]; h [d_h]; the branch output
+ * [d] (after LN for the LN memory); the normalised values' 1 / sqrt(var + eps)
+ * (LN memory only, one value). */
+static void orc_mlp_forward(const orc_cfg* g, const double* state, const double* x, double* z_out,
+                            double* w_out, double* h_out, double* out, double* inv_sd) {
+  int d = g->d_k, dh = g->d_h;
+  const double* W1 = state;                  /* d  x dh */
+  const double* W2 = state + (long)d * dh;   /* dh x d  */
+  const double* W3 = state + 2L * d * dh;    /* dh x d  (gated memory) */
+  double* h = (double*)malloc(sizeof(double) * dh);
+  for (int j = 0; j < dh; ++j) {
+    double z = 0.0;
+    for (int i = 0; i < d; ++i) z += W2[(long)j * d + i] * x[i];
+    double w = 1.0;
+    if (g->mem == ORC_MEM_MLP_GATED) {
+      w = 0.0;
+      for (int i = 0; i < d; ++i) w += W3[(long)j * d + i] * x[i];
+    }
+    if (z_out) z_out[j] = z;
+    if (w_out) w_out[j] = w;
+    h[j] = orc_gelu(z) * w;
+    if (h_out) h_out[j] = h[j];
+  }
+  for (int r = 0; r < d; ++r) {
+    double s = 0.0;
+    for (int j = 0; j < dh; ++j) s += W1[(long)r * dh + j] * h[j];
+    out[r] = s;
+  }
+  if (g->mem == ORC_MEM_MLP_LN) {
+    double mu = 0.0, var = 0.0;
+    for (int r = 0; r < d; ++r) mu += out[r];
+    mu /= d;
+    for (int r = 0; r < d; ++r) var += (out[r] - mu) * (out[r] - mu);
+    var /= d;
+    const double is = 1.0 / sqrt(var + ORC_LN_EPS);
+    for (int r = 0; r < d; ++r) out[r] = (out[r] - mu) * is;
+    if (inv_sd) *inv_sd = is;
+  }
+  free(h);
+}
+
 /* Memory output M(x) for a key/query x (before Phi).
  * Linear: M Phi(x).  MLP: x + W1 GELU(W2 x)  ([ATLAS-s] App. E; [Titans]
- * Memory Architecture).  `out` has d_v entries. */
+ * Memory Architecture); LN: x + LN(W1 GELU(W2 x)) ([Miras] Moneta, Yaad,
+ * Memora memory; [ATLAS-s] §6); gated: x + W1 (GELU(W2 x) * (W3 x))
+ * ([ATLAS-s] §5, Atlas++).  `out` has d_v entries. */
 void orc_memory_apply(const orc_cfg* g, const double* state, const double* x, double* out) {
   if (g->mem == ORC_MEM_LINEAR) {
     int D = orc_feature_dim(g);
@@ -141,21 +199,11 @@ void orc_memory_apply(const orc_cfg* g, const double* state, const double* x, do
     free(f);
     return;
   }
-  int d = g->d_k, dh = g->d_h;
-  const double* W1 = state;                  /* d  x dh */
-  const double* W2 = state + (long)d * dh;   /* dh x d  */
-  double* h = (double*)malloc(sizeof(double) * dh);
-  for (int j = 0; j < dh; ++j) {
-    double z = 0.0;
-    for (int i = 0; i < d; ++i) z += W2[(long)j * d + i] * x[i];
-    h[j] = orc_gelu(z);
-  }
-  for (int r = 0; r < d; ++r) {
-    double s = x[r];
-    for (int j = 0; j < dh; ++j) s += W1[(long)r * dh + j] * h[j];
-    out[r] = s;
-  }
-  free(h);
+  int d = g->d_k;
+  double* u = (double*)malloc(sizeof(double) * d);
+  orc_mlp_forward(g, state, x, NULL, NULL, NULL, u, NULL);
+  for (int r = 0; r < d; ++r) out[r] = x[r] + u[r];
+  free(u);
 }
 
 /* ------------------------------------------------------- loss gradient */
@@ -184,8 +232,8 @@ static double orc_bias_dy(const orc_cfg* g, double e) {
  *   l2  ([Titans] Objective; [ATLAS] §3.1):  l = ||M(Phi(k)) - v||^2.
  *   dot ([Miras] Associative Memory & Attentional Bias): l = -2 <M(Phi(k)), v>.
  *   l_p, Huber ([Miras] #1 Alternative Attentional Biases): orc_bias_dy.
- * For the MLP the gradient is plain backpropagation through
- * y = k + W1 h, h = GELU(z), z = W2 k. */
+ * For the MLP memories the gradient is plain backpropagation through the
+ * branch of orc_mlp_forward (and LN's mean and variance for the LN memory). */
 void orc_grad(const orc_cfg* g, const double* state, const double* k, const double* v, double* G) {
   if (g->mem == ORC_MEM_LINEAR) {
     int D = orc_feature_dim(g), dv = g->d_v;
@@ -209,44 +257,52 @@ void orc_grad(const orc_cfg* g, const double* state, const double* k, const doub
   }
   int d = g->d_k, dh = g->d_h;
   const double* W1 = state;
-  const double* W2 = state + (long)d * dh;
   double* G1 = G;
   double* G2 = G + (long)d * dh;
+  double* G3 = G + 2L * d * dh;
   double* z = (double*)malloc(sizeof(double) * dh);
+  double* w = (double*)malloc(sizeof(double) * dh);
   double* h = (double*)malloc(sizeof(double) * dh);
+  double* o = (double*)malloc(sizeof(double) * d);
   double* dy = (double*)malloc(sizeof(double) * d);
-  double* dz = (double*)malloc(sizeof(double) * dh);
+  double* du = (double*)malloc(sizeof(double) * d);
+  double is = 1.0;
+  orc_mlp_forward(g, state, k, z, w, h, o, &is);
+  for (int r = 0; r < d; ++r)
+    dy[r] = g->loss == ORC_LOSS_DOT ? -2.0 * v[r] : orc_bias_dy(g, k[r] + o[r] - v[r]);
+  /* through LN: du = is (dy - mean(dy) - n mean(dy * n)), n = the normalised values */
+  if (g->mem == ORC_MEM_MLP_LN) {
+    double m1 = 0.0, m2 = 0.0;
+    for (int r = 0; r < d; ++r) {
+      m1 += dy[r];
+      m2 += dy[r] * o[r];
+    }
+    m1 /= d;
+    m2 /= d;
+    for (int r = 0; r < d; ++r) du[r] = is * (dy[r] - m1 - o[r] * m2);
+  } else {
+    for (int r = 0; r < d; ++r) du[r] = dy[r];
+  }
+  /* dl/dW1 = du h^T */
+  for (int r = 0; r < d; ++r)
+    for (int j = 0; j < dh; ++j) G1[(long)r * dh + j] = du[r] * h[j];
+  /* dl/dh = W1^T du; h = GELU(z) w: dl/dz = dl/dh w GELU'(z), dl/dw = dl/dh GELU(z) */
   for (int j = 0; j < dh; ++j) {
     double s = 0.0;
-    for (int i = 0; i < d; ++i) s += W2[(long)j * d + i] * k[i];
-    z[j] = s;
-    h[j] = orc_gelu(s);
-  }
-  for (int r = 0; r < d; ++r) {
-    if (g->loss == ORC_LOSS_DOT) {
-      dy[r] = -2.0 * v[r];
-    } else {
-      double y = k[r];
-      for (int j = 0; j < dh; ++j) y += W1[(long)r * dh + j] * h[j];
-      dy[r] = orc_bias_dy(g, y - v[r]);
+    for (int r = 0; r < d; ++r) s += W1[(long)r * dh + j] * du[r];
+    const double dz = s * w[j] * orc_gelu_prime(z[j]);
+    for (int i = 0; i < d; ++i) G2[(long)j * d + i] = dz * k[i];
+    if (g->mem == ORC_MEM_MLP_GATED) {
+      const double dw = s * orc_gelu(z[j]);
+      for (int i = 0; i < d; ++i) G3[(long)j * d + i] = dw * k[i];
     }
   }
-  /* dl/dW1 = dy h^T */
-  for (int r = 0; r < d; ++r)
-    for (int j = 0; j < dh; ++j) G1[(long)r * dh + j] = dy[r] * h[j];
-  /* dl/dz = (W1^T dy) * GELU'(z) */
-  for (int j = 0; j < dh; ++j) {
-    double s = 0.0;
-    for (int r = 0; r < d; ++r) s += W1[(long)r * dh + j] * dy[r];
-    dz[j] = s * orc_gelu_prime(z[j]);
-  }
-  /* dl/dW2 = dz k^T */
-  for (int j = 0; j < dh; ++j)
-    for (int i = 0; i < d; ++i) G2[(long)j * d + i] = dz[j] * k[i];
   free(z);
+  free(w);
   free(h);
+  free(o);
   free(dy);
-  free(dz);
+  free(du);
 }
 
 /* ------------------------------------------------------ Newton-Schulz */
@@ -308,6 +364,9 @@ static void orc_momentum_update(const orc_cfg* g, const double* S, double* out) 
   orc_newton_schulz(g->d_k, g->d_h, S, g->ns_steps, g->ns_a, g->ns_b, g->ns_c, g->ns_eps, out);
   orc_newton_schulz(g->d_h, g->d_k, S + half, g->ns_steps, g->ns_a, g->ns_b, g->ns_c, g->ns_eps,
                     out + half);
+  if (g->mem == ORC_MEM_MLP_GATED)  /* W3, like W2 */
+    orc_newton_schulz(g->d_h, g->d_k, S + 2 * half, g->ns_steps, g->ns_a, g->ns_b, g->ns_c,
+                      g->ns_eps, out + 2 * half);
 }
 
 /* ------------------------------------------------------- one head, one token */
@@ -422,8 +481,8 @@ static void* orc_worker(void* p) {
 static int orc_check(const orc_cfg* g) {
   if (g->N < 0 || g->d_k <= 0 || g->d_v <= 0 || g->c < 1 || g->b < 1) return -1;
   if (g->n_history < 0) return -1;
-  if (g->mem == ORC_MEM_MLP && (g->d_h <= 0 || g->d_k != g->d_v)) return -1;
-  if (g->mem != ORC_MEM_LINEAR && g->mem != ORC_MEM_MLP) return -1;
+  if (g->mem < ORC_MEM_LINEAR || g->mem > ORC_MEM_MLP_GATED) return -1;
+  if (g->mem != ORC_MEM_LINEAR && (g->d_h <= 0 || g->d_k != g->d_v)) return -1;
   if (g->loss < ORC_LOSS_L2 || g->loss > ORC_LOSS_HUBER) return -1;
   if (g->loss == ORC_LOSS_LP && !(g->loss_param >= 1.0 && g->loss_param < 1e6)) return -1;
   if (g->loss == ORC_LOSS_HUBER && !(g->loss_param > 0.0)) return -1;

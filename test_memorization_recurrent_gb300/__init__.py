@@ -15,7 +15,7 @@ import threading
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "libatlasmem.so")
 
-MEM_LINEAR, MEM_MLP = 0, 1
+MEM_LINEAR, MEM_MLP, MEM_MLP_LN, MEM_MLP_GATED = 0, 1, 2, 3
 PHI_IDENTITY, PHI_POLY2 = 0, 1
 LOSS_L2, LOSS_DOT, LOSS_LP, LOSS_HUBER = 0, 1, 2, 3
 F32, BF16 = 0, 1

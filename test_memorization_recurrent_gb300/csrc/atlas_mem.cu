@@ -26,7 +26,7 @@ int check_cfg(const atlas_mem_cfg* c) {
   if (!c) return ATLAS_ERR_INVALID;
   if (c->B < 0 || c->H < 0 || c->N < 0) return ATLAS_ERR_INVALID;
   if (c->d_k <= 0 || c->d_v <= 0 || c->c < 1 || c->b < 1) return ATLAS_ERR_INVALID;
-  if (c->mem != ATLAS_MEM_LINEAR && c->mem != ATLAS_MEM_MLP) return ATLAS_ERR_INVALID;
+  if (c->mem < ATLAS_MEM_LINEAR || c->mem > ATLAS_MEM_MLP_GATED) return ATLAS_ERR_INVALID;
   if (c->phi != ATLAS_PHI_IDENTITY && c->phi != ATLAS_PHI_POLY2) return ATLAS_ERR_INVALID;
   if (c->loss < ATLAS_LOSS_L2 || c->loss > ATLAS_LOSS_HUBER) return ATLAS_ERR_INVALID;
   if (c->loss == ATLAS_LOSS_LP && !(c->loss_param >= 1.f && c->loss_param < 1e6f))
@@ -36,9 +36,10 @@ int check_cfg(const atlas_mem_cfg* c) {
   if (c->in_dtype != ATLAS_F32 && c->in_dtype != ATLAS_BF16) return ATLAS_ERR_INVALID;
   if (c->ns_steps < 0 || c->n_history < 0) return ATLAS_ERR_INVALID;
   if ((long)c->B * c->H > 65535L * 1024) return ATLAS_ERR_UNSUPPORTED;
-  if (c->mem == ATLAS_MEM_MLP) {
+  if (c->mem != ATLAS_MEM_LINEAR) {
     if (c->d_h <= 0 || c->d_k != c->d_v) return ATLAS_ERR_INVALID;
     if (c->phi != ATLAS_PHI_IDENTITY) return ATLAS_ERR_INVALID;
+    if (c->mem != ATLAS_MEM_MLP) return ATLAS_ERR_UNSUPPORTED;  // LN, gated: oracle only
     if (c->loss == ATLAS_LOSS_DOT) return ATLAS_ERR_UNSUPPORTED;
   } else {
     if (c->ns_steps > 0) return ATLAS_ERR_UNSUPPORTED;

@@ -81,6 +81,10 @@ def _bad(**kw):
     (dict(mem=A.MEM_MLP, d_h=0), A.ERR_INVALID),
     (dict(mem=A.MEM_MLP, d_h=16, d_v=4), A.ERR_INVALID),
     (dict(mem=A.MEM_MLP, d_h=16, loss=A.LOSS_DOT), A.ERR_UNSUPPORTED),
+    (dict(mem=4, d_h=16), A.ERR_INVALID),
+    (dict(mem=A.MEM_MLP_LN, d_h=16), A.ERR_UNSUPPORTED),     # oracle only so far
+    (dict(mem=A.MEM_MLP_GATED, d_h=16), A.ERR_UNSUPPORTED),
+    (dict(mem=A.MEM_MLP_GATED, d_h=0), A.ERR_INVALID),
     (dict(ns_steps=5), A.ERR_UNSUPPORTED),
     (dict(phi=A.PHI_POLY2, d_k=80), A.ERR_UNSUPPORTED),
 ])

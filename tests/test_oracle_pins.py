@@ -121,11 +121,17 @@ BIASES = [(oracle.LOSS_L2, 0.0), (oracle.LOSS_DOT, 0.0), (oracle.LOSS_LP, 3.0),
           (oracle.LOSS_LP, 1.5), (oracle.LOSS_HUBER, 0.4)]
 
 
+MLPS = [oracle.MEM_MLP, oracle.MEM_MLP_LN, oracle.MEM_MLP_GATED]
+
+
+@pytest.mark.parametrize("mem", MLPS)
 @pytest.mark.parametrize("loss,prm", BIASES)
-def test_mlp_gradient_by_finite_differences(loss, prm):
+def test_mlp_gradient_by_finite_differences(mem, loss, prm):
+    """Every MLP memory (plain, layer-normalised, gated) and every bias: the
+    backpropagated gradient against central differences of the written-out loss."""
     d, dh = 4, 6
-    cfg = oracle.make_cfg(1, d, d, dh, mem=oracle.MEM_MLP, loss=loss, loss_param=prm)
-    state = RNG.standard_normal(2 * d * dh) * 0.7
+    cfg = oracle.make_cfg(1, d, d, dh, mem=mem, loss=loss, loss_param=prm)
+    state = RNG.standard_normal(oracle.state_size(cfg)) * 0.7
     k, v = RNG.standard_normal(d), RNG.standard_normal(d)
     np.testing.assert_allclose(oracle.grad(cfg, state, k, v), _fd_grad(cfg, state, k, v),
                                rtol=1e-7, atol=1e-8)
@@ -207,6 +213,41 @@ def test_mlp_memory_apply_residual_form():
     cfg = oracle.make_cfg(1, d, d, dh, mem=oracle.MEM_MLP)
     y = oracle.memory_apply(cfg, np.concatenate([W1.ravel(), W2.ravel()]), x)
     np.testing.assert_allclose(y, x + x * norm.cdf(x), rtol=0, atol=1e-15)
+
+
+def test_layer_normalised_memory_is_ln_of_the_plain_branch():
+    """M_LN(x) - x is the plain branch M(x) - x = W1 GELU(W2 x) normalised to zero
+    mean and unit variance (biased variance over the d outputs, eps 1e-5 inside
+    the square root), with the same W1, W2."""
+    d, dh = 6, 9
+    state = RNG.standard_normal(2 * d * dh) * 0.6
+    x = RNG.standard_normal(d)
+    u = oracle.memory_apply(oracle.make_cfg(1, d, d, dh, mem=oracle.MEM_MLP), state, x) - x
+    y = oracle.memory_apply(oracle.make_cfg(1, d, d, dh, mem=oracle.MEM_MLP_LN), state, x)
+    ref = (u - u.mean()) / np.sqrt(u.var() + 1e-5)
+    np.testing.assert_allclose(y - x, ref, rtol=0, atol=1e-13)
+    assert abs((y - x).mean()) < 1e-13
+
+
+def test_gated_memory_reduces_to_the_plain_one_when_the_gate_is_one():
+    """x = e_0 and W3 with a first column of ones give W3 x = 1 for every hidden
+    unit: the gated memory x + W1 (GELU(W2 x) * (W3 x)) equals the plain one.  With
+    W3 = 0 it is the identity, and only W3's gradient is non-zero."""
+    d, dh = 5, 7
+    W12 = RNG.standard_normal(2 * d * dh) * 0.6
+    W3 = RNG.standard_normal((dh, d))
+    W3[:, 0] = 1.0
+    x = np.zeros(d)
+    x[0] = 1.0
+    plain = oracle.memory_apply(oracle.make_cfg(1, d, d, dh, mem=oracle.MEM_MLP), W12, x)
+    cfg = oracle.make_cfg(1, d, d, dh, mem=oracle.MEM_MLP_GATED)
+    gated = oracle.memory_apply(cfg, np.concatenate([W12, W3.ravel()]), x)
+    np.testing.assert_allclose(gated, plain, rtol=0, atol=1e-15)
+    state = np.concatenate([W12, np.zeros(dh * d)])
+    k, v = RNG.standard_normal(d), RNG.standard_normal(d)
+    np.testing.assert_array_equal(oracle.memory_apply(cfg, state, k), k)
+    G = oracle.grad(cfg, state, k, v)
+    assert not G[:2 * d * dh].any() and G[2 * d * dh:].any()
 
 
 # ------------------------------------------------------------- Newton-Schulz
@@ -434,18 +475,20 @@ def _ns_scalar(s, steps=5):
     return s
 
 
-@pytest.mark.parametrize("mem", [oracle.MEM_LINEAR, oracle.MEM_MLP])
+@pytest.mark.parametrize("mem", [oracle.MEM_LINEAR, oracle.MEM_MLP, oracle.MEM_MLP_LN,
+                                 oracle.MEM_MLP_GATED])
 def test_first_step_with_newton_schulz(mem):
     """First token from S0 = 0: S_1 = -theta_1 grad, a rank-1 matrix per weight,
     whose Newton-Schulz image is p^(5)(s/(s+eps)) times its direction; so
     M_1 = (1 - alpha_1) M_0 - p5 grad/||grad||_F per weight matrix (ATLAS
     summary §5, Muon in place of GD, as read in the design notes)."""
     d, dh, eps = 4, 6, 1e-7
-    if mem == oracle.MEM_MLP:
+    if mem != oracle.MEM_LINEAR:
         cfg = oracle.make_cfg(1, d, d, dh, mem=mem, c=1, b=1, ns_steps=5, ns_a=NS[0],
                               ns_b=NS[1], ns_c=NS[2], ns_eps=eps)
-        M0 = RNG.standard_normal((1, 2 * d * dh)) * 0.5
-        blocks = [slice(0, d * dh), slice(d * dh, 2 * d * dh)]
+        nb = 3 if mem == oracle.MEM_MLP_GATED else 2
+        M0 = RNG.standard_normal((1, nb * d * dh)) * 0.5
+        blocks = [slice(i * d * dh, (i + 1) * d * dh) for i in range(nb)]
     else:
         cfg = oracle.make_cfg(1, d, 3, c=1, b=1, ns_steps=5, ns_a=NS[0], ns_b=NS[1],
                               ns_c=NS[2], ns_eps=eps)
