@@ -217,6 +217,12 @@ def run_reference(args, w):
     cores = os.cpu_count() or 1
     for _ in range(args.warmup):
         oracle_rate(w, heads[:1], min(n, 64))
+    # keep the whole timed run near two minutes at most: one step on the full sample
+    # measures its cost, and the heads per step shrink if K steps would take longer
+    _, dt0 = oracle_rate(w, heads, n)
+    budget = 120.0 / max(1, args.steps)
+    if dt0 > budget:  # (never fewer heads than host cores: the oracle threads over heads)
+        heads = heads[:max(min(cores, len(heads)), int(len(heads) * budget / dt0))]
     rates, times = [], []
     for _ in range(args.steps):
         r, dt = oracle_rate(w, heads, n)
