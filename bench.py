@@ -251,9 +251,201 @@ KERNEL_OF_PATH = {
     "linear_simt": ("linear_simt.cu", "linear_simt_{wname}.md"),
     "linear_seq": ("linear_seq.cu", "linear_seq_{wname}.md"),
     "linear_chunk": ("tc_gemm.cu", "linear_chunk_{wname}.md"),
-    "mlp_simt": ("mlp_simt.cu", "mlp_simt_{wname}.md"),
+    "mlp_simt": ("ns_fused.cu", "ns_fused_{wname}.md"),
     "mlp_tc": ("mlp_tc.cu", "mlp_tc_{wname}.md"),
 }
+
+# Workloads measured beside the headline one, and the token prefix each is timed
+# on (None = the whole workload).  The Newton-Schulz workload runs on a prefix of
+# all 16 heads: its full million-token length is ~70 s per call at today's rate.
+PER_CONFIG = ((1, None), (3, None), (4, None), (5, 1024))
+
+
+def time_device(w, run, d, steps, warmup, stream, clk=None, world=1):
+    """Device-resident timing of `steps` calls (each preceded by the reset of the
+    state buffer to M_0).  A call whose data fits in L2 is preceded by a write
+    of a buffer twice the L2 size, outside its events, and the step time is the
+    sum of the per-step events; otherwise the steps run back to back and the
+    step time is the whole loop's.  Returns (elapsed_s, kernel_s per call, flush)."""
+    import torch
+    import test_memorization_recurrent_gb300 as A
+    bytes_launch = w.tokens * W.bytes_per_token(w) + 2 * 4 * w.heads * w.state_size
+    flush = bytes_launch < 2 * L2_BYTES
+    dev = run.Y.device
+    scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    s_start, s_end = [ev() for _ in range(steps)], [ev() for _ in range(steps)]
+    k_start, k_end = [ev() for _ in range(steps)], [ev() for _ in range(steps)]
+    t_start, t_end = ev(), ev()
+    for _ in range(warmup):
+        run(d)
+    torch.cuda.synchronize()
+    if clk is not None:
+        clk.wait_ready()
+    barrier(world)
+    torch.cuda.synchronize()
+    if clk is not None:
+        clk.mark_start()
+    t_start.record(stream)
+    for i in range(steps):
+        if flush:
+            scrub.fill_(float(i))
+        s_start[i].record(stream)
+        run.M.copy_(d["M0"])
+        k_start[i].record(stream)
+        A.atlas_mem_forward(d["K"], d["Q"], d["V"], d["alpha"], d["eta"], d["theta"],
+                            d["gamma"], run.cfg, run.Y, run.M, stream)
+        k_end[i].record(stream)
+        s_end[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if clk is not None:
+        clk.mark_end()
+    barrier(world)
+    if flush:
+        elapsed = sum(a.elapsed_time(b) for a, b in zip(s_start, s_end)) / 1e3
+    else:
+        elapsed = t_start.elapsed_time(t_end) / 1e3
+    kernel_s = sum(a.elapsed_time(b) for a, b in zip(k_start, k_end)) / 1e3 / steps
+    status = int(run.status.item())
+    if status != 0:
+        raise SystemExit(f"device status {status}: {A.atlas_mem_strerror(status)}")
+    return elapsed, kernel_s, flush
+
+
+def roofline(w, path, kernel_s):
+    """Roofline record of one launch of workload `w` taking `kernel_s`: HBM-bound
+    when its arithmetic intensity is below the ridge, else against the sustained
+    bf16 tensor peak.  `traffic` comes from the committed ncu summary of the
+    dominant kernel when that summary was taken on the current source."""
+    hbm, tf, tf_sus, peak_kind = load_peaks()
+    tokens = w.tokens
+    bytes_launch = tokens * W.bytes_per_token(w) + 2 * 4 * w.heads * w.state_size
+    flops_launch = tokens * W.flop_per_token(w)
+    ridge = tf * 1e12 / (hbm * 1e9)
+    if flops_launch / bytes_launch < ridge:
+        achieved = bytes_launch / kernel_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "peak_kind": f"{peak_kind} hbm_gbs"}
+    else:
+        achieved = flops_launch / kernel_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tf_sus, "unit": "TFLOP/s",
+                "frac": achieved / tf_sus, "peak_kind": f"{peak_kind} bf16_tflops_sustained"}
+    src, prof = KERNEL_OF_PATH.get(path, ("", ""))
+    src_path = os.path.join(ROOT, "test_memorization_recurrent_gb300", "csrc", src)
+    roof["traffic"] = (profile_traffic(src_path, prof.format(wname=w.name), tokens)
+                       if src else None)
+    roof["kernel"] = path
+    roof["kernel_ms"] = kernel_s * 1e3
+    roof["algorithmic_bytes"] = bytes_launch
+    roof["algorithmic_flops"] = flops_launch
+    return roof
+
+
+def measure_config(wid, n_tokens, steps, warmup, dev, with_cpu):
+    """One workload measured on its own (rank 0, one GPU): rate, roofline, clocks
+    during its timed region, and the oracle on a bounded sample of it."""
+    import torch
+    import test_memorization_recurrent_gb300 as A
+    from test_memorization_recurrent_gb300.harness import Runner, to_device
+    w = W.workload(wid, bounded=True)
+    if n_tokens:
+        w = w.with_(N=min(n_tokens, w.N))
+    inp = W.generate(w)
+    d = to_device(w, inp, dev)
+    run = Runner(w, w.heads, w.N, device=dev)
+    path = A.atlas_mem_path(run.cfg)
+    stream = torch.cuda.current_stream()
+    with Clocks(torch.cuda.current_device()) as clk:
+        elapsed, kernel_s, flush = time_device(w, run, d, steps, warmup, stream, clk)
+    rec = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "path": path,
+           "tokens_per_call": w.tokens, "steps": steps,
+           "value": w.tokens * steps / elapsed, "unit": UNIT,
+           "ms_per_step": elapsed / steps * 1e3,
+           "launches_per_call": A.atlas_mem_launch_count(run.cfg),
+           "roofline": roofline(w, path, kernel_s), "clocks": clk.summary(),
+           "l2": "flushed before every step" if flush else "inputs larger than L2"}
+    if n_tokens:
+        rec["sample"] = f"first {w.N} tokens of every head (all {w.heads} heads)"
+    del d, run
+    torch.cuda.empty_cache()
+    if with_cpu:
+        heads, n = oracle_sample(w)
+        rate, dt = oracle_rate(w, heads, n)
+        rec["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": os.cpu_count(),
+                               "kind": "oracle",
+                               "sample": f"{len(heads)} heads x {n} tokens of {w.name}, {dt:.1f} s"}
+    return rec
+
+
+def e2e_rate(w, d, run, steps, warmup, stream, world, dev, groups=4):
+    """End to end through the C ABI from pinned host buffers: every step copies
+    that step's inputs host -> device and the outputs (Y and M_final) back.  The
+    heads are split into `groups`; each group's copy-in, update and copy-out run
+    in order on a stream of its own, so one group's copies overlap another's
+    compute and the two copy directions overlap each other.  Returns (seconds
+    for all steps, h2d bytes per step, d2h bytes per step)."""
+    import torch
+    import test_memorization_recurrent_gb300 as A
+    from test_memorization_recurrent_gb300.harness import cfg_for
+    host = {k: v.cpu().pin_memory() for k, v in d.items()}
+    Yh = torch.empty(run.Y.shape, dtype=torch.float32).pin_memory()
+    Mh = torch.empty(run.M.shape, dtype=torch.float32).pin_memory()
+    dd = {k: torch.empty_like(v) for k, v in d.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = Yh.numel() * 4 + Mh.numel() * 4
+    G = max(1, min(groups, w.heads))
+    bounds = [w.heads * g // G for g in range(G + 1)]
+    streams = [torch.cuda.Stream(device=dev) for _ in range(G)]
+    per_head = ("K", "Q", "V", "alpha", "eta", "theta", "M0")
+    cfgs, wss = [], []
+    for g in range(G):
+        hg = bounds[g + 1] - bounds[g]
+        probe = cfg_for(w, hg, w.N)
+        nb = A.atlas_mem_workspace_bytes(probe)
+        ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev) if nb else None
+        wss.append(ws)
+        cfgs.append(cfg_for(w, hg, w.N, workspace=ws, workspace_bytes=nb,
+                            status_dev=run.status))
+
+    def step():
+        dd["gamma"].copy_(host["gamma"], non_blocking=True)  # shared by every group
+        start = torch.cuda.Event()
+        start.record(stream)
+        done = []
+        for g in range(G):
+            lo, hi = bounds[g], bounds[g + 1]
+            sg = streams[g]
+            sg.wait_event(start)
+            with torch.cuda.stream(sg):
+                for k in per_head:
+                    dd[k][lo:hi].copy_(host[k][lo:hi], non_blocking=True)
+                run.M[lo:hi].copy_(dd["M0"][lo:hi])
+            A.atlas_mem_forward(dd["K"][lo:hi], dd["Q"][lo:hi], dd["V"][lo:hi],
+                                dd["alpha"][lo:hi], dd["eta"][lo:hi], dd["theta"][lo:hi],
+                                dd["gamma"], cfgs[g], run.Y[lo:hi], run.M[lo:hi], sg)
+            with torch.cuda.stream(sg):
+                Yh[lo:hi].copy_(run.Y[lo:hi], non_blocking=True)
+                Mh[lo:hi].copy_(run.M[lo:hi], non_blocking=True)
+            e = torch.cuda.Event()
+            e.record(sg)
+            done.append(e)
+        for e in done:
+            stream.wait_event(e)
+
+    for _ in range(max(1, warmup)):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return e0.elapsed_time(e1) / 1e3, h2d, d2h
 
 
 def run_atlas(args, w):
@@ -278,109 +470,28 @@ def run_atlas(args, w):
     launches_per_step = A.atlas_mem_launch_count(run.cfg)
     stream = torch.cuda.current_stream()
 
-    # -- device-resident timing.  A step whose data fits in L2 is preceded by a
-    # write of a buffer twice the L2 size, outside its events, and the step
-    # time is the sum of the per-step events; otherwise the steps run back to
-    # back and the step time is the whole loop's.
-    bytes_launch = w.tokens * W.bytes_per_token(w) + 2 * 4 * w.heads * w.state_size
-    flush = bytes_launch < 2 * L2_BYTES
-    scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
-    s_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    s_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    k_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    k_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
     with Clocks(torch.cuda.current_device()) as clk:
-        for _ in range(args.warmup):
-            run(d)
-        torch.cuda.synchronize()
-        clk.wait_ready()
-        barrier(world)
-        torch.cuda.synchronize()
-        clk.mark_start()
-        t_start.record(stream)
-        for i in range(args.steps):
-            if flush:
-                scrub.fill_(float(i))
-            s_start[i].record(stream)
-            run.M.copy_(d["M0"])
-            k_start[i].record(stream)
-            A.atlas_mem_forward(d["K"], d["Q"], d["V"], d["alpha"], d["eta"], d["theta"],
-                                d["gamma"], run.cfg, run.Y, run.M, stream)
-            k_end[i].record(stream)
-            s_end[i].record(stream)
-        t_end.record(stream)
-        torch.cuda.synchronize()
-        clk.mark_end()
-        barrier(world)
-    if flush:
-        elapsed = sum(a.elapsed_time(b) for a, b in zip(s_start, s_end)) / 1e3
-    else:
-        elapsed = t_start.elapsed_time(t_end) / 1e3
-    kernel_s = sum(a.elapsed_time(b) for a, b in zip(k_start, k_end)) / 1e3 / args.steps
+        elapsed, kernel_s, flush = time_device(w, run, d, args.steps, args.warmup, stream, clk,
+                                               world)
     elapsed_max = max_over_ranks(elapsed, world, dev)
-    status = int(run.status.item())
-    if status != 0:
-        raise SystemExit(f"device status {status}: {A.atlas_mem_strerror(status)}")
+    e2e_s, h2d, d2h = e2e_rate(w, d, run, args.steps, args.warmup, stream, world, dev)
+    e2e_s = max_over_ranks(e2e_s, world, dev)
+    if int(run.status.item()) != 0:
+        raise SystemExit(f"device status {int(run.status.item())} in the end-to-end leg")
 
-    # -- end to end through the C ABI with host buffers (pinned), copies timed
-    host = {k: v.cpu().pin_memory() for k, v in d.items()}
-    Yh = torch.empty(run.Y.shape, dtype=torch.float32).pin_memory()
-    Mh = torch.empty(run.M.shape, dtype=torch.float32).pin_memory()
-    dd = {k: torch.empty_like(v) for k, v in d.items()}
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = Yh.numel() * 4 + Mh.numel() * 4
-
-    def e2e_step():
-        for k in host:
-            dd[k].copy_(host[k], non_blocking=True)
-        run.M.copy_(dd["M0"])
-        A.atlas_mem_forward(dd["K"], dd["Q"], dd["V"], dd["alpha"], dd["eta"], dd["theta"],
-                            dd["gamma"], run.cfg, run.Y, run.M, stream)
-        Yh.copy_(run.Y, non_blocking=True)
-        Mh.copy_(run.M, non_blocking=True)
-
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
+    per_config = None
+    if world == 1 and not args.no_per_config and not args.tokens and args.loss == "l2":
+        del d
+        torch.cuda.empty_cache()
+        per_config = [measure_config(wid, n, min(args.steps, 10), max(3, min(args.warmup, 3)),
+                                     dev, not args.no_cpu_baseline)
+                      for wid, n in PER_CONFIG if wid != w.wid]
 
     if rank != 0:
         return
     tokens = w.tokens
     value = aggregate(tokens, world, elapsed_max, args.steps)
-    hbm, tf, tf_sus, peak_kind = load_peaks()
-    flops_launch = tokens * W.flop_per_token(w)
-    ai = flops_launch / bytes_launch
-    ridge = tf * 1e12 / (hbm * 1e9)
-    src, prof = KERNEL_OF_PATH.get(path, ("", ""))
-    src_path = os.path.join(ROOT, "test_memorization_recurrent_gb300", "csrc", src)
-    prof_name = prof.format(wname=w.name)
-    if ai < ridge:
-        achieved = bytes_launch / kernel_s / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "peak_kind": f"{peak_kind} hbm_gbs"}
-        units = tokens
-    else:
-        achieved = flops_launch / kernel_s / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": tf_sus, "unit": "TFLOP/s",
-                "frac": achieved / tf_sus, "peak_kind": f"{peak_kind} bf16_tflops_sustained"}
-        units = tokens
-    roof["traffic"] = profile_traffic(src_path, prof_name, units) if src else None
-    roof["kernel"] = path
-    roof["kernel_ms"] = kernel_s * 1e3
-    roof["algorithmic_bytes"] = bytes_launch
-    roof["algorithmic_flops"] = flops_launch
+    bytes_launch = tokens * W.bytes_per_token(w) + 2 * 4 * w.heads * w.state_size
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -399,13 +510,15 @@ def run_atlas(args, w):
                    "l2": ("L2 flushed before every step (%.2f MB per step)" if flush else
                           "inputs larger than L2 (K,Q,V,Y %.0f MB per step)")
                          % (bytes_launch / 1e6)},
-        "roofline": roof,
+        "roofline": roofline(w, path, kernel_s),
         "cpu_baseline": cpu,
         "e2e": {"value": aggregate(tokens, world, e2e_s, args.steps), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
+    if per_config is not None:
+        line["per_config"] = per_config
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -420,6 +533,8 @@ def main(argv=None):
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="atlas", choices=["atlas", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="measure the chosen workload only (no per_config record)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="run only the first TOKENS tokens of every head (0 = the whole workload)")
     ap.add_argument("--loss", default="l2", choices=["l2", "lp", "huber"],

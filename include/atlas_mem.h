@@ -144,9 +144,20 @@ int atlas_mem_forward(const void* K, const void* Q, const void* V, const float* 
  * - The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
  *   before any stream capture.
+ * - Start-up: the CUDA runtime loads a library's device code lazily by
+ *   default, on first use, and loading it is what places the scratch array
+ *   (and each kernel family's code) in device memory.  So the first call on
+ *   a device can take device memory, and a first call of another kernel
+ *   family can too.  A caller that must not allocate later makes one call
+ *   per problem description it will use at start-up, before it reserves or
+ *   hands out its memory, or runs with CUDA_MODULE_LOADING=EAGER so that
+ *   everything is loaded with the library.
  * - All calls on a device share the one array and each call overwrites it:
  *   calls whose work overlaps on the GPU (different streams, or threads)
  *   race and give wrong results.  Serialise them, e.g. on one stream.
+ * - The array's address is cached per device for the life of the process;
+ *   cudaDeviceReset (or any teardown of the device's primary context)
+ *   invalidates it, so do not call this entry point after one.
  * Returns what atlas_mem_forward returns. */
 int atlas_mem_forward_noalloc(const void* K, const void* Q, const void* V, const float* alpha,
                               const float* eta, const float* theta, const float* gamma,

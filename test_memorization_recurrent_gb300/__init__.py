@@ -53,33 +53,38 @@ _lock = threading.Lock()
 _lib = None
 
 
+def open_library(path: str):
+    """Open a build of the library at ``path`` with the entry points' argument
+    types set (tests also open separately built copies this way)."""
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with "
+                          "test_memorization_recurrent_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    cp = ctypes.POINTER(AtlasMemCfg)
+    vp = ctypes.c_void_p
+    lib.atlas_mem_state_size.argtypes = [cp]
+    lib.atlas_mem_state_size.restype = ctypes.c_size_t
+    lib.atlas_mem_workspace_bytes.argtypes = [cp]
+    lib.atlas_mem_workspace_bytes.restype = ctypes.c_size_t
+    lib.atlas_mem_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, cp, vp, vp, vp]
+    lib.atlas_mem_forward.restype = ctypes.c_int
+    lib.atlas_mem_strerror.argtypes = [ctypes.c_int]
+    lib.atlas_mem_strerror.restype = ctypes.c_char_p
+    lib.atlas_mem_path.argtypes = [cp]
+    lib.atlas_mem_path.restype = ctypes.c_char_p
+    lib.atlas_mem_launch_count.argtypes = [cp]
+    lib.atlas_mem_launch_count.restype = ctypes.c_long
+    lib.atlas_mem_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, cp, vp, vp, vp]
+    lib.atlas_mem_forward_noalloc.restype = ctypes.c_int
+    return lib
+
+
 def load_library(path: str = LIB_PATH):
     """Load libatlasmem.so (built by ``build.build()``); raises if absent."""
     global _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(path):
-                raise ImportError(f"{path} is missing: build it with "
-                                  "test_memorization_recurrent_gb300.build.build()")
-            lib = ctypes.CDLL(path)
-            cp = ctypes.POINTER(AtlasMemCfg)
-            vp = ctypes.c_void_p
-            lib.atlas_mem_state_size.argtypes = [cp]
-            lib.atlas_mem_state_size.restype = ctypes.c_size_t
-            lib.atlas_mem_workspace_bytes.argtypes = [cp]
-            lib.atlas_mem_workspace_bytes.restype = ctypes.c_size_t
-            lib.atlas_mem_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, cp, vp, vp, vp]
-            lib.atlas_mem_forward.restype = ctypes.c_int
-            lib.atlas_mem_strerror.argtypes = [ctypes.c_int]
-            lib.atlas_mem_strerror.restype = ctypes.c_char_p
-            lib.atlas_mem_path.argtypes = [cp]
-            lib.atlas_mem_path.restype = ctypes.c_char_p
-            lib.atlas_mem_launch_count.argtypes = [cp]
-            lib.atlas_mem_launch_count.restype = ctypes.c_long
-            lib.atlas_mem_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, cp, vp, vp,
-                                                      vp]
-            lib.atlas_mem_forward_noalloc.restype = ctypes.c_int
-            _lib = lib
+            _lib = open_library(path)
     return _lib
 
 

@@ -60,6 +60,17 @@ constexpr int kDim = 128;
 constexpr long long kWaitLimit = 2000000000LL;  // clock cycles (~1 s)
 constexpr float kMinSuffix = 1e-30f;            // smallest s_0 handled here
 
+// Test builds only: with ATLAS_TEST_WITHHOLD_LOADS defined, the producer of
+// head 0 never issues the loads of chunk 1, so the consumers' bounded wait on
+// that stage runs out and the abort path (status word, drain, TMEM release)
+// runs.  Every access stays in bounds and every wait still ends.  The library
+// the package builds never defines it.
+#ifdef ATLAS_TEST_WITHHOLD_LOADS
+constexpr bool kWithholdChunk1OfHead0 = true;
+#else
+constexpr bool kWithholdChunk1OfHead0 = false;
+#endif
+
 // shared-memory map (bytes from a 1024-aligned base)
 //   stage: Phi kb0 | Q kb0 | Phi kb1 | Q kb1 (8 KB each, 128B-swizzled, loaded by
 //   TMA) | P''hi | P''lo ([i][n], 128B-swizzled, written by the epilogue) |
@@ -248,6 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           timeout();
           break;
         }
+        if (kWithholdChunk1OfHead0 && head == 0 && j == 1) continue;  // test builds only
         unsigned char* st = sm + OFF_STAGE0 + s * STAGE_BYTES;
         uint64_t* fb = &bars[B_FULL0 + s];
         mbar_arrive_expect_tx(fb, p.gate_tma ? STAGE_TX : STAGE_TX_NOGATES);
