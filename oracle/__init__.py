@@ -84,6 +84,8 @@ def _load():
             lib.orc_forward_chunked.restype = ctypes.c_int
             lib.orc_forward_recurrent.argtypes = fwd
             lib.orc_forward_recurrent.restype = ctypes.c_int
+            lib.orc_backward_chunked.argtypes = [cp, ctypes.c_int] + [dp] * 19 + [ctypes.c_int]
+            lib.orc_backward_chunked.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -179,3 +181,39 @@ def forward(cfg: OrcCfg, K, Q, V, alpha, eta, theta, gamma, M0=None, S0=None,
     if rc != 0:
         raise ValueError("oracle rejected the problem description")
     return Y, M, S
+
+
+def backward(cfg: OrcCfg, K, Q, V, alpha, eta, theta, gamma, M0, S0, dY, dM_N=None, dS_N=None,
+             n_threads: int = 0) -> dict:
+    """Gradients of L = sum <dY, Y> + <dM_N, M_N> + <dS_N, S_N> through the chunked
+    forward (linear memory, no Newton-Schulz) with respect to every input.
+
+    Shapes as in ``forward``; dY: [H, N, d_v]; dM_N, dS_N: [H, state] or None (zero).
+    Returns a dict of fp64 arrays: dK, dV [H, n_history + N, .], dQ [H, N, d_k],
+    dalpha, deta, dtheta [H, N], dgamma [c] (summed over heads), dM0, dS0 [H, state].
+    """
+    K, Q, V = _f64(K), _f64(Q), _f64(V)
+    H = K.shape[0]
+    nkv = cfg.N + cfg.n_history
+    ns = state_size(cfg)
+    alpha, eta, theta, gamma = _f64(alpha), _f64(eta), _f64(theta), _f64(gamma)
+    M = np.zeros((H, ns)) if M0 is None else _f64(M0).reshape(H, ns).copy()
+    S = np.zeros((H, ns)) if S0 is None else _f64(S0).reshape(H, ns).copy()
+    dY = _f64(dY)
+    assert dY.shape == (H, cfg.N, cfg.d_v)
+    dM = np.zeros((H, ns)) if dM_N is None else _f64(dM_N).reshape(H, ns).copy()
+    dS = np.zeros((H, ns)) if dS_N is None else _f64(dS_N).reshape(H, ns).copy()
+    out = dict(dK=np.zeros((H, nkv, cfg.d_k)), dQ=np.zeros((H, cfg.N, cfg.d_k)),
+               dV=np.zeros((H, nkv, cfg.d_v)), dalpha=np.zeros((H, cfg.N)),
+               deta=np.zeros((H, cfg.N)), dtheta=np.zeros((H, cfg.N)),
+               dgamma=np.zeros((H, cfg.c)))
+    rc = _load().orc_backward_chunked(
+        ctypes.byref(cfg), H, _p(K), _p(Q), _p(V), _p(alpha), _p(eta), _p(theta), _p(gamma),
+        _p(M), _p(S), _p(dY), _p(dM), _p(dS), _p(out["dK"]), _p(out["dQ"]), _p(out["dV"]),
+        _p(out["dalpha"]), _p(out["deta"]), _p(out["dtheta"]), _p(out["dgamma"]),
+        int(n_threads))
+    if rc != 0:
+        raise ValueError("backward oracle: unsupported or invalid problem description")
+    out["dgamma"] = out["dgamma"].sum(axis=0)
+    out["dM0"], out["dS0"] = dM, dS
+    return out

@@ -532,3 +532,277 @@ int orc_forward_recurrent(const orc_cfg* g, int n_heads, const double* K, const 
                           double* Y, int n_threads) {
   return orc_run(g, 1, n_heads, K, Q, V, alpha, eta, theta, gamma, M, S, Y, n_threads);
 }
+
+/* ============================================================== backward
+ *
+ * Gradients of a scalar loss on the outputs with respect to every input of
+ * the chunked update: the outer loop that trains what the inner loop does not
+ * ([ATLAS] "Deep Memory Module": the memory is optimised at test time inside,
+ * the projections producing k, q, v and the gates by an outer loop; [Miras]
+ * Associative Memory & Attentional Bias, Remark 2).  The loss is
+ *     L = sum_t <dY_t, y_t> + <dM_N, M_N> + <dS_N, S_N>
+ * for given upstream gradients dY, dM_N, dS_N.  This is the literal reverse of
+ * orc_head_chunked for a linear memory (any feature map, bias, window, chunk,
+ * momentum; no Newton-Schulz): the chunk-start states are kept, each chunk's
+ * token states are recomputed from them, and every step of the forward loop
+ * is differentiated in reverse order. */
+
+/* d/de of orc_bias_dy (the second derivative of the bias). */
+static double orc_bias_d2(const orc_cfg* g, double e) {
+  if (g->loss == ORC_LOSS_LP) {
+    const double p = g->loss_param;
+    if (p == 2.0) return 2.0;
+    if (e == 0.0) return 0.0;  /* the limit for p > 2; undefined for p < 2 */
+    return p * (p - 1.0) * pow(fabs(e), p - 2.0);
+  }
+  if (g->loss == ORC_LOSS_HUBER) return fabs(e) <= g->loss_param ? 2.0 : 0.0;
+  return 2.0;
+}
+
+/* dx += (dPhi/dx)^T dphi for the map of orc_phi. */
+static void orc_phi_backward(const orc_cfg* g, const double* x, const double* dphi, double* dx) {
+  int d = g->d_k;
+  for (int i = 0; i < d; ++i) dx[i] += dphi[i];
+  if (g->phi == ORC_PHI_IDENTITY) return;
+  int p = d;
+  for (int i = 0; i < d; ++i)
+    for (int j = i; j < d; ++j) {
+      dx[i] += dphi[p] * x[j];
+      dx[j] += dphi[p] * x[i];
+      ++p;
+    }
+}
+
+/* Reverse of orc_grad for a linear memory: given dG (state layout), add the
+ * gradients with respect to the state M0 (dM0), the key k (dk) and the value
+ * v (dv).  G = psi Phi(k)^T with psi = bias_dy(M0 Phi(k) - v) (dot: -2 v). */
+static void orc_grad_backward(const orc_cfg* g, const double* M0, const double* k,
+                              const double* v, const double* dG, double* dM0, double* dk,
+                              double* dv) {
+  int D = orc_feature_dim(g), nv = g->d_v;
+  double* f = (double*)malloc(sizeof(double) * D);
+  double* df = (double*)calloc(D, sizeof(double));
+  orc_phi(g, k, f);
+  for (int r = 0; r < nv; ++r) {
+    double s = 0.0, dpsi = 0.0;
+    for (int j = 0; j < D; ++j) {
+      s += M0[(long)r * D + j] * f[j];
+      dpsi += dG[(long)r * D + j] * f[j];
+    }
+    if (g->loss == ORC_LOSS_DOT) {
+      for (int j = 0; j < D; ++j) df[j] += dG[(long)r * D + j] * (-2.0 * v[r]);
+      dv[r] += -2.0 * dpsi;
+      continue;
+    }
+    const double e = s - v[r];
+    const double psi = orc_bias_dy(g, e);
+    const double ds = dpsi * orc_bias_d2(g, e);
+    dv[r] -= ds;
+    for (int j = 0; j < D; ++j) {
+      df[j] += dG[(long)r * D + j] * psi + M0[(long)r * D + j] * ds;
+      dM0[(long)r * D + j] += ds * f[j];
+    }
+  }
+  orc_phi_backward(g, k, df, dk);
+  free(f);
+  free(df);
+}
+
+static double orc_dot(long n, const double* a, const double* b) {
+  double s = 0.0;
+  for (long i = 0; i < n; ++i) s += a[i] * b[i];
+  return s;
+}
+
+/* One chunk [t0, t1) forward from (M, S), as orc_head_chunked; with the
+ * recording arrays given, the state before each token (Mb, Sb) and its
+ * windowed gradient (Gs) are kept, b entries of the state size each. */
+static void orc_chunk_forward(const orc_cfg* g, int t0, int t1, const double* K, const double* Q,
+                              const double* V, const double* alpha, const double* eta,
+                              const double* theta, const double* gamma, double* M, double* S,
+                              double* Mb, double* Sb, double* Gs) {
+  long n = orc_state_size(g);
+  int dk = g->d_k, dv = g->d_v, nh = g->n_history;
+  double* M0 = (double*)malloc(sizeof(double) * n);
+  double* gsum = (double*)malloc(sizeof(double) * n);
+  double* Gi = (double*)malloc(sizeof(double) * n);
+  double* upd = (double*)malloc(sizeof(double) * n);
+  double* y = (double*)malloc(sizeof(double) * dv);
+  memcpy(M0, M, sizeof(double) * n);
+  for (int t = t0; t < t1; ++t) {
+    for (long j = 0; j < n; ++j) gsum[j] = 0.0;
+    int i0 = t - g->c + 1 < -nh ? -nh : t - g->c + 1;
+    for (int i = i0; i <= t; ++i) {
+      orc_grad(g, M0, K + (long)(i + nh) * dk, V + (long)(i + nh) * dv, Gi);
+      for (long j = 0; j < n; ++j) gsum[j] += gamma[t - i] * Gi[j];
+    }
+    if (Mb) {
+      memcpy(Mb + (long)(t - t0) * n, M, sizeof(double) * n);
+      memcpy(Sb + (long)(t - t0) * n, S, sizeof(double) * n);
+      memcpy(Gs + (long)(t - t0) * n, gsum, sizeof(double) * n);
+    }
+    orc_token_step(g, alpha[t], eta[t], theta[t], gsum, Q + (long)t * dk, M, S, upd, y);
+  }
+  free(M0);
+  free(gsum);
+  free(Gi);
+  free(upd);
+  free(y);
+}
+
+/* Reverse pass of one head.  In: the forward inputs, M and S at the start
+ * (M_in, S_in), dY [N, d_v], and dM, dS holding dL/dM_N, dL/dS_N.  Out: dM, dS
+ * overwritten with dL/dM_0, dL/dS_0; dK, dV [n_history + N, .], dQ [N, d_k],
+ * dalpha, deta, dtheta [N], dgamma [c] (all overwritten). */
+static void orc_head_backward(const orc_cfg* g, const double* K, const double* Q,
+                              const double* V, const double* alpha, const double* eta,
+                              const double* theta, const double* gamma, const double* M_in,
+                              const double* S_in, const double* dY, double* dM, double* dS,
+                              double* dK, double* dQ, double* dV, double* dalpha, double* deta,
+                              double* dtheta, double* dgamma) {
+  long n = orc_state_size(g);
+  int D = orc_feature_dim(g), dk = g->d_k, dv = g->d_v, nh = g->n_history, b = g->b;
+  int nchunks = (g->N + b - 1) / b;
+  memset(dK, 0, sizeof(double) * (long)(nh + g->N) * dk);
+  memset(dV, 0, sizeof(double) * (long)(nh + g->N) * dv);
+  memset(dQ, 0, sizeof(double) * (long)g->N * dk);
+  memset(dgamma, 0, sizeof(double) * g->c);
+  /* forward once: the state at every chunk start */
+  double* Mc = (double*)malloc(sizeof(double) * n * (nchunks > 0 ? nchunks : 1));
+  double* Sc = (double*)malloc(sizeof(double) * n * (nchunks > 0 ? nchunks : 1));
+  double* M = (double*)malloc(sizeof(double) * n);
+  double* S = (double*)malloc(sizeof(double) * n);
+  memcpy(M, M_in, sizeof(double) * n);
+  memcpy(S, S_in, sizeof(double) * n);
+  for (int c = 0; c < nchunks; ++c) {
+    int t0 = c * b, t1 = t0 + b < g->N ? t0 + b : g->N;
+    memcpy(Mc + (long)c * n, M, sizeof(double) * n);
+    memcpy(Sc + (long)c * n, S, sizeof(double) * n);
+    orc_chunk_forward(g, t0, t1, K, Q, V, alpha, eta, theta, gamma, M, S, NULL, NULL, NULL);
+  }
+  double* Mb = (double*)malloc(sizeof(double) * n * b);
+  double* Sb = (double*)malloc(sizeof(double) * n * b);
+  double* Gs = (double*)malloc(sizeof(double) * n * b);
+  double* Mt = (double*)malloc(sizeof(double) * n);
+  double* St = (double*)malloc(sizeof(double) * n);
+  double* dg = (double*)malloc(sizeof(double) * n);
+  double* dG = (double*)malloc(sizeof(double) * n);
+  double* Gi = (double*)malloc(sizeof(double) * n);
+  double* dMc = (double*)malloc(sizeof(double) * n);
+  double* fq = (double*)malloc(sizeof(double) * D);
+  double* dfq = (double*)malloc(sizeof(double) * D);
+  for (int c = nchunks - 1; c >= 0; --c) {
+    int t0 = c * b, t1 = t0 + b < g->N ? t0 + b : g->N;
+    const double* M0 = Mc + (long)c * n;
+    memcpy(M, M0, sizeof(double) * n);
+    memcpy(S, Sc + (long)c * n, sizeof(double) * n);
+    orc_chunk_forward(g, t0, t1, K, Q, V, alpha, eta, theta, gamma, M, S, Mb, Sb, Gs);
+    for (long j = 0; j < n; ++j) dMc[j] = 0.0;
+    for (int t = t1 - 1; t >= t0; --t) {
+      const double* Mp = Mb + (long)(t - t0) * n;  /* M_{t-1} */
+      const double* Sp = Sb + (long)(t - t0) * n;  /* S_{t-1} */
+      const double* gt = Gs + (long)(t - t0) * n;  /* g_t */
+      /* the token's states: S_t = eta S_{t-1} - theta g_t, M_t = (1-alpha) M_{t-1} + S_t */
+      for (long j = 0; j < n; ++j) {
+        St[j] = eta[t] * Sp[j] - theta[t] * gt[j];
+        Mt[j] = (1.0 - alpha[t]) * Mp[j] + St[j];
+      }
+      /* y_t = M_t Phi(q_t) */
+      orc_phi(g, Q + (long)t * dk, fq);
+      for (int j = 0; j < D; ++j) dfq[j] = 0.0;
+      for (int r = 0; r < dv; ++r) {
+        const double dy = dY[(long)t * dv + r];
+        for (int j = 0; j < D; ++j) {
+          dM[(long)r * D + j] += dy * fq[j];
+          dfq[j] += Mt[(long)r * D + j] * dy;
+        }
+      }
+      orc_phi_backward(g, Q + (long)t * dk, dfq, dQ + (long)t * dk);
+      /* M_t = (1 - alpha_t) M_{t-1} + S_t */
+      dalpha[t] = -orc_dot(n, dM, Mp);
+      for (long j = 0; j < n; ++j) {
+        dS[j] += dM[j];
+        dM[j] *= 1.0 - alpha[t];
+      }
+      /* S_t = eta_t S_{t-1} - theta_t g_t */
+      deta[t] = orc_dot(n, dS, Sp);
+      dtheta[t] = -orc_dot(n, dS, gt);
+      for (long j = 0; j < n; ++j) {
+        dg[j] = -theta[t] * dS[j];
+        dS[j] *= eta[t];
+      }
+      /* g_t = sum over the window of gamma[t - i] grad(M0; k_i, v_i) */
+      int i0 = t - g->c + 1 < -nh ? -nh : t - g->c + 1;
+      for (int i = i0; i <= t; ++i) {
+        const double* ki = K + (long)(i + nh) * dk;
+        const double* vi = V + (long)(i + nh) * dv;
+        orc_grad(g, M0, ki, vi, Gi);
+        dgamma[t - i] += orc_dot(n, dg, Gi);
+        for (long j = 0; j < n; ++j) dG[j] = gamma[t - i] * dg[j];
+        orc_grad_backward(g, M0, ki, vi, dG, dMc, dK + (long)(i + nh) * dk,
+                          dV + (long)(i + nh) * dv);
+      }
+    }
+    /* the chunk-start state M0 is the state the previous chunk ended with */
+    for (long j = 0; j < n; ++j) dM[j] += dMc[j];
+  }
+  free(Mc); free(Sc); free(M); free(S); free(Mb); free(Sb); free(Gs); free(Mt); free(St);
+  free(dg); free(dG); free(Gi); free(dMc); free(fq); free(dfq);
+}
+
+typedef struct {
+  const orc_cfg* g;
+  int h0, h1;
+  const double *K, *Q, *V, *alpha, *eta, *theta, *gamma, *M, *S, *dY;
+  double *dM, *dS, *dK, *dQ, *dV, *dalpha, *deta, *dtheta, *dgamma;
+} orc_bjob;
+
+static void* orc_bworker(void* p) {
+  orc_bjob* j = (orc_bjob*)p;
+  const orc_cfg* g = j->g;
+  long ns = orc_state_size(g);
+  const long nkv = (long)g->N + g->n_history;
+  for (int h = j->h0; h < j->h1; ++h) {
+    orc_head_backward(g, j->K + h * nkv * g->d_k, j->Q + (long)h * g->N * g->d_k,
+                      j->V + h * nkv * g->d_v, j->alpha + (long)h * g->N,
+                      j->eta + (long)h * g->N, j->theta + (long)h * g->N, j->gamma,
+                      j->M + h * ns, j->S + h * ns, j->dY + (long)h * g->N * g->d_v,
+                      j->dM + h * ns, j->dS + h * ns, j->dK + h * nkv * g->d_k,
+                      j->dQ + (long)h * g->N * g->d_k, j->dV + h * nkv * g->d_v,
+                      j->dalpha + (long)h * g->N, j->deta + (long)h * g->N,
+                      j->dtheta + (long)h * g->N, j->dgamma + (long)h * g->c);
+  }
+  return NULL;
+}
+
+/* Backward of orc_forward_chunked over n_heads heads (linear memory without
+ * Newton-Schulz; -1 otherwise).  M, S: [heads, state] at the start of the
+ * forward; dY: [heads, N, d_v]; dM, dS: [heads, state], in: dL/dM_N, dL/dS_N,
+ * out: dL/dM_0, dL/dS_0; dK, dV: [heads, n_history + N, .]; dQ: [heads, N, d_k];
+ * dalpha, deta, dtheta: [heads, N]; dgamma: [heads, c] (per head: gamma is
+ * shared, so its gradient is the sum over heads). */
+int orc_backward_chunked(const orc_cfg* g, int n_heads, const double* K, const double* Q,
+                         const double* V, const double* alpha, const double* eta,
+                         const double* theta, const double* gamma, const double* M,
+                         const double* S, const double* dY, double* dM, double* dS, double* dK,
+                         double* dQ, double* dV, double* dalpha, double* deta, double* dtheta,
+                         double* dgamma, int n_threads) {
+  if (orc_check(g) != 0 || n_heads < 0) return -1;
+  if (g->mem != ORC_MEM_LINEAR || g->ns_steps > 0) return -1;
+  if (n_threads <= 0) n_threads = (int)sysconf(_SC_NPROCESSORS_ONLN);
+  if (n_threads > n_heads) n_threads = n_heads;
+  if (n_threads < 1) n_threads = 1;
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * n_threads);
+  orc_bjob* jobs = (orc_bjob*)malloc(sizeof(orc_bjob) * n_threads);
+  for (int w = 0; w < n_threads; ++w) {
+    orc_bjob j = {g, (int)((long)n_heads * w / n_threads),
+                  (int)((long)n_heads * (w + 1) / n_threads), K, Q, V, alpha, eta, theta,
+                  gamma, M, S, dY, dM, dS, dK, dQ, dV, dalpha, deta, dtheta, dgamma};
+    jobs[w] = j;
+    pthread_create(&th[w], NULL, orc_bworker, &jobs[w]);
+  }
+  for (int w = 0; w < n_threads; ++w) pthread_join(th[w], NULL);
+  free(th);
+  free(jobs);
+  return 0;
+}
