@@ -23,7 +23,7 @@ F32, BF16 = 0, 1
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
 
 EXPORTS = ("atlas_mem_state_size", "atlas_mem_workspace_bytes", "atlas_mem_forward",
-           "atlas_mem_forward_noalloc",
+           "atlas_mem_forward_noalloc", "atlas_mem_backward", "atlas_mem_backward_workspace_bytes",
            "atlas_mem_strerror", "atlas_mem_path", "atlas_mem_launch_count")
 
 
@@ -76,6 +76,10 @@ def open_library(path: str):
     lib.atlas_mem_launch_count.restype = ctypes.c_long
     lib.atlas_mem_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, cp, vp, vp, vp]
     lib.atlas_mem_forward_noalloc.restype = ctypes.c_int
+    lib.atlas_mem_backward_workspace_bytes.argtypes = [cp]
+    lib.atlas_mem_backward_workspace_bytes.restype = ctypes.c_size_t
+    lib.atlas_mem_backward.argtypes = [vp] * 7 + [cp] + [vp] * 10
+    lib.atlas_mem_backward.restype = ctypes.c_int
     return lib
 
 
@@ -171,5 +175,30 @@ def atlas_mem_forward_noalloc(K, Q, V, alpha, eta, theta, gamma, cfg: AtlasMemCf
         need = atlas_mem_workspace_bytes(cfg)
         raise AtlasError(rc, f"problem needs {need} bytes of scratch; the built-in array holds "
                              f"{NOALLOC_SCRATCH_BYTES} (split the heads over several calls)")
+    if rc != OK:
+        raise AtlasError(rc, atlas_mem_strerror(rc))
+
+
+def atlas_mem_backward_workspace_bytes(cfg: AtlasMemCfg) -> int:
+    n = int(load_library().atlas_mem_backward_workspace_bytes(ctypes.byref(cfg)))
+    if n == 2 ** 64 - 1:
+        raise AtlasError(ERR_UNSUPPORTED, "description not covered by the backward pass")
+    return n
+
+
+def atlas_mem_backward(K, Q, V, alpha, eta, theta, gamma, cfg: AtlasMemCfg, M0, dY, dM, dK, dQ,
+                       dV, dalpha, deta, dtheta, stream=None) -> None:
+    """Enqueue the backward pass (see include/atlas_mem.h): dM holds dL/dM_N on
+    entry and dL/dM_0 on return; dK, dQ, dV, dalpha, deta, dtheta are written.
+    Raises AtlasError on a non-zero status."""
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream().cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    rc = load_library().atlas_mem_backward(
+        _ptr(K), _ptr(Q), _ptr(V), _ptr(alpha), _ptr(eta), _ptr(theta), _ptr(gamma),
+        ctypes.byref(cfg), _ptr(M0), _ptr(dY), _ptr(dM), _ptr(dK), _ptr(dQ), _ptr(dV),
+        _ptr(dalpha), _ptr(deta), _ptr(dtheta), ctypes.c_void_p(stream))
     if rc != OK:
         raise AtlasError(rc, atlas_mem_strerror(rc))

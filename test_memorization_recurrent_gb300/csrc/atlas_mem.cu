@@ -208,6 +208,49 @@ int atlas_mem_forward(const void* K, const void* Q, const void* V, const float* 
   return linear_simt_launch(a, (int)heads, st);
 }
 
+namespace {
+
+// Structural checks of a backward description (no pointers).
+int backward_plan(const atlas_mem_cfg* cfg, LinArgs* out) {
+  const int rc = check_cfg(cfg);
+  if (rc != ATLAS_OK) return rc;
+  if (cfg->mem != ATLAS_MEM_LINEAR || cfg->ns_steps > 0) return ATLAS_ERR_UNSUPPORTED;
+  if (cfg->loss != ATLAS_LOSS_L2 && cfg->loss != ATLAS_LOSS_LP && cfg->loss != ATLAS_LOSS_HUBER)
+    return ATLAS_ERR_UNSUPPORTED;
+  *out = lin_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, cfg, nullptr,
+                  nullptr);
+  return linear_bwd_supported(*out) ? ATLAS_OK : ATLAS_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+size_t atlas_mem_backward_workspace_bytes(const atlas_mem_cfg* cfg) {
+  LinArgs a;
+  if (backward_plan(cfg, &a) != ATLAS_OK) return (size_t)-1;
+  return linear_bwd_workspace_bytes(a, cfg->B * cfg->H);
+}
+
+int atlas_mem_backward(const void* K, const void* Q, const void* V, const float* alpha,
+                       const float* eta, const float* theta, const float* gamma,
+                       const atlas_mem_cfg* cfg, const float* M0, const float* dY, float* dM,
+                       float* dK, float* dQ, float* dV, float* dalpha, float* deta,
+                       float* dtheta, void* stream) {
+  LinArgs a;
+  const int rc = backward_plan(cfg, &a);
+  if (rc != ATLAS_OK) return rc;
+  const long heads = (long)cfg->B * cfg->H;
+  if (heads == 0) return ATLAS_OK;
+  if (!M0 || !dM || !gamma) return ATLAS_ERR_INVALID;
+  if (cfg->N > 0 && (!K || !Q || !V || !alpha || !eta || !theta || !dY || !dK || !dQ || !dV ||
+                     !dalpha || !deta || !dtheta))
+    return ATLAS_ERR_INVALID;
+  const size_t need = linear_bwd_workspace_bytes(a, (int)heads);
+  if (!cfg->workspace || cfg->workspace_bytes < need) return ATLAS_ERR_WORKSPACE;
+  a = lin_args(K, Q, V, alpha, eta, theta, gamma, cfg, nullptr, nullptr);
+  return linear_bwd_launch(a, (int)heads, M0, dY, dM, dK, dQ, dV, dalpha, deta, dtheta,
+                           cfg->status_dev, cfg->workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
 const char* atlas_mem_strerror(int status) {
   switch (status) {
     case ATLAS_OK: return "ok";

@@ -49,6 +49,16 @@ bool linear_tc_supported(const LinArgs& a);
 size_t linear_tc_workspace_bytes(int heads);
 int linear_tc_launch(const LinArgs& a, int heads, int* status, void* workspace, cudaStream_t st);
 
+// Backward pass (linear_bwd.cu): identity map, d_k = d_v = 128, b = 64, c = 1,
+// eta = 0 in the forward, no history rows, no momentum state in or out.
+// Three launches; the workspace holds the chunk-start states, the gate tables
+// and the per-row-block partial sums.
+bool linear_bwd_supported(const LinArgs& a);
+size_t linear_bwd_workspace_bytes(const LinArgs& a, int heads);
+int linear_bwd_launch(const LinArgs& a, int heads, const float* M0, const float* dY, float* dM,
+                      float* dK, float* dQ, float* dV, float* dalpha, float* deta, float* dtheta,
+                      int* status, void* ws, cudaStream_t st);
+
 // Batched strided GEMM on fp32 operands (tc_gemm.cu, tensor cores with bf16
 // hi/lo operand splitting), used by the MLP-memory path:
 //   C[b](m,n) = alpha rowscale[b](m) sum_k A[b](m,k) kscale[b](k) B[b](k,n) + beta D[b](m,n)

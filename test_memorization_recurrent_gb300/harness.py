@@ -65,3 +65,35 @@ class Runner:
         atlas_mem_forward(d["K"], d["Q"], d["V"], d["alpha"], d["eta"], d["theta"], d["gamma"],
                           self.cfg, self.Y, self.M, stream)
         return self.Y, self.M
+
+
+class BackwardRunner:
+    """Owns the gradient buffers and the workspace of ``atlas_mem_backward``."""
+
+    def __init__(self, w, heads: int, N: int, device="cuda"):
+        from . import atlas_mem_backward_workspace_bytes
+        self.w, self.heads, self.N = w, heads, N
+        f32 = dict(device=device, dtype=torch.float32)
+        self.dK = torch.empty((heads, N, w.d_k), **f32)
+        self.dQ = torch.empty((heads, N, w.d_k), **f32)
+        self.dV = torch.empty((heads, N, w.d_v), **f32)
+        self.dalpha = torch.empty((heads, N), **f32)
+        self.deta = torch.empty((heads, N), **f32)
+        self.dtheta = torch.empty((heads, N), **f32)
+        self.dM = torch.empty((heads, w.state_size), **f32)
+        self.status = torch.zeros(1, device=device, dtype=torch.int32)
+        nbytes = atlas_mem_backward_workspace_bytes(cfg_for(w, heads, N))
+        self.ws = torch.empty(max(nbytes, 1), device=device, dtype=torch.uint8)
+        self.cfg = cfg_for(w, heads, N, workspace=self.ws, workspace_bytes=nbytes,
+                           status_dev=self.status)
+
+    def __call__(self, d: dict, dY, dM_N, stream=None):
+        """Gradients for device inputs ``d`` (its "M0" is the forward's initial state),
+        upstream dY [heads, N, d_v] and dM_N [heads, state] (device fp32)."""
+        from . import atlas_mem_backward
+        self.dM.copy_(dM_N)
+        atlas_mem_backward(d["K"], d["Q"], d["V"], d["alpha"], d["eta"], d["theta"], d["gamma"],
+                           self.cfg, d["M0"], dY, self.dM, self.dK, self.dQ, self.dV,
+                           self.dalpha, self.deta, self.dtheta, stream)
+        return dict(dK=self.dK, dQ=self.dQ, dV=self.dV, dalpha=self.dalpha, deta=self.deta,
+                    dtheta=self.dtheta, dM0=self.dM)

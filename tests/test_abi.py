@@ -143,3 +143,30 @@ def test_bias_launches_are_counted():
         base = A.atlas_mem_launch_count(cfg_for(w, 2, N))
         wb = w.__class__(**{**w.__dict__, "loss": A.LOSS_HUBER, "loss_param": 0.3})
         assert A.atlas_mem_launch_count(cfg_for(wb, 2, N)) == base + extra, wid
+
+
+@pytest.mark.parametrize("kw", [
+    dict(mem=A.MEM_MLP, d_h=512),              # MLP memory
+    dict(c=2),                                 # window longer than one token
+    dict(b=32),                                # another chunk length
+    dict(d_k=64, d_v=64),                      # another width
+    dict(loss=A.LOSS_DOT),                     # dot-product bias
+    dict(n_history=3),                         # history rows
+    dict(phi=A.PHI_POLY2, d_k=16, d_v=128),    # feature map
+])
+def test_backward_rejects_uncovered_descriptions(lib, kw):
+    base = dict(B=1, H=2, N=100, d_k=128, d_v=128, c=1, b=64)
+    base.update(kw)
+    cfg = A.make_cfg(**base)
+    with pytest.raises(A.AtlasError):
+        A.atlas_mem_backward_workspace_bytes(cfg)
+    rc = lib.atlas_mem_backward(*([1] * 7), ctypes.byref(cfg), *([1] * 10))
+    assert rc == A.ERR_UNSUPPORTED
+
+
+def test_backward_workspace_and_missing_workspace(lib):
+    cfg = A.make_cfg(B=2, H=3, N=130, d_k=128, d_v=128, c=1, b=64)
+    n = A.atlas_mem_backward_workspace_bytes(cfg)
+    assert n >= 6 * 130 * 128 * 4 * 4  # at least the four row blocks' dK, dQ partials
+    rc = lib.atlas_mem_backward(*([1] * 7), ctypes.byref(cfg), *([1] * 10))
+    assert rc == A.ERR_WORKSPACE
