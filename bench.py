@@ -323,7 +323,12 @@ def roofline(w, path, kernel_s):
     bytes_launch = tokens * W.bytes_per_token(w) + 2 * 4 * w.heads * w.state_size
     flops_launch = tokens * W.flop_per_token(w)
     ridge = tf * 1e12 / (hbm * 1e9)
-    if flops_launch / bytes_launch < ridge:
+    if path == "linear_seq":  # fp32 FMAs on CUDA cores, one token after another
+        peak = fp32_alu_peak_tflops()
+        achieved = flops_launch / kernel_s / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_kind": "fp32 FMA peak from unit counts and clock"}
+    elif flops_launch / bytes_launch < ridge:
         achieved = bytes_launch / kernel_s / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": achieved / hbm, "peak_kind": f"{peak_kind} hbm_gbs"}
@@ -378,70 +383,123 @@ def measure_config(wid, n_tokens, steps, warmup, dev, with_cpu):
     return rec
 
 
-def e2e_rate(w, d, run, steps, warmup, stream, world, dev, groups=4):
+def fp32_alu_peak_tflops():
+    """fp32 FMA peak of one GB300 from its unit counts and clock: 152 SMs x 128
+    FP32 lanes x 2 FLOP per FMA x the maximum SM clock (2070 MHz)."""
+    return 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def measure_backward(steps, warmup, dev):
+    """The backward pass over the whole DeltaNet-like workload (every head, every
+    token): rate, and the fraction of the fp32 CUDA-core peak it reaches."""
+    import torch
+    from test_memorization_recurrent_gb300.harness import BackwardRunner, to_device
+    w = W.workload(2)
+    inp = W.generate(w)
+    d = to_device(w, inp, dev)
+    r = np.random.default_rng(3)
+    dY = torch.from_numpy(r.standard_normal((w.heads, w.N, w.d_v)).astype(np.float32)).to(dev)
+    dMN = torch.zeros((w.heads, w.state_size), dtype=torch.float32, device=dev)
+    run = BackwardRunner(w, w.heads, w.N, device=dev)
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    with Clocks(torch.cuda.current_device()) as clk:
+        for _ in range(warmup):
+            run(d, dY, dMN)
+        torch.cuda.synchronize()
+        clk.wait_ready()
+        clk.mark_start()
+        ev[0].record(stream)
+        for _ in range(steps):
+            run(d, dY, dMN)
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+        clk.mark_end()
+    if int(run.status.item()) != 0:
+        raise SystemExit(f"backward status {int(run.status.item())}")
+    s = ev[0].elapsed_time(ev[1]) / 1e3 / steps
+    flops = w.tokens * W.bwd_flop_per_token(w)
+    peak = fp32_alu_peak_tflops()
+    rec = {"workload": w.name, "what": "backward pass (dK, dQ, dV, dalpha, deta, dtheta, dM_0)",
+           "tokens_per_call": w.tokens, "steps": steps, "value": w.tokens / s, "unit": UNIT,
+           "ms_per_step": s * 1e3, "launches_per_call": 3,
+           "roofline": {"bound": "alu", "achieved": flops / s / 1e12, "peak": peak,
+                        "unit": "TFLOP/s", "frac": flops / s / 1e12 / peak,
+                        "peak_kind": "fp32 FMA peak from unit counts and clock",
+                        "traffic": None, "kernel": "linear_bwd", "kernel_ms": s * 1e3,
+                        "algorithmic_flops": flops,
+                        "algorithmic_bytes": w.tokens * W.bwd_bytes_per_token(w)},
+           "clocks": clk.summary()}
+    del d, run, dY
+    torch.cuda.empty_cache()
+    return rec
+
+
+def e2e_rate(w, d, run, steps, warmup, stream, world, dev, groups=8):
     """End to end through the C ABI from pinned host buffers: every step copies
     that step's inputs host -> device and the outputs (Y and M_final) back.  The
     heads are split into `groups`; each group's copy-in, update and copy-out run
-    in order on a stream of its own, so one group's copies overlap another's
-    compute and the two copy directions overlap each other.  Returns (seconds
-    for all steps, h2d bytes per step, d2h bytes per step)."""
+    in order on a stream of its own, step after step, so one group's copies
+    overlap the other groups' compute and the two copy directions overlap each
+    other.  The timed region starts before the first group's first copy-in and
+    ends after every group's last copy-out.  Returns (seconds for all steps, h2d
+    bytes per step, d2h bytes per step)."""
     import torch
     import test_memorization_recurrent_gb300 as A
     from test_memorization_recurrent_gb300.harness import cfg_for
     host = {k: v.cpu().pin_memory() for k, v in d.items()}
     Yh = torch.empty(run.Y.shape, dtype=torch.float32).pin_memory()
     Mh = torch.empty(run.M.shape, dtype=torch.float32).pin_memory()
-    dd = {k: torch.empty_like(v) for k, v in d.items()}
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = Yh.numel() * 4 + Mh.numel() * 4
+    per_head = ("K", "Q", "V", "alpha", "eta", "theta", "M0")
+    dd = {k: torch.empty_like(d[k]) for k in per_head}
     G = max(1, min(groups, w.heads))
+    gam = [torch.empty_like(d["gamma"]) for _ in range(G)]  # each group's own copy
+    h2d = sum(host[k].numel() * host[k].element_size() for k in per_head) + \
+        G * host["gamma"].numel() * host["gamma"].element_size()
+    d2h = Yh.numel() * 4 + Mh.numel() * 4
     bounds = [w.heads * g // G for g in range(G + 1)]
     streams = [torch.cuda.Stream(device=dev) for _ in range(G)]
-    per_head = ("K", "Q", "V", "alpha", "eta", "theta", "M0")
     cfgs, wss = [], []
     for g in range(G):
         hg = bounds[g + 1] - bounds[g]
-        probe = cfg_for(w, hg, w.N)
-        nb = A.atlas_mem_workspace_bytes(probe)
+        nb = A.atlas_mem_workspace_bytes(cfg_for(w, hg, w.N))
         ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev) if nb else None
         wss.append(ws)
         cfgs.append(cfg_for(w, hg, w.N, workspace=ws, workspace_bytes=nb,
                             status_dev=run.status))
 
-    def step():
-        dd["gamma"].copy_(host["gamma"], non_blocking=True)  # shared by every group
+    def steps_of(n):
         start = torch.cuda.Event()
         start.record(stream)
-        done = []
-        for g in range(G):
-            lo, hi = bounds[g], bounds[g + 1]
-            sg = streams[g]
+        for sg in streams:
             sg.wait_event(start)
-            with torch.cuda.stream(sg):
-                for k in per_head:
-                    dd[k][lo:hi].copy_(host[k][lo:hi], non_blocking=True)
-                run.M[lo:hi].copy_(dd["M0"][lo:hi])
-            A.atlas_mem_forward(dd["K"][lo:hi], dd["Q"][lo:hi], dd["V"][lo:hi],
-                                dd["alpha"][lo:hi], dd["eta"][lo:hi], dd["theta"][lo:hi],
-                                dd["gamma"], cfgs[g], run.Y[lo:hi], run.M[lo:hi], sg)
-            with torch.cuda.stream(sg):
-                Yh[lo:hi].copy_(run.Y[lo:hi], non_blocking=True)
-                Mh[lo:hi].copy_(run.M[lo:hi], non_blocking=True)
+        for _ in range(n):
+            for g in range(G):
+                lo, hi = bounds[g], bounds[g + 1]
+                sg = streams[g]
+                with torch.cuda.stream(sg):
+                    for k in per_head:
+                        dd[k][lo:hi].copy_(host[k][lo:hi], non_blocking=True)
+                    gam[g].copy_(host["gamma"], non_blocking=True)
+                    run.M[lo:hi].copy_(dd["M0"][lo:hi])
+                A.atlas_mem_forward(dd["K"][lo:hi], dd["Q"][lo:hi], dd["V"][lo:hi],
+                                    dd["alpha"][lo:hi], dd["eta"][lo:hi], dd["theta"][lo:hi],
+                                    gam[g], cfgs[g], run.Y[lo:hi], run.M[lo:hi], sg)
+                with torch.cuda.stream(sg):
+                    Yh[lo:hi].copy_(run.Y[lo:hi], non_blocking=True)
+                    Mh[lo:hi].copy_(run.M[lo:hi], non_blocking=True)
+        for sg in streams:
             e = torch.cuda.Event()
             e.record(sg)
-            done.append(e)
-        for e in done:
             stream.wait_event(e)
 
-    for _ in range(max(1, warmup)):
-        step()
+    steps_of(max(1, warmup))
     torch.cuda.synchronize()
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(steps):
-        step()
+    steps_of(steps)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -487,6 +545,10 @@ def run_atlas(args, w):
                                      dev, not args.no_cpu_baseline)
                       for wid, n in PER_CONFIG if wid != w.wid]
 
+    backward = None
+    if world == 1 and not args.no_per_config and not args.tokens and args.loss == "l2":
+        backward = measure_backward(min(args.steps, 5), 2, dev)
+
     if rank != 0:
         return
     tokens = w.tokens
@@ -519,6 +581,8 @@ def run_atlas(args, w):
     }
     if per_config is not None:
         line["per_config"] = per_config
+    if backward is not None:
+        line["backward"] = backward
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

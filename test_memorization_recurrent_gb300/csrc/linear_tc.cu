@@ -54,7 +54,8 @@ using namespace tc;
 
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
+constexpr int kTablesWarp = 10;
 constexpr int kChunk = 64;
 constexpr int kDim = 128;
 constexpr long long kWaitLimit = 2000000000LL;  // clock cycles (~1 s)
@@ -72,14 +73,16 @@ constexpr bool kWithholdChunk1OfHead0 = false;
 #endif
 
 // shared-memory map (bytes from a 1024-aligned base)
-//   stage: Phi kb0 | Q kb0 | Phi kb1 | Q kb1 (8 KB each, 128B-swizzled, loaded by
-//   TMA) | P''hi | P''lo ([i][n], 128B-swizzled, written by the epilogue) |
-//   V (64 x 128 bf16, row-major) | alpha | eta | theta
-constexpr uint32_t ST_PHI = 32768;
+//   stage, per 64-feature half kb (KB_STRIDE apart): Phi | Q | Phi again (8 KB
+//   each, 128B-swizzled, loaded by TMA; the second copy of Phi makes [Q; Phi] an
+//   M = 128 operand beside [Phi; Q]) | P''hi | P''lo ([i][n], 128B-swizzled,
+//   written by the epilogue) | V (64 x 128 bf16, row-major) | alpha | eta | theta
+constexpr uint32_t KB_STRIDE = 24576;
+constexpr uint32_t ST_PHI = 2 * KB_STRIDE;  // third MN-major atom after Phi kb0, kb1
 constexpr uint32_t ST_PLO = ST_PHI + 8192;
 constexpr uint32_t ST_V = ST_PLO + 8192;
 constexpr uint32_t ST_GATES = ST_V + 16384;
-constexpr uint32_t STAGE_BYTES = ST_GATES + 1024;  // 66560 = 65 x 1024
+constexpr uint32_t STAGE_BYTES = ST_GATES + 1024;  // 82944 = 81 x 1024
 constexpr int kStages = 2;
 constexpr uint32_t OFF_STAGE0 = 0;
 constexpr uint32_t OFF_Y = kStages * STAGE_BYTES;     // y tile [64 n][128 v] fp32, 32 KB
@@ -90,13 +93,13 @@ constexpr uint32_t OFF_BARS = OFF_ELAST + kDim * 4;
 constexpr uint32_t SMEM_USED = OFF_BARS + 256;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;    // alignment slack
 
-constexpr uint32_t STAGE_TX = 4 * 8192 + 16384 + 3 * 256;  // with the gates (N % 4 == 0)
-constexpr uint32_t STAGE_TX_NOGATES = 4 * 8192 + 16384;
+constexpr uint32_t STAGE_TX = 6 * 8192 + 16384 + 3 * 256;  // with the gates (N % 4 == 0)
+constexpr uint32_t STAGE_TX_NOGATES = 6 * 8192 + 16384;
 
 // TMEM columns
 constexpr uint32_t TM_T = 0;       // [T | Qy]            (128)
 constexpr uint32_t TM_QY = 64;
-constexpr uint32_t TM_QP = 128;    // k_i . q_n           (64)
+constexpr uint32_t TM_QP = 128;    // k_i . q_n: n < 32 in lanes 0..63, n >= 32 in lanes 64..127
 constexpr uint32_t TM_DM = 192;    // [dM | Yi]           (192)
 constexpr uint32_t TM_YI = 320;
 constexpr uint32_t TM_MHI = 384;   // A operand M0: hi (64 cols = 128 bf16), lo
@@ -107,7 +110,7 @@ constexpr uint32_t TM_COLS = 512;
 
 enum Bar {
   B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_QP, B_D1, B_DM, B_E, B_P, B_M, B_TAB0, B_TAB1,
-  B_S, B_DRAIN, B_YS, B_YF, B_COUNT
+  B_TFREE0, B_TFREE1, B_S, B_DRAIN, B_YS, B_YF, B_COUNT
 };
 
 // abort_flag values
@@ -157,6 +160,23 @@ __device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
 
 __device__ __forceinline__ void st_shared_u4(uint32_t addr, const uint4& v) {
   st_shared_v4(addr, v.x, v.y, v.z, v.w);
+}
+
+// Load 16 consecutive fp32 columns of this thread's lane (load and wait in one
+// statement, like tmem_ld32).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // 16 consecutive 32-bit TMEM columns of this thread's lane.
@@ -221,8 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int b = 0; b < B_COUNT; ++b) {
       uint32_t cnt = 1;
-      if (b == B_P) cnt = 4;
-      if (b == B_E || b == B_M || b == B_S || b == B_YS) cnt = 8;
+      if (b == B_P || b == B_E || b == B_M || b == B_S || b == B_YS || b == B_TFREE0 ||
+          b == B_TFREE1)
+        cnt = 8;
       mbar_init(&bars[b], cnt);
     }
     *abort_flag = kRun;
@@ -264,10 +285,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t* fb = &bars[B_FULL0 + s];
         mbar_arrive_expect_tx(fb, p.gate_tma ? STAGE_TX : STAGE_TX_NOGATES);
         const int t0 = j * kChunk;
-        tma_load_3d(st + 0, &maps.k, fb, 0, t0, head);
-        tma_load_3d(st + 8192, &maps.q, fb, 0, t0, head);
-        tma_load_3d(st + 16384, &maps.k, fb, 64, t0, head);
-        tma_load_3d(st + 24576, &maps.q, fb, 64, t0, head);
+        for (int kb = 0; kb < 2; ++kb) {
+          unsigned char* sk = st + kb * KB_STRIDE;
+          tma_load_3d(sk, &maps.k, fb, 64 * kb, t0, head);
+          tma_load_3d(sk + 8192, &maps.q, fb, 64 * kb, t0, head);
+          tma_load_3d(sk + 16384, &maps.k, fb, 64 * kb, t0, head);
+        }
         tma_load_3d(st + ST_V, &maps.v, fb, 0, t0, head);
         if (p.gate_tma) {  // gate rows of N floats start 16-byte aligned
           tma_load_2d(st + ST_GATES, &maps.alpha, fb, t0, head);
@@ -284,7 +307,92 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------- tables + MMA issuer
+    // ------------------------------------------------------- MMA issuer
+    // descriptor constants: address bits are added per use
+    const uint64_t dK = sdesc_sw128(0, 16, 1024);       // K-major, 128-byte rows
+    const uint64_t dMN = sdesc_sw128(0, KB_STRIDE, 1024);  // MN-major, atoms KB_STRIDE apart
+    constexpr uint32_t kId128 = idesc_bf16(128, 128, false, false);
+    constexpr uint32_t kId32 = idesc_bf16(128, 32, false, false);
+    constexpr uint32_t kId192mn = idesc_bf16(128, 192, false, true);
+    constexpr uint32_t kId64mn = idesc_bf16(128, 64, false, true);
+    // QP: [Phi; Q] Q[0:32]^T into columns 0..31 (rows 0..63: k_i . q_n, n < 32) and
+    // [Q; Phi] Q[32:64]^T into columns 32..63 (rows 64..127: k_i . q_n, n >= 32), so
+    // that all four TMEM lane quadrants hold a quarter of the 64 x 64 block
+    auto issue_qp = [&](int j) {
+      const uint32_t st = sbase + OFF_STAGE0 + (j % kStages) * STAGE_BYTES;
+      const uint64_t dst = dK | (uint64_t)((st >> 4) & 0x3FFFu);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t off = (k >> 2) * KB_STRIDE + (k & 3) * 32;
+        mma_bf16(tmem + TM_QP, dst + (off >> 4), dst + ((off + 8192) >> 4), kId32, k > 0);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t off = (k >> 2) * KB_STRIDE + (k & 3) * 32 + 8192;
+        mma_bf16(tmem + TM_QP + 32, dst + (off >> 4), dst + ((off + 4096) >> 4), kId32, k > 0);
+      }
+      mma_commit(&bars[B_QP]);
+    };
+    // tables(0) published: its stage has landed
+    bool ok = mbar_wait(&bars[B_TAB0], 0, abort_flag, kWaitLimit);
+    if (ok && lane == 0) issue_qp(0);
+    __syncwarp();
+    for (int j = 0; ok && j < nchunks; ++j) {
+      const int s = j % kStages;
+      const uint32_t st = sbase + OFF_STAGE0 + s * STAGE_BYTES;
+      // M0 in TMEM and the previous chunk's [T | Qy] read out
+      if (!mbar_wait(&bars[B_M], j & 1, abort_flag, kWaitLimit)) { ok = false; break; }
+      tc_fence_after();
+      if (lane == 0) {  // [T | Qy] = M0 [Phi; Q]^T; hi then lo halves of M0
+        const uint64_t dst = dK | (uint64_t)((st >> 4) & 0x3FFFu);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const uint32_t am = tmem + (k < 8 ? TM_MHI : TM_MLO) + 8 * (k & 7);
+          const uint32_t off = ((k & 7) >> 2) * KB_STRIDE + (k & 3) * 32;
+          mma_bf16_ta(tmem + TM_T, am, dst + (off >> 4), kId128, k > 0);
+        }
+        mma_commit(&bars[B_D1]);
+      }
+      __syncwarp();
+      if (!mbar_wait(&bars[B_E], j & 1, abort_flag, kWaitLimit)) { ok = false; break; }
+      if (!mbar_wait(&bars[B_P], j & 1, abort_flag, kWaitLimit)) { ok = false; break; }
+      tc_fence_after();
+      if (lane == 0) {
+        // [dM | Yi] = Ew^T [Phi | P''hi] (Ew hi, then lo), then Yi += Ew_hi^T P''lo
+        const uint64_t dph = dMN | (uint64_t)((st >> 4) & 0x3FFFu);
+        const uint64_t dpl = dMN | (uint64_t)(((st + ST_PLO) >> 4) & 0x3FFFu);
+#pragma unroll
+        for (int k = 0; k < 12; ++k) {
+          const uint32_t ae = tmem + ((k >> 2) == 1 ? TM_EWLO : TM_EWHI) + 8 * (k & 3);
+          const uint64_t b = ((k >> 2) == 2 ? dpl : dph) + (((k & 3) * 2048) >> 4);
+          if (k < 8)
+            mma_bf16_ta(tmem + TM_DM, ae, b, kId192mn, k > 0);
+          else
+            mma_bf16_ta(tmem + TM_YI, ae, b, kId64mn, 1);
+        }
+        mma_commit(&bars[B_DM]);
+        mma_commit(&bars[B_EMPTY0 + s]);
+      }
+      __syncwarp();
+      // the next chunk's QP once its tables (and so its stage) are in place; the
+      // P-epilogue of j is done, so its QP was read
+      if (j + 1 < nchunks) {
+        if (!mbar_wait(&bars[B_TAB0 + ((j + 1) & 1)], ((j + 1) >> 1) & 1, abort_flag,
+                       kWaitLimit)) { ok = false; break; }
+        if (lane == 0) issue_qp(j + 1);
+        __syncwarp();
+      }
+    }
+    if (!ok) timeout();
+    if (lane == 0) {
+      // no MMA may outlive the TMEM: wait for everything this thread issued
+      volatile int zero = 0;
+      mma_commit(&bars[B_DRAIN]);
+      mbar_wait(&bars[B_DRAIN], 0, &zero, kWaitLimit);
+    }
+    __syncwarp();
+  } else if (warp == kTablesWarp) {
+    // -------------------------------------------------------- gate tables
     const float g0 = p.gamma[0];
     // Gate tables of chunk j (warp-wide scans, lane l owns tokens 2l, 2l+1):
     // a_n = prod_{l<=n}(1-alpha_l), wb_i = gamma_0 theta_i s_i, cn_n = -2 / s_n.
@@ -348,83 +456,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars[B_TAB0 + (j & 1)]);
       return true;
     };
-    // descriptor constants: address bits are added per use
-    const uint64_t dK = sdesc_sw128(0, 16, 1024);       // K-major, 128-byte rows
-    const uint64_t dMN = sdesc_sw128(0, 16384, 1024);   // MN-major, atoms 16 KB apart
-    constexpr uint32_t kId128 = idesc_bf16(128, 128, false, false);
-    constexpr uint32_t kId64 = idesc_bf16(128, 64, false, false);
-    constexpr uint32_t kId192mn = idesc_bf16(128, 192, false, true);
-    constexpr uint32_t kId64mn = idesc_bf16(128, 64, false, true);
-    auto issue_qp = [&](int j) {  // QP = [Phi; Q] Q^T (rows 0..63: k_i . q_n)
-      const uint32_t st = sbase + OFF_STAGE0 + (j % kStages) * STAGE_BYTES;
-      const uint64_t dst = dK | (uint64_t)((st >> 4) & 0x3FFFu);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-        mma_bf16(tmem + TM_QP, dst + (off >> 4), dst + ((off + 8192) >> 4), kId64, k > 0);
+    // chunk j's tables go into buffer j & 1 once the epilogue is done with
+    // chunk j - 2's (B_TFREE); the MMA issuer and the epilogue wait on B_TAB
+    for (int j = 0; j < nchunks; ++j) {
+      if (j >= 2 && !mbar_wait(&bars[B_TFREE0 + (j & 1)], ((j - 2) >> 1) & 1, abort_flag,
+                               kWaitLimit)) {
+        timeout();
+        break;
       }
-      mma_commit(&bars[B_QP]);
-    };
-    bool ok = tables(0);
-    if (ok && lane == 0) issue_qp(0);
-    __syncwarp();
-    for (int j = 0; ok && j < nchunks; ++j) {
-      const int s = j % kStages;
-      const uint32_t st = sbase + OFF_STAGE0 + s * STAGE_BYTES;
-      // M0 in TMEM and the previous chunk's [T | Qy] read out
-      if (!mbar_wait(&bars[B_M], j & 1, abort_flag, kWaitLimit)) { ok = false; break; }
-      tc_fence_after();
-      if (lane == 0) {  // [T | Qy] = M0 [Phi; Q]^T; hi then lo halves of M0
-        const uint64_t dst = dK | (uint64_t)((st >> 4) & 0x3FFFu);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const uint32_t am = tmem + (k < 8 ? TM_MHI : TM_MLO) + 8 * (k & 7);
-          const uint32_t off = ((k & 7) >> 2) * 16384 + (k & 3) * 32;
-          mma_bf16_ta(tmem + TM_T, am, dst + (off >> 4), kId128, k > 0);
-        }
-        mma_commit(&bars[B_D1]);
-      }
-      __syncwarp();
-      // the next chunk's gate tables while this chunk's products run (the
-      // buffer's previous readers, chunk j-1's epilogue, are done: B_M was complete)
-      if (j + 1 < nchunks && !tables(j + 1)) { ok = false; break; }
-      if (!mbar_wait(&bars[B_E], j & 1, abort_flag, kWaitLimit)) { ok = false; break; }
-      if (!mbar_wait(&bars[B_P], j & 1, abort_flag, kWaitLimit)) { ok = false; break; }
-      tc_fence_after();
-      if (lane == 0) {
-        // [dM | Yi] = Ew^T [Phi | P''hi] (Ew hi, then lo), then Yi += Ew_hi^T P''lo
-        const uint64_t dph = dMN | (uint64_t)((st >> 4) & 0x3FFFu);
-        const uint64_t dpl = dMN | (uint64_t)(((st + ST_PLO) >> 4) & 0x3FFFu);
-#pragma unroll
-        for (int k = 0; k < 12; ++k) {
-          const uint32_t ae = tmem + ((k >> 2) == 1 ? TM_EWLO : TM_EWHI) + 8 * (k & 3);
-          const uint64_t b = ((k >> 2) == 2 ? dpl : dph) + (((k & 3) * 2048) >> 4);
-          if (k < 8)
-            mma_bf16_ta(tmem + TM_DM, ae, b, kId192mn, k > 0);
-          else
-            mma_bf16_ta(tmem + TM_YI, ae, b, kId64mn, 1);
-        }
-        mma_commit(&bars[B_DM]);
-        mma_commit(&bars[B_EMPTY0 + s]);
-        if (j + 1 < nchunks) issue_qp(j + 1);  // P-epilogue of j done: its QP was read
-      }
-      __syncwarp();
+      if (!tables(j)) break;
     }
-    if (!ok) timeout();
-    if (lane == 0) {
-      // no MMA may outlive the TMEM: wait for everything this thread issued
-      volatile int zero = 0;
-      mma_commit(&bars[B_DRAIN]);
-      mbar_wait(&bars[B_DRAIN], 0, &zero, kWaitLimit);
-    }
-    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;             // TMEM lane quadrant
     const int h = (warp - 2) >> 2;      // half: columns / tokens / queries
     const int v = 32 * q + lane;        // TMEM lane = value index v (or token i)
     const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
-    const bool low = q < 2;
     const bool elected = warp == 2 && lane == 0;
     float m[64];                        // M0[v][64h .. 64h+63]
     {
@@ -461,17 +508,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int x = 0; x < 32; ++x) vt[x] = __bfloat162float(Vs[(32 * h + x) * kDim + v]);
       }
-      if (low) {
-        // ---- P''[n][i] = -2 [i <= n] (k_i . q_n) / s_n, token i = v, queries n in [32h, 32h+32)
-        const int i = v;
+      {
+        // ---- P''[i][n] = -2 [i <= n] (k_i . q_n) / s_n for token i and 16 queries:
+        // lanes 0..63 hold the queries n < 32, lanes 64..127 the queries n >= 32
+        const int i = 32 * (q & 1) + lane;
+        const int n0 = (q >= 2 ? 32 : 0) + 16 * h;
         if (!mbar_wait(&bars[B_QP], par, abort_flag, kWaitLimit)) { ok = false; break; }
         tc_fence_after();
-        float pv[32];
-        tmem_ld32(tl + TM_QP + 32 * h, pv);
+        float pv[16];
+        tmem_ld16(tl + TM_QP + n0, pv);  // column = query: n0 .. n0 + 15
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
-          const float4 c4 = reinterpret_cast<const float4*>(tcn + 32 * h)[x];
-          const int n = 32 * h + 4 * x;
+        for (int x = 0; x < 4; ++x) {
+          const float4 c4 = reinterpret_cast<const float4*>(tcn + n0)[x];
+          const int n = n0 + 4 * x;
           pv[4 * x] = n >= i ? c4.x * pv[4 * x] : 0.f;
           pv[4 * x + 1] = n + 1 >= i ? c4.y * pv[4 * x + 1] : 0.f;
           pv[4 * x + 2] = n + 2 >= i ? c4.z * pv[4 * x + 2] : 0.f;
@@ -479,10 +528,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t ph = smem_u32(stg + ST_PHI), pl = smem_u32(stg + ST_PLO);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint4 hi, lo;
           split8(pv + 8 * c, hi, lo);
-          const uint32_t o = sw128_offset(i, 4 * h + c);
+          const uint32_t o = sw128_offset(i, n0 / 8 + c);
           st_shared_u4(ph + o, hi);
           st_shared_u4(pl + o, lo);
         }
@@ -572,7 +621,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[B_M]);
+        if (lane == 0) {
+          mbar_arrive(&bars[B_M]);
+          mbar_arrive(&bars[B_TFREE0 + (j & 1)]);  // table j is no longer read
+        }
       }
       if (elected) {
         if (!mbar_wait(&bars[B_YS], par, abort_flag, kWaitLimit)) { ok = false; break; }

@@ -229,3 +229,23 @@ def bytes_per_token(w: Workload) -> float:
     """Algorithmic HBM bytes per token: K, Q, V in, three fp32 gates in, Y (fp32) out."""
     e = 2 if w.bf16 else 4
     return (2 * w.d_k + w.d_v) * e + 3 * 4 + w.d_v * 4
+
+
+def bwd_flop_per_token(w: Workload) -> float:
+    """Algorithmic FLOPs per token of the backward pass of a linear memory with a
+    one-token window (d = d_k = d_v, chunk b): per chunk, the forward replayed
+    once to recover the chunk-start states (errors, state update), then the
+    errors, K dM^T and M0 q again, C^T dY, the two terms of dM_0, the two of dK,
+    dQ, dC = dY E^T, the tables' Q K^T and the finishing dP^T Q, dP K."""
+    d, b = w.d_k, w.b
+    X = 2.0 * b * d * d      # a (b x d) by (d x d) product
+    Y = 2.0 * b * b * d      # a (b x b) by (b x d) product
+    return (10 * X + 5 * Y) / b
+
+
+def bwd_bytes_per_token(w: Workload) -> float:
+    """Algorithmic HBM bytes per token of the backward pass: K, Q, V in their
+    dtype, dY fp32 and three fp32 gates in; dK, dQ, dV and three gate gradients
+    (fp32) out."""
+    e = 2 if w.bf16 else 4
+    return (2 * w.d_k + w.d_v) * e + w.d_v * 4 + 3 * 4 + (2 * w.d_k + w.d_v) * 4 + 3 * 4
