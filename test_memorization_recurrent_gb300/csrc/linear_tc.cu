@@ -20,8 +20,8 @@
 // and recomputed from scratch by the CUDA-core kernel.
 //
 // Products per chunk, with the value index v on the TMEM lanes (fp32 accumulators):
-//   [T | Qy]   = M0 [Phi; Q]^T           (128 x 128)  T -> Ew^T = s.theta.(T - V^T)
-//   QP         = [Phi; Q] Q^T, rows 0..63: k_i . q_n    -> P'' = -2 [i<=n] k_i.q_n / s_n
+//   [Qy | T]   = M0 [Q; Phi]^T           (128 x 128)  T -> Ew^T = s.theta.(T - V^T)
+//   QP         = [Phi; Phi] Q^T, rows i, 64+i: k_i . q_n -> P'' = -2 [i<=n] k_i.q_n / s_n
 //   [dM | Yi]  = Ew^T [Phi | P'']        (128 x 192)  one MMA chain for both
 //   y^T        = a_n Qy + Yi,            M_end = a_63 M0 - 2 dM
 // M0 and Ew are A operands held in TMEM (bf16 hi + lo halves, x = hi + lo to
@@ -73,16 +73,18 @@ constexpr bool kWithholdChunk1OfHead0 = false;
 #endif
 
 // shared-memory map (bytes from a 1024-aligned base)
-//   stage, per 64-feature half kb (KB_STRIDE apart): Phi | Q | Phi again (8 KB
-//   each, 128B-swizzled, loaded by TMA; the second copy of Phi makes [Q; Phi] an
-//   M = 128 operand beside [Phi; Q]) | P''hi | P''lo ([i][n], 128B-swizzled,
-//   written by the epilogue) | V (64 x 128 bf16, row-major) | alpha | eta | theta
+//   stage, per 64-feature half kb (KB_STRIDE apart): Q | Phi | Phi again (8 KB
+//   each, 128B-swizzled, loaded by TMA; [Q; Phi] is the state product's B
+//   operand, [Phi; Phi] the M = 128 A operand of QP, which so puts the k.q block
+//   in both lane halves) | P''hi | P''lo ([i][n], 128B-swizzled, written by the
+//   epilogue) | V (64 x 128 bf16, row-major) | alpha | eta | theta
 constexpr uint32_t KB_STRIDE = 24576;
-constexpr uint32_t ST_PHI = 2 * KB_STRIDE;  // third MN-major atom after Phi kb0, kb1
+constexpr uint32_t ST_K = 8192;                      // Phi kb0 (kb1 at + KB_STRIDE)
+constexpr uint32_t ST_PHI = ST_K + 2 * KB_STRIDE;    // third MN-major atom after Phi kb0, kb1
 constexpr uint32_t ST_PLO = ST_PHI + 8192;
 constexpr uint32_t ST_V = ST_PLO + 8192;
 constexpr uint32_t ST_GATES = ST_V + 16384;
-constexpr uint32_t STAGE_BYTES = ST_GATES + 1024;  // 82944 = 81 x 1024
+constexpr uint32_t STAGE_BYTES = ST_GATES + 1024;  // 91136 = 89 x 1024
 constexpr int kStages = 2;
 constexpr uint32_t OFF_STAGE0 = 0;
 constexpr uint32_t OFF_Y = kStages * STAGE_BYTES;     // y tile [64 n][128 v] fp32, 32 KB
@@ -97,9 +99,9 @@ constexpr uint32_t STAGE_TX = 6 * 8192 + 16384 + 3 * 256;  // with the gates (N 
 constexpr uint32_t STAGE_TX_NOGATES = 6 * 8192 + 16384;
 
 // TMEM columns
-constexpr uint32_t TM_T = 0;       // [T | Qy]            (128)
-constexpr uint32_t TM_QY = 64;
-constexpr uint32_t TM_QP = 128;    // k_i . q_n: n < 32 in lanes 0..63, n >= 32 in lanes 64..127
+constexpr uint32_t TM_QY = 0;      // [Qy | T]            (128)
+constexpr uint32_t TM_T = 64;
+constexpr uint32_t TM_QP = 128;    // k_i . q_n (64 queries), token i in lanes i and 64 + i
 constexpr uint32_t TM_DM = 192;    // [dM | Yi]           (192)
 constexpr uint32_t TM_YI = 320;
 constexpr uint32_t TM_MHI = 384;   // A operand M0: hi (64 cols = 128 bf16), lo
@@ -287,8 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t0 = j * kChunk;
         for (int kb = 0; kb < 2; ++kb) {
           unsigned char* sk = st + kb * KB_STRIDE;
-          tma_load_3d(sk, &maps.k, fb, 64 * kb, t0, head);
-          tma_load_3d(sk + 8192, &maps.q, fb, 64 * kb, t0, head);
+          tma_load_3d(sk, &maps.q, fb, 64 * kb, t0, head);
+          tma_load_3d(sk + 8192, &maps.k, fb, 64 * kb, t0, head);
           tma_load_3d(sk + 16384, &maps.k, fb, 64 * kb, t0, head);
         }
         tma_load_3d(st + ST_V, &maps.v, fb, 0, t0, head);
@@ -312,24 +314,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dK = sdesc_sw128(0, 16, 1024);       // K-major, 128-byte rows
     const uint64_t dMN = sdesc_sw128(0, KB_STRIDE, 1024);  // MN-major, atoms KB_STRIDE apart
     constexpr uint32_t kId128 = idesc_bf16(128, 128, false, false);
-    constexpr uint32_t kId32 = idesc_bf16(128, 32, false, false);
+    constexpr uint32_t kId64 = idesc_bf16(128, 64, false, false);
     constexpr uint32_t kId192mn = idesc_bf16(128, 192, false, true);
     constexpr uint32_t kId64mn = idesc_bf16(128, 64, false, true);
-    // QP: [Phi; Q] Q[0:32]^T into columns 0..31 (rows 0..63: k_i . q_n, n < 32) and
-    // [Q; Phi] Q[32:64]^T into columns 32..63 (rows 64..127: k_i . q_n, n >= 32), so
-    // that all four TMEM lane quadrants hold a quarter of the 64 x 64 block
+    // QP = [Phi; Phi] Q^T: rows i and 64 + i both hold k_i . q_n for the 64
+    // queries, so every TMEM lane quadrant can read the block for its tokens
     auto issue_qp = [&](int j) {
       const uint32_t st = sbase + OFF_STAGE0 + (j % kStages) * STAGE_BYTES;
       const uint64_t dst = dK | (uint64_t)((st >> 4) & 0x3FFFu);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const uint32_t off = (k >> 2) * KB_STRIDE + (k & 3) * 32;
-        mma_bf16(tmem + TM_QP, dst + (off >> 4), dst + ((off + 8192) >> 4), kId32, k > 0);
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t off = (k >> 2) * KB_STRIDE + (k & 3) * 32 + 8192;
-        mma_bf16(tmem + TM_QP + 32, dst + (off >> 4), dst + ((off + 4096) >> 4), kId32, k > 0);
+        mma_bf16(tmem + TM_QP, dst + ((off + ST_K) >> 4), dst + (off >> 4), kId64, k > 0);
       }
       mma_commit(&bars[B_QP]);
     };
@@ -340,16 +336,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; ok && j < nchunks; ++j) {
       const int s = j % kStages;
       const uint32_t st = sbase + OFF_STAGE0 + s * STAGE_BYTES;
-      // M0 in TMEM and the previous chunk's [T | Qy] read out
+      // M0 in TMEM and the previous chunk's [Qy | T] read out
       if (!mbar_wait(&bars[B_M], j & 1, abort_flag, kWaitLimit)) { ok = false; break; }
       tc_fence_after();
-      if (lane == 0) {  // [T | Qy] = M0 [Phi; Q]^T; hi then lo halves of M0
+      if (lane == 0) {  // [Qy | T] = M0 [Q; Phi]^T; hi then lo halves of M0
         const uint64_t dst = dK | (uint64_t)((st >> 4) & 0x3FFFu);
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           const uint32_t am = tmem + (k < 8 ? TM_MHI : TM_MLO) + 8 * (k & 7);
           const uint32_t off = ((k & 7) >> 2) * KB_STRIDE + (k & 3) * 32;
-          mma_bf16_ta(tmem + TM_T, am, dst + (off >> 4), kId128, k > 0);
+          mma_bf16_ta(tmem + TM_QY, am, dst + (off >> 4), kId128, k > 0);  // [Qy | T]
         }
         mma_commit(&bars[B_D1]);
       }
@@ -359,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       if (lane == 0) {
         // [dM | Yi] = Ew^T [Phi | P''hi] (Ew hi, then lo), then Yi += Ew_hi^T P''lo
-        const uint64_t dph = dMN | (uint64_t)((st >> 4) & 0x3FFFu);
+        const uint64_t dph = dMN | (uint64_t)(((st + ST_K) >> 4) & 0x3FFFu);
         const uint64_t dpl = dMN | (uint64_t)(((st + ST_PLO) >> 4) & 0x3FFFu);
 #pragma unroll
         for (int k = 0; k < 12; ++k) {
@@ -510,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       {
         // ---- P''[i][n] = -2 [i <= n] (k_i . q_n) / s_n for token i and 16 queries:
-        // lanes 0..63 hold the queries n < 32, lanes 64..127 the queries n >= 32
+        // the low lane quadrants take the queries n < 32, the high ones n >= 32
         const int i = 32 * (q & 1) + lane;
         const int n0 = (q >= 2 ? 32 : 0) + 16 * h;
         if (!mbar_wait(&bars[B_QP], par, abort_flag, kWaitLimit)) { ok = false; break; }
@@ -578,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_E]);
       }
-      // ---- [dM | Yi] done: readout first (frees [T | Qy]), then the state update
+      // ---- [dM | Yi] done: readout first (frees [Qy | T]), then the state update
       if (!mbar_wait(&bars[B_DM], par, abort_flag, kWaitLimit)) { ok = false; break; }
       tc_fence_after();
       {
