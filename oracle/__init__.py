@@ -25,7 +25,8 @@ _SRC = os.path.join(_HERE, "atlas_oracle.c")
 _LIB = os.path.join(_HERE, "_build", "libatlas_oracle.so")
 
 MEM_LINEAR, MEM_MLP, MEM_MLP_LN, MEM_MLP_GATED = 0, 1, 2, 3
-PHI_IDENTITY, PHI_POLY2 = 0, 1
+PHI_IDENTITY, PHI_POLY2, PHI_POLY = 0, 1, 2
+PHI_MAX_DEGREE = 4
 LOSS_L2, LOSS_DOT, LOSS_LP, LOSS_HUBER = 0, 1, 2, 3
 
 
@@ -38,6 +39,7 @@ class OrcCfg(ctypes.Structure):
         ("ns_b", ctypes.c_double), ("ns_c", ctypes.c_double),
         ("ns_eps", ctypes.c_double), ("n_history", ctypes.c_int),
         ("loss_param", ctypes.c_double),
+        ("phi_degree", ctypes.c_int), ("phi_coef", ctypes.c_double * (PHI_MAX_DEGREE + 1)),
     ]
 
 
@@ -100,11 +102,16 @@ def _f64(a) -> np.ndarray:
 
 def make_cfg(N, d_k, d_v, d_h=0, mem=MEM_LINEAR, phi=PHI_IDENTITY, loss=LOSS_L2, c=1, b=1,
              ns_steps=0, ns_a=0.0, ns_b=0.0, ns_c=0.0, ns_eps=0.0, n_history=0,
-             loss_param=0.0) -> OrcCfg:
-    """loss_param: p of the l_p bias, delta of the Huber bias (unused otherwise)."""
+             loss_param=0.0, phi_coef=None) -> OrcCfg:
+    """loss_param: p of the l_p bias, delta of the Huber bias (unused otherwise).
+    phi_coef: a_0 .. a_p of the gated polynomial map (phi = PHI_POLY); p = len - 1."""
+    coef = list(phi_coef or [])
+    arr = (ctypes.c_double * (PHI_MAX_DEGREE + 1))(*([float(a) for a in coef] +
+                                                     [0.0] * (PHI_MAX_DEGREE + 1 - len(coef))))
     return OrcCfg(int(N), int(d_k), int(d_v), int(d_h), int(mem), int(phi), int(loss),
                   int(c), int(b), int(ns_steps), float(ns_a), float(ns_b), float(ns_c),
-                  float(ns_eps), int(n_history), float(loss_param))
+                  float(ns_eps), int(n_history), float(loss_param),
+                  max(0, len(coef) - 1), arr)
 
 
 def feature_dim(cfg: OrcCfg) -> int:

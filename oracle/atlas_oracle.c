@@ -43,6 +43,12 @@
  *   - readout is after the write: y_t = M_t(Phi(q_t));
  *   - Phi_2(x) = [x_1..x_d, x_i x_j for i <= j, i-major], no constant term and
  *     no multinomial weights (d = 32 gives 560 features);
+ *   - the general map with input gating ([ATLAS] §3.1, "Input gating": a_i
+ *     switches the features of degree i on or off) is
+ *     Phi(x) = [a_0; a_1 x; a_2 (x_i x_j)_{i<=j}; ...; a_p (degree-p monomials)],
+ *     every degree's monomials once, without multinomial weights, in
+ *     lexicographic order of their sorted index tuples; a degree whose a_d is 0
+ *     is left out of the feature vector (so a = (0, 1, 1) is Phi_2 above);
  *   - MLP memory M(x) = x + W1 GELU(W2 x) without LayerNorm, exact (erf) GELU;
  *   - Newton-Schulz (when enabled) acts on the momentum of each weight matrix
  *     separately, per token: M_t = (1 - alpha_t) M_{t-1} + NS(S_t), with
@@ -70,6 +76,8 @@
 #define ORC_LN_EPS 1e-5
 #define ORC_PHI_IDENTITY 0
 #define ORC_PHI_POLY2 1
+#define ORC_PHI_POLY 2       /* degree phi_degree, input-gating coefficients phi_coef */
+#define ORC_PHI_MAX_DEGREE 4
 #define ORC_LOSS_L2 0
 #define ORC_LOSS_DOT 1
 #define ORC_LOSS_LP 2
@@ -92,15 +100,31 @@ typedef struct {
   int n_history; /* tokens before the first processed one: K, V rows that only
                     enter the windows of processed tokens (they update nothing) */
   double loss_param; /* p of the l_p bias (>= 1), delta of the Huber bias (> 0) */
+  int phi_degree;    /* ORC_PHI_POLY: highest degree p (1..ORC_PHI_MAX_DEGREE) */
+  double phi_coef[ORC_PHI_MAX_DEGREE + 1]; /* ORC_PHI_POLY: a_0 .. a_p */
 } orc_cfg;
 
 /* ------------------------------------------------------------------ sizes */
 
+/* Number of monomials of degree exactly e in d variables: C(d + e - 1, e). */
+static long orc_monomials(int d, int e) {
+  long c = 1;
+  for (int i = 1; i <= e; ++i) c = c * (d + i - 1) / i;
+  return c;
+}
+
 /* Width of Phi(x).  [ATLAS] §3.1: Phi_p(x) = [x^beta]_{|beta| <= p}; with the
- * constant dropped and p = 2 that is d linear terms and d(d+1)/2 products. */
+ * constant dropped and p = 2 that is d linear terms and d(d+1)/2 products; the
+ * gated map keeps the degrees whose coefficient is non-zero. */
 int orc_feature_dim(const orc_cfg* g) {
   if (g->mem != ORC_MEM_LINEAR) return g->d_k;
   if (g->phi == ORC_PHI_POLY2) return g->d_k + g->d_k * (g->d_k + 1) / 2;
+  if (g->phi == ORC_PHI_POLY) {
+    long D = 0;
+    for (int e = 0; e <= g->phi_degree; ++e)
+      if (g->phi_coef[e] != 0.0) D += orc_monomials(g->d_k, e);
+    return (int)D;
+  }
   return g->d_k;
 }
 
@@ -113,9 +137,54 @@ long orc_state_size(const orc_cfg* g) {
 
 /* --------------------------------------------------------- feature map Phi */
 
-/* [ATLAS] §3.1 polynomial map, degree 2, read as described above. */
+/* Visit the sorted index tuples i_1 <= ... <= i_e over [0, d) in lexicographic
+ * order: the first tuple is all zeros, the next raises the last entry that can
+ * still grow and resets the entries after it to that value.  Returns 0 after
+ * the last tuple. */
+static int orc_next_tuple(int* idx, int e, int d) {
+  int r = e - 1;
+  while (r >= 0 && idx[r] == d - 1) --r;
+  if (r < 0) return 0;
+  ++idx[r];
+  for (int s = r + 1; s < e; ++s) idx[s] = idx[r];
+  return 1;
+}
+
+/* Apply fn(ctx, feature, degree, idx) to every feature of the gated map in order. */
+static void orc_poly_features(const orc_cfg* g, void (*fn)(void*, int, int, const int*),
+                              void* ctx) {
+  int j = 0, idx[ORC_PHI_MAX_DEGREE];
+  for (int e = 0; e <= g->phi_degree; ++e) {
+    if (g->phi_coef[e] == 0.0) continue;
+    for (int r = 0; r < e; ++r) idx[r] = 0;
+    do {
+      fn(ctx, j++, e, idx);
+    } while (e > 0 && orc_next_tuple(idx, e, g->d_k));
+  }
+}
+
+typedef struct {
+  const orc_cfg* g;
+  const double* x;
+  double* out;
+} orc_phi_ctx;
+
+static void orc_phi_one(void* c, int j, int e, const int* idx) {
+  orc_phi_ctx* p = (orc_phi_ctx*)c;
+  double v = p->g->phi_coef[e];
+  for (int r = 0; r < e; ++r) v *= p->x[idx[r]];
+  p->out[j] = v;
+}
+
+/* [ATLAS] §3.1 polynomial map (degree 2, or general with input gating), read as
+ * described above. */
 void orc_phi(const orc_cfg* g, const double* x, double* out) {
   int d = g->d_k;
+  if (g->mem == ORC_MEM_LINEAR && g->phi == ORC_PHI_POLY) {
+    orc_phi_ctx c = {g, x, out};
+    orc_poly_features(g, orc_phi_one, &c);
+    return;
+  }
   for (int i = 0; i < d; ++i) out[i] = x[i];
   if (g->mem != ORC_MEM_LINEAR || g->phi == ORC_PHI_IDENTITY) return;
   int p = d;
@@ -486,6 +555,10 @@ static int orc_check(const orc_cfg* g) {
   if (g->loss < ORC_LOSS_L2 || g->loss > ORC_LOSS_HUBER) return -1;
   if (g->loss == ORC_LOSS_LP && !(g->loss_param >= 1.0 && g->loss_param < 1e6)) return -1;
   if (g->loss == ORC_LOSS_HUBER && !(g->loss_param > 0.0)) return -1;
+  if (g->phi == ORC_PHI_POLY) {
+    if (g->phi_degree < 1 || g->phi_degree > ORC_PHI_MAX_DEGREE) return -1;
+    if (orc_feature_dim(g) < 1) return -1;
+  }
   return 0;
 }
 
@@ -559,9 +632,32 @@ static double orc_bias_d2(const orc_cfg* g, double e) {
   return 2.0;
 }
 
+typedef struct {
+  const orc_cfg* g;
+  const double* x;
+  const double* dphi;
+  double* dx;
+} orc_phib_ctx;
+
+/* d(a_e x_{i_1} ... x_{i_e}) / dx_{i_r}: the product of the other factors. */
+static void orc_phib_one(void* c, int j, int e, const int* idx) {
+  orc_phib_ctx* p = (orc_phib_ctx*)c;
+  for (int r = 0; r < e; ++r) {
+    double v = p->g->phi_coef[e] * p->dphi[j];
+    for (int s = 0; s < e; ++s)
+      if (s != r) v *= p->x[idx[s]];
+    p->dx[idx[r]] += v;
+  }
+}
+
 /* dx += (dPhi/dx)^T dphi for the map of orc_phi. */
 static void orc_phi_backward(const orc_cfg* g, const double* x, const double* dphi, double* dx) {
   int d = g->d_k;
+  if (g->phi == ORC_PHI_POLY) {
+    orc_phib_ctx c = {g, x, dphi, dx};
+    orc_poly_features(g, orc_phib_one, &c);
+    return;
+  }
   for (int i = 0; i < d; ++i) dx[i] += dphi[i];
   if (g->phi == ORC_PHI_IDENTITY) return;
   int p = d;
