@@ -188,7 +188,8 @@ def oracle_rate(w, heads, n_tokens, seed=0):
     inp = W.generate(w, seed=seed, heads=heads, n_tokens=n_tokens)
     a, b_, c_ = w.ns_coef
     cfg = oracle.make_cfg(n_tokens, w.d_k, w.d_v, w.d_h, w.mem, w.phi, w.loss, w.c, w.b,
-                          w.ns_steps, a, b_, c_, w.ns_eps, loss_param=w.loss_param)
+                          w.ns_steps, a, b_, c_, w.ns_eps, loss_param=w.loss_param,
+                          phi_coef=w.phi_coef)
     t = time.perf_counter()
     oracle.forward(cfg, inp["K"], inp["Q"], inp["V"], inp["alpha"], inp["eta"], inp["theta"],
                    inp["gamma"], inp["M0"])
@@ -203,7 +204,7 @@ def oracle_sample(w):
     if w.wid in (1, 2):
         return list(range(w.heads)), w.N
     if w.wid == 3:
-        return list(range(min(w.heads, cores))), 512
+        return list(range(min(w.heads, cores))), 512 if w.phi != W.PHI_POLY else 128
     if w.wid == 4:
         return list(range(min(w.heads, cores))), 2048
     return list(range(min(w.heads, cores))), 16
@@ -259,6 +260,14 @@ KERNEL_OF_PATH = {
 # on (None = the whole workload).  The Newton-Schulz workload runs on a prefix of
 # all 16 heads: its full million-token length is ~70 s per call at today's rate.
 PER_CONFIG = ((1, None), (3, None), (4, None), (5, 1024))
+
+
+def variant_workloads():
+    """Variants measured beside the five workloads: the gated degree-3 polynomial
+    map (input gating a = (0, 1, 1, 1)) on the wide-feature workload's shape with
+    d_k = 16 (D = 968 features), window 64, momentum and decay, bounded step."""
+    return [W.workload(3, bounded=True, d_k=16, phi=W.PHI_POLY, phi_coef=(0.0, 1.0, 1.0, 1.0),
+                       N=2048, theta_scale=0.002, name="poly3-gated-omega-c64-bf16")]
 
 
 def time_device(w, run, d, steps, warmup, stream, clk=None, world=1):
@@ -323,7 +332,7 @@ def roofline(w, path, kernel_s):
     bytes_launch = tokens * W.bytes_per_token(w) + 2 * 4 * w.heads * w.state_size
     flops_launch = tokens * W.flop_per_token(w)
     ridge = tf * 1e12 / (hbm * 1e9)
-    if path == "linear_seq":  # fp32 FMAs on CUDA cores, one token after another
+    if path in ("linear_seq", "linear_simt"):  # fp32 FMAs on CUDA cores
         peak = fp32_alu_peak_tflops()
         achieved = flops_launch / kernel_s / 1e12
         roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -348,12 +357,13 @@ def roofline(w, path, kernel_s):
 
 
 def measure_config(wid, n_tokens, steps, warmup, dev, with_cpu):
-    """One workload measured on its own (rank 0, one GPU): rate, roofline, clocks
-    during its timed region, and the oracle on a bounded sample of it."""
+    """One workload (an id, or a Workload) measured on its own (rank 0, one GPU):
+    rate, roofline, clocks during its timed region, and the oracle on a bounded
+    sample of it."""
     import torch
     import test_memorization_recurrent_gb300 as A
     from test_memorization_recurrent_gb300.harness import Runner, to_device
-    w = W.workload(wid, bounded=True)
+    w = W.workload(wid, bounded=True) if isinstance(wid, int) else wid
     if n_tokens:
         w = w.with_(N=min(n_tokens, w.N))
     inp = W.generate(w)
@@ -545,9 +555,11 @@ def run_atlas(args, w):
                                      dev, not args.no_cpu_baseline)
                       for wid, n in PER_CONFIG if wid != w.wid]
 
-    backward = None
+    backward = variants = None
     if world == 1 and not args.no_per_config and not args.tokens and args.loss == "l2":
         backward = measure_backward(min(args.steps, 5), 2, dev)
+        variants = [measure_config(v, None, min(args.steps, 5), 3, dev, not args.no_cpu_baseline)
+                    for v in variant_workloads()]
 
     if rank != 0:
         return
@@ -583,6 +595,8 @@ def run_atlas(args, w):
         line["per_config"] = per_config
     if backward is not None:
         line["backward"] = backward
+    if variants is not None:
+        line["variants"] = variants
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

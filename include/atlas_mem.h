@@ -56,6 +56,16 @@ extern "C" {
 /* feature map (linear memory only; the MLP takes x itself) */
 #define ATLAS_PHI_IDENTITY 0 /* D = d_k */
 #define ATLAS_PHI_POLY2 1    /* D = d_k + d_k(d_k+1)/2: [x_i] then [x_i x_j, i<=j, i-major] */
+/* Gated polynomial map of degree p = cfg->phi_degree ("논문 리뷰 Google ATLAS",
+ * §3.1 Polynomial Feature Mapping and Input gating):
+ *   Phi(x) = [a_0; a_1 x; a_2 (x_i x_j)_{i<=j}; ...; a_p (degree-p monomials)]
+ * with a_e = cfg->phi_coef[e]; each degree's monomials appear once (no
+ * multinomial weights), in lexicographic order of their sorted index tuples; a
+ * degree whose a_e is 0 is left out, so D = sum over kept e of C(d_k + e - 1, e).
+ * a = (0, 1, 1) is ATLAS_PHI_POLY2.  Runs on the CUDA-core linear kernel;
+ * d_k <= 255, D <= 16384. */
+#define ATLAS_PHI_POLY 2
+#define ATLAS_PHI_MAX_DEGREE 4
 /* attentional bias */
 #define ATLAS_LOSS_L2 0  /* ||M(Phi(k)) - v||^2 (gradient carries the factor 2) */
 #define ATLAS_LOSS_DOT 1 /* -2 <M(Phi(k)), v> (linear memory only: linear attention) */
@@ -101,6 +111,8 @@ typedef struct atlas_mem_cfg {
   size_t workspace_bytes;
   int* status_dev;    /* optional device int; set to ATLAS_ERR_TIMEOUT by a kernel
                          whose bounded wait ran out (never cleared by the library) */
+  int phi_degree;     /* ATLAS_PHI_POLY: p, 1..ATLAS_PHI_MAX_DEGREE (ignored otherwise) */
+  float phi_coef[ATLAS_PHI_MAX_DEGREE + 1]; /* ATLAS_PHI_POLY: a_0 .. a_p */
 } atlas_mem_cfg;
 
 /* Number of fp32 entries in one head's memory state (and momentum):

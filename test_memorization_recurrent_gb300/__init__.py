@@ -16,7 +16,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "libatlasmem.so")
 
 MEM_LINEAR, MEM_MLP, MEM_MLP_LN, MEM_MLP_GATED = 0, 1, 2, 3
-PHI_IDENTITY, PHI_POLY2 = 0, 1
+PHI_IDENTITY, PHI_POLY2, PHI_POLY = 0, 1, 2
+PHI_MAX_DEGREE = 4
 LOSS_L2, LOSS_DOT, LOSS_LP, LOSS_HUBER = 0, 1, 2, 3
 F32, BF16 = 0, 1
 
@@ -40,6 +41,7 @@ class AtlasMemCfg(ctypes.Structure):
         ("S_state", ctypes.c_void_p), ("n_history", ctypes.c_int),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("status_dev", ctypes.c_void_p),
+        ("phi_degree", ctypes.c_int), ("phi_coef", ctypes.c_float * (PHI_MAX_DEGREE + 1)),
     ]
 
 
@@ -95,13 +97,19 @@ def load_library(path: str = LIB_PATH):
 def make_cfg(B, H, N, d_k, d_v, d_h=0, mem=MEM_LINEAR, phi=PHI_IDENTITY, loss=LOSS_L2, c=1,
              b=1, ns_steps=0, ns_a=0.0, ns_b=0.0, ns_c=0.0, ns_eps=0.0, in_dtype=BF16,
              S_state=None, workspace=None, workspace_bytes=0, status_dev=None,
-             n_history=0, loss_param=0.0) -> AtlasMemCfg:
-    """loss_param: p of LOSS_LP, delta of LOSS_HUBER (unused otherwise)."""
+             n_history=0, loss_param=0.0, phi_coef=None) -> AtlasMemCfg:
+    """loss_param: p of LOSS_LP, delta of LOSS_HUBER (unused otherwise).
+    phi_coef: a_0 .. a_p of the gated polynomial map (phi = PHI_POLY); p = len - 1."""
+    coef = [float(a) for a in (phi_coef or [])]
+    if len(coef) > PHI_MAX_DEGREE + 1:
+        raise ValueError(f"at most {PHI_MAX_DEGREE + 1} coefficients (degree {PHI_MAX_DEGREE})")
+    arr = (ctypes.c_float * (PHI_MAX_DEGREE + 1))(*(coef + [0.0] * (PHI_MAX_DEGREE + 1 - len(coef))))
     return AtlasMemCfg(int(B), int(H), int(N), int(d_k), int(d_v), int(d_h), int(mem), int(phi),
                        int(loss), float(loss_param), int(c), int(b), int(ns_steps), float(ns_a),
                        float(ns_b),
                        float(ns_c), float(ns_eps), int(in_dtype), _ptr(S_state), int(n_history),
-                       _ptr(workspace), int(workspace_bytes), _ptr(status_dev))
+                       _ptr(workspace), int(workspace_bytes), _ptr(status_dev),
+                       max(0, len(coef) - 1), arr)
 
 
 def _ptr(t):

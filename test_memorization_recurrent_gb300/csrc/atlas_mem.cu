@@ -15,11 +15,26 @@ enum Path {
   PATH_MLP_SIMT, PATH_MLP_TC
 };
 
-int feature_dim(const atlas_mem_cfg* c) {
+// Monomials of degree exactly e in d variables: C(d + e - 1, e).
+long monomials(long d, int e) {
+  long c = 1;
+  for (int i = 1; i <= e; ++i) c = c * (d + i - 1) / i;
+  return c;
+}
+
+long feature_dim_long(const atlas_mem_cfg* c) {
   if (c->mem == ATLAS_MEM_LINEAR && c->phi == ATLAS_PHI_POLY2)
-    return c->d_k + c->d_k * (c->d_k + 1) / 2;
+    return (long)c->d_k + (long)c->d_k * (c->d_k + 1) / 2;
+  if (c->mem == ATLAS_MEM_LINEAR && c->phi == ATLAS_PHI_POLY) {
+    long D = 0;
+    for (int e = 0; e <= c->phi_degree; ++e)
+      if (c->phi_coef[e] != 0.f) D += monomials(c->d_k, e);
+    return D;
+  }
   return c->d_k;
 }
+
+int feature_dim(const atlas_mem_cfg* c) { return (int)feature_dim_long(c); }
 
 // Structural validation (no pointers).  Returns ATLAS_OK, INVALID or UNSUPPORTED.
 int check_cfg(const atlas_mem_cfg* c) {
@@ -27,7 +42,18 @@ int check_cfg(const atlas_mem_cfg* c) {
   if (c->B < 0 || c->H < 0 || c->N < 0) return ATLAS_ERR_INVALID;
   if (c->d_k <= 0 || c->d_v <= 0 || c->c < 1 || c->b < 1) return ATLAS_ERR_INVALID;
   if (c->mem < ATLAS_MEM_LINEAR || c->mem > ATLAS_MEM_MLP_GATED) return ATLAS_ERR_INVALID;
-  if (c->phi != ATLAS_PHI_IDENTITY && c->phi != ATLAS_PHI_POLY2) return ATLAS_ERR_INVALID;
+  if (c->phi != ATLAS_PHI_IDENTITY && c->phi != ATLAS_PHI_POLY2 && c->phi != ATLAS_PHI_POLY)
+    return ATLAS_ERR_INVALID;
+  if (c->phi == ATLAS_PHI_POLY) {
+    if (c->phi_degree < 1 || c->phi_degree > ATLAS_PHI_MAX_DEGREE) return ATLAS_ERR_INVALID;
+    for (int e = 0; e <= c->phi_degree; ++e)
+      if (!(c->phi_coef[e] == c->phi_coef[e]) || c->phi_coef[e] > 3e38f || c->phi_coef[e] < -3e38f)
+        return ATLAS_ERR_INVALID;  // NaN or infinite
+    if (c->d_k > 255) return ATLAS_ERR_UNSUPPORTED;
+    const long D = feature_dim_long(c);
+    if (D < 1) return ATLAS_ERR_INVALID;
+    if (D > 16384) return ATLAS_ERR_UNSUPPORTED;
+  }
   if (c->loss < ATLAS_LOSS_L2 || c->loss > ATLAS_LOSS_HUBER) return ATLAS_ERR_INVALID;
   if (c->loss == ATLAS_LOSS_LP && !(c->loss_param >= 1.f && c->loss_param < 1e6f))
     return ATLAS_ERR_INVALID;
@@ -63,6 +89,9 @@ LinArgs lin_args(const void* K, const void* Q, const void* V, const float* alpha
   a.lp = c->loss_param;
   a.bf16 = c->in_dtype == ATLAS_BF16;
   a.nh = c->n_history;
+  a.pgen = c->phi == ATLAS_PHI_POLY;
+  a.pdeg = a.pgen ? c->phi_degree : 0;
+  for (int e = 0; e < 5; ++e) a.pcoef[e] = (a.pgen && e <= c->phi_degree) ? c->phi_coef[e] : 0.f;
   return a;
 }
 
@@ -96,6 +125,12 @@ Path choose_path(const atlas_mem_cfg* c) {
   }
   LinArgs a = lin_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, c,
                        nullptr, nullptr);
+  if (a.pgen) {  // the gated polynomial map: CUDA-core kernel only
+    int RV;
+    size_t smem;
+    return linear_simt_plan(a, c->B * c->H, &RV, &smem) == ATLAS_OK ? PATH_LINEAR_SIMT
+                                                                      : PATH_INVALID;
+  }
   if (a.nh == 0 && linear_tc_supported(a)) return PATH_LINEAR_TC;
   if (linear_seq_supported(a)) return PATH_LINEAR_SEQ;
   if (linear_chunk_supported(a)) return PATH_LINEAR_CHUNK;

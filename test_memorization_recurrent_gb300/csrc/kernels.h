@@ -22,6 +22,9 @@ struct LinArgs {
   int lk;    // attentional bias: 0 l2, 1 dot, 2 l_p, 3 Huber (ATLAS_LOSS_*)
   float lp;  // its parameter (p, delta)
   int nh;  // history rows ahead of token 0 in K and V (head stride (nh + N) rows)
+  int pgen;        // gated polynomial map of degree pdeg (poly is 0 then)
+  int pdeg;
+  float pcoef[5];  // a_0 .. a_pdeg
 };
 
 int linear_simt_launch(const LinArgs& a, int heads, cudaStream_t st);

@@ -562,6 +562,7 @@ constexpr size_t kFinishSmem = sizeof(float) * ((size_t)2 * kB * kD + 3 * kB * k
 
 bool linear_bwd_supported(const LinArgs& a) {
   return a.d_k == kD && a.d_v == kD && a.D == kD && a.b == kB && a.c == 1 && !a.poly && !a.dot &&
+         !a.pgen &&
          a.nh == 0 && a.S == nullptr;
 }
 

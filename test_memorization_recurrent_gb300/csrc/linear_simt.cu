@@ -18,23 +18,27 @@
 //   S[r,:]  = eps_b S0 - 2 sum_i U[b,i] E[i,r] Phi(k_i)
 // with the scalar tables of chunk_tables_warp.  Phi(q).Phi(k) for the degree-2
 // map is evaluated as s + (s^2 + sum_j q_j^2 k_j^2)/2 with s = q.k, which is the
-// same sum regrouped.
+// same sum regrouped.  The gated polynomial map of any degree ("논문 리뷰 Google
+// ATLAS" §3.1, Input gating) keeps one 32-bit entry per feature (its sorted
+// monomial indices, 0xFF past its degree) in shared memory, and its lifted inner
+// product is sum_e a_e^2 h_e(z), z_j = q_j k_j, with the complete homogeneous
+// symmetric polynomials h_e from the power sums of z (Newton's identities).
 #include "common.cuh"
 #include "kernels.h"
 
 namespace atlas {
 
 struct LinSimtSmem {
-  int RV, D, Lmax, b, d_k;
+  int RV, D, Lmax, b, d_k, pgen;
   // float offsets
   long Ms, Ss, Kw, Qc, Vw, E, P, Urun, Wrun, sa, se, sb, total_floats;
   long pairs_bytes;
   size_t bytes() const { return total_floats * sizeof(float) + pairs_bytes; }
 };
 
-static LinSimtSmem lin_simt_layout(int RV, int D, int Lmax, int b, int d_k) {
+static LinSimtSmem lin_simt_layout(int RV, int D, int Lmax, int b, int d_k, int pgen) {
   LinSimtSmem s;
-  s.RV = RV; s.D = D; s.Lmax = Lmax; s.b = b; s.d_k = d_k;
+  s.RV = RV; s.D = D; s.Lmax = Lmax; s.b = b; s.d_k = d_k; s.pgen = pgen;
   long o = 0;
   s.Ms = o; o += (long)RV * D;
   s.Ss = o; o += (long)RV * D;
@@ -49,8 +53,51 @@ static LinSimtSmem lin_simt_layout(int RV, int D, int Lmax, int b, int d_k) {
   s.se = o; o += b;
   s.sb = o; o += b;
   s.total_floats = o;
-  s.pairs_bytes = 2L * (D - d_k > 0 ? D - d_k : 0);
+  s.pairs_bytes = pgen ? 4L * D : 2L * (D - d_k > 0 ? D - d_k : 0);
   return s;
+}
+
+// Feature j of the gated polynomial map: a_e times the product of the e indexed
+// entries of x (entry t of the monomial table; 0xFF marks unused index bytes).
+__device__ __forceinline__ float phi_gated(const float* x, uint32_t t, const float* a) {
+  float v = 1.f;
+  int e = 0;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const uint32_t i = (t >> (8 * r)) & 0xFFu;
+    if (i != 0xFFu) {
+      v *= x[i];
+      ++e;
+    }
+  }
+  return a[e] * v;
+}
+
+// Phi(q).Phi(k) of the gated map: sum_e a_e^2 h_e(z), z_j = q_j k_j.
+__device__ __forceinline__ float phi_gated_dot(const float* q, const float* k, int dk,
+                                               const float* a, int deg) {
+  float pw[5] = {0.f, 0.f, 0.f, 0.f, 0.f};  // power sums p_1 .. p_4
+  for (int j = 0; j < dk; ++j) {
+    const float z = q[j] * k[j];
+    float zz = z;
+#pragma unroll
+    for (int m = 1; m <= 4; ++m) {
+      if (m <= deg) pw[m] += zz;
+      zz *= z;
+    }
+  }
+  float h[5];
+  h[0] = 1.f;
+  float v = a[0] * a[0];
+#pragma unroll
+  for (int m = 1; m <= 4; ++m) {
+    float s = 0.f;
+#pragma unroll
+    for (int i = 1; i <= m; ++i) s += pw[i] * h[m - i];
+    h[m] = s / (float)m;
+    if (m <= deg) v += a[m] * a[m] * h[m];
+  }
+  return v;
 }
 
 // One CTA: rows [r0, r0 + RV) of one head, the whole sequence.
@@ -91,6 +138,7 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
   float* sb = sm + L.sb;
   uint8_t* pp = reinterpret_cast<uint8_t*>(sm + L.total_floats);
   uint8_t* pq = pp + (L.D - p.d_k > 0 ? L.D - p.d_k : 0);
+  uint32_t* ftab = reinterpret_cast<uint32_t*>(sm + L.total_floats);  // gated map
 
 
   const int rv = min(L.RV, p.d_v - r0);
@@ -106,6 +154,29 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
         for (int j = i; j < dk; ++j) { pp[o] = (uint8_t)i; pq[o] = (uint8_t)j; ++o; }
     }
   }
+  // monomial table of the gated map: degrees with a non-zero coefficient, each
+  // degree's sorted index tuples in lexicographic order (the next tuple raises
+  // the last entry that can still grow and resets the entries after it)
+  if (p.pgen && tid == 0) {
+    int o = 0;
+    for (int e = 0; e <= p.pdeg; ++e) {
+      if (p.pcoef[e] == 0.f) continue;
+      int idx[4] = {0, 0, 0, 0};
+      while (true) {
+        uint32_t t = 0xFFFFFFFFu;
+        for (int r = 0; r < e; ++r) t = (t & ~(0xFFu << (8 * r))) | ((uint32_t)idx[r] << (8 * r));
+        ftab[o++] = t;
+        int r = e - 1;
+        while (r >= 0 && idx[r] == dk - 1) --r;
+        if (r < 0) break;
+        ++idx[r];
+        for (int s2 = r + 1; s2 < e; ++s2) idx[s2] = idx[r];
+      }
+    }
+  }
+  auto feat = [&](const float* x, int j) -> float {
+    return p.pgen ? phi_gated(x, ftab[j], p.pcoef) : phi_at(x, j, dk, pp, pq, p.poly);
+  };
   float* Mg = p.M + head * state + (long)r0 * D;
   float* Sg = p.S ? p.S + head * state + (long)r0 * D : nullptr;
   for (long x = tid; x < (long)rv * D; x += nt) {
@@ -147,7 +218,7 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
         const float* m = Ms + (long)r * D;
         const float* k = Kw + i * dk;
         float s = 0.f;
-        for (int j = 0; j < D; ++j) s += m[j] * phi_at(k, j, dk, pp, pq, p.poly);
+        for (int j = 0; j < D; ++j) s += m[j] * feat(k, j);
         e = bias_grad(s - Vw[x], p.lk, p.lp);
       }
       E[x] = e;
@@ -160,13 +231,17 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
       if (w != 0.f) {
         const float* q = Qc + n * dk;
         const float* k = Kw + i * dk;
-        float s = 0.f, s2 = 0.f;
-        for (int j = 0; j < dk; ++j) {
-          const float qk = q[j] * k[j];
-          s += qk;
-          s2 += qk * qk;
+        if (p.pgen) {
+          v = phi_gated_dot(q, k, dk, p.pcoef, p.pdeg);
+        } else {
+          float s = 0.f, s2 = 0.f;
+          for (int j = 0; j < dk; ++j) {
+            const float qk = q[j] * k[j];
+            s += qk;
+            s2 += qk * qk;
+          }
+          v = p.poly ? s + 0.5f * (s * s + s2) : s;
         }
-        v = p.poly ? s + 0.5f * (s * s + s2) : s;
         v *= w;
       }
       P[n * L.Lmax + i] = v;
@@ -180,7 +255,7 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
       const float* s = Ss + (long)r * D;
       float ym = 0.f, ys = 0.f;
       for (int j = 0; j < D; ++j) {
-        const float f = phi_at(q, j, dk, pp, pq, p.poly);
+        const float f = feat(q, j);
         ym += m[j] * f;
         ys += s[j] * f;
       }
@@ -195,7 +270,7 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
       const int r = (int)(x / D), j = (int)(x % D);
       float gw = 0.f, gu = 0.f;
       for (int i = 0; i < Lw; ++i) {
-        const float f = E[i * rv + r] * phi_at(Kw + i * dk, j, dk, pp, pq, p.poly);
+        const float f = E[i * rv + r] * feat(Kw + i * dk, j);
         gw += Wrun[i] * f;
         gu += Urun[i] * f;
       }
@@ -216,12 +291,12 @@ int linear_simt_plan(const LinArgs& a, int heads, int* RV_out, size_t* smem_out)
   const size_t limit = 200 * 1024;
   int RV = a.d_v;
   while (RV > 1) {
-    LinSimtSmem s = lin_simt_layout(RV, a.D, Lmax, a.b, a.d_k);
+    LinSimtSmem s = lin_simt_layout(RV, a.D, Lmax, a.b, a.d_k, a.pgen);
     const long ctas = (long)heads * ((a.d_v + RV - 1) / RV);
     if (s.bytes() <= limit && (ctas >= 152 || RV <= 4)) break;
     RV = (RV + 1) / 2;
   }
-  LinSimtSmem s = lin_simt_layout(RV, a.D, Lmax, a.b, a.d_k);
+  LinSimtSmem s = lin_simt_layout(RV, a.D, Lmax, a.b, a.d_k, a.pgen);
   if (s.bytes() > limit) return ATLAS_ERR_UNSUPPORTED;
   *RV_out = RV;
   *smem_out = s.bytes();
@@ -233,7 +308,7 @@ static int launch(const LinArgs& a, int heads, const int* flags, cudaStream_t st
   size_t smem;
   int rc = linear_simt_plan(a, heads, &RV, &smem);
   if (rc) return rc;
-  LinSimtSmem s = lin_simt_layout(RV, a.D, a.b + a.c - 1, a.b, a.d_k);
+  LinSimtSmem s = lin_simt_layout(RV, a.D, a.b + a.c - 1, a.b, a.d_k, a.pgen);
   if (cudaFuncSetAttribute(linear_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return ATLAS_ERR_CUDA;

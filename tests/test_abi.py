@@ -87,6 +87,10 @@ def _bad(**kw):
     (dict(mem=A.MEM_MLP_GATED, d_h=0), A.ERR_INVALID),
     (dict(ns_steps=5), A.ERR_UNSUPPORTED),
     (dict(phi=A.PHI_POLY2, d_k=80), A.ERR_UNSUPPORTED),
+    (dict(phi=A.PHI_POLY), A.ERR_INVALID),                             # degree 0
+    (dict(phi=A.PHI_POLY, phi_coef=(0.0, 0.0)), A.ERR_INVALID),        # no feature left
+    (dict(phi=A.PHI_POLY, phi_coef=(0, 1, 1, 1, 1), d_k=40), A.ERR_UNSUPPORTED),  # D > 16384
+    (dict(phi=A.PHI_POLY, phi_coef=(0, 1), mem=A.MEM_MLP, d_h=16), A.ERR_INVALID),
 ])
 def test_invalid_descriptions_rejected_before_launch(lib, kw, code):
     cfg = _bad(**kw)
@@ -170,3 +174,27 @@ def test_backward_workspace_and_missing_workspace(lib):
     assert n >= 6 * 130 * 128 * 4 * 4  # at least the four row blocks' dK, dQ partials
     rc = lib.atlas_mem_backward(*([1] * 7), ctypes.byref(cfg), *([1] * 10))
     assert rc == A.ERR_WORKSPACE
+
+
+def test_gated_polynomial_map_sizes(lib):
+    """D counts the monomials of every degree whose coefficient is non-zero, and the
+    gated map always runs on the CUDA-core linear kernel."""
+    import math
+    for d, coef in ((8, (0, 1, 1, 1)), (6, (0.5, 1, 0, 0.8, 0.4)), (32, (0, 1, 1))):
+        cfg = A.make_cfg(B=1, H=2, N=64, d_k=d, d_v=16, phi=A.PHI_POLY, phi_coef=coef, c=2, b=8)
+        D = sum(math.comb(d + e - 1, e) for e, a in enumerate(coef) if a != 0)
+        assert A.atlas_mem_state_size(cfg) == 16 * D
+        assert A.atlas_mem_path(cfg) == "linear_simt"
+    # a = (0, 1, 1) describes the same features as the degree-2 map
+    g = A.make_cfg(B=1, H=1, N=8, d_k=32, d_v=64, phi=A.PHI_POLY, phi_coef=(0, 1, 1))
+    p2 = A.make_cfg(B=1, H=1, N=8, d_k=32, d_v=64, phi=A.PHI_POLY2)
+    assert A.atlas_mem_state_size(g) == A.atlas_mem_state_size(p2) == 64 * 560
+
+
+def test_gated_map_degree_beyond_the_maximum_is_rejected(lib):
+    cfg = _bad(phi=A.PHI_POLY, phi_coef=(0, 1, 1, 1, 1))
+    cfg.phi_degree = A.PHI_MAX_DEGREE + 1
+    rc = lib.atlas_mem_forward(1, 1, 1, 1, 1, 1, 1, ctypes.byref(cfg), 1, 1, None)
+    assert rc == A.ERR_INVALID
+    with pytest.raises(ValueError):
+        A.make_cfg(1, 1, 8, 4, 4, phi=A.PHI_POLY, phi_coef=(0, 1, 1, 1, 1, 1))

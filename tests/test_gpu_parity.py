@@ -356,3 +356,26 @@ def test_alternative_biases(wid, N, heads, loss, prm):
     Yo, Mo, _ = run_oracle(w, inp)
     Yg, Mg, _ = gpu_run(w, inp)
     check(w, Yg, Mg, Yo, Mo, f"workload {wid} loss {loss} ({prm})")
+
+
+# ------------------------------------------- gated polynomial feature map
+
+@pytest.mark.parametrize("d_k,coef,c,b,N,heads", [
+    (8, (0.0, 1.0, 1.0, 1.0), 4, 16, 70, [0, 3]),         # degree 3, D = 164
+    (6, (0.5, 1.0, 0.0, 0.8, 0.4), 2, 8, 41, [1]),        # constant, degree 2 gated off, degree 4
+    (16, (0.0, 1.0, 0.7, 0.3), 1, 64, 130, [0, 2]),       # degree 3, D = 968, one-token window
+])
+def test_gated_polynomial_map(d_k, coef, c, b, N, heads):
+    """The gated polynomial map of degree 3 and 4 ("논문 리뷰 Google ATLAS" §3.1,
+    Polynomial Feature Mapping and Input gating) on the CUDA-core linear kernel,
+    against the oracle; momentum and decay as in the poly2 workload (bounded step)."""
+    from test_memorization_recurrent_gb300.harness import cfg_for
+    import test_memorization_recurrent_gb300 as A
+    w = W.workload(3, bounded=True, d_k=d_k, phi=W.PHI_POLY, phi_coef=coef, c=c, b=b, N=N,
+                   theta_scale=0.002)
+    assert A.atlas_mem_path(cfg_for(w, len(heads), N)) == "linear_simt"
+    inp = W.generate(w, heads=heads, n_tokens=N)
+    Yo, Mo, So = run_oracle(w, inp)
+    Yg, Mg, Sg = gpu_run(w, inp, with_S=True)
+    check(w, Yg, Mg, Yo, Mo, f"gated map {coef}")
+    assert rel_err(Sg, So, w.bf16) <= tol(w)

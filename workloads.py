@@ -24,7 +24,7 @@ import numpy as np
 BLOCK = 256  # tokens per independently seeded block
 
 MEM_LINEAR, MEM_MLP = 0, 1
-PHI_IDENTITY, PHI_POLY2 = 0, 1
+PHI_IDENTITY, PHI_POLY2, PHI_POLY = 0, 1, 2
 LOSS_L2, LOSS_DOT, LOSS_LP, LOSS_HUBER = 0, 1, 2, 3
 
 
@@ -55,6 +55,7 @@ class Workload:
     ns_steps: int = 0
     ns_coef: tuple = (0.0, 0.0, 0.0)
     ns_eps: float = 1e-7
+    phi_coef: tuple = ()           # PHI_POLY: input-gating coefficients a_0 .. a_p
 
     @property
     def heads(self) -> int:
@@ -64,6 +65,9 @@ class Workload:
     def D(self) -> int:
         if self.mem == MEM_LINEAR and self.phi == PHI_POLY2:
             return self.d_k + self.d_k * (self.d_k + 1) // 2
+        if self.mem == MEM_LINEAR and self.phi == PHI_POLY:
+            return sum(math.comb(self.d_k + e - 1, e) for e, a in enumerate(self.phi_coef)
+                       if a != 0.0)
         return self.d_k
 
     @property
