@@ -77,20 +77,30 @@ def load_peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def profile_traffic(kernel_src: str, profile_name: str, units_per_launch: float):
-    """DRAM bytes per launch from a committed ncu summary, scaled to this launch,
-    or None if the summary is missing or was taken on another kernel source."""
+CSRC = os.path.join(ROOT, "test_memorization_recurrent_gb300", "csrc")
+
+
+def source_hashes(files):
+    """sha256 of each named file under the package's csrc/."""
+    out = {}
+    for f in files:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            out[f] = hashlib.sha256(fh.read()).hexdigest()
+    return out
+
+
+def profile_traffic(files, profile_name: str, units_per_launch: float):
+    """DRAM bytes per call from a committed ncu summary, scaled to this call, or
+    None if the summary is missing or any of the sources it was taken on (one
+    `source_sha256: <hash> <file>` line each) has changed since."""
     path = os.path.join(ROOT, "profiles", profile_name)
     if not os.path.exists(path):
         return None
     text = open(path).read()
-    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    listed = dict((f, h) for h, f in re.findall(r"source_sha256:\s*([0-9a-f]{64})\s+(\S+)", text))
     m_b = re.search(r"dram_bytes_per_unit:\s*([0-9.eE+-]+)", text)
-    if not m_sha or not m_b:
+    if not m_b or set(listed) != set(files) or listed != source_hashes(files):
         return None
-    with open(kernel_src, "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest() != m_sha.group(1):
-            return None
     return float(m_b.group(1)) * units_per_launch
 
 
@@ -247,13 +257,17 @@ def run_reference(args, w):
 
 # ------------------------------------------------------------------- GPU leg
 
+# Per path: the sources its kernels are compiled from (a profile summary counts
+# only while all of them are unchanged) and the summary's file name.
+_TC = ["tc_primitives.cuh", "common.cuh", "kernels.h"]
 KERNEL_OF_PATH = {
-    "linear_tc": ("linear_tc.cu", "linear_tc_{wname}.md"),
-    "linear_simt": ("linear_simt.cu", "linear_simt_{wname}.md"),
-    "linear_seq": ("linear_seq.cu", "linear_seq_{wname}.md"),
-    "linear_chunk": ("tc_gemm.cu", "linear_chunk_{wname}.md"),
-    "mlp_simt": ("ns_fused.cu", "ns_fused_{wname}.md"),
-    "mlp_tc": ("mlp_tc.cu", "mlp_tc_{wname}.md"),
+    "linear_tc": (["linear_tc.cu", "linear_simt.cu"] + _TC, "linear_tc_{wname}.md"),
+    "linear_simt": (["linear_simt.cu", "common.cuh", "kernels.h"], "linear_simt_{wname}.md"),
+    "linear_seq": (["linear_seq.cu", "common.cuh", "kernels.h"], "linear_seq_{wname}.md"),
+    "linear_chunk": (["linear_chunk.cu", "tc_gemm.cu"] + _TC, "linear_chunk_{wname}.md"),
+    "mlp_simt": (["mlp_simt.cu", "tc_gemm.cu", "ns_fused.cu"] + _TC, "mlp_simt_{wname}.md"),
+    "mlp_tc": (["mlp_tc.cu"] + _TC, "mlp_tc_{wname}.md"),
+    "linear_bwd": (["linear_bwd.cu", "common.cuh", "kernels.h"], "linear_bwd_{wname}.md"),
 }
 
 # Workloads measured beside the headline one, and the token prefix each is timed
@@ -345,10 +359,8 @@ def roofline(w, path, kernel_s):
         achieved = flops_launch / kernel_s / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": tf_sus, "unit": "TFLOP/s",
                 "frac": achieved / tf_sus, "peak_kind": f"{peak_kind} bf16_tflops_sustained"}
-    src, prof = KERNEL_OF_PATH.get(path, ("", ""))
-    src_path = os.path.join(ROOT, "test_memorization_recurrent_gb300", "csrc", src)
-    roof["traffic"] = (profile_traffic(src_path, prof.format(wname=w.name), tokens)
-                       if src else None)
+    files, prof = KERNEL_OF_PATH.get(path, ([], ""))
+    roof["traffic"] = profile_traffic(files, prof.format(wname=w.name), tokens) if files else None
     roof["kernel"] = path
     roof["kernel_ms"] = kernel_s * 1e3
     roof["algorithmic_bytes"] = bytes_launch
@@ -399,6 +411,11 @@ def fp32_alu_peak_tflops():
     return 152 * 128 * 2 * 2.07e9 / 1e12
 
 
+def _bwd_prof(w):
+    files, prof = KERNEL_OF_PATH["linear_bwd"]
+    return files, prof.format(wname=w.name), w.tokens
+
+
 def measure_backward(steps, warmup, dev):
     """The backward pass over the whole DeltaNet-like workload (every head, every
     token): rate, and the fraction of the fp32 CUDA-core peak it reaches."""
@@ -436,7 +453,8 @@ def measure_backward(steps, warmup, dev):
            "roofline": {"bound": "alu", "achieved": flops / s / 1e12, "peak": peak,
                         "unit": "TFLOP/s", "frac": flops / s / 1e12 / peak,
                         "peak_kind": "fp32 FMA peak from unit counts and clock",
-                        "traffic": None, "kernel": "linear_bwd", "kernel_ms": s * 1e3,
+                        "traffic": profile_traffic(*_bwd_prof(w)),
+                        "kernel": "linear_bwd", "kernel_ms": s * 1e3,
                         "algorithmic_flops": flops,
                         "algorithmic_bytes": w.tokens * W.bwd_bytes_per_token(w)},
            "clocks": clk.summary()}
@@ -603,6 +621,44 @@ def run_atlas(args, w):
         dist.destroy_process_group()
 
 
+def profile_one_call(args, w):
+    """Warm up, then run exactly one call (the forward over the workload, or the
+    backward pass) between cudaProfilerStart and cudaProfilerStop, so that
+    `ncu --profile-from-start off` captures that call's kernels and nothing else."""
+    import torch
+    import test_memorization_recurrent_gb300 as A
+    from test_memorization_recurrent_gb300 import build as B
+    from test_memorization_recurrent_gb300.harness import BackwardRunner, Runner, to_device
+    B.build()
+    torch.cuda.set_device(0)
+    d = to_device(w, W.generate(w))
+    if args.profile_call == "backward":
+        r = np.random.default_rng(3)
+        dY = torch.from_numpy(r.standard_normal((w.heads, w.N, w.d_v)).astype(np.float32)).cuda()
+        dMN = torch.zeros((w.heads, w.state_size), dtype=torch.float32, device="cuda")
+        run = BackwardRunner(w, w.heads, w.N)
+        call = lambda: run(d, dY, dMN)  # noqa: E731
+        launches = 3
+    else:
+        run = Runner(w, w.heads, w.N)
+        call = lambda: run(d)  # noqa: E731
+        launches = A.atlas_mem_launch_count(run.cfg)
+    for _ in range(max(3, args.warmup)):
+        call()
+    if w.tokens * W.bytes_per_token(w) + 2 * 4 * w.heads * w.state_size < 2 * L2_BYTES:
+        # a workload that fits in L2 is timed after an L2 scrub: profile it cold too
+        torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda").fill_(1.0)
+    torch.cuda.synchronize()
+    torch.cuda.profiler.start()
+    call()
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    if int(run.status.item()) != 0:
+        raise SystemExit(f"device status {int(run.status.item())}")
+    print(json.dumps({"profiled": args.profile_call, "workload": w.name, "tokens": w.tokens,
+                      "launches": launches}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -611,6 +667,11 @@ def main(argv=None):
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="atlas", choices=["atlas", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-call", choices=["forward", "backward"], default=None,
+                    help="warm up, then run one call between cudaProfilerStart/Stop and exit "
+                         "(for ncu --profile-from-start off)")
+    ap.add_argument("--variant", type=int, default=None,
+                    help="with --profile-call: the variant workload of that index")
     ap.add_argument("--no-per-config", action="store_true",
                     help="measure the chosen workload only (no per_config record)")
     ap.add_argument("--tokens", type=int, default=0,
@@ -627,7 +688,11 @@ def main(argv=None):
         kind = W.LOSS_LP if args.loss == "lp" else W.LOSS_HUBER
         prm = args.loss_param or (3.0 if args.loss == "lp" else 0.3)
         w = w.with_(loss=kind, loss_param=prm, name=f"{w.name}-{args.loss}{prm:g}")
-    if args.impl == "reference":
+    if args.profile_call:
+        if args.variant is not None:
+            w = variant_workloads()[args.variant]
+        profile_one_call(args, w)
+    elif args.impl == "reference":
         run_reference(args, w)
     else:
         run_atlas(args, w)
