@@ -65,7 +65,6 @@ int check_cfg(const atlas_mem_cfg* c) {
   if (c->mem != ATLAS_MEM_LINEAR) {
     if (c->d_h <= 0 || c->d_k != c->d_v) return ATLAS_ERR_INVALID;
     if (c->phi != ATLAS_PHI_IDENTITY) return ATLAS_ERR_INVALID;
-    if (c->mem != ATLAS_MEM_MLP) return ATLAS_ERR_UNSUPPORTED;  // LN, gated: oracle only
     if (c->loss == ATLAS_LOSS_DOT) return ATLAS_ERR_UNSUPPORTED;
   } else {
     if (c->ns_steps > 0) return ATLAS_ERR_UNSUPPORTED;
@@ -111,12 +110,14 @@ MlpArgs mlp_args(const void* K, const void* Q, const void* V, const float* alpha
   a.ns_a = c->ns_a; a.ns_b = c->ns_b; a.ns_c = c->ns_c; a.ns_eps = c->ns_eps;
   a.s_is_zero = c->S_state == nullptr;
   a.status = c->status_dev;
+  a.ln = c->mem == ATLAS_MEM_MLP_LN;
+  a.gated = c->mem == ATLAS_MEM_MLP_GATED;
   return a;
 }
 
 Path choose_path(const atlas_mem_cfg* c) {
   if (check_cfg(c) != ATLAS_OK) return PATH_INVALID;
-  if (c->mem == ATLAS_MEM_MLP) {
+  if (c->mem != ATLAS_MEM_LINEAR) {
     MlpArgs m = mlp_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, c,
                          nullptr, nullptr);
     // the tensor-core kernels take no history rows (with c = 1 they would not matter,
@@ -146,13 +147,14 @@ extern "C" {
 
 size_t atlas_mem_state_size(const atlas_mem_cfg* cfg) {
   if (check_cfg(cfg) != ATLAS_OK) return 0;
-  if (cfg->mem == ATLAS_MEM_MLP) return (size_t)2 * cfg->d_k * cfg->d_h;
+  if (cfg->mem == ATLAS_MEM_MLP_GATED) return (size_t)3 * cfg->d_k * cfg->d_h;
+  if (cfg->mem != ATLAS_MEM_LINEAR) return (size_t)2 * cfg->d_k * cfg->d_h;
   return (size_t)cfg->d_v * feature_dim(cfg);
 }
 
 size_t atlas_mem_workspace_bytes(const atlas_mem_cfg* cfg) {
   if (check_cfg(cfg) != ATLAS_OK) return (size_t)-1;
-  if (cfg->mem == ATLAS_MEM_MLP) {
+  if (cfg->mem != ATLAS_MEM_LINEAR) {
     MlpArgs a = mlp_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, cfg,
                          nullptr, nullptr);
     return choose_path(cfg) == PATH_MLP_TC ? mlp_tc_workspace_bytes(a)

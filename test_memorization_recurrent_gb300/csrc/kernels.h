@@ -112,6 +112,8 @@ struct MlpArgs {
   float ns_a, ns_b, ns_c, ns_eps;
   int s_is_zero;  // S must be cleared before the first chunk
   int* status;    // optional device status word (timeouts)
+  int ln;         // layer-normalised memory x + LN(W1 GELU(W2 x)) (CUDA-core path only)
+  int gated;      // gated memory x + W1 (GELU(W2 x) * (W3 x)), W3 after W2 (CUDA-core path only)
 };
 
 size_t mlp_simt_workspace_bytes(const MlpArgs& a);

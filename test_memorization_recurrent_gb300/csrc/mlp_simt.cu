@@ -25,6 +25,25 @@
 //   y_n  = q_n + a_n W1_0 hq_n + sum_{m<=n} r[n,m] N1_m hq_n.
 // NS uses the Gram matrix of the short side: (X X^T) X = X (X^T X).  These
 // batched products run on the tensor cores (tc_gemm.cu, bf16 hi/lo operands).
+//
+// The layer-normalised memory M(x) = x + LN(W1 GELU(W2 x)) ("It's All Connected
+// (Miras)", the Moneta / Yaad / Memora memory; plain LN over the d outputs, no
+// scale or shift, 1e-5 under the square root) changes two places.  At the
+// chunk-start state the branch output u_i = W1 h_i is normalised per token,
+// e_i = k_i + LN(u_i) - v_i, and the error rows are replaced by the gradient
+// with respect to u: is (dy - mean(dy) - n mean(dy n)) with n = LN(u), is the
+// inverse standard deviation and dy the bias derivative of e; everything after
+// that (Delta, the state updates, the readout's intra-chunk terms) uses those rows
+// as the plain memory uses its errors.  The readout accumulates u_q for every
+// query (no residual) and finishes with y = q + LN(u_q).
+//
+// The gated memory M(x) = x + W1 (GELU(W2 x) * (W3 x)) ("ATLAS ... (paperlayer)"
+// §5, Atlas++: a gated MLP with three linear maps; W3 is d_h x d like W2 and is
+// stored after it) has the hidden activation h = GELU(z) * w with z = W2 x,
+// w = W3 x, and with dh = E W1 the gradient factors delta = dh * w * GELU'(z) of
+// W2 and delta3 = dh * GELU(z) of W3.  W3 is carried like W2 (its readout
+// wq = W3_n q decomposes the same way), and Newton-Schulz treats it as a third
+// weight block (batched products; the fused kernel takes two blocks).
 #include <math.h>
 
 #include "common.cuh"
@@ -140,6 +159,9 @@ static int run_gemm(const Gemm& g, cudaStream_t st) {
 struct MlpWs {
   long Kw, Vw, E, Qc, H, Gp, Dl, ta, te, tb, U, W, P1, P2, Zq, Gq, Ew, Eu, Dw, Du, X, T1, T2,
       A, nrm, per_head;
+  // gated memory: gate w = K W3^T, gated hidden h, E W1, delta3 and its weighted
+  // rows, the readout's gate wq (zero-sized otherwise)
+  long Wg, Hg, Dh, D3, D3w, D3u, Wq;
   long S;  // S buffer (all heads), when the caller gives none
   // Newton-Schulz, all (head, token) instances of a chunk: S_n / NS iterate,
   // the second iterate, Gram and its square, and the readout products.
@@ -177,18 +199,27 @@ static MlpWs mlp_layout(const MlpArgs& a) {
   w.T2 = o; o += big * small;
   w.A = o; o += small * small;
   w.nrm = o; o += 4;
+  const long gl = a.gated ? L * dh : 0, gb = a.gated ? b * dh : 0;
+  w.Wg = o; o += gl;
+  w.Hg = o; o += gl;
+  w.Dh = o; o += gl;
+  w.D3 = o; o += gl;
+  w.D3w = o; o += gl;
+  w.D3u = o; o += gl;
+  w.Wq = o; o += gb;
   o = (o + 63) & ~63L;
   w.per_head = o;
   w.S = o * a.heads;
-  long total = w.S + (a.S ? 0 : (long)a.heads * 2 * d * dh);
+  const long nblk = a.gated ? 3 : 2;
+  long total = w.S + (a.S ? 0 : (long)a.heads * nblk * d * dh);
   w.nsX = w.nsT = w.nsA = w.nsA2 = w.nsP = w.nsR = 0;
   if (a.ns_steps > 0) {
-    const long inst = (long)a.heads * b, state = 2 * d * dh;
+    const long inst = (long)a.heads * b, state = nblk * d * dh;
     w.nsX = total; total += inst * state;
     w.nsT = total; total += inst * state;
-    w.nsA = total; total += inst * 2 * small * small;
-    w.nsA2 = total; total += inst * 2 * small * small;
-    w.nsP = total; total += inst * dh * b;
+    w.nsA = total; total += inst * nblk * small * small;
+    w.nsA2 = total; total += inst * nblk * small * small;
+    w.nsP = total; total += inst * dh * b * (a.gated ? 2 : 1);
     w.nsR = total; total += inst * d * b;
   }
   w.bytes = (size_t)total * sizeof(float);
@@ -232,6 +263,32 @@ __global__ void mlp_gather_kernel(MlpArgs p, MlpWs w, float* ws, int t0, int nb,
   }
 }
 
+// Gated memory, window rows: Hg = H * Wg (H = GELU(Z)), in all heads.
+__global__ void gate_hidden_kernel(float* ws, long per_head, long Hg, long H, long Wg, long n) {
+  float* base = ws + (long)blockIdx.y * per_head;
+  for (long x = blockIdx.x * (long)blockDim.x + threadIdx.x; x < n; x += (long)gridDim.x * blockDim.x)
+    base[Hg + x] = base[H + x] * base[Wg + x];
+}
+
+// Gated memory, window rows: from dh = E W1 (in Dh), Delta = dh * w * GELU'(z) and
+// Delta3 = dh * GELU(z).
+__global__ void gate_grad_kernel(float* ws, long per_head, long Dl, long D3, long Dh, long Wg,
+                                 long Gp, long H, long n) {
+  float* base = ws + (long)blockIdx.y * per_head;
+  for (long x = blockIdx.x * (long)blockDim.x + threadIdx.x; x < n; x += (long)gridDim.x * blockDim.x) {
+    const float dh = base[Dh + x];
+    base[Dl + x] = dh * base[Wg + x] * base[Gp + x];
+    base[D3 + x] = dh * base[H + x];
+  }
+}
+
+// Gated memory, query rows: Zq (holding GELU(zq)) <- GELU(zq) * wq.
+__global__ void gate_query_kernel(float* ws, long per_head, long Zq, long Wq, long n) {
+  float* base = ws + (long)blockIdx.y * per_head;
+  for (long x = blockIdx.x * (long)blockDim.x + threadIdx.x; x < n; x += (long)gridDim.x * blockDim.x)
+    base[Zq + x] *= base[Wq + x];
+}
+
 // dst[i, :] = s[i] * src[i, :] for the rows of the window (s = last table row).
 __global__ void scale_rows_kernel(float* ws, long per_head, long dst, long src, long svec,
                                   int rows, int cols) {
@@ -259,13 +316,72 @@ __global__ void state_carry_kernel(float* M, float* S, long state, const float* 
   }
 }
 
-// Y rows of the chunk start as the residual q.
+// Y rows of the chunk start as the residual q (or 0 when the branch output is
+// normalised before the residual is added).
 __global__ void copy_q_kernel(const float* ws, long per_head, long Qc, float* Y, long N, int d,
-                              int t0, int n_lo, int n_hi) {
+                              int t0, int n_lo, int n_hi, int zero) {
   const int h = blockIdx.x;
   const float* q = ws + h * per_head + Qc;
   for (int x = threadIdx.x; x < (n_hi - n_lo) * d; x += blockDim.x)
-    Y[(long)h * N * d + (long)(t0 + n_lo) * d + x] = q[n_lo * d + x];
+    Y[(long)h * N * d + (long)(t0 + n_lo) * d + x] = zero ? 0.f : q[n_lo * d + x];
+}
+
+__device__ __forceinline__ float warp_allsum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+  return x;
+}
+
+constexpr float kLnEps = 1e-5f;
+
+// Layer-normalised memory, window rows (one warp per row): U holds the branch
+// output u = h W1^T at the chunk-start state, E holds k - v.  Leaves in E the
+// gradient factor of u, in units of the l2 bias's 2e:
+//   n = (u - mean u) is,  is = 1 / sqrt(var u + eps),  e = (k - v) + n,
+//   dy = bias'(e),  E <- is (dy - mean(dy) - n mean(dy n)).
+__global__ void ln_error_kernel(float* ws, long per_head, long Eo, long Uo, int rows, int d,
+                                int kind, float prm) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  float* base = ws + (long)blockIdx.y * per_head;
+  float* u = base + Uo + (long)row * d;
+  float* e = base + Eo + (long)row * d;
+  float s = 0.f;
+  for (int j = lane; j < d; j += 32) s += u[j];
+  const float mu = warp_allsum(s) / d;
+  float v = 0.f;
+  for (int j = lane; j < d; j += 32) v += (u[j] - mu) * (u[j] - mu);
+  const float is = rsqrtf(warp_allsum(v) / d + kLnEps);
+  float s1 = 0.f, s2 = 0.f;
+  for (int j = lane; j < d; j += 32) {
+    const float n = (u[j] - mu) * is;
+    const float dy = bias_grad(e[j] + n, kind, prm);
+    u[j] = n;
+    e[j] = dy;
+    s1 += dy;
+    s2 += dy * n;
+  }
+  const float m1 = warp_allsum(s1) / d, m2 = warp_allsum(s2) / d;
+  for (int j = lane; j < d; j += 32) e[j] = is * (e[j] - m1 - u[j] * m2);
+}
+
+// Layer-normalised memory, query rows of the chunk (one warp per row): Y holds
+// the branch output u_q; y = q + LN(u_q).
+__global__ void ln_readout_kernel(const float* ws, long per_head, long Qc, float* Y, long N,
+                                  int d, int t0, int nb) {
+  const int lane = threadIdx.x & 31;
+  const int n = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (n >= nb) return;
+  const float* q = ws + (long)blockIdx.y * per_head + Qc + (long)n * d;
+  float* y = Y + (long)blockIdx.y * N * d + (long)(t0 + n) * d;
+  float s = 0.f;
+  for (int j = lane; j < d; j += 32) s += y[j];
+  const float mu = warp_allsum(s) / d;
+  float v = 0.f;
+  for (int j = lane; j < d; j += 32) v += (y[j] - mu) * (y[j] - mu);
+  const float is = rsqrtf(warp_allsum(v) / d + kLnEps);
+  for (int j = lane; j < d; j += 32) y[j] = q[j] + (y[j] - mu) * is;
 }
 
 // E <- the attentional bias's derivative of E (in units of the l2 bias's 2e),
@@ -361,17 +477,26 @@ static dim3 ew_grid(long n, int heads) {
 
 long mlp_simt_launch_count(const MlpArgs& a) {
   const long chunks = (a.N + a.b - 1) / a.b;
-  const long bias = a.lk != ATLAS_LOSS_L2 ? 1 : 0;  // the bias kernel on E
-  if (a.ns_steps > 0)
-    return 1 + chunks * (bias + (ns_fused_supported(a.d, a.dh) ? 16 : 16 + 6L * a.ns_steps));
-  return 1 + chunks * (bias + 4 + 1 + 3 + 1 + 4 + 4 + 1 + 4);
+  // the bias kernel on E; the layer-normalised memory instead adds the LN of the
+  // error rows and the LN of the readout rows
+  long extra = a.ln ? 2 : (a.lk != ATLAS_LOSS_L2 ? 1 : 0);
+  // the gated memory: the gate's product, the gated hidden, the gate gradients;
+  // without Newton-Schulz the gate's three readout products, its product with
+  // GELU(zq), two weighted-row kernels and two state products; with it, the third
+  // block's momentum product, its readout product, the add and the product with
+  // GELU(zq), three more products per block and step (unfused), and no fusion
+  if (a.gated) extra += 3 + (a.ns_steps > 0 ? 5 + 3L * a.ns_steps : 3 + 1 + 2 + 2);
+  const bool fused = ns_fused_supported(a.d, a.dh) && !a.gated;
+  if (a.ns_steps > 0) return 1 + chunks * (extra + (fused ? 16 : 16 + 6L * a.ns_steps));
+  return 1 + chunks * (extra + 4 + 1 + 3 + 1 + 4 + 4 + 1 + 4);
 }
 
 int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
   MlpArgs p = p0;
   MlpWs w = mlp_layout(p);
   float* ws = reinterpret_cast<float*>(wsv);
-  const long d = p.d, dh = p.dh, half = d * dh, state = 2 * half;
+  const long d = p.d, dh = p.dh, half = d * dh;
+  const long nblk = p.gated ? 3 : 2, state = nblk * half;
   const int H = p.heads;
   if (!p.S) {
     p.S = ws + w.S;
@@ -382,6 +507,8 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
   float* W2 = p.M + half;
   float* S1 = p.S;
   float* S2 = p.S + half;
+  float* W3 = p.M + 2 * half;  // gated memory only
+  float* S3 = p.S + 2 * half;
   const long PH = w.per_head;
   for (int t0 = 0; t0 < p.N; t0 += p.b) {
     const int t1 = min(p.N, t0 + p.b), nb = t1 - t0;
@@ -396,27 +523,52 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
     g.C = ws + w.H; g.sCb = PH; g.sCm = dh; g.sCn = 1;
     g.epi = 1; g.C2 = ws + w.Gp; g.sC2b = PH; g.sC2m = dh; g.sC2n = 1;
     CK(run_gemm(g, st));
-    // E = (K_w - V_w) + H W1^T
+    // the hidden activation the rest uses: H, or for the gated memory Hg = H * (K_w W3^T)
+    const long hid = p.gated ? w.Hg : w.H;
+    if (p.gated) {
+      g = gemm0();
+      g.batch = H; g.M = L; g.N = (int)dh; g.K = (int)d;
+      g.A = ws + w.Kw; g.sAb = PH; g.sAm = d; g.sAk = 1;
+      g.B = W3; g.sBb = state; g.sBk = 1; g.sBn = d;
+      g.C = ws + w.Wg; g.sCb = PH; g.sCm = dh; g.sCn = 1;
+      CK(run_gemm(g, st));
+      gate_hidden_kernel<<<ew_grid((long)L * dh, H), 256, 0, st>>>(ws, PH, w.Hg, w.H, w.Wg,
+                                                                   (long)L * dh);
+      CL();
+    }
+    // E = (K_w - V_w) + H W1^T  (layer-normalised memory: U = H W1^T into the Ew
+    // scratch, which is free until the state carry, then E from U)
     g = gemm0();
     g.batch = H; g.M = L; g.N = (int)d; g.K = (int)dh;
-    g.A = ws + w.H; g.sAb = PH; g.sAm = dh; g.sAk = 1;
+    g.A = ws + hid; g.sAb = PH; g.sAm = dh; g.sAk = 1;
     g.B = W1; g.sBb = state; g.sBk = 1; g.sBn = dh;
-    g.C = ws + w.E; g.sCb = PH; g.sCm = d; g.sCn = 1;
-    g.accumulate = 1;
+    g.C = ws + (p.ln ? w.Ew : w.E); g.sCb = PH; g.sCm = d; g.sCn = 1;
+    g.accumulate = p.ln ? 0 : 1;
     CK(run_gemm(g, st));
-    if (p.lk != ATLAS_LOSS_L2) {  // the attentional bias acts on E elementwise
+    if (p.ln) {
+      ln_error_kernel<<<dim3((unsigned)((L + 7) / 8), H), 256, 0, st>>>(ws, PH, w.E, w.Ew, L,
+                                                                         (int)d, p.lk, p.lp);
+      CL();
+    } else if (p.lk != ATLAS_LOSS_L2) {  // the attentional bias acts on E elementwise
       bias_rows_kernel<<<ew_grid((long)L * d, H), 256, 0, st>>>(ws + w.E, PH, (long)L * d, p.lk,
                                                                p.lp);
       CL();
     }
-    // Delta = (E W1) * GELU'(Z)
+    // Delta = (E W1) * GELU'(Z)  (gated: dh = E W1, then Delta and Delta3)
     g = gemm0();
     g.batch = H; g.M = L; g.N = (int)dh; g.K = (int)d;
     g.A = ws + w.E; g.sAb = PH; g.sAm = d; g.sAk = 1;
     g.B = W1; g.sBb = state; g.sBk = dh; g.sBn = 1;
-    g.emul = ws + w.Gp; g.sEb = PH; g.sEm = dh; g.sEn = 1;
-    g.C = ws + w.Dl; g.sCb = PH; g.sCm = dh; g.sCn = 1;
+    if (!p.gated) {
+      g.emul = ws + w.Gp; g.sEb = PH; g.sEm = dh; g.sEn = 1;
+    }
+    g.C = ws + (p.gated ? w.Dh : w.Dl); g.sCb = PH; g.sCm = dh; g.sCn = 1;
     CK(run_gemm(g, st));
+    if (p.gated) {
+      gate_grad_kernel<<<ew_grid((long)L * dh, H), 256, 0, st>>>(ws, PH, w.Dl, w.D3, w.Dh, w.Wg,
+                                                                 w.Gp, w.H, (long)L * dh);
+      CL();
+    }
 
     if (p.ns_steps <= 0) {
       // P1 = W * (Q K_w^T)
@@ -445,16 +597,37 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
       g.alpha = -2.f; g.accumulate = 1; g.epi = 1;
       g.C2 = ws + w.Gq; g.sC2b = PH; g.sC2m = dh; g.sC2n = 1;
       CK(run_gemm(g, st));
+      if (p.gated) {  // wq = a (Q W3^T) + beta (Q S3^T) - 2 P1 Delta3 ; Hq = GELU(zq) * wq
+        g = gemm0();
+        g.batch = H; g.M = nb; g.N = (int)dh; g.K = (int)d;
+        g.A = ws + w.Qc; g.sAb = PH; g.sAm = d; g.sAk = 1;
+        g.B = W3; g.sBb = state; g.sBk = 1; g.sBn = d;
+        g.rowscale = ws + w.ta; g.sRb = PH;
+        g.C = ws + w.Wq; g.sCb = PH; g.sCm = dh; g.sCn = 1;
+        CK(run_gemm(g, st));
+        g.B = S3; g.rowscale = ws + w.tb; g.accumulate = 1;
+        CK(run_gemm(g, st));
+        g = gemm0();
+        g.batch = H; g.M = nb; g.N = (int)dh; g.K = L;
+        g.A = ws + w.P1; g.sAb = PH; g.sAm = L; g.sAk = 1;
+        g.B = ws + w.D3; g.sBb = PH; g.sBk = dh; g.sBn = 1;
+        g.C = ws + w.Wq; g.sCb = PH; g.sCm = dh; g.sCn = 1;
+        g.alpha = -2.f; g.accumulate = 1;
+        CK(run_gemm(g, st));
+        gate_query_kernel<<<ew_grid((long)nb * dh, H), 256, 0, st>>>(ws, PH, w.Zq, w.Wq,
+                                                                     (long)nb * dh);
+        CL();
+      }
       // P2 = W * (Hq H^T)
       g = gemm0();
       g.batch = H; g.M = nb; g.N = L; g.K = (int)dh;
       g.A = ws + w.Zq; g.sAb = PH; g.sAm = dh; g.sAk = 1;
-      g.B = ws + w.H; g.sBb = PH; g.sBk = 1; g.sBn = dh;
+      g.B = ws + hid; g.sBb = PH; g.sBk = 1; g.sBn = dh;
       g.emul = ws + w.W; g.sEb = PH; g.sEm = L; g.sEn = 1;
       g.C = ws + w.P2; g.sCb = PH; g.sCm = L; g.sCn = 1;
       CK(run_gemm(g, st));
       // Y = q + a (Hq W1^T) + beta (Hq S1^T) - 2 P2 E
-      copy_q_kernel<<<H, 256, 0, st>>>(ws, PH, w.Qc, p.Y, p.N, (int)d, t0, 0, nb);
+      copy_q_kernel<<<H, 256, 0, st>>>(ws, PH, w.Qc, p.Y, p.N, (int)d, t0, 0, nb, p.ln);
       CL();
       g = gemm0();
       g.batch = H; g.M = nb; g.N = (int)d; g.K = (int)dh;
@@ -473,6 +646,11 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
       g.C = p.Y + (long)t0 * d; g.sCb = (long)p.N * d; g.sCm = d; g.sCn = 1;
       g.alpha = -2.f; g.accumulate = 1;
       CK(run_gemm(g, st));
+      if (p.ln) {
+        ln_readout_kernel<<<dim3((unsigned)((nb + 7) / 8), H), 256, 0, st>>>(ws, PH, w.Qc, p.Y,
+                                                                            p.N, (int)d, t0, nb);
+        CL();
+      }
       // state carry: rows of E and Delta weighted by the last W / U rows
       const long lastW = w.W + (long)(nb - 1) * L, lastU = w.U + (long)(nb - 1) * L;
       dim3 eg = ew_grid((long)L * dh, H);
@@ -480,6 +658,10 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
       scale_rows_kernel<<<eg, 256, 0, st>>>(ws, PH, w.Eu, w.E, lastU, L, (int)d);
       scale_rows_kernel<<<eg, 256, 0, st>>>(ws, PH, w.Dw, w.Dl, lastW, L, (int)dh);
       scale_rows_kernel<<<eg, 256, 0, st>>>(ws, PH, w.Du, w.Dl, lastU, L, (int)dh);
+      if (p.gated) {
+        scale_rows_kernel<<<eg, 256, 0, st>>>(ws, PH, w.D3w, w.D3, lastW, L, (int)dh);
+        scale_rows_kernel<<<eg, 256, 0, st>>>(ws, PH, w.D3u, w.D3, lastU, L, (int)dh);
+      }
       CL();
       state_carry_kernel<<<ew_grid(state, H), 256, 0, st>>>(p.M, p.S, state, ws, PH, w.ta, w.te,
                                                             w.tb, nb - 1);
@@ -488,7 +670,7 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
       g = gemm0();
       g.batch = H; g.M = (int)d; g.N = (int)dh; g.K = L;
       g.A = ws + w.Ew; g.sAb = PH; g.sAm = 1; g.sAk = d;
-      g.B = ws + w.H; g.sBb = PH; g.sBk = dh; g.sBn = 1;
+      g.B = ws + hid; g.sBb = PH; g.sBk = dh; g.sBn = 1;
       g.C = W1; g.sCb = state; g.sCm = dh; g.sCn = 1;
       g.alpha = -2.f; g.accumulate = 1;
       CK(run_gemm(g, st));
@@ -504,6 +686,12 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
       CK(run_gemm(g, st));
       g.A = ws + w.Du; g.C = S2;
       CK(run_gemm(g, st));
+      if (p.gated) {  // W3 += -2 D3w^T K_w ; S3 += -2 D3u^T K_w
+        g.A = ws + w.D3w; g.C = W3;
+        CK(run_gemm(g, st));
+        g.A = ws + w.D3u; g.C = S3;
+        CK(run_gemm(g, st));
+      }
       continue;
     }
 
@@ -521,7 +709,7 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
         TcGemm t = tc0();
         t.batch = (int)inst; t.bdiv = nb; t.M = (int)d; t.N = (int)dh; t.K = L;
         t.A = ws + w.E; t.sAb = PH; t.sAm = 1; t.sAk = d;
-        t.B = ws + w.H; t.sBb = PH; t.sBk = dh; t.sBn = 1;
+        t.B = ws + hid; t.sBb = PH; t.sBk = dh; t.sBn = 1;
         t.kscale = ws + w.U; t.sKb = PH; t.sKb2 = L;
         t.C = X; t.sCb = (long)nb * state; t.sCb2 = state; t.sCm = dh; t.sCn = 1;
         t.alpha = -2.f;
@@ -534,42 +722,50 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
         t.C = X + half; t.sCm = d;
         t.D = p.S + half; t.sDm = d;
         CK(tc_gemm_launch(t, st));
+        if (p.gated) {  // the W3 block, from Delta3 like W2 from Delta
+          t.A = ws + w.D3;
+          t.C = X + 2 * half;
+          t.D = p.S + 2 * half;
+          CK(tc_gemm_launch(t, st));
+        }
       }
       ns_copy_last_kernel<<<ew_grid(state, H), 256, 0, st>>>(p.S, X, state, nb);
       CL();
       // N_n = NS(S_n), per weight block; X0 = S / (||S|| + eps)
-      if (ns_fused_supported((int)d, (int)dh)) {  // every instance on chip for all steps
+      if (ns_fused_supported((int)d, (int)dh) && !p.gated) {  // every instance on chip
         NsArgs n;
         n.X = X; n.inst_stride = state; n.half = half; n.n_inst = (int)inst;
         n.steps = p.ns_steps; n.a = p.ns_a; n.b = p.ns_b; n.c = p.ns_c; n.eps = p.ns_eps;
         n.status = p.status;
         CK(ns_fused_launch(n, st));
       } else {
-      ns_normalize_kernel<<<dim3((unsigned)inst, 2), 256, 0, st>>>(X, state, half, p.ns_eps);
+      ns_normalize_kernel<<<dim3((unsigned)inst, (unsigned)nblk), 256, 0, st>>>(X, state, half,
+                                                                                p.ns_eps);
       CL();
       for (int it = 0; it < p.ns_steps; ++it) {
-        for (int blk = 0; blk < 2; ++blk) {
-          // block 0: W1 (d x dh); block 1: W2 (dh x d); Gram of the short side
+        for (int blk = 0; blk < nblk; ++blk) {
+          // block 0: W1 (d x dh); block 1: W2 (dh x d); block 2 (gated): W3 (dh x d);
+          // Gram of the short side
           const long rows = blk == 0 ? d : dh, cols = blk == 0 ? dh : d;
           const bool wide = rows <= cols;
           const long sm = wide ? rows : cols;
-          const long off = blk == 0 ? 0 : half, aoff = blk * sq;
+          const long off = blk * half, aoff = blk * sq;
           TcGemm g1 = tc0();  // G = X X^T (wide) or X^T X (tall)
           g1.batch = (int)inst; g1.M = (int)sm; g1.N = (int)sm; g1.K = (int)(wide ? cols : rows);
           g1.A = X + off; g1.sAb = state;
           g1.B = X + off; g1.sBb = state;
           if (wide) { g1.sAm = cols; g1.sAk = 1; g1.sBk = 1; g1.sBn = cols; }
           else { g1.sAm = 1; g1.sAk = cols; g1.sBk = cols; g1.sBn = 1; }
-          g1.C = Ag + aoff; g1.sCb = 2 * sq; g1.sCm = sm; g1.sCn = 1;
+          g1.C = Ag + aoff; g1.sCb = nblk * sq; g1.sCm = sm; g1.sCn = 1;
           g1.symmetric = sm == 128;  // both operands are the same tile of X
           CK(tc_gemm_launch(g1, st));
           TcGemm g2 = tc0();  // b G + c G^2
           g2.batch = (int)inst; g2.M = (int)sm; g2.N = (int)sm; g2.K = (int)sm;  // G^2
-          g2.A = Ag + aoff; g2.sAb = 2 * sq; g2.sAm = sm; g2.sAk = 1;
-          g2.B = Ag + aoff; g2.sBb = 2 * sq; g2.sBk = sm; g2.sBn = 1;
-          g2.C = A2 + aoff; g2.sCb = 2 * sq; g2.sCm = sm; g2.sCn = 1;
+          g2.A = Ag + aoff; g2.sAb = nblk * sq; g2.sAm = sm; g2.sAk = 1;
+          g2.B = Ag + aoff; g2.sBb = nblk * sq; g2.sBk = sm; g2.sBn = 1;
+          g2.C = A2 + aoff; g2.sCb = nblk * sq; g2.sCm = sm; g2.sCn = 1;
           g2.alpha = p.ns_c;  // b G + c G^2
-          g2.D = Ag + aoff; g2.sDb = 2 * sq; g2.sDm = sm; g2.sDn = 1; g2.beta = p.ns_b;
+          g2.D = Ag + aoff; g2.sDb = nblk * sq; g2.sDm = sm; g2.sDn = 1; g2.beta = p.ns_b;
           CK(tc_gemm_launch(g2, st));
           // T = a X + (b G + c G^2) X  (wide)  or  a X + X (b G + c G^2)  (tall)
           TcGemm g3 = tc0();
@@ -578,12 +774,12 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
           g3.D = X + off; g3.sDb = state; g3.sDm = cols; g3.sDn = 1; g3.beta = p.ns_a;
           if (wide) {
             g3.K = (int)rows;
-            g3.A = A2 + aoff; g3.sAb = 2 * sq; g3.sAm = sm; g3.sAk = 1;
+            g3.A = A2 + aoff; g3.sAb = nblk * sq; g3.sAm = sm; g3.sAk = 1;
             g3.B = X + off; g3.sBb = state; g3.sBk = cols; g3.sBn = 1;
           } else {
             g3.K = (int)cols;
             g3.A = X + off; g3.sAb = state; g3.sAm = cols; g3.sAk = 1;
-            g3.B = A2 + aoff; g3.sBb = 2 * sq; g3.sBk = sm; g3.sBn = 1;
+            g3.B = A2 + aoff; g3.sBb = nblk * sq; g3.sBk = sm; g3.sBn = 1;
           }
           CK(tc_gemm_launch(g3, st));
         }
@@ -611,8 +807,30 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
       ns_readout_add_kernel<<<ew_grid((long)nb * dh, H), 256, 0, st>>>(
           ws + w.Zq, PH, dh, P, (int)dh, nb, p.alpha, p.N, t0, 1);
       CL();
+      if (p.gated) {  // wq_n = a_n W3_0 q_n + sum_{m<=n} r[n,m] N3_m q_n ; hq = GELU(zq) * wq
+        g = gemm0();
+        g.batch = H; g.M = nb; g.N = (int)dh; g.K = (int)d;
+        g.A = ws + w.Qc; g.sAb = PH; g.sAm = d; g.sAk = 1;
+        g.B = W3; g.sBb = state; g.sBk = 1; g.sBn = d;
+        g.rowscale = ws + w.ta; g.sRb = PH;
+        g.C = ws + w.Wq; g.sCb = PH; g.sCm = dh; g.sCn = 1;
+        CK(run_gemm(g, st));
+        float* P3 = P + inst * dh * nb;
+        TcGemm t = tc0();
+        t.batch = (int)inst; t.bdiv = nb; t.M = (int)dh; t.N = nb; t.K = (int)d;
+        t.A = X + 2 * half; t.sAb = (long)nb * state; t.sAb2 = state; t.sAm = d; t.sAk = 1;
+        t.B = ws + w.Qc; t.sBb = PH; t.sBk = 1; t.sBn = d;
+        t.C = P3; t.sCb = (long)nb * dh * nb; t.sCb2 = dh * nb; t.sCm = nb; t.sCn = 1;
+        CK(tc_gemm_launch(t, st));
+        ns_readout_add_kernel<<<ew_grid((long)nb * dh, H), 256, 0, st>>>(
+            ws + w.Wq, PH, dh, P3, (int)dh, nb, p.alpha, p.N, t0, 0);
+        CL();
+        gate_query_kernel<<<ew_grid((long)nb * dh, H), 256, 0, st>>>(ws, PH, w.Zq, w.Wq,
+                                                                     (long)nb * dh);
+        CL();
+      }
       // y_n = q_n + a_n W1_0 hq_n + sum_{m<=n} r[n,m] N1_m hq_n
-      copy_q_kernel<<<H, 256, 0, st>>>(ws, PH, w.Qc, p.Y, p.N, (int)d, t0, 0, nb);
+      copy_q_kernel<<<H, 256, 0, st>>>(ws, PH, w.Qc, p.Y, p.N, (int)d, t0, 0, nb, p.ln);
       CL();
       g = gemm0();
       g.batch = H; g.M = nb; g.N = (int)d; g.K = (int)dh;
@@ -633,6 +851,11 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
       ns_readout_add_kernel<<<ew_grid((long)nb * d, H), 256, 0, st>>>(
           p.Y + (long)t0 * d, (long)p.N * d, d, R, (int)d, nb, p.alpha, p.N, t0, 0);
       CL();
+      if (p.ln) {
+        ln_readout_kernel<<<dim3((unsigned)((nb + 7) / 8), H), 256, 0, st>>>(ws, PH, w.Qc, p.Y,
+                                                                            p.N, (int)d, t0, nb);
+        CL();
+      }
       // M = a_L M0 + sum_m r[L,m] N_m (after the readout, which used M0)
       ns_state_kernel<<<ew_grid(state, H), 256, 0, st>>>(p.M, state, X, nb, ws, PH, w.ta,
                                                           p.alpha, p.N, t0);

@@ -82,8 +82,6 @@ def _bad(**kw):
     (dict(mem=A.MEM_MLP, d_h=16, d_v=4), A.ERR_INVALID),
     (dict(mem=A.MEM_MLP, d_h=16, loss=A.LOSS_DOT), A.ERR_UNSUPPORTED),
     (dict(mem=4, d_h=16), A.ERR_INVALID),
-    (dict(mem=A.MEM_MLP_LN, d_h=16), A.ERR_UNSUPPORTED),     # oracle only so far
-    (dict(mem=A.MEM_MLP_GATED, d_h=16), A.ERR_UNSUPPORTED),
     (dict(mem=A.MEM_MLP_GATED, d_h=0), A.ERR_INVALID),
     (dict(ns_steps=5), A.ERR_UNSUPPORTED),
     (dict(phi=A.PHI_POLY2, d_k=80), A.ERR_UNSUPPORTED),
@@ -198,3 +196,22 @@ def test_gated_map_degree_beyond_the_maximum_is_rejected(lib):
     assert rc == A.ERR_INVALID
     with pytest.raises(ValueError):
         A.make_cfg(1, 1, 8, 4, 4, phi=A.PHI_POLY, phi_coef=(0, 1, 1, 1, 1, 1))
+
+
+def test_layer_normalised_memory_runs_on_the_cuda_core_mlp_path(lib):
+    from test_memorization_recurrent_gb300.harness import cfg_for
+    w = W.workload(4).with_(mem=W.MEM_MLP_LN)
+    cfg = cfg_for(w, 4, 256)
+    assert A.atlas_mem_path(cfg) == "mlp_simt"
+    assert A.atlas_mem_state_size(cfg) == 2 * 128 * 512
+    assert A.atlas_mem_workspace_bytes(cfg) > 0
+
+
+def test_gated_memory_runs_on_the_cuda_core_mlp_path(lib):
+    from test_memorization_recurrent_gb300.harness import cfg_for
+    for wid in (4, 5):
+        w = W.workload(wid).with_(mem=W.MEM_MLP_GATED)
+        cfg = cfg_for(w, 2, 130)
+        assert A.atlas_mem_path(cfg) == "mlp_simt"
+        assert A.atlas_mem_state_size(cfg) == 3 * 128 * 512
+        assert A.atlas_mem_workspace_bytes(cfg) > 0

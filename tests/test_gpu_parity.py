@@ -379,3 +379,59 @@ def test_gated_polynomial_map(d_k, coef, c, b, N, heads):
     Yg, Mg, Sg = gpu_run(w, inp, with_S=True)
     check(w, Yg, Mg, Yo, Mo, f"gated map {coef}")
     assert rel_err(Sg, So, w.bf16) <= tol(w)
+
+
+# ------------------------------------------- layer-normalised MLP memory
+
+@pytest.mark.parametrize("wid,kw,N,heads", [
+    (4, dict(), 64 + 19, [0, 7]),                        # MLP shape, c = 1, momentum
+    (4, dict(c=3, b=16, d_k=32, d_v=32, d_h=64), 70, [1, 2]),   # window, smaller widths
+    (5, dict(), 64 + 11, [0]),                           # Newton-Schulz, window 256
+    (4, dict(loss=W.LOSS_HUBER, loss_param=0.3), 64 + 5, [3]),  # Huber bias through LN
+])
+def test_layer_normalised_mlp_memory(wid, kw, N, heads):
+    """x + LN(W1 GELU(W2 x)) ("It's All Connected (Miras)": the Moneta / Yaad /
+    Memora memory) on the CUDA-core MLP path against the oracle."""
+    w = W.workload(wid, bounded=True, mem=W.MEM_MLP_LN, **kw)
+    inp = W.generate(w, heads=heads, n_tokens=N)
+    Yo, Mo, So = run_oracle(w, inp)
+    Yg, Mg, Sg = gpu_run(w, inp, with_S=True)
+    check(w, Yg, Mg, Yo, Mo, f"LN memory {kw}")
+    assert rel_err(Sg, So, w.bf16) <= tol(w)
+
+
+def test_layer_normalised_mlp_memory_history_rows():
+    from test_memorization_recurrent_gb300.harness import Runner, to_device
+    import oracle
+    w = W.workload(4, bounded=True, mem=W.MEM_MLP_LN, c=3)
+    N, nh, heads = 60, 2, [0, 5]
+    full = W.generate(w.with_(N=N + nh), heads=heads, n_tokens=N + nh)
+    inp = dict(full)
+    for k in ("Q", "alpha", "eta", "theta"):
+        inp[k] = full[k][:, nh:]
+    Yo, Mo, So = oracle.forward(oracle_cfg(w, N, nh), inp["K"], inp["Q"], inp["V"],
+                                inp["alpha"], inp["eta"], inp["theta"], inp["gamma"], inp["M0"])
+    r = Runner(w, len(heads), N, with_S=True, n_history=nh)
+    Yg, Mg = r(to_device(w, inp))
+    torch.cuda.synchronize()
+    check(w, Yg.cpu().numpy(), Mg.cpu().numpy(), Yo, Mo, "LN history")
+
+
+# ------------------------------------------------ gated (Atlas++) MLP memory
+
+@pytest.mark.parametrize("wid,kw,N,heads", [
+    (4, dict(), 64 + 19, [0, 7]),                               # MLP shape, momentum
+    (4, dict(w_std=0.2), 64 + 19, [4]),                         # a gate far from zero
+    (4, dict(c=3, b=16, d_k=32, d_v=32, d_h=64, w_std=0.2), 70, [1, 2]),  # window
+    (5, dict(), 64 + 11, [0]),                                  # Newton-Schulz on all three blocks
+    (4, dict(loss=W.LOSS_LP, loss_param=3.0), 64 + 5, [3]),     # l_p bias
+])
+def test_gated_mlp_memory(wid, kw, N, heads):
+    """x + W1 (GELU(W2 x) * (W3 x)) (the paperlayer ATLAS summary §5, Atlas++) on the
+    CUDA-core MLP path against the oracle, momentum S included."""
+    w = W.workload(wid, bounded=True, mem=W.MEM_MLP_GATED, **kw)
+    inp = W.generate(w, heads=heads, n_tokens=N)
+    Yo, Mo, So = run_oracle(w, inp)
+    Yg, Mg, Sg = gpu_run(w, inp, with_S=True)
+    check(w, Yg, Mg, Yo, Mo, f"gated memory {kw}")
+    assert rel_err(Sg, So, w.bf16) <= tol(w)

@@ -23,7 +23,7 @@ import numpy as np
 
 BLOCK = 256  # tokens per independently seeded block
 
-MEM_LINEAR, MEM_MLP = 0, 1
+MEM_LINEAR, MEM_MLP, MEM_MLP_LN, MEM_MLP_GATED = 0, 1, 2, 3
 PHI_IDENTITY, PHI_POLY2, PHI_POLY = 0, 1, 2
 LOSS_L2, LOSS_DOT, LOSS_LP, LOSS_HUBER = 0, 1, 2, 3
 
@@ -72,8 +72,10 @@ class Workload:
 
     @property
     def state_size(self) -> int:
-        if self.mem == MEM_MLP:
+        if self.mem in (MEM_MLP, MEM_MLP_LN):
             return 2 * self.d_k * self.d_h
+        if self.mem == MEM_MLP_GATED:
+            return 3 * self.d_k * self.d_h
         return self.d_v * self.D
 
     @property
