@@ -216,7 +216,7 @@ def oracle_sample(w):
     if w.wid == 3:
         return list(range(min(w.heads, cores))), 512 if w.phi != W.PHI_POLY else 128
     if w.wid == 4:
-        return list(range(min(w.heads, cores))), 2048
+        return list(range(min(w.heads, cores))), min(2048, w.N)
     return list(range(min(w.heads, cores))), 16
 
 
@@ -279,9 +279,15 @@ PER_CONFIG = ((1, None), (3, None), (4, None), (5, 1024))
 def variant_workloads():
     """Variants measured beside the five workloads: the gated degree-3 polynomial
     map (input gating a = (0, 1, 1, 1)) on the wide-feature workload's shape with
-    d_k = 16 (D = 968 features), window 64, momentum and decay, bounded step."""
+    d_k = 16 (D = 968 features), window 64, momentum and decay, bounded step; the
+    layer-normalised and the gated MLP memories on the MLP workload's shape (first
+    1024 tokens of all 32 heads; they run on the CUDA-core MLP path)."""
     return [W.workload(3, bounded=True, d_k=16, phi=W.PHI_POLY, phi_coef=(0.0, 1.0, 1.0, 1.0),
-                       N=2048, theta_scale=0.002, name="poly3-gated-omega-c64-bf16")]
+                       N=2048, theta_scale=0.002, name="poly3-gated-omega-c64-bf16"),
+            W.workload(4, bounded=True, mem=W.MEM_MLP_LN, N=1024,
+                       name="mlp-ln-momentum-b64-bf16"),
+            W.workload(4, bounded=True, mem=W.MEM_MLP_GATED, N=1024,
+                       name="mlp-gated-momentum-b64-bf16")]
 
 
 def time_device(w, run, d, steps, warmup, stream, clk=None, world=1):
@@ -346,7 +352,9 @@ def roofline(w, path, kernel_s):
     bytes_launch = tokens * W.bytes_per_token(w) + 2 * 4 * w.heads * w.state_size
     flops_launch = tokens * W.flop_per_token(w)
     ridge = tf * 1e12 / (hbm * 1e9)
-    if path in ("linear_seq", "linear_simt"):  # fp32 FMAs on CUDA cores
+    # fp32 FMAs on CUDA cores: the token-serial and CUDA-core linear kernels, and the
+    # CUDA-core MLP path when no Newton-Schulz products go to the tensor cores
+    if path in ("linear_seq", "linear_simt") or (path == "mlp_simt" and w.ns_steps == 0):
         peak = fp32_alu_peak_tflops()
         achieved = flops_launch / kernel_s / 1e12
         roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

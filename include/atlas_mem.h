@@ -49,10 +49,13 @@ extern "C" {
 /* memory architecture */
 #define ATLAS_MEM_LINEAR 0 /* M: d_v x D matrix, y = M Phi(x) */
 #define ATLAS_MEM_MLP 1    /* M(x) = x + W1 GELU(W2 x), d_k = d_v = d */
-/* Memory variants defined (and pinned) in the oracle, with no kernel here yet:
- * atlas_mem_forward returns ATLAS_ERR_UNSUPPORTED for them. */
-#define ATLAS_MEM_MLP_LN 2    /* x + LN(W1 GELU(W2 x)), plain LN over the d outputs */
-#define ATLAS_MEM_MLP_GATED 3 /* x + W1 (GELU(W2 x) * (W3 x)), W3 d_h x d after W2 */
+/* MLP memory variants ("It's All Connected (Miras)": the Moneta / Yaad / Memora
+ * memory with LN; paperlayer ATLAS summary §5: the Atlas++ gated MLP), any window,
+ * chunk, momentum and Newton-Schulz, on the CUDA-core MLP path: */
+#define ATLAS_MEM_MLP_LN 2    /* x + LN(W1 GELU(W2 x)), plain LN over the d outputs (no
+                                 scale or shift, variance over d, 1e-5 under the root) */
+#define ATLAS_MEM_MLP_GATED 3 /* x + W1 (GELU(W2 x) * (W3 x)), W3 d_h x d after W2; state
+                                 and momentum 3 d d_h; Newton-Schulz on all three blocks */
 /* feature map (linear memory only; the MLP takes x itself) */
 #define ATLAS_PHI_IDENTITY 0 /* D = d_k */
 #define ATLAS_PHI_POLY2 1    /* D = d_k + d_k(d_k+1)/2: [x_i] then [x_i x_j, i<=j, i-major] */
@@ -116,7 +119,8 @@ typedef struct atlas_mem_cfg {
 } atlas_mem_cfg;
 
 /* Number of fp32 entries in one head's memory state (and momentum):
- * linear d_v * D; MLP 2 * d * d_h.  0 for an invalid description. */
+ * linear d_v * D; MLP and LN MLP 2 * d * d_h; gated MLP 3 * d * d_h.  0 for an
+ * invalid description. */
 size_t atlas_mem_state_size(const atlas_mem_cfg* cfg);
 
 /* Bytes of device workspace atlas_mem_forward needs for this description
@@ -132,7 +136,7 @@ size_t atlas_mem_workspace_bytes(const atlas_mem_cfg* cfg);
  *   Y      [B,H,N,d_v]  fp32 out: y_t = M_t(Phi(q_t))
  *   M_final [B,H,state] fp32 in/out: M_0 on entry, M_N on return.  Linear
  *          layout d_v x D row-major; MLP layout W1 (d x d_h) then W2
- *          (d_h x d), both row-major.
+ *          (d_h x d), both row-major (gated: then W3, d_h x d).
  * Returns ATLAS_OK or a negative ATLAS_ERR_* code. */
 int atlas_mem_forward(const void* K, const void* Q, const void* V, const float* alpha,
                       const float* eta, const float* theta, const float* gamma,

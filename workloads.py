@@ -221,6 +221,9 @@ def flop_per_token(w: Workload) -> float:
         return per_chunk / b
     d, dh = w.d_k, w.d_h
     fwd_bwd = 6.0 * L * d * dh            # W2 k, W1 h, W1^T e over the window
+    gate = w.mem == MEM_MLP_GATED         # W3 k over the window, W3 / S3 updates and readouts
+    if gate:
+        fwd_bwd += 2.0 * L * d * dh
     if w.ns_steps:
         # per token: the Newton-Schulz iterations on both momenta (short-side
         # Gram, its square, one apply GEMM each), plus the readout matvecs
@@ -228,6 +231,9 @@ def flop_per_token(w: Workload) -> float:
         return fwd_bwd / b + ns + 4.0 * d * dh
     update = 8.0 * L * d * dh             # rank-L updates of W1, W2, S1, S2
     readout = 8.0 * b * d * dh + 2.0 * b * L * (2 * d + 2 * dh)
+    if gate:
+        update += 4.0 * L * d * dh
+        readout += 4.0 * b * d * dh + 2.0 * b * L * dh
     return (fwd_bwd + update + readout) / b
 
 
