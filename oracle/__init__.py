@@ -27,7 +27,8 @@ _LIB = os.path.join(_HERE, "_build", "libatlas_oracle.so")
 MEM_LINEAR, MEM_MLP, MEM_MLP_LN, MEM_MLP_GATED = 0, 1, 2, 3
 PHI_IDENTITY, PHI_POLY2, PHI_POLY = 0, 1, 2
 PHI_MAX_DEGREE = 4
-LOSS_L2, LOSS_DOT, LOSS_LP, LOSS_HUBER = 0, 1, 2, 3
+LOSS_L2, LOSS_DOT, LOSS_LP, LOSS_HUBER, LOSS_ROBUST = 0, 1, 2, 3, 4
+RET_L2, RET_ELASTIC, RET_BREGMAN, RET_KL, RET_LQ = 0, 1, 2, 3, 4
 
 
 class OrcCfg(ctypes.Structure):
@@ -40,6 +41,7 @@ class OrcCfg(ctypes.Structure):
         ("ns_eps", ctypes.c_double), ("n_history", ctypes.c_int),
         ("loss_param", ctypes.c_double),
         ("phi_degree", ctypes.c_int), ("phi_coef", ctypes.c_double * (PHI_MAX_DEGREE + 1)),
+        ("retention", ctypes.c_int), ("ret_param", ctypes.c_double),
     ]
 
 
@@ -102,16 +104,18 @@ def _f64(a) -> np.ndarray:
 
 def make_cfg(N, d_k, d_v, d_h=0, mem=MEM_LINEAR, phi=PHI_IDENTITY, loss=LOSS_L2, c=1, b=1,
              ns_steps=0, ns_a=0.0, ns_b=0.0, ns_c=0.0, ns_eps=0.0, n_history=0,
-             loss_param=0.0, phi_coef=None) -> OrcCfg:
-    """loss_param: p of the l_p bias, delta of the Huber bias (unused otherwise).
-    phi_coef: a_0 .. a_p of the gated polynomial map (phi = PHI_POLY); p = len - 1."""
+             loss_param=0.0, phi_coef=None, retention=RET_L2, ret_param=0.0) -> OrcCfg:
+    """loss_param: p of the l_p bias, delta of the Huber bias, Delta of the robust
+    bias (unused otherwise).  phi_coef: a_0 .. a_p of the gated polynomial map
+    (phi = PHI_POLY); p = len - 1.  retention / ret_param: the retention gate and
+    its parameter (gamma of RET_ELASTIC, c of RET_KL, q of RET_LQ)."""
     coef = list(phi_coef or [])
     arr = (ctypes.c_double * (PHI_MAX_DEGREE + 1))(*([float(a) for a in coef] +
                                                      [0.0] * (PHI_MAX_DEGREE + 1 - len(coef))))
     return OrcCfg(int(N), int(d_k), int(d_v), int(d_h), int(mem), int(phi), int(loss),
                   int(c), int(b), int(ns_steps), float(ns_a), float(ns_b), float(ns_c),
                   float(ns_eps), int(n_history), float(loss_param),
-                  max(0, len(coef) - 1), arr)
+                  max(0, len(coef) - 1), arr, int(retention), float(ret_param))
 
 
 def feature_dim(cfg: OrcCfg) -> int:

@@ -61,7 +61,23 @@
  *   - the Huber bias is taken per coordinate with one threshold delta for all
  *     tokens, scaled to agree with the l2 bias inside the threshold:
  *     h(e) = e^2 for |e| <= delta, 2 delta |e| - delta^2 beyond (the pages let
- *     delta vary per token and channel; a constant is the plainest case).
+ *     delta vary per token and channel; a constant is the plainest case);
+ *   - the value-shift robust bias ([Miras] #1: the worst case over a shift of v
+ *     within radius Delta, closed form 1/2 ||e||^2 + Delta ||e|| + 1/2 Delta^2)
+ *     is scaled by 2 like the Huber bias, ||e||^2 + 2 Delta ||e|| + Delta^2, so
+ *     Delta = 0 is the l2 bias; its gradient 2 e (1 + Delta / ||e||) is 0 at e = 0;
+ *   - retention gates ([Miras] #2 Alternative Retention Gates, linear memory):
+ *     the l2 gate's step U = (1 - alpha_t) M_{t-1} + S_t becomes
+ *       elastic net: M_t = sign(U) max(|U| - gamma, 0) (soft thresholding);
+ *       Bregman with a sigmoid link: M_t = sigmoid((1 - alpha_t) logit(M_{t-1}) + S_t);
+ *       KL: each row of M a distribution of mass c,
+ *           M_t = c softmax((1 - alpha_t) log M_{t-1} + S_t) per row;
+ *       l_q (Moneta): the state is the accumulator A_t = (1 - alpha_t) A_{t-1} + S_t
+ *           and the memory is A / ||A||_q^(q-2) per row, the normaliser taken at
+ *           each chunk start ("Moneta applies the l_q normalisation at the chunk
+ *           end"; b = 1 renormalises every token);
+ *     alpha_t keeps its role of retention strength and S_t the (momentum) step;
+ *     the rows are the memory's output rows (one per value coordinate);
  */
 #include <math.h>
 #include <pthread.h>
@@ -82,6 +98,13 @@
 #define ORC_LOSS_DOT 1
 #define ORC_LOSS_LP 2
 #define ORC_LOSS_HUBER 3
+#define ORC_LOSS_ROBUST 4   /* value-shift robust bias, radius loss_param */
+/* retention gates (linear memory): the map from the decayed step to the new state */
+#define ORC_RET_L2 0        /* M = (1 - alpha) M + S */
+#define ORC_RET_ELASTIC 1   /* then soft thresholding by ret_param */
+#define ORC_RET_BREGMAN 2   /* M = sigmoid((1 - alpha) logit(M) + S) */
+#define ORC_RET_KL 3        /* per row: M = c softmax((1 - alpha) log M + S), c = ret_param */
+#define ORC_RET_LQ 4        /* A = (1 - alpha) A + S, memory A / ||A||_q^(q-2) per row, q = ret_param */
 
 /* Per-head problem description.  All tensors handed to the oracle are fp64,
  * one head after another. */
@@ -102,6 +125,8 @@ typedef struct {
   double loss_param; /* p of the l_p bias (>= 1), delta of the Huber bias (> 0) */
   int phi_degree;    /* ORC_PHI_POLY: highest degree p (1..ORC_PHI_MAX_DEGREE) */
   double phi_coef[ORC_PHI_MAX_DEGREE + 1]; /* ORC_PHI_POLY: a_0 .. a_p */
+  int retention;     /* ORC_RET_* (linear memory; ORC_RET_L2 for the MLP memories) */
+  double ret_param;  /* gamma of ELASTIC, c of KL, q of LQ */
 } orc_cfg;
 
 /* ------------------------------------------------------------------ sizes */
@@ -296,6 +321,20 @@ static double orc_bias_dy(const orc_cfg* g, double e) {
   return 2.0 * e;
 }
 
+/* Derivative of the bias with respect to the whole output vector y (n entries),
+ * e = y - v: orc_bias_dy per coordinate, or the robust bias
+ * 2 e (1 + Delta / ||e||) (0 at e = 0). */
+static void orc_bias_vec(const orc_cfg* g, const double* e, int n, double* out) {
+  if (g->loss == ORC_LOSS_ROBUST) {
+    double ne = 0.0;
+    for (int r = 0; r < n; ++r) ne += e[r] * e[r];
+    ne = sqrt(ne);
+    for (int r = 0; r < n; ++r) out[r] = ne > 0.0 ? 2.0 * e[r] * (1.0 + g->loss_param / ne) : 0.0;
+    return;
+  }
+  for (int r = 0; r < n; ++r) out[r] = orc_bias_dy(g, e[r]);
+}
+
 /* Gradient of the attentional bias with respect to the memory state, written
  * into G (state layout).
  *   l2  ([Titans] Objective; [ATLAS] §3.1):  l = ||M(Phi(k)) - v||^2.
@@ -315,9 +354,10 @@ void orc_grad(const orc_cfg* g, const double* state, const double* k, const doub
       } else {
         double s = 0.0;
         for (int j = 0; j < D; ++j) s += state[(long)r * D + j] * f[j];
-        e[r] = orc_bias_dy(g, s - v[r]);  /* l2: dl/d(M Phi) = 2 (M Phi - v) */
+        e[r] = s - v[r];
       }
     }
+    if (g->loss != ORC_LOSS_DOT) orc_bias_vec(g, e, dv, e);  /* l2: 2 (M Phi - v) */
     for (int r = 0; r < dv; ++r)
       for (int j = 0; j < D; ++j) G[(long)r * D + j] = e[r] * f[j];
     free(f);
@@ -337,8 +377,8 @@ void orc_grad(const orc_cfg* g, const double* state, const double* k, const doub
   double* du = (double*)malloc(sizeof(double) * d);
   double is = 1.0;
   orc_mlp_forward(g, state, k, z, w, h, o, &is);
-  for (int r = 0; r < d; ++r)
-    dy[r] = g->loss == ORC_LOSS_DOT ? -2.0 * v[r] : orc_bias_dy(g, k[r] + o[r] - v[r]);
+  for (int r = 0; r < d; ++r) dy[r] = g->loss == ORC_LOSS_DOT ? -2.0 * v[r] : k[r] + o[r] - v[r];
+  if (g->loss != ORC_LOSS_DOT) orc_bias_vec(g, dy, d, dy);
   /* through LN: du = is (dy - mean(dy) - n mean(dy * n)), n = the normalised values */
   if (g->mem == ORC_MEM_MLP_LN) {
     double m1 = 0.0, m2 = 0.0;
@@ -440,16 +480,88 @@ static void orc_momentum_update(const orc_cfg* g, const double* S, double* out) 
 
 /* ------------------------------------------------------- one head, one token */
 
-/* Shared token step: S = eta S - theta g; M = (1 - alpha) M + U(S);
- * y = M(Phi(q)).  ([Titans] Surprise Metric, Forgetting Mechanism, Retrieving.) */
+/* l_q gate: per-row normalisers z_r = ||A_r||_q^(q-2) of the accumulator A. */
+static void orc_lq_norms(const orc_cfg* g, const double* A, double* z) {
+  int D = orc_feature_dim(g);
+  double q = g->ret_param;
+  for (int r = 0; r < g->d_v; ++r) {
+    double s = 0.0;
+    for (int j = 0; j < D; ++j) s += pow(fabs(A[(long)r * D + j]), q);
+    z[r] = s > 0.0 ? pow(s, (q - 2.0) / q) : 0.0;
+  }
+}
+
+/* The memory a state describes: the state itself, or for the l_q gate the
+ * accumulator divided per row by its normalisers (a zero row stays zero). */
+static void orc_memory_of(const orc_cfg* g, const double* M, const double* z, double* W) {
+  long n = orc_state_size(g);
+  if (g->retention != ORC_RET_LQ) {
+    memcpy(W, M, sizeof(double) * n);
+    return;
+  }
+  int D = orc_feature_dim(g);
+  for (int r = 0; r < g->d_v; ++r)
+    for (int j = 0; j < D; ++j) {
+      long x = (long)r * D + j;
+      W[x] = z[r] > 0.0 ? M[x] / z[r] : M[x];
+    }
+}
+
+/* The retention gate's map from the state and the step to the new state
+ * ([Titans] Forgetting Mechanism for the l2 gate; [Miras] #2 Alternative
+ * Retention Gates for the others, read as described at the top). */
+static void orc_retain(const orc_cfg* g, double alpha, const double* upd, double* M) {
+  long n = orc_state_size(g);
+  switch (g->retention) {
+    case ORC_RET_ELASTIC:
+      for (long j = 0; j < n; ++j) {
+        double u = (1.0 - alpha) * M[j] + upd[j];
+        double m = fabs(u) - g->ret_param;
+        M[j] = m > 0.0 ? (u > 0.0 ? m : -m) : 0.0;
+      }
+      return;
+    case ORC_RET_BREGMAN:
+      for (long j = 0; j < n; ++j) {
+        double u = (1.0 - alpha) * log(M[j] / (1.0 - M[j])) + upd[j];
+        M[j] = 1.0 / (1.0 + exp(-u));
+      }
+      return;
+    case ORC_RET_KL: {
+      int D = orc_feature_dim(g);
+      for (int r = 0; r < g->d_v; ++r) {
+        double* m = M + (long)r * D;
+        const double* u = upd + (long)r * D;
+        double mx = -INFINITY;
+        for (int j = 0; j < D; ++j) {
+          m[j] = (1.0 - alpha) * log(m[j]) + u[j];
+          if (m[j] > mx) mx = m[j];
+        }
+        double s = 0.0;
+        for (int j = 0; j < D; ++j) {
+          m[j] = exp(m[j] - mx);
+          s += m[j];
+        }
+        for (int j = 0; j < D; ++j) m[j] *= g->ret_param / s;
+      }
+      return;
+    }
+    default:  /* l2 and the l_q accumulator */
+      for (long j = 0; j < n; ++j) M[j] = (1.0 - alpha) * M[j] + upd[j];
+  }
+}
+
+/* Shared token step: S = eta S - theta g; M = retain(M, U(S)); y = memory(M)(Phi(q)).
+ * ([Titans] Surprise Metric, Forgetting Mechanism, Retrieving.)  z: the l_q
+ * gate's normalisers of the current chunk (else unused); W: scratch. */
 static void orc_token_step(const orc_cfg* g, double alpha, double eta, double theta,
                            const double* grad, const double* q, double* M, double* S,
-                           double* upd, double* y) {
+                           double* upd, double* y, const double* z, double* W) {
   long n = orc_state_size(g);
   for (long j = 0; j < n; ++j) S[j] = eta * S[j] - theta * grad[j];
   orc_momentum_update(g, S, upd);
-  for (long j = 0; j < n; ++j) M[j] = (1.0 - alpha) * M[j] + upd[j];
-  orc_memory_apply(g, M, q, y);
+  orc_retain(g, alpha, upd, M);
+  orc_memory_of(g, M, z, W);
+  orc_memory_apply(g, W, q, y);
 }
 
 /* Chunked Omega rule for one head ([ATLAS] §3.3, [Miras] Training): for every
@@ -464,10 +576,14 @@ static void orc_head_chunked(const orc_cfg* g, const double* K, const double* Q,
   double* gsum = (double*)malloc(sizeof(double) * n);
   double* Gi = (double*)malloc(sizeof(double) * n);
   double* upd = (double*)malloc(sizeof(double) * n);
+  double* W = (double*)malloc(sizeof(double) * n);
+  double* z = (double*)malloc(sizeof(double) * (g->d_v > 0 ? g->d_v : 1));
   int dk = g->d_k, dv = g->d_v, nh = g->n_history;
   /* K, V rows: token i (from -nh) is row i + nh */
   for (int t0 = 0; t0 < g->N; t0 += g->b) {
-    memcpy(M0, M, sizeof(double) * n);
+    /* the chunk-start memory (the l_q gate renormalises here only) */
+    if (g->retention == ORC_RET_LQ) orc_lq_norms(g, M, z);
+    orc_memory_of(g, M, z, M0);
     int t1 = t0 + g->b < g->N ? t0 + g->b : g->N;
     for (int t = t0; t < t1; ++t) {
       for (long j = 0; j < n; ++j) gsum[j] = 0.0;
@@ -478,13 +594,15 @@ static void orc_head_chunked(const orc_cfg* g, const double* K, const double* Q,
         for (long j = 0; j < n; ++j) gsum[j] += w * Gi[j];
       }
       orc_token_step(g, alpha[t], eta[t], theta[t], gsum, Q + (long)t * dk, M, S, upd,
-                     Y + (long)t * dv);
+                     Y + (long)t * dv, z, W);
     }
   }
   free(M0);
   free(gsum);
   free(Gi);
   free(upd);
+  free(W);
+  free(z);
 }
 
 /* Token recurrence for one head, written separately from the chunked loop:
@@ -498,20 +616,29 @@ static void orc_head_recurrent(const orc_cfg* g, const double* K, const double* 
   double* gsum = (double*)malloc(sizeof(double) * n);
   double* Gi = (double*)malloc(sizeof(double) * n);
   double* upd = (double*)malloc(sizeof(double) * n);
+  double* W = (double*)malloc(sizeof(double) * n);
+  double* Wt = (double*)malloc(sizeof(double) * n);
+  double* z = (double*)malloc(sizeof(double) * (g->d_v > 0 ? g->d_v : 1));
   int dk = g->d_k, dv = g->d_v, nh = g->n_history;
   for (int t = 0; t < g->N; ++t) {
+    /* the memory before the token (the l_q gate renormalises every token) */
+    if (g->retention == ORC_RET_LQ) orc_lq_norms(g, M, z);
+    orc_memory_of(g, M, z, Wt);
     for (long j = 0; j < n; ++j) gsum[j] = 0.0;
     for (int lag = 0; lag < g->c && t - lag >= -nh; ++lag) {
       int i = t - lag;
-      orc_grad(g, M, K + (long)(i + nh) * dk, V + (long)(i + nh) * dv, Gi);
+      orc_grad(g, Wt, K + (long)(i + nh) * dk, V + (long)(i + nh) * dv, Gi);
       for (long j = 0; j < n; ++j) gsum[j] += gamma[lag] * Gi[j];
     }
     orc_token_step(g, alpha[t], eta[t], theta[t], gsum, Q + (long)t * dk, M, S, upd,
-                   Y + (long)t * dv);
+                   Y + (long)t * dv, z, W);
   }
   free(gsum);
   free(Gi);
   free(upd);
+  free(W);
+  free(Wt);
+  free(z);
 }
 
 /* ----------------------------------------------------- threads over heads */
@@ -552,7 +679,15 @@ static int orc_check(const orc_cfg* g) {
   if (g->n_history < 0) return -1;
   if (g->mem < ORC_MEM_LINEAR || g->mem > ORC_MEM_MLP_GATED) return -1;
   if (g->mem != ORC_MEM_LINEAR && (g->d_h <= 0 || g->d_k != g->d_v)) return -1;
-  if (g->loss < ORC_LOSS_L2 || g->loss > ORC_LOSS_HUBER) return -1;
+  if (g->loss < ORC_LOSS_L2 || g->loss > ORC_LOSS_ROBUST) return -1;
+  if (g->loss == ORC_LOSS_ROBUST && !(g->loss_param >= 0.0)) return -1;
+  if (g->retention < ORC_RET_L2 || g->retention > ORC_RET_LQ) return -1;
+  if (g->retention != ORC_RET_L2) {
+    if (g->mem != ORC_MEM_LINEAR || g->ns_steps > 0) return -1;
+    if (g->retention == ORC_RET_ELASTIC && !(g->ret_param >= 0.0)) return -1;
+    if (g->retention == ORC_RET_KL && !(g->ret_param > 0.0)) return -1;
+    if (g->retention == ORC_RET_LQ && !(g->ret_param >= 1.0)) return -1;
+  }
   if (g->loss == ORC_LOSS_LP && !(g->loss_param >= 1.0 && g->loss_param < 1e6)) return -1;
   if (g->loss == ORC_LOSS_HUBER && !(g->loss_param > 0.0)) return -1;
   if (g->phi == ORC_PHI_POLY) {
@@ -724,6 +859,7 @@ static void orc_chunk_forward(const orc_cfg* g, int t0, int t1, const double* K,
   double* Gi = (double*)malloc(sizeof(double) * n);
   double* upd = (double*)malloc(sizeof(double) * n);
   double* y = (double*)malloc(sizeof(double) * dv);
+  double* W = (double*)malloc(sizeof(double) * n);
   memcpy(M0, M, sizeof(double) * n);
   for (int t = t0; t < t1; ++t) {
     for (long j = 0; j < n; ++j) gsum[j] = 0.0;
@@ -737,13 +873,14 @@ static void orc_chunk_forward(const orc_cfg* g, int t0, int t1, const double* K,
       memcpy(Sb + (long)(t - t0) * n, S, sizeof(double) * n);
       memcpy(Gs + (long)(t - t0) * n, gsum, sizeof(double) * n);
     }
-    orc_token_step(g, alpha[t], eta[t], theta[t], gsum, Q + (long)t * dk, M, S, upd, y);
+    orc_token_step(g, alpha[t], eta[t], theta[t], gsum, Q + (long)t * dk, M, S, upd, y, NULL, W);
   }
   free(M0);
   free(gsum);
   free(Gi);
   free(upd);
   free(y);
+  free(W);
 }
 
 /* Reverse pass of one head.  In: the forward inputs, M and S at the start
@@ -885,6 +1022,7 @@ int orc_backward_chunked(const orc_cfg* g, int n_heads, const double* K, const d
                          double* dgamma, int n_threads) {
   if (orc_check(g) != 0 || n_heads < 0) return -1;
   if (g->mem != ORC_MEM_LINEAR || g->ns_steps > 0) return -1;
+  if (g->retention != ORC_RET_L2 || g->loss == ORC_LOSS_ROBUST) return -1;
   if (n_threads <= 0) n_threads = (int)sysconf(_SC_NPROCESSORS_ONLN);
   if (n_threads > n_heads) n_threads = n_heads;
   if (n_threads < 1) n_threads = 1;

@@ -13,6 +13,8 @@ Two independent checks:
   Memory & Attentional Bias), whose gradients with respect to K, Q, V and the
   three gates follow from the masked products written out below.
 """
+import zlib
+
 import numpy as np
 import pytest
 
@@ -57,7 +59,7 @@ CASES = {
 @pytest.mark.parametrize("case", sorted(CASES))
 def test_backward_matches_finite_differences(case):
     cfg = oracle.make_cfg(**CASES[case])
-    x = _inputs(cfg, seed=hash(case) % 1000)
+    x = _inputs(cfg, seed=zlib.crc32(case.encode()) % 1000)  # fixed across processes
     r = np.random.default_rng(5)
     ns = oracle.state_size(cfg)
     dY = r.standard_normal((H, cfg.N, cfg.d_v))
@@ -79,7 +81,10 @@ def test_backward_matches_finite_differences(case):
             arr[idx] = old
             fd = (lp - lm) / (2 * h)
             an = g[gname][idx]
-            assert abs(fd - an) <= 1e-6 * max(1.0, abs(fd)), (case, name, idx, fd, an)
+            # central differences with h = 1e-6; the l_p and Huber biases are not
+            # smooth to third order at e = 0 / |e| = delta, hence 1e-5, still far
+            # below the O(1) relative error of a dropped or mis-signed term
+            assert abs(fd - an) <= 1e-5 * max(1.0, abs(fd)), (case, name, idx, fd, an)
 
 
 @pytest.mark.parametrize("b", [1, 5])
