@@ -24,8 +24,9 @@
  *     (paperlayer summary): 5 Memory Optimization (Muon / Newton-Schulz),
  *     App. E (2-layer residual MLP memory, GELU).
  *   "It's All Connected: ... (Miras)": Associative Memory & Attentional Bias
- *     (dot-product bias = linear attention), Training (chunk-wise
- *     parallelisation; the layer outputs M(q_t)).
+ *     (dot-product bias = linear attention), #1 Alternative Attentional Biases
+ *     (l_p, Huber, robust), #2 Alternative Retention Gates, Training
+ *     (chunk-wise parallelisation; the layer outputs M(q_t)).
  *
  * Conventions shared by every entry point:
  *   - All tensor arguments are DEVICE pointers owned by the caller, contiguous,
@@ -77,6 +78,32 @@ extern "C" {
 #define ATLAS_LOSS_LP 2    /* sum |e|^p, p = loss_param >= 1 (gradient p |e|^(p-1) sign e) */
 #define ATLAS_LOSS_HUBER 3 /* sum e^2 for |e| <= delta, 2 delta |e| - delta^2 beyond, with
                               delta = loss_param > 0 (gradient 2 clamp(e, -delta, delta)) */
+/* Robust bias against a value shift of norm at most Delta = loss_param >= 0,
+ * read as its worst case (||e|| + Delta)^2 over the whole value vector e:
+ * gradient 2 e (1 + Delta / ||e||), 0 at e = 0.  Delta = 0 is ATLAS_LOSS_L2.
+ * Couples the d_v coordinates of a token, so the CUDA-core kernels run it
+ * (linear memory: one CTA holds all d_v rows of a head). */
+#define ATLAS_LOSS_ROBUST 4
+/* Retention gate of the linear memory ("It's All Connected: ... (Miras)", #2
+ * Alternative Retention Gates), the map from (M_{t-1}, alpha_t, U_t), U_t the
+ * momentum's contribution S_t, to M_t.  Every gate other than ATLAS_RET_L2
+ * takes the identity or degree-2 map or the gated polynomial map, no
+ * Newton-Schulz, and runs on the CUDA-core linear kernel; elastic net, Bregman
+ * and KL walk the tokens of a chunk one by one (the map is not linear in the
+ * gradients), l_q keeps the chunk tables.  ret_param is the gate's parameter. */
+#define ATLAS_RET_L2 0      /* M = (1 - alpha) M + U */
+#define ATLAS_RET_ELASTIC 1 /* then soft thresholding: M = sign(u) max(|u| - lambda, 0),
+                               lambda = ret_param >= 0 (the proximal step of an l1 term) */
+#define ATLAS_RET_BREGMAN 2 /* Bregman retention with the sigmoid link: M = sigmoid(
+                               (1 - alpha) logit(M) + U), entries in (0, 1); M_0 must lie
+                               in (0, 1) (entries outside give NaN); ret_param unused */
+#define ATLAS_RET_KL 3      /* per row: M = c softmax((1 - alpha) log M + U), c = ret_param
+                               > 0 the row mass; M_0 entries must be > 0 */
+#define ATLAS_RET_LQ 4      /* l_q memory (Moneta): A = (1 - alpha) A + U is the state
+                               (M_final holds A), the memory reads A_r / ||A_r||_q^(q-2)
+                               per row r (a zero row stays zero), q = ret_param in
+                               [1, 1e6); the normaliser is taken at each chunk start and
+                               held over the chunk (every token when b = 1) */
 /* K, Q, V element type */
 #define ATLAS_F32 0
 #define ATLAS_BF16 1
@@ -95,7 +122,8 @@ typedef struct atlas_mem_cfg {
   int mem;            /* ATLAS_MEM_* */
   int phi;            /* ATLAS_PHI_* */
   int loss;           /* ATLAS_LOSS_* */
-  float loss_param;   /* p of ATLAS_LOSS_LP, delta of ATLAS_LOSS_HUBER; unused otherwise */
+  float loss_param;   /* p of ATLAS_LOSS_LP, delta of ATLAS_LOSS_HUBER, Delta of
+                         ATLAS_LOSS_ROBUST; unused otherwise */
   int c;              /* Omega window length (>= 1); gamma has c entries */
   int b;              /* chunk length (>= 1); 1 = token recurrence */
   int ns_steps;       /* Newton-Schulz iterations on the momentum, 0 = plain momentum */
@@ -116,6 +144,8 @@ typedef struct atlas_mem_cfg {
                          whose bounded wait ran out (never cleared by the library) */
   int phi_degree;     /* ATLAS_PHI_POLY: p, 1..ATLAS_PHI_MAX_DEGREE (ignored otherwise) */
   float phi_coef[ATLAS_PHI_MAX_DEGREE + 1]; /* ATLAS_PHI_POLY: a_0 .. a_p */
+  int retention;      /* ATLAS_RET_* (linear memory; ATLAS_RET_L2 otherwise) */
+  float ret_param;    /* lambda, c or q of the gate (see ATLAS_RET_*) */
 } atlas_mem_cfg;
 
 /* Number of fp32 entries in one head's memory state (and momentum):

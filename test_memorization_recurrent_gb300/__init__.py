@@ -18,7 +18,8 @@ LIB_PATH = os.path.join(HERE, "_build", "libatlasmem.so")
 MEM_LINEAR, MEM_MLP, MEM_MLP_LN, MEM_MLP_GATED = 0, 1, 2, 3
 PHI_IDENTITY, PHI_POLY2, PHI_POLY = 0, 1, 2
 PHI_MAX_DEGREE = 4
-LOSS_L2, LOSS_DOT, LOSS_LP, LOSS_HUBER = 0, 1, 2, 3
+LOSS_L2, LOSS_DOT, LOSS_LP, LOSS_HUBER, LOSS_ROBUST = 0, 1, 2, 3, 4
+RET_L2, RET_ELASTIC, RET_BREGMAN, RET_KL, RET_LQ = 0, 1, 2, 3, 4
 F32, BF16 = 0, 1
 
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
@@ -42,6 +43,7 @@ class AtlasMemCfg(ctypes.Structure):
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("status_dev", ctypes.c_void_p),
         ("phi_degree", ctypes.c_int), ("phi_coef", ctypes.c_float * (PHI_MAX_DEGREE + 1)),
+        ("retention", ctypes.c_int), ("ret_param", ctypes.c_float),
     ]
 
 
@@ -97,9 +99,12 @@ def load_library(path: str = LIB_PATH):
 def make_cfg(B, H, N, d_k, d_v, d_h=0, mem=MEM_LINEAR, phi=PHI_IDENTITY, loss=LOSS_L2, c=1,
              b=1, ns_steps=0, ns_a=0.0, ns_b=0.0, ns_c=0.0, ns_eps=0.0, in_dtype=BF16,
              S_state=None, workspace=None, workspace_bytes=0, status_dev=None,
-             n_history=0, loss_param=0.0, phi_coef=None) -> AtlasMemCfg:
-    """loss_param: p of LOSS_LP, delta of LOSS_HUBER (unused otherwise).
-    phi_coef: a_0 .. a_p of the gated polynomial map (phi = PHI_POLY); p = len - 1."""
+             n_history=0, loss_param=0.0, phi_coef=None, retention=RET_L2,
+             ret_param=0.0) -> AtlasMemCfg:
+    """loss_param: p of LOSS_LP, delta of LOSS_HUBER, Delta of LOSS_ROBUST (unused
+    otherwise).  phi_coef: a_0 .. a_p of the gated polynomial map (phi = PHI_POLY);
+    p = len - 1.  retention / ret_param: the linear memory's retention gate and its
+    parameter (lambda of RET_ELASTIC, c of RET_KL, q of RET_LQ)."""
     coef = [float(a) for a in (phi_coef or [])]
     if len(coef) > PHI_MAX_DEGREE + 1:
         raise ValueError(f"at most {PHI_MAX_DEGREE + 1} coefficients (degree {PHI_MAX_DEGREE})")
@@ -109,7 +114,7 @@ def make_cfg(B, H, N, d_k, d_v, d_h=0, mem=MEM_LINEAR, phi=PHI_IDENTITY, loss=LO
                        float(ns_b),
                        float(ns_c), float(ns_eps), int(in_dtype), _ptr(S_state), int(n_history),
                        _ptr(workspace), int(workspace_bytes), _ptr(status_dev),
-                       max(0, len(coef) - 1), arr)
+                       max(0, len(coef) - 1), arr, int(retention), float(ret_param))
 
 
 def _ptr(t):

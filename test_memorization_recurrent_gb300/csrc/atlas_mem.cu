@@ -54,7 +54,16 @@ int check_cfg(const atlas_mem_cfg* c) {
     if (D < 1) return ATLAS_ERR_INVALID;
     if (D > 16384) return ATLAS_ERR_UNSUPPORTED;
   }
-  if (c->loss < ATLAS_LOSS_L2 || c->loss > ATLAS_LOSS_HUBER) return ATLAS_ERR_INVALID;
+  if (c->loss < ATLAS_LOSS_L2 || c->loss > ATLAS_LOSS_ROBUST) return ATLAS_ERR_INVALID;
+  if (c->loss == ATLAS_LOSS_ROBUST && !(c->loss_param >= 0.f && c->loss_param < 3e38f))
+    return ATLAS_ERR_INVALID;
+  if (c->retention < ATLAS_RET_L2 || c->retention > ATLAS_RET_LQ) return ATLAS_ERR_INVALID;
+  if (c->retention == ATLAS_RET_ELASTIC && !(c->ret_param >= 0.f && c->ret_param < 3e38f))
+    return ATLAS_ERR_INVALID;
+  if (c->retention == ATLAS_RET_KL && !(c->ret_param > 0.f && c->ret_param < 3e38f))
+    return ATLAS_ERR_INVALID;
+  if (c->retention == ATLAS_RET_LQ && !(c->ret_param >= 1.f && c->ret_param < 1e6f))
+    return ATLAS_ERR_INVALID;
   if (c->loss == ATLAS_LOSS_LP && !(c->loss_param >= 1.f && c->loss_param < 1e6f))
     return ATLAS_ERR_INVALID;
   if (c->loss == ATLAS_LOSS_HUBER && !(c->loss_param > 0.f && c->loss_param < 3e38f))
@@ -66,6 +75,7 @@ int check_cfg(const atlas_mem_cfg* c) {
     if (c->d_h <= 0 || c->d_k != c->d_v) return ATLAS_ERR_INVALID;
     if (c->phi != ATLAS_PHI_IDENTITY) return ATLAS_ERR_INVALID;
     if (c->loss == ATLAS_LOSS_DOT) return ATLAS_ERR_UNSUPPORTED;
+    if (c->retention != ATLAS_RET_L2) return ATLAS_ERR_UNSUPPORTED;
   } else {
     if (c->ns_steps > 0) return ATLAS_ERR_UNSUPPORTED;
     if (c->phi == ATLAS_PHI_POLY2 && c->d_k > 64) return ATLAS_ERR_UNSUPPORTED;
@@ -91,6 +101,8 @@ LinArgs lin_args(const void* K, const void* Q, const void* V, const float* alpha
   a.pgen = c->phi == ATLAS_PHI_POLY;
   a.pdeg = a.pgen ? c->phi_degree : 0;
   for (int e = 0; e < 5; ++e) a.pcoef[e] = (a.pgen && e <= c->phi_degree) ? c->phi_coef[e] : 0.f;
+  a.ret = c->retention;
+  a.rp = c->ret_param;
   return a;
 }
 
@@ -126,7 +138,8 @@ Path choose_path(const atlas_mem_cfg* c) {
   }
   LinArgs a = lin_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, c,
                        nullptr, nullptr);
-  if (a.pgen) {  // the gated polynomial map: CUDA-core kernel only
+  // the gated polynomial map, the retention gates and the robust bias: CUDA-core kernel only
+  if (a.pgen || a.ret != ATLAS_RET_L2 || a.lk == ATLAS_LOSS_ROBUST) {
     int RV;
     size_t smem;
     return linear_simt_plan(a, c->B * c->H, &RV, &smem) == ATLAS_OK ? PATH_LINEAR_SIMT
@@ -254,6 +267,7 @@ int backward_plan(const atlas_mem_cfg* cfg, LinArgs* out) {
   if (cfg->mem != ATLAS_MEM_LINEAR || cfg->ns_steps > 0) return ATLAS_ERR_UNSUPPORTED;
   if (cfg->loss != ATLAS_LOSS_L2 && cfg->loss != ATLAS_LOSS_LP && cfg->loss != ATLAS_LOSS_HUBER)
     return ATLAS_ERR_UNSUPPORTED;
+  if (cfg->retention != ATLAS_RET_L2) return ATLAS_ERR_UNSUPPORTED;
   *out = lin_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, cfg, nullptr,
                   nullptr);
   return linear_bwd_supported(*out) ? ATLAS_OK : ATLAS_ERR_UNSUPPORTED;

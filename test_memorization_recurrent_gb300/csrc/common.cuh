@@ -33,10 +33,17 @@ __device__ __forceinline__ float lp_grad(float e, float p) {
 __device__ __forceinline__ float huber_grad(float e, float delta) {
   return fminf(fmaxf(e, -delta), delta);
 }
+// Half the bias's derivative per coordinate (l2: e).  The robust bias returns e
+// here and is finished per token by robust_scale, since it needs ||e||.
 __device__ __forceinline__ float bias_grad(float e, int kind, float prm) {
   if (kind == ATLAS_LOSS_LP) return lp_grad(e, prm);
   if (kind == ATLAS_LOSS_HUBER) return huber_grad(e, prm);
   return e;
+}
+// Robust bias ("It's All Connected (Miras)", #1 Alternative Attentional Biases,
+// read as (||e|| + Delta)^2): half its gradient is e (1 + Delta / ||e||), 0 at e = 0.
+__device__ __forceinline__ float robust_scale(float norm, float delta) {
+  return norm > 0.f ? 1.f + delta / norm : 0.f;
 }
 
 // Feature j of Phi(x) for x in shared memory.  Degree-2 map (ATLAS review

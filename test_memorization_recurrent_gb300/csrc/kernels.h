@@ -19,12 +19,14 @@ struct LinArgs {
   float* S;  // [heads, d_v, D] in/out, or nullptr (start at zero, not returned)
   int N, d_k, d_v, D, c, b;
   int poly, dot, bf16;
-  int lk;    // attentional bias: 0 l2, 1 dot, 2 l_p, 3 Huber (ATLAS_LOSS_*)
+  int lk;    // attentional bias: 0 l2, 1 dot, 2 l_p, 3 Huber, 4 robust (ATLAS_LOSS_*)
   float lp;  // its parameter (p, delta)
   int nh;  // history rows ahead of token 0 in K and V (head stride (nh + N) rows)
   int pgen;        // gated polynomial map of degree pdeg (poly is 0 then)
   int pdeg;
   float pcoef[5];  // a_0 .. a_pdeg
+  int ret;         // retention gate (ATLAS_RET_*)
+  float rp;        // its parameter (lambda, c, q)
 };
 
 int linear_simt_launch(const LinArgs& a, int heads, cudaStream_t st);
@@ -106,7 +108,7 @@ struct MlpArgs {
   int heads, N, d, dh, c, b;
   int nh;  // history rows ahead of token 0 in K and V
   int bf16;
-  int lk;    // attentional bias: 0 l2, 2 l_p, 3 Huber (ATLAS_LOSS_*)
+  int lk;    // attentional bias: 0 l2, 2 l_p, 3 Huber, 4 robust (ATLAS_LOSS_*)
   float lp;  // its parameter (p, delta)
   int ns_steps;
   float ns_a, ns_b, ns_c, ns_eps;

@@ -562,7 +562,7 @@ constexpr size_t kFinishSmem = sizeof(float) * ((size_t)2 * kB * kD + 3 * kB * k
 
 bool linear_bwd_supported(const LinArgs& a) {
   return a.d_k == kD && a.d_v == kD && a.D == kD && a.b == kB && a.c == 1 && !a.poly && !a.dot &&
-         !a.pgen &&
+         !a.pgen && a.ret == ATLAS_RET_L2 && a.lk != ATLAS_LOSS_ROBUST &&
          a.nh == 0 && a.S == nullptr;
 }
 

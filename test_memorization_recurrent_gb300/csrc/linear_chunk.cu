@@ -188,7 +188,10 @@ dim3 ew_grid(long n, int heads) {
 
 }  // namespace
 
-bool linear_chunk_supported(const LinArgs& a) { return !a.pgen && a.D >= 256 && a.d_v <= 512; }
+bool linear_chunk_supported(const LinArgs& a) {
+  return !a.pgen && a.ret == ATLAS_RET_L2 && a.lk != ATLAS_LOSS_ROBUST && a.D >= 256 &&
+         a.d_v <= 512;
+}
 
 size_t linear_chunk_workspace_bytes(const LinArgs& a, int heads) {
   const size_t s = (size_t)heads * a.d_v * a.D * sizeof(float);  // S when none is given

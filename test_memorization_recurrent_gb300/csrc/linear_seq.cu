@@ -237,7 +237,8 @@ __global__ void __launch_bounds__(kThr) linear_seq_kernel(LinArgs p) {
 }
 
 bool linear_seq_supported(const LinArgs& a) {
-  return !a.poly && !a.pgen && a.d_k == 32 && a.D == 32 && a.d_v >= 1 && a.c >= 1 && a.c <= kMaxC;
+  return !a.poly && !a.pgen && a.ret == ATLAS_RET_L2 && a.lk != ATLAS_LOSS_ROBUST &&
+         a.d_k == 32 && a.D == 32 && a.d_v >= 1 && a.c >= 1 && a.c <= kMaxC;
 }
 
 int linear_seq_launch(const LinArgs& a, int heads, cudaStream_t st) {

@@ -23,6 +23,27 @@
 // monomial indices, 0xFF past its degree) in shared memory, and its lifted inner
 // product is sum_e a_e^2 h_e(z), z_j = q_j k_j, with the complete homogeneous
 // symmetric polynomials h_e from the power sums of z (Newton's identities).
+//
+// Retention gates other than l2 ("It's All Connected (Miras)", #2 Alternative
+// Retention Gates).  The l_q memory keeps the tables: its state is the plain
+// accumulator A, and the memory A_r / z_r with the per-row normaliser
+// z_r = ||A_r||_q^(q-2) taken at the chunk start enters the errors and the
+// readout as one scale per row.  Elastic net, Bregman (sigmoid link) and KL map
+// the decayed step through a non-linear function at every token, so their chunk
+// walks the tokens one by one after the errors E: per token, one warp per row r
+// forms the window gradient sum_i gamma[t-i] E[i,r] Phi(k_i), steps S and the
+// state, and reads the row out.  The Bregman state is kept as logits and the KL
+// state as log M (the same maps, without a log per step); both are converted at
+// load and store.
+//
+// The robust bias scales each window token's error row by 1 + Delta/||e||, which
+// needs the norm over all d_v rows of the head.  Its row blocks therefore form
+// one thread-block cluster per head (at most 8 CTAs): each CTA writes the partial
+// squared norms of its rows to shared memory, and after a cluster barrier every
+// CTA adds the partials of all ranks through distributed shared memory; a second
+// barrier keeps them until every rank has read them.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -30,15 +51,16 @@ namespace atlas {
 
 struct LinSimtSmem {
   int RV, D, Lmax, b, d_k, pgen;
+  int ncl;  // CTAs per head in one cluster (robust bias), else 1
   // float offsets
-  long Ms, Ss, Kw, Qc, Vw, E, P, Urun, Wrun, sa, se, sb, total_floats;
+  long Ms, Ss, Kw, Qc, Vw, E, P, Urun, Wrun, sa, se, sb, Z, NR, total_floats;
   long pairs_bytes;
   size_t bytes() const { return total_floats * sizeof(float) + pairs_bytes; }
 };
 
 static LinSimtSmem lin_simt_layout(int RV, int D, int Lmax, int b, int d_k, int pgen) {
   LinSimtSmem s;
-  s.RV = RV; s.D = D; s.Lmax = Lmax; s.b = b; s.d_k = d_k; s.pgen = pgen;
+  s.RV = RV; s.D = D; s.Lmax = Lmax; s.b = b; s.d_k = d_k; s.pgen = pgen; s.ncl = 1;
   long o = 0;
   s.Ms = o; o += (long)RV * D;
   s.Ss = o; o += (long)RV * D;
@@ -52,6 +74,8 @@ static LinSimtSmem lin_simt_layout(int RV, int D, int Lmax, int b, int d_k, int 
   s.sa = o; o += b;
   s.se = o; o += b;
   s.sb = o; o += b;
+  s.Z = o; o += RV;
+  s.NR = o; o += Lmax;
   s.total_floats = o;
   s.pairs_bytes = pgen ? 4L * D : 2L * (D - d_k > 0 ? D - d_k : 0);
   return s;
@@ -141,7 +165,7 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
   uint32_t* ftab = reinterpret_cast<uint32_t*>(sm + L.total_floats);  // gated map
 
 
-  const int rv = min(L.RV, p.d_v - r0);
+  const int rv = max(0, min(L.RV, p.d_v - r0));  // a cluster's last CTA may hold none
   const int D = L.D, dk = p.d_k, dv = p.d_v;
   const int tid = threadIdx.x, nt = blockDim.x;
   const long state = (long)dv * D;
@@ -179,10 +203,22 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
   };
   float* Mg = p.M + head * state + (long)r0 * D;
   float* Sg = p.S ? p.S + head * state + (long)r0 * D : nullptr;
+  const int ret = p.ret;
+  const bool serial = ret == ATLAS_RET_ELASTIC || ret == ATLAS_RET_BREGMAN || ret == ATLAS_RET_KL;
   for (long x = tid; x < (long)rv * D; x += nt) {
-    Ms[x] = Mg[x];
+    float m = Mg[x];
+    if (ret == ATLAS_RET_BREGMAN) m = logf(m / (1.f - m));  // state as logits
+    if (ret == ATLAS_RET_KL) m = logf(m);                   // state as log M
+    Ms[x] = m;
     Ss[x] = Sg ? Sg[x] : 0.f;
   }
+  // the memory entry a state entry stands for at a chunk start (l_q: before the
+  // row scale Z)
+  auto mem_of = [&](float m) -> float {
+    if (ret == ATLAS_RET_BREGMAN) return 1.f / (1.f + expf(-m));
+    if (ret == ATLAS_RET_KL) return expf(m);
+    return m;
+  };
   const float* alpha = p.alpha + (long)head * p.N;
   const float* eta = p.eta + (long)head * p.N;
   const float* theta = p.theta + (long)head * p.N;
@@ -191,6 +227,9 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
   const long vbase = ((long)head * (p.N + p.nh) + p.nh) * dv;
   const long qbase = (long)head * p.N * dk;
   const long ybase = (long)head * p.N * dv;
+  const int lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+  float* Z = sm + L.Z;
+  const float logc = ret == ATLAS_RET_KL ? logf(p.rp) : 0.f;
 
   for (int t0 = 0; t0 < p.N; t0 += p.b) {
     const int t1 = min(p.N, t0 + p.b);
@@ -204,11 +243,30 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
       const int i = x / rv, r = x % rv;
       Vw[x] = ld_in(p.V, vbase + (long)(i0 + i) * dv + r0 + r, p.bf16);
     }
-    if (tid < 32)
+    if (serial) {  // the gates of the chunk's tokens, and gamma by lag
+      for (int n = tid; n < nb; n += nt) {
+        sa[n] = alpha[t0 + n];
+        se[n] = eta[t0 + n];
+        sb[n] = theta[t0 + n];
+      }
+      for (int l = tid; l < p.c; l += nt) Urun[l] = p.gamma[l];
+    } else if (tid < 32) {
       chunk_tables_warp(alpha, eta, theta, p.gamma, t0, nb, i0, Lw, p.c, Urun, Wrun, P, L.Lmax,
                         nullptr, sa, se, sb);
+    }
+    // l_q: Z[r] = 1 / ||A_r||_q^(q-2) of the chunk-start accumulator (1 for a zero row)
+    if (ret == ATLAS_RET_LQ) {
+      for (int r = warp; r < rv; r += nw) {
+        const float* m = Ms + (long)r * D;
+        float acc = 0.f;
+        for (int j = lane; j < D; j += 32) acc += powf(fabsf(m[j]), p.rp);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+        if (lane == 0) Z[r] = acc > 0.f ? 1.f / powf(acc, (p.rp - 2.f) / p.rp) : 1.f;
+      }
+    }
     __syncthreads();
-    // errors at the chunk-start state
+    // errors at the chunk-start memory
     for (int x = tid; x < Lw * rv; x += nt) {
       const int i = x / rv, r = x % rv;
       float e;
@@ -218,10 +276,100 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
         const float* m = Ms + (long)r * D;
         const float* k = Kw + i * dk;
         float s = 0.f;
-        for (int j = 0; j < D; ++j) s += m[j] * feat(k, j);
+        for (int j = 0; j < D; ++j) s += mem_of(m[j]) * feat(k, j);
+        if (ret == ATLAS_RET_LQ) s *= Z[r];
         e = bias_grad(s - Vw[x], p.lk, p.lp);
       }
       E[x] = e;
+    }
+    if (p.lk == ATLAS_LOSS_ROBUST) {
+      float* NR = sm + L.NR;
+      __syncthreads();
+      for (int i = warp; i < Lw; i += nw) {  // this CTA's part of ||e_i||^2
+        const float* e = E + i * rv;
+        float ss = 0.f;
+        for (int r = lane; r < rv; r += 32) ss += e[r] * e[r];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+        if (lane == 0) NR[i] = ss;
+      }
+      namespace cg = cooperative_groups;
+      if (L.ncl > 1)
+        cg::this_cluster().sync();
+      else
+        __syncthreads();
+      for (int i = warp; i < Lw; i += nw) {
+        float part = 0.f;
+        if (L.ncl > 1) {
+          if (lane < L.ncl) part = *cg::this_cluster().map_shared_rank(NR + i, lane);
+        } else if (lane == 0) {
+          part = NR[i];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o);
+        const float f = robust_scale(sqrtf(part), p.lp);
+        float* e = E + i * rv;
+        for (int r = lane; r < rv; r += 32) e[r] *= f;
+      }
+      if (L.ncl > 1) cg::this_cluster().sync();  // every rank has read NR
+    }
+    if (serial) {
+      __syncthreads();
+      // token by token; warp w owns rows w, w + nw, ... for the whole chunk
+      for (int n = 0; n < nb; ++n) {
+        const int t = t0 + n;
+        const float keep = 1.f - sa[n], et = se[n], th2 = 2.f * sb[n];
+        const int hi = t - i0, lo = max(0, hi - p.c + 1);  // window rows of token t
+        const float* q = Qc + n * dk;
+        for (int r = warp; r < rv; r += nw) {
+          float* m = Ms + (long)r * D;
+          float* sr = Ss + (long)r * D;
+          float acc = 0.f, mx = -INFINITY, den = 0.f;
+          for (int j = lane; j < D; j += 32) {
+            float g = 0.f;
+            for (int i = lo; i <= hi; ++i) g += Urun[hi - i] * E[i * rv + r] * feat(Kw + i * dk, j);
+            const float sv = et * sr[j] - th2 * g;
+            sr[j] = sv;
+            float u = keep * m[j] + sv;
+            if (ret == ATLAS_RET_ELASTIC) {
+              const float a = fabsf(u) - p.rp;
+              u = a > 0.f ? copysignf(a, u) : 0.f;
+              acc += u * feat(q, j);
+            } else if (ret == ATLAS_RET_BREGMAN) {
+              acc += feat(q, j) / (1.f + expf(-u));
+            } else {  // KL: running max and sum of exp for the row's softmax
+              if (u > mx) {
+                den = den * expf(mx - u) + 1.f;
+                mx = u;
+              } else {
+                den += expf(u - mx);
+              }
+            }
+            m[j] = u;
+          }
+          if (ret == ATLAS_RET_KL) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+              const float om = __shfl_xor_sync(0xFFFFFFFFu, mx, o);
+              const float od = __shfl_xor_sync(0xFFFFFFFFu, den, o);
+              const float nm = fmaxf(mx, om);
+              den = (den > 0.f ? den * expf(mx - nm) : 0.f) + (od > 0.f ? od * expf(om - nm) : 0.f);
+              mx = nm;
+            }
+            // log M = u - logsumexp(u) + log c
+            const float shift = mx + logf(den) - logc;
+            for (int j = lane; j < D; j += 32) {
+              const float lm = m[j] - shift;
+              m[j] = lm;
+              acc += expf(lm) * feat(q, j);
+            }
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+          if (lane == 0) p.Y[ybase + (long)t * dv + r0 + r] = acc;
+        }
+      }
+      continue;
     }
     // masked query-key products P[n,i] = W[n,i] * Phi(q_n).Phi(k_i)
     for (int x = tid; x < nb * Lw; x += nt) {
@@ -247,7 +395,7 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
       P[n * L.Lmax + i] = v;
     }
     __syncthreads();
-    // readout y_n = M_n Phi(q_n)
+    // readout y_n = M_n Phi(q_n) (l_q: the accumulator's row times Z)
     for (int x = tid; x < nb * rv; x += nt) {
       const int n = x / rv, r = x % rv;
       const float* q = Qc + n * dk;
@@ -261,7 +409,9 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
       }
       float acc = 0.f;
       for (int i = 0; i < Lw; ++i) acc += P[n * L.Lmax + i] * E[i * rv + r];
-      p.Y[ybase + (long)(t0 + n) * dv + r0 + r] = sa[n] * ym + sb[n] * ys - 2.f * acc;
+      float y = sa[n] * ym + sb[n] * ys - 2.f * acc;
+      if (ret == ATLAS_RET_LQ) y *= Z[r];
+      p.Y[ybase + (long)(t0 + n) * dv + r0 + r] = y;
     }
     __syncthreads();
     // carry the state to the end of the chunk
@@ -281,39 +431,72 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
   }
   __syncthreads();
   for (long x = tid; x < (long)rv * D; x += nt) {
-    Mg[x] = Ms[x];
+    Mg[x] = serial ? mem_of(Ms[x]) : Ms[x];
     if (Sg) Sg[x] = Ss[x];
   }
 }
 
-int linear_simt_plan(const LinArgs& a, int heads, int* RV_out, size_t* smem_out) {
+// Rows per CTA (RV) and CTAs per cluster (robust bias only; a head's row blocks
+// form one cluster of ncl <= 8 CTAs, so RV = ceil(d_v / ncl)).
+static int plan(const LinArgs& a, int heads, LinSimtSmem* out) {
   const int Lmax = a.b + a.c - 1;
   const size_t limit = 200 * 1024;
-  int RV = a.d_v;
+  const bool robust = a.lk == ATLAS_LOSS_ROBUST;
+  int RV = a.d_v, ncl = 1;
   while (RV > 1) {
     LinSimtSmem s = lin_simt_layout(RV, a.D, Lmax, a.b, a.d_k, a.pgen);
     const long ctas = (long)heads * ((a.d_v + RV - 1) / RV);
     if (s.bytes() <= limit && (ctas >= 152 || RV <= 4)) break;
-    RV = (RV + 1) / 2;
+    if (robust) {
+      if (ncl == 8) break;
+      ncl *= 2;
+      RV = (a.d_v + ncl - 1) / ncl;
+    } else {
+      RV = (RV + 1) / 2;
+    }
   }
   LinSimtSmem s = lin_simt_layout(RV, a.D, Lmax, a.b, a.d_k, a.pgen);
   if (s.bytes() > limit) return ATLAS_ERR_UNSUPPORTED;
-  *RV_out = RV;
+  s.ncl = robust ? ncl : 1;
+  *out = s;
+  return ATLAS_OK;
+}
+
+int linear_simt_plan(const LinArgs& a, int heads, int* RV_out, size_t* smem_out) {
+  LinSimtSmem s;
+  const int rc = plan(a, heads, &s);
+  if (rc) return rc;
+  *RV_out = s.RV;
   *smem_out = s.bytes();
   return ATLAS_OK;
 }
 
 static int launch(const LinArgs& a, int heads, const int* flags, cudaStream_t st) {
-  int RV;
-  size_t smem;
-  int rc = linear_simt_plan(a, heads, &RV, &smem);
+  LinSimtSmem s;
+  int rc = plan(a, heads, &s);
   if (rc) return rc;
-  LinSimtSmem s = lin_simt_layout(RV, a.D, a.b + a.c - 1, a.b, a.d_k, a.pgen);
+  if (flags && s.ncl > 1) return ATLAS_ERR_UNSUPPORTED;
+  const size_t smem = s.bytes();
   if (cudaFuncSetAttribute(linear_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return ATLAS_ERR_CUDA;
-  dim3 grid(heads, flags ? 1 : (a.d_v + RV - 1) / RV);
-  linear_simt_kernel<<<grid, 256, smem, st>>>(a, s, flags);
+  const int rows = flags ? 1 : (s.ncl > 1 ? s.ncl : (a.d_v + s.RV - 1) / s.RV);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(heads, rows);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  if (s.ncl > 1) {  // one cluster per head: its ncl row blocks
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = s.ncl;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  if (cudaLaunchKernelEx(&cfg, linear_simt_kernel, a, s, flags) != cudaSuccess)
+    return ATLAS_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? ATLAS_OK : ATLAS_ERR_CUDA;
 }
 

@@ -720,7 +720,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 bool linear_tc_supported(const LinArgs& a) {
   return a.d_k == kDim && a.d_v == kDim && a.D == kDim && a.b == kChunk && a.c == 1 && !a.poly &&
-         !a.pgen &&
+         !a.pgen && a.ret == ATLAS_RET_L2 && a.lk != ATLAS_LOSS_ROBUST &&
          !a.dot && a.bf16 && a.N > 0;
 }
 

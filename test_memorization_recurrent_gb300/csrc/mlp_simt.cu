@@ -44,6 +44,10 @@
 // W2 and delta3 = dh * GELU(z) of W3.  W3 is carried like W2 (its readout
 // wq = W3_n q decomposes the same way), and Newton-Schulz treats it as a third
 // weight block (batched products; the fused kernel takes two blocks).
+//
+// The robust bias ("It's All Connected (Miras)", #1 Alternative Attentional
+// Biases) scales each token's error row e by 1 + Delta / ||e|| (one warp per row;
+// for the layer-normalised memory inside the LN error kernel, on e = k + LN(u) - v).
 #include <math.h>
 
 #include "common.cuh"
@@ -353,10 +357,19 @@ __global__ void ln_error_kernel(float* ws, long per_head, long Eo, long Uo, int 
   float v = 0.f;
   for (int j = lane; j < d; j += 32) v += (u[j] - mu) * (u[j] - mu);
   const float is = rsqrtf(warp_allsum(v) / d + kLnEps);
+  float rs = 1.f;  // robust bias: the row's scale 1 + Delta / ||e||
+  if (kind == ATLAS_LOSS_ROBUST) {
+    float ss = 0.f;
+    for (int j = lane; j < d; j += 32) {
+      const float r = e[j] + (u[j] - mu) * is;
+      ss += r * r;
+    }
+    rs = robust_scale(sqrtf(warp_allsum(ss)), prm);
+  }
   float s1 = 0.f, s2 = 0.f;
   for (int j = lane; j < d; j += 32) {
     const float n = (u[j] - mu) * is;
-    const float dy = bias_grad(e[j] + n, kind, prm);
+    const float dy = bias_grad(e[j] + n, kind, prm) * rs;
     u[j] = n;
     e[j] = dy;
     s1 += dy;
@@ -390,6 +403,20 @@ __global__ void bias_rows_kernel(float* ws, long per_head, long n, int kind, flo
   float* e = ws + (long)blockIdx.y * per_head;
   for (long x = blockIdx.x * (long)blockDim.x + threadIdx.x; x < n; x += (long)gridDim.x * blockDim.x)
     e[x] = bias_grad(e[x], kind, prm);
+}
+
+// Robust bias: each E row (one token's d coordinates, every head) times
+// 1 + Delta / ||row|| (0 for a zero row); one warp per row.
+__global__ void robust_rows_kernel(float* ws, long per_head, long Eo, int rows, int d,
+                                   float delta) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  float* e = ws + (long)blockIdx.y * per_head + Eo + (long)row * d;
+  float ss = 0.f;
+  for (int j = lane; j < d; j += 32) ss += e[j] * e[j];
+  const float f = robust_scale(sqrtf(warp_allsum(ss)), delta);
+  for (int j = lane; j < d; j += 32) e[j] *= f;
 }
 
 // X[inst][block] = S[inst][block] / (||S[inst][block]||_F + eps), in place; one
@@ -548,6 +575,10 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
     if (p.ln) {
       ln_error_kernel<<<dim3((unsigned)((L + 7) / 8), H), 256, 0, st>>>(ws, PH, w.E, w.Ew, L,
                                                                          (int)d, p.lk, p.lp);
+      CL();
+    } else if (p.lk == ATLAS_LOSS_ROBUST) {  // the robust bias scales whole E rows
+      robust_rows_kernel<<<dim3((unsigned)((L + 7) / 8), H), 256, 0, st>>>(ws, PH, w.E, L, (int)d,
+                                                                           p.lp);
       CL();
     } else if (p.lk != ATLAS_LOSS_L2) {  // the attentional bias acts on E elementwise
       bias_rows_kernel<<<ew_grid((long)L * d, H), 256, 0, st>>>(ws + w.E, PH, (long)L * d, p.lk,

@@ -1110,7 +1110,7 @@ bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 bool mlp_tc_supported(const MlpArgs& a) {
   return a.d == kD && a.dh == kHid && a.c == 1 && a.b == kL && a.bf16 && a.ns_steps == 0 &&
-         !a.ln && !a.gated && a.N > 0 && a.heads > 0 && a.heads <= 65535;
+         !a.ln && !a.gated && a.lk != ATLAS_LOSS_ROBUST && a.N > 0 && a.heads > 0 && a.heads <= 65535;
 }
 
 size_t mlp_tc_workspace_bytes(const MlpArgs& a) {

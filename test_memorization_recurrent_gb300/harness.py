@@ -22,7 +22,7 @@ def cfg_for(w, heads: int, N: int, S_state=None, workspace=None, workspace_bytes
                     b=w.b, ns_steps=w.ns_steps, ns_a=a, ns_b=b_, ns_c=c_, ns_eps=w.ns_eps,
                     in_dtype=BF16 if w.bf16 else F32, S_state=S_state, workspace=workspace,
                     workspace_bytes=workspace_bytes, status_dev=status_dev, n_history=n_history,
-                    phi_coef=w.phi_coef)
+                    phi_coef=w.phi_coef, retention=w.retention, ret_param=w.ret_param)
 
 
 def to_device(w, inp: dict, device="cuda") -> dict:

@@ -27,7 +27,8 @@ def oracle_cfg(w, N, n_history=0):
     a, b, c = w.ns_coef
     return oracle.make_cfg(N, w.d_k, w.d_v, w.d_h, w.mem, w.phi, w.loss, w.c, w.b,
                            w.ns_steps, a, b, c, w.ns_eps, n_history=n_history,
-                           loss_param=w.loss_param, phi_coef=w.phi_coef)
+                           loss_param=w.loss_param, phi_coef=w.phi_coef,
+                           retention=w.retention, ret_param=w.ret_param)
 
 
 def run_oracle(w, inp, N=None, recurrent=False, S0=None, n_threads=0):

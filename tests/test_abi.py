@@ -74,7 +74,14 @@ def _bad(**kw):
     (dict(b=0), A.ERR_INVALID),
     (dict(mem=7), A.ERR_INVALID),
     (dict(phi=3), A.ERR_INVALID),
-    (dict(loss=4), A.ERR_INVALID),
+    (dict(loss=5), A.ERR_INVALID),
+    (dict(loss=A.LOSS_ROBUST, loss_param=-0.1), A.ERR_INVALID),  # Delta >= 0
+    (dict(retention=5), A.ERR_INVALID),
+    (dict(retention=A.RET_ELASTIC, ret_param=-1e-3), A.ERR_INVALID),  # lambda >= 0
+    (dict(retention=A.RET_KL, ret_param=0.0), A.ERR_INVALID),         # mass c > 0
+    (dict(retention=A.RET_LQ, ret_param=0.5), A.ERR_INVALID),         # q >= 1
+    (dict(retention=A.RET_BREGMAN, mem=A.MEM_MLP, d_h=16), A.ERR_UNSUPPORTED),
+    (dict(retention=A.RET_ELASTIC, ns_steps=5), A.ERR_UNSUPPORTED),
     (dict(loss=A.LOSS_LP, loss_param=0.5), A.ERR_INVALID),      # p < 1
     (dict(loss=A.LOSS_HUBER, loss_param=0.0), A.ERR_INVALID),   # delta must be > 0
     (dict(in_dtype=5), A.ERR_INVALID),
@@ -155,6 +162,8 @@ def test_bias_launches_are_counted():
     dict(loss=A.LOSS_DOT),                     # dot-product bias
     dict(n_history=3),                         # history rows
     dict(phi=A.PHI_POLY2, d_k=16, d_v=128),    # feature map
+    dict(loss=A.LOSS_ROBUST, loss_param=0.5),  # robust bias
+    dict(retention=A.RET_LQ, ret_param=3.0),   # a retention gate
 ])
 def test_backward_rejects_uncovered_descriptions(lib, kw):
     base = dict(B=1, H=2, N=100, d_k=128, d_v=128, c=1, b=64)
@@ -215,3 +224,39 @@ def test_gated_memory_runs_on_the_cuda_core_mlp_path(lib):
         assert A.atlas_mem_path(cfg) == "mlp_simt"
         assert A.atlas_mem_state_size(cfg) == 3 * 128 * 512
         assert A.atlas_mem_workspace_bytes(cfg) > 0
+
+
+def test_retention_gates_and_robust_bias_run_on_the_cuda_core_kernels(lib):
+    """Every retention gate other than l2 and the robust bias select the CUDA-core
+    linear kernel (one launch); the robust bias on an MLP memory the CUDA-core MLP
+    path, one row-scaling launch per chunk where the l2 bias has none."""
+    from test_memorization_recurrent_gb300.harness import cfg_for
+    for ret, prm in ((A.RET_ELASTIC, 0.01), (A.RET_BREGMAN, 0.0), (A.RET_KL, 1.0),
+                     (A.RET_LQ, 3.0)):
+        for wid in (1, 2, 3):
+            w = W.workload(wid, retention=ret, ret_param=prm)
+            cfg = cfg_for(w, 2, 256)
+            assert A.atlas_mem_path(cfg) == "linear_simt", (wid, ret)
+            assert A.atlas_mem_launch_count(cfg) == 1
+            assert A.atlas_mem_state_size(cfg) == w.state_size
+    for wid in (1, 2, 3):
+        w = W.workload(wid, loss=A.LOSS_ROBUST, loss_param=0.5)
+        assert A.atlas_mem_path(cfg_for(w, 2, 256)) == "linear_simt"
+    N = 64 * 3 + 5  # four chunks
+    for wid, extra in ((4, 4), (5, 4)):
+        w = W.workload(wid)
+        base = A.atlas_mem_launch_count(cfg_for(w, 2, N))
+        wr = w.with_(loss=A.LOSS_ROBUST, loss_param=0.5)
+        assert A.atlas_mem_path(cfg_for(wr, 2, N)) == "mlp_simt"
+        if A.atlas_mem_path(cfg_for(w, 2, N)) == "mlp_simt":
+            assert A.atlas_mem_launch_count(cfg_for(wr, 2, N)) == base + extra, wid
+
+
+def test_robust_bias_on_wide_memories_is_planned_in_clusters(lib):
+    """The robust bias needs every row of a head; d_v = 128 rows of D = 128 do not
+    fit one CTA's shared memory, so the plan splits them over a cluster (the
+    call is supported, the state size unchanged)."""
+    cfg = A.make_cfg(B=1, H=2, N=300, d_k=128, d_v=128, c=1, b=64, loss=A.LOSS_ROBUST,
+                     loss_param=0.5)
+    assert A.atlas_mem_path(cfg) == "linear_simt"
+    assert A.atlas_mem_workspace_bytes(cfg) == 0

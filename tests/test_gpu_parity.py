@@ -435,3 +435,84 @@ def test_gated_mlp_memory(wid, kw, N, heads):
     Yg, Mg, Sg = gpu_run(w, inp, with_S=True)
     check(w, Yg, Mg, Yo, Mo, f"gated memory {kw}")
     assert rel_err(Sg, So, w.bf16) <= tol(w)
+
+
+# ------------------------------------------------- retention gates, robust bias
+
+RET_GATES = [(W.RET_ELASTIC, 0.01), (W.RET_BREGMAN, 0.0), (W.RET_KL, 1.0), (W.RET_LQ, 3.0),
+             (W.RET_LQ, 2.5)]
+RET_CASES = {
+    2: (dict(eta=(0.5, 0.9)), 64 * 2 + 17, [0, 9]),  # d = 128, b = 64, momentum, ragged tail
+    1: (dict(), 150, [0]),                            # fp32, c = 4, b = 1: the recurrence
+    3: (dict(), 64 + 9, [2]),                         # degree-2 map, window 64
+}
+
+
+# q = 4 reads A / ||A||_4^2, which grows as the accumulator shrinks: in the
+# recurrence from a zero state it has no well-conditioned trajectory (and q < 2
+# feeds the memory's growth back into itself), so q = 4 runs with chunk-start
+# normalisers only (b = 64).  The degree-2 workload's steps are
+# small (theta scaled down), hence its smaller elastic threshold.
+@pytest.mark.parametrize("wid,ret,prm", [(wid, r, p) for wid in (2, 1, 3) for r, p in RET_GATES]
+                         + [(2, W.RET_LQ, 4.0), (3, W.RET_LQ, 4.0)])
+def test_retention_gates(wid, ret, prm):
+    """The Miras retention gates (elastic net, Bregman with a sigmoid link, KL,
+    l_q) on the CUDA-core linear kernel against the oracle, from the gate's
+    neutral memory, momentum S included."""
+    from test_memorization_recurrent_gb300.harness import cfg_for
+    import test_memorization_recurrent_gb300 as A
+    kw, N, heads = RET_CASES[wid]
+    if wid == 3 and ret == W.RET_ELASTIC:
+        prm = 1e-4
+    w = W.workload(wid, bounded=True, retention=ret, ret_param=prm, **kw)
+    assert A.atlas_mem_path(cfg_for(w, len(heads), N)) == "linear_simt"
+    inp = W.generate(w, heads=heads, n_tokens=N)
+    Yo, Mo, So = run_oracle(w, inp)
+    Yg, Mg, Sg = gpu_run(w, inp, with_S=True)
+    check(w, Yg, Mg, Yo, Mo, f"workload {wid} retention {ret} ({prm})")
+    assert rel_err(Sg, So, w.bf16) <= tol(w)
+    if ret == W.RET_ELASTIC:  # the thresholded memory is sparse: zeros land on zeros
+        assert np.mean((Mg == 0) == (Mo == 0)) > 0.99
+
+
+@pytest.mark.parametrize("ret,prm", RET_GATES[:4])
+def test_retention_gates_from_a_random_state(ret, prm):
+    """A random start memory (in (0.2, 0.8) for Bregman, positive rows of any mass
+    for KL, Gaussian otherwise) and a random start momentum."""
+    w = W.workload(2, bounded=True, retention=ret, ret_param=prm, eta=(0.5, 0.9), N=64 + 30)
+    heads = [1, 4]
+    inp = W.generate(w, heads=heads)
+    r = np.random.default_rng(7)
+    shape = inp["M0"].shape
+    if ret in (W.RET_BREGMAN, W.RET_KL):
+        inp["M0"] = r.uniform(0.2, 0.8, shape).astype(np.float32)
+    else:
+        inp["M0"] = (r.standard_normal(shape) * 0.05).astype(np.float32)
+    S0 = (r.standard_normal(shape) * 0.02).astype(np.float32)
+    Yo, Mo, So = run_oracle(w, inp, S0=S0.astype(np.float64))
+    Yg, Mg, Sg = gpu_run(w, inp, S0=S0)
+    check(w, Yg, Mg, Yo, Mo, f"retention {ret} from a random state")
+    assert rel_err(Sg, So, w.bf16) <= tol(w)
+
+
+@pytest.mark.parametrize("wid,kw,N,heads,path", [
+    (2, dict(eta=(0.5, 0.9)), 64 + 13, [0, 5], "linear_simt"),    # 8-CTA clusters per head
+    (1, dict(), 120, [0], "linear_simt"),                          # fp32 recurrence, c = 4
+    (3, dict(), 64 + 9, [0], "linear_simt"),                       # degree-2 map, d_v = 64
+    (2, dict(retention=W.RET_ELASTIC, ret_param=0.01), 64 + 5, [3], "linear_simt"),
+    (4, dict(), 64 + 19, [0, 7], "mlp_simt"),                      # MLP memory, momentum
+    (4, dict(mem=W.MEM_MLP_LN), 64 + 5, [1], "mlp_simt"),          # through LN
+    (5, dict(), 12, [0], "mlp_simt"),                              # Newton-Schulz, window 256
+])
+def test_robust_bias(wid, kw, N, heads, path):
+    """The value-shift robust bias (Miras alternative attentional biases, read as
+    (||e|| + Delta)^2) against the oracle; it couples a token's coordinates, so
+    the linear memory's row blocks exchange partial norms within a cluster."""
+    from test_memorization_recurrent_gb300.harness import cfg_for
+    import test_memorization_recurrent_gb300 as A
+    w = W.workload(wid, bounded=True, loss=W.LOSS_ROBUST, loss_param=0.5, **kw)
+    assert A.atlas_mem_path(cfg_for(w, len(heads), N)) == path
+    inp = W.generate(w, heads=heads, n_tokens=N)
+    Yo, Mo, _ = run_oracle(w, inp)
+    Yg, Mg, _ = gpu_run(w, inp)
+    check(w, Yg, Mg, Yo, Mo, f"workload {wid} robust {kw}")

@@ -25,7 +25,8 @@ BLOCK = 256  # tokens per independently seeded block
 
 MEM_LINEAR, MEM_MLP, MEM_MLP_LN, MEM_MLP_GATED = 0, 1, 2, 3
 PHI_IDENTITY, PHI_POLY2, PHI_POLY = 0, 1, 2
-LOSS_L2, LOSS_DOT, LOSS_LP, LOSS_HUBER = 0, 1, 2, 3
+LOSS_L2, LOSS_DOT, LOSS_LP, LOSS_HUBER, LOSS_ROBUST = 0, 1, 2, 3, 4
+RET_L2, RET_ELASTIC, RET_BREGMAN, RET_KL, RET_LQ = 0, 1, 2, 3, 4
 
 
 @dataclasses.dataclass(frozen=True)
@@ -56,6 +57,8 @@ class Workload:
     ns_coef: tuple = (0.0, 0.0, 0.0)
     ns_eps: float = 1e-7
     phi_coef: tuple = ()           # PHI_POLY: input-gating coefficients a_0 .. a_p
+    retention: int = RET_L2        # retention gate of the linear memory
+    ret_param: float = 0.0         # its parameter (lambda, c, q)
 
     @property
     def heads(self) -> int:
@@ -167,9 +170,15 @@ def _block(w: Workload, seed: int, head: int, blk: int):
 
 
 def init_state(w: Workload, seed: int, head: int) -> np.ndarray:
-    """Initial memory M_0 of one head (fp32): zeros for a linear memory; the
-    MLP weights W1 (d x d_h) then W2 (d_h x d), each N(0, w_std^2)."""
+    """Initial memory M_0 of one head (fp32): the gate's neutral memory for a
+    linear memory (zeros; 1/2, logit 0, for the Bregman gate; rows of mass c
+    spread evenly, c / D, for the KL gate); the MLP weights W1 (d x d_h) then W2
+    (d_h x d), each N(0, w_std^2)."""
     if w.mem == MEM_LINEAR:
+        if w.retention == RET_BREGMAN:
+            return np.full(w.state_size, 0.5, dtype=np.float32)
+        if w.retention == RET_KL:
+            return np.full(w.state_size, w.ret_param / w.D, dtype=np.float32)
         return np.zeros(w.state_size, dtype=np.float32)
     r = _rng(seed, w, head, 1 << 30)
     return (r.standard_normal(w.state_size) * w.w_std).astype(np.float32)
