@@ -281,13 +281,23 @@ def variant_workloads():
     map (input gating a = (0, 1, 1, 1)) on the wide-feature workload's shape with
     d_k = 16 (D = 968 features), window 64, momentum and decay, bounded step; the
     layer-normalised and the gated MLP memories on the MLP workload's shape (first
-    1024 tokens of all 32 heads; they run on the CUDA-core MLP path)."""
+    1024 tokens of all 32 heads; they run on the CUDA-core MLP path); the Miras
+    retention gates (elastic net lambda = 0.01, Bregman with the sigmoid link, KL of
+    row mass 1, l_q with q = 3) and the robust bias (Delta = 0.5) on the DeltaNet
+    workload's shape (first 1024 tokens of all 128 heads; CUDA-core linear kernel)."""
     return [W.workload(3, bounded=True, d_k=16, phi=W.PHI_POLY, phi_coef=(0.0, 1.0, 1.0, 1.0),
                        N=2048, theta_scale=0.002, name="poly3-gated-omega-c64-bf16"),
             W.workload(4, bounded=True, mem=W.MEM_MLP_LN, N=1024,
                        name="mlp-ln-momentum-b64-bf16"),
             W.workload(4, bounded=True, mem=W.MEM_MLP_GATED, N=1024,
-                       name="mlp-gated-momentum-b64-bf16")]
+                       name="mlp-gated-momentum-b64-bf16"),
+            W.workload(2, retention=W.RET_ELASTIC, ret_param=0.01, N=1024,
+                       name="linear-elastic-b64-bf16"),
+            W.workload(2, retention=W.RET_BREGMAN, N=1024, name="linear-bregman-b64-bf16"),
+            W.workload(2, retention=W.RET_KL, ret_param=1.0, N=1024, name="linear-kl-b64-bf16"),
+            W.workload(2, retention=W.RET_LQ, ret_param=3.0, N=1024, name="linear-lq3-b64-bf16"),
+            W.workload(2, loss=W.LOSS_ROBUST, loss_param=0.5, N=1024,
+                       name="linear-robust-b64-bf16")]
 
 
 def time_device(w, run, d, steps, warmup, stream, clk=None, world=1):

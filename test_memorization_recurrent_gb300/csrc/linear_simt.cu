@@ -36,6 +36,15 @@
 // state as log M (the same maps, without a log per step); both are converted at
 // load and store.
 //
+// Every product of a chunk is a small dense contraction over shared memory,
+// computed by register tiles: 256 threads form a TY x TX grid and each thread
+// accumulates TM x TN outputs spaced TY and TX apart, so a k-step loads TM + TN
+// operands for TM TN FMAs.  Rows of M, S, K and Q are stored with odd strides,
+// which keeps the column walks free of bank conflicts.  The token-serial walk
+// has a fast form for D <= 128: each lane holds the features of its (at most
+// four) columns of q and of the window keys in registers and a warp steps two
+// rows at a time.
+//
 // The robust bias scales each window token's error row by 1 + Delta/||e||, which
 // needs the norm over all d_v rows of the head.  Its row blocks therefore form
 // one thread-block cluster per head (at most 8 CTAs): each CTA writes the partial
@@ -51,9 +60,10 @@ namespace atlas {
 
 struct LinSimtSmem {
   int RV, D, Lmax, b, d_k, pgen;
-  int ncl;  // CTAs per head in one cluster (robust bias), else 1
+  int Dp, dkp;  // odd row strides of M / S and of K / Q (conflict-free column walks)
+  int ncl;      // CTAs per head in one cluster (robust bias), else 1
   // float offsets
-  long Ms, Ss, Kw, Qc, Vw, E, P, Urun, Wrun, sa, se, sb, Z, NR, total_floats;
+  long Ms, Ss, Kw, Qc, Vw, E, P, Urun, Wrun, sa, se, sb, Z, NR, coef, total_floats;
   long pairs_bytes;
   size_t bytes() const { return total_floats * sizeof(float) + pairs_bytes; }
 };
@@ -61,11 +71,13 @@ struct LinSimtSmem {
 static LinSimtSmem lin_simt_layout(int RV, int D, int Lmax, int b, int d_k, int pgen) {
   LinSimtSmem s;
   s.RV = RV; s.D = D; s.Lmax = Lmax; s.b = b; s.d_k = d_k; s.pgen = pgen; s.ncl = 1;
+  s.Dp = D | 1;
+  s.dkp = d_k | 1;
   long o = 0;
-  s.Ms = o; o += (long)RV * D;
-  s.Ss = o; o += (long)RV * D;
-  s.Kw = o; o += (long)Lmax * d_k;
-  s.Qc = o; o += (long)b * d_k;
+  s.Ms = o; o += (long)RV * s.Dp;
+  s.Ss = o; o += (long)RV * s.Dp;
+  s.Kw = o; o += (long)Lmax * s.dkp;
+  s.Qc = o; o += (long)b * s.dkp;
   s.Vw = o; o += (long)Lmax * RV;
   s.E = o; o += (long)Lmax * RV;
   s.P = o; o += (long)b * Lmax;
@@ -76,6 +88,7 @@ static LinSimtSmem lin_simt_layout(int RV, int D, int Lmax, int b, int d_k, int 
   s.sb = o; o += b;
   s.Z = o; o += RV;
   s.NR = o; o += Lmax;
+  s.coef = o; o += 8;
   s.total_floats = o;
   s.pairs_bytes = pgen ? 4L * D : 2L * (D - d_k > 0 ? D - d_k : 0);
   return s;
@@ -97,31 +110,424 @@ __device__ __forceinline__ float phi_gated(const float* x, uint32_t t, const flo
   return a[e] * v;
 }
 
-// Phi(q).Phi(k) of the gated map: sum_e a_e^2 h_e(z), z_j = q_j k_j.
-__device__ __forceinline__ float phi_gated_dot(const float* q, const float* k, int dk,
-                                               const float* a, int deg) {
-  float pw[5] = {0.f, 0.f, 0.f, 0.f, 0.f};  // power sums p_1 .. p_4
-  for (int j = 0; j < dk; ++j) {
-    const float z = q[j] * k[j];
-    float zz = z;
+// Phi of the rows of x (shared memory, row stride ld): identity, the degree-2
+// map (pair table pp, pq) or the gated map (monomial table ftab, coefficients a).
+struct Feat {
+  const float* x;
+  int ld, dk, poly, pgen;
+  const uint8_t* pp;
+  const uint8_t* pq;
+  const uint32_t* ftab;
+  const float* a;
+  __device__ __forceinline__ float operator()(int row, int j) const {
+    const float* r = x + row * ld;
+    if (pgen) return phi_gated(r, ftab[j], a);
+    if (!poly || j < dk) return r[j];
+    return r[pp[j - dk]] * r[pq[j - dk]];
+  }
+};
+
+// C = A B over k < K for an m x n output: thread (ty, tx) of a TY x TX grid
+// (TY TX = 256) owns rows ty + TY u and columns tx + TX v of each block; fe
+// receives each finished output.  Operand indices are clamped into range, so
+// the loads stay in bounds and only in-range outputs are delivered.
+template <int TX, int TM, int TN, class FA, class FB, class FE>
+__device__ __forceinline__ void tile_gemm(int m, int n, int K, const FA& fa, const FB& fb,
+                                          const FE& fe) {
+  constexpr int TY = 256 / TX;
+  const int tx = threadIdx.x % TX, ty = threadIdx.x / TX;
+  for (int m0 = 0; m0 < m; m0 += TY * TM)
+    for (int n0 = 0; n0 < n; n0 += TX * TN) {
+      int mi[TM], nj[TN];
 #pragma unroll
-    for (int m = 1; m <= 4; ++m) {
-      if (m <= deg) pw[m] += zz;
-      zz *= z;
+      for (int u = 0; u < TM; ++u) mi[u] = min(m0 + ty + TY * u, m - 1);
+#pragma unroll
+      for (int v = 0; v < TN; ++v) nj[v] = min(n0 + tx + TX * v, n - 1);
+      float acc[TM][TN];
+#pragma unroll
+      for (int u = 0; u < TM; ++u)
+#pragma unroll
+        for (int v = 0; v < TN; ++v) acc[u][v] = 0.f;
+      for (int k = 0; k < K; ++k) {
+        float a[TM], b[TN];
+#pragma unroll
+        for (int u = 0; u < TM; ++u) a[u] = fa(mi[u], k);
+#pragma unroll
+        for (int v = 0; v < TN; ++v) b[v] = fb(k, nj[v]);
+#pragma unroll
+        for (int u = 0; u < TM; ++u)
+#pragma unroll
+          for (int v = 0; v < TN; ++v) acc[u][v] = fmaf(a[u], b[v], acc[u][v]);
+      }
+#pragma unroll
+      for (int u = 0; u < TM; ++u)
+#pragma unroll
+        for (int v = 0; v < TN; ++v) {
+          const int r = m0 + ty + TY * u, c = n0 + tx + TX * v;
+          if (r < m && c < n) fe(r, c, acc[u][v]);
+        }
+    }
+}
+
+// Tile shapes by the number of rows a CTA owns: class 0..4 for rv <= 8, 16, 32,
+// 64 and beyond.
+__device__ __forceinline__ int rows_class(int rv) {
+  return rv <= 8 ? 0 : rv <= 16 ? 1 : rv <= 32 ? 2 : rv <= 64 ? 3 : 4;
+}
+
+// m x rv outputs with the rows r as columns (errors, readout operands).
+template <class FA, class FB, class FE>
+__device__ __forceinline__ void gemm_by_rows(int cls, int m, int rv, int K, const FA& fa,
+                                             const FB& fb, const FE& fe) {
+  switch (cls) {
+    case 0: tile_gemm<8, 4, 1>(m, rv, K, fa, fb, fe); break;
+    case 1: tile_gemm<16, 4, 1>(m, rv, K, fa, fb, fe); break;
+    case 2: tile_gemm<16, 4, 2>(m, rv, K, fa, fb, fe); break;
+    case 3: tile_gemm<16, 4, 4>(m, rv, K, fa, fb, fe); break;
+    default: tile_gemm<16, 4, 8>(m, rv, K, fa, fb, fe); break;
+  }
+}
+
+// Readout of the chunk's queries: y[n, r] = z_r (sa_n Phi(q_n).M[r] + sb_n
+// Phi(q_n).S[r] - 2 sum_i P[n, i] E[i, r]); the S term is skipped when every
+// sb_n of the chunk is 0.
+template <int TX, int TM, int TN>
+__device__ __forceinline__ void readout_tile(int nb, int rv, int D, int Lw, const Feat& fq,
+                                             const float* Ms, const float* Ss, int Dp,
+                                             const float* P, int ldp, const float* E,
+                                             const float* sa, const float* sb, bool with_s,
+                                             const float* Z, float* Y, int dv) {
+  constexpr int TY = 256 / TX;
+  const int tx = threadIdx.x % TX, ty = threadIdx.x / TX;
+  for (int m0 = 0; m0 < nb; m0 += TY * TM)
+    for (int n0 = 0; n0 < rv; n0 += TX * TN) {
+      int mi[TM], nj[TN];
+#pragma unroll
+      for (int u = 0; u < TM; ++u) mi[u] = min(m0 + ty + TY * u, nb - 1);
+#pragma unroll
+      for (int v = 0; v < TN; ++v) nj[v] = min(n0 + tx + TX * v, rv - 1);
+      float am[TM][TN], as[TM][TN];
+#pragma unroll
+      for (int u = 0; u < TM; ++u)
+#pragma unroll
+        for (int v = 0; v < TN; ++v) am[u][v] = as[u][v] = 0.f;
+      for (int j = 0; j < D; ++j) {
+        float a[TM], bm[TN];
+#pragma unroll
+        for (int u = 0; u < TM; ++u) a[u] = fq(mi[u], j);
+#pragma unroll
+        for (int v = 0; v < TN; ++v) bm[v] = Ms[nj[v] * Dp + j];
+#pragma unroll
+        for (int u = 0; u < TM; ++u)
+#pragma unroll
+          for (int v = 0; v < TN; ++v) am[u][v] = fmaf(a[u], bm[v], am[u][v]);
+        if (with_s) {
+          float bs[TN];
+#pragma unroll
+          for (int v = 0; v < TN; ++v) bs[v] = Ss[nj[v] * Dp + j];
+#pragma unroll
+          for (int u = 0; u < TM; ++u)
+#pragma unroll
+            for (int v = 0; v < TN; ++v) as[u][v] = fmaf(a[u], bs[v], as[u][v]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < TM; ++u)
+#pragma unroll
+        for (int v = 0; v < TN; ++v) am[u][v] = sa[mi[u]] * am[u][v] + sb[mi[u]] * as[u][v];
+      for (int i = 0; i < Lw; ++i) {
+        float a[TM], be[TN];
+#pragma unroll
+        for (int u = 0; u < TM; ++u) a[u] = -2.f * P[mi[u] * ldp + i];
+#pragma unroll
+        for (int v = 0; v < TN; ++v) be[v] = E[i * rv + nj[v]];
+#pragma unroll
+        for (int u = 0; u < TM; ++u)
+#pragma unroll
+          for (int v = 0; v < TN; ++v) am[u][v] = fmaf(a[u], be[v], am[u][v]);
+      }
+#pragma unroll
+      for (int u = 0; u < TM; ++u)
+#pragma unroll
+        for (int v = 0; v < TN; ++v) {
+          const int n = m0 + ty + TY * u, r = n0 + tx + TX * v;
+          if (n < nb && r < rv) Y[(long)n * dv + r] = Z ? am[u][v] * Z[r] : am[u][v];
+        }
+    }
+}
+
+// State carry to the chunk end: with gw[r, j] = sum_i W_b[i] E[i, r] Phi(k_i)[j]
+// and gu likewise with U_b,  M = a_b M + beta_b S - 2 gw,  S = eps_b S - 2 gu.
+template <int TX, int TM, int TN>
+__device__ __forceinline__ void carry_tile(int rv, int D, int Lw, const Feat& fk, const float* E,
+                                           const float* Wrun, const float* Urun, float* Ms,
+                                           float* Ss, int Dp, float a_b, float b_b, float e_b) {
+  constexpr int TY = 256 / TX;
+  const int tx = threadIdx.x % TX, ty = threadIdx.x / TX;
+  for (int m0 = 0; m0 < rv; m0 += TY * TM)
+    for (int n0 = 0; n0 < D; n0 += TX * TN) {
+      int mi[TM], nj[TN];
+#pragma unroll
+      for (int u = 0; u < TM; ++u) mi[u] = min(m0 + ty + TY * u, rv - 1);
+#pragma unroll
+      for (int v = 0; v < TN; ++v) nj[v] = min(n0 + tx + TX * v, D - 1);
+      float gw[TM][TN], gu[TM][TN];
+#pragma unroll
+      for (int u = 0; u < TM; ++u)
+#pragma unroll
+        for (int v = 0; v < TN; ++v) gw[u][v] = gu[u][v] = 0.f;
+      for (int i = 0; i < Lw; ++i) {
+        const float w = Wrun[i], uu = Urun[i];
+        float ew[TM], eu[TM], f[TN];
+#pragma unroll
+        for (int u = 0; u < TM; ++u) {
+          const float e = E[i * rv + mi[u]];
+          ew[u] = e * w;
+          eu[u] = e * uu;
+        }
+#pragma unroll
+        for (int v = 0; v < TN; ++v) f[v] = fk(i, nj[v]);
+#pragma unroll
+        for (int u = 0; u < TM; ++u)
+#pragma unroll
+          for (int v = 0; v < TN; ++v) {
+            gw[u][v] = fmaf(ew[u], f[v], gw[u][v]);
+            gu[u][v] = fmaf(eu[u], f[v], gu[u][v]);
+          }
+      }
+#pragma unroll
+      for (int u = 0; u < TM; ++u)
+#pragma unroll
+        for (int v = 0; v < TN; ++v) {
+          const int r = m0 + ty + TY * u, j = n0 + tx + TX * v;
+          if (r < rv && j < D) {
+            const long x = (long)r * Dp + j;
+            const float m0v = Ms[x], s0v = Ss[x];
+            Ms[x] = a_b * m0v + b_b * s0v - 2.f * gw[u][v];
+            Ss[x] = e_b * s0v - 2.f * gu[u][v];
+          }
+        }
+    }
+}
+
+// P[n, i] <- P[n, i] (the W table on entry) times Phi(q_n).Phi(k_i), from the
+// power sums p_m = sum_j (q_j k_j)^m, m <= NP, of 64 x 64 blocks (thread tile
+// 4 x 4): kind 0 the identity map (p_1), 1 the degree-2 map, p_1 + (p_1^2 + p_2)/2,
+// 2 the gated map, sum_e a_e^2 h_e with the complete homogeneous symmetric
+// polynomials h_e from the power sums (Newton's identities).
+template <int NP>
+__device__ __forceinline__ void qk_tile(int nb, int Lw, int dk, const float* Qc, const float* Kw,
+                                        int dkp, float* P, int ldp, int kind, const float* a,
+                                        int deg) {
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  for (int m0 = 0; m0 < nb; m0 += 64)
+    for (int n0 = 0; n0 < Lw; n0 += 64) {
+      int mi[4], nj[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        mi[u] = min(m0 + ty + 16 * u, nb - 1);
+        nj[u] = min(n0 + tx + 16 * u, Lw - 1);
+      }
+      float ps[NP][4][4];
+#pragma unroll
+      for (int e = 0; e < NP; ++e)
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int v = 0; v < 4; ++v) ps[e][u][v] = 0.f;
+      for (int j = 0; j < dk; ++j) {
+        float q[4], k[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          q[u] = Qc[mi[u] * dkp + j];
+          k[u] = Kw[nj[u] * dkp + j];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const float z = q[u] * k[v];
+            float zz = z;
+#pragma unroll
+            for (int e = 0; e < NP; ++e) {
+              ps[e][u][v] += zz;
+              zz *= z;
+            }
+          }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int n = m0 + ty + 16 * u, i = n0 + tx + 16 * v;
+          if (n >= nb || i >= Lw) continue;
+          float val;
+          if (kind == 0) {
+            val = ps[0][u][v];
+          } else if (kind == 1) {
+            val = ps[0][u][v] + 0.5f * (ps[0][u][v] * ps[0][u][v] + ps[NP > 1 ? 1 : 0][u][v]);
+          } else {
+            float h[5];
+            h[0] = 1.f;
+            val = a[0] * a[0];
+#pragma unroll
+            for (int m = 1; m <= 4; ++m) {
+              float acc = 0.f;
+#pragma unroll
+              for (int l = 1; l <= m; ++l) acc += (l <= NP ? ps[l <= NP ? l - 1 : 0][u][v] : 0.f) * h[m - l];
+              h[m] = acc / (float)m;
+              if (m <= deg) val += a[m] * a[m] * h[m];
+            }
+          }
+          P[n * ldp + i] *= val;
+        }
+    }
+}
+
+// The memory entry a state entry stands for: the state itself (MK 0), the
+// sigmoid of a logit (MK 1, Bregman) or the exponential of log M (MK 2, KL).
+template <int MK>
+__device__ __forceinline__ float mem_entry(float m) {
+  if (MK == 1) return 1.f / (1.f + expf(-m));
+  if (MK == 2) return expf(m);
+  return m;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+  return x;
+}
+
+// Running (max, sum of exp) pairs of a softmax, combined across the warp.
+__device__ __forceinline__ void warp_lse(float& mx, float& den) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float om = __shfl_xor_sync(0xFFFFFFFFu, mx, o);
+    const float od = __shfl_xor_sync(0xFFFFFFFFu, den, o);
+    const float nm = fmaxf(mx, om);
+    den = (den > 0.f ? den * expf(mx - nm) : 0.f) + (od > 0.f ? od * expf(om - nm) : 0.f);
+    mx = nm;
+  }
+}
+
+// One token of the token-serial walk for a non-linear gate (RK: ATLAS_RET_*),
+// D <= 32 JPL: lane l holds columns l + 32 u.  Two rows (r, r + 8) per step.
+// kf: window-key features by lag (lags < 4), ge: gamma by lag.
+template <int JPL, int RK>
+__device__ __forceinline__ void serial_token_fast(int rv, int D, int Dp, float* Ms, float* Ss,
+                                                  const float* E, int hi, int nwin,
+                                                  const float (&qf)[JPL],
+                                                  const float (&kf)[4][JPL], const float* gam,
+                                                  const Feat& fk, float keep, float et, float th2,
+                                                  float lam, float logc, float* Yrow) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw4 = min(nwin, 4);
+  for (int rb = warp; rb < rv; rb += 16) {
+    const int rr[2] = {rb, rb + 8};
+    float uval[2][JPL], acc[2] = {0.f, 0.f}, mx[2] = {-INFINITY, -INFINITY}, den[2] = {0.f, 0.f};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = rr[h];
+      if (r >= rv) continue;
+      float ge[4];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) ge[w] = w < nw4 ? gam[w] * E[(hi - w) * rv + r] : 0.f;
+#pragma unroll
+      for (int u = 0; u < JPL; ++u) {
+        const int j = lane + 32 * u;
+        uval[h][u] = 0.f;
+        if (j >= D) continue;
+        float g = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) g = fmaf(ge[w], kf[w][u], g);
+        for (int w = 4; w < nwin; ++w) g = fmaf(gam[w] * E[(hi - w) * rv + r], fk(hi - w, j), g);
+        const long x = (long)r * Dp + j;
+        const float sv = et * Ss[x] - th2 * g;
+        Ss[x] = sv;
+        float v = fmaf(keep, Ms[x], sv);
+        if (RK == ATLAS_RET_ELASTIC) {
+          const float a = fabsf(v) - lam;
+          v = a > 0.f ? copysignf(a, v) : 0.f;
+          acc[h] = fmaf(v, qf[u], acc[h]);
+        } else if (RK == ATLAS_RET_BREGMAN) {
+          acc[h] = fmaf(qf[u], 1.f / (1.f + expf(-v)), acc[h]);
+        } else {
+          if (v > mx[h]) {
+            den[h] = den[h] * expf(mx[h] - v) + 1.f;
+            mx[h] = v;
+          } else {
+            den[h] += expf(v - mx[h]);
+          }
+        }
+        uval[h][u] = v;
+        if (RK != ATLAS_RET_KL) Ms[x] = v;
+      }
+    }
+    if (RK == ATLAS_RET_KL) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) warp_lse(mx[h], den[h]);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = rr[h];
+        if (r >= rv) continue;
+        const float shift = mx[h] + logf(den[h]) - logc;  // log M = u - lse(u) + log c
+#pragma unroll
+        for (int u = 0; u < JPL; ++u) {
+          const int j = lane + 32 * u;
+          if (j >= D) continue;
+          const float lm = uval[h][u] - shift;
+          Ms[(long)r * Dp + j] = lm;
+          acc[h] = fmaf(expf(lm), qf[u], acc[h]);
+        }
+      }
+    }
+    const float y0 = warp_sum(acc[0]), y1 = warp_sum(acc[1]);
+    if (lane == 0) {
+      Yrow[rr[0]] = y0;
+      if (rr[1] < rv) Yrow[rr[1]] = y1;
     }
   }
-  float h[5];
-  h[0] = 1.f;
-  float v = a[0] * a[0];
+}
+
+template <int JPL, int RK>
+__device__ __forceinline__ void serial_chunk_fast(int nb, int t0, int i0, int c, int rv, int D,
+                                                  int Dp, float* Ms, float* Ss, const float* E,
+                                                  const Feat& fq, const Feat& fk,
+                                                  const float* sa, const float* se,
+                                                  const float* sb, const float* gam, float lam,
+                                                  float logc, float* Y, int dv) {
+  const int lane = threadIdx.x & 31;
+  for (int n = 0; n < nb; ++n) {
+    const int t = t0 + n;
+    const int hi = t - i0, nwin = min(c, hi + 1);  // window rows hi, hi - 1, ... of token t
+    float qf[JPL], kf[4][JPL];
 #pragma unroll
-  for (int m = 1; m <= 4; ++m) {
-    float s = 0.f;
+    for (int u = 0; u < JPL; ++u) {
+      const int j = min(lane + 32 * u, D - 1);
+      qf[u] = fq(n, j);
 #pragma unroll
-    for (int i = 1; i <= m; ++i) s += pw[i] * h[m - i];
-    h[m] = s / (float)m;
-    if (m <= deg) v += a[m] * a[m] * h[m];
+      for (int w = 0; w < 4; ++w) kf[w][u] = w < nwin ? fk(hi - w, j) : 0.f;
+    }
+    serial_token_fast<JPL, RK>(rv, D, Dp, Ms, Ss, E, hi, nwin, qf, kf, gam, fk, 1.f - sa[n],
+                               se[n], 2.f * sb[n], lam, logc, Y + (long)t * dv);
   }
-  return v;
+}
+
+template <int RK>
+__device__ __forceinline__ void serial_chunk_dispatch(int jpl, int nb, int t0, int i0, int c,
+                                                      int rv, int D, int Dp, float* Ms, float* Ss,
+                                                      const float* E, const Feat& fq,
+                                                      const Feat& fk, const float* sa,
+                                                      const float* se, const float* sb,
+                                                      const float* gam, float lam, float logc,
+                                                      float* Y, int dv) {
+  switch (jpl) {
+    case 1: serial_chunk_fast<1, RK>(nb, t0, i0, c, rv, D, Dp, Ms, Ss, E, fq, fk, sa, se, sb, gam, lam, logc, Y, dv); break;
+    case 2: serial_chunk_fast<2, RK>(nb, t0, i0, c, rv, D, Dp, Ms, Ss, E, fq, fk, sa, se, sb, gam, lam, logc, Y, dv); break;
+    case 3: serial_chunk_fast<3, RK>(nb, t0, i0, c, rv, D, Dp, Ms, Ss, E, fq, fk, sa, se, sb, gam, lam, logc, Y, dv); break;
+    default: serial_chunk_fast<4, RK>(nb, t0, i0, c, rv, D, Dp, Ms, Ss, E, fq, fk, sa, se, sb, gam, lam, logc, Y, dv); break;
+  }
 }
 
 // One CTA: rows [r0, r0 + RV) of one head, the whole sequence.
@@ -160,23 +566,25 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
   float* sa = sm + L.sa;
   float* se = sm + L.se;
   float* sb = sm + L.sb;
+  float* Z = sm + L.Z;
+  float* coef = sm + L.coef;
   uint8_t* pp = reinterpret_cast<uint8_t*>(sm + L.total_floats);
   uint8_t* pq = pp + (L.D - p.d_k > 0 ? L.D - p.d_k : 0);
   uint32_t* ftab = reinterpret_cast<uint32_t*>(sm + L.total_floats);  // gated map
 
-
   const int rv = max(0, min(L.RV, p.d_v - r0));  // a cluster's last CTA may hold none
   const int D = L.D, dk = p.d_k, dv = p.d_v;
   const int tid = threadIdx.x, nt = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
   const long state = (long)dv * D;
+  const int Dp = L.Dp, dkp = L.dkp;
 
+  if (tid < 5) coef[tid] = p.pcoef[tid];
   // pair table of the degree-2 map
-  if (p.poly) {
-    if (tid == 0) {
-      int o = 0;
-      for (int i = 0; i < dk; ++i)
-        for (int j = i; j < dk; ++j) { pp[o] = (uint8_t)i; pq[o] = (uint8_t)j; ++o; }
-    }
+  if (p.poly && tid == 0) {
+    int o = 0;
+    for (int i = 0; i < dk; ++i)
+      for (int j = i; j < dk; ++j) { pp[o] = (uint8_t)i; pq[o] = (uint8_t)j; ++o; }
   }
   // monomial table of the gated map: degrees with a non-zero coefficient, each
   // degree's sorted index tuples in lexicographic order (the next tuple raises
@@ -198,27 +606,21 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
       }
     }
   }
-  auto feat = [&](const float* x, int j) -> float {
-    return p.pgen ? phi_gated(x, ftab[j], p.pcoef) : phi_at(x, j, dk, pp, pq, p.poly);
-  };
+  const Feat fk{Kw, dkp, dk, p.poly, p.pgen, pp, pq, ftab, coef};
+  const Feat fq{Qc, dkp, dk, p.poly, p.pgen, pp, pq, ftab, coef};
   float* Mg = p.M + head * state + (long)r0 * D;
   float* Sg = p.S ? p.S + head * state + (long)r0 * D : nullptr;
   const int ret = p.ret;
   const bool serial = ret == ATLAS_RET_ELASTIC || ret == ATLAS_RET_BREGMAN || ret == ATLAS_RET_KL;
+  const int mk = ret == ATLAS_RET_BREGMAN ? 1 : ret == ATLAS_RET_KL ? 2 : 0;
   for (long x = tid; x < (long)rv * D; x += nt) {
     float m = Mg[x];
     if (ret == ATLAS_RET_BREGMAN) m = logf(m / (1.f - m));  // state as logits
     if (ret == ATLAS_RET_KL) m = logf(m);                   // state as log M
-    Ms[x] = m;
-    Ss[x] = Sg ? Sg[x] : 0.f;
+    const long xs = (x / D) * Dp + x % D;
+    Ms[xs] = m;
+    Ss[xs] = Sg ? Sg[x] : 0.f;
   }
-  // the memory entry a state entry stands for at a chunk start (l_q: before the
-  // row scale Z)
-  auto mem_of = [&](float m) -> float {
-    if (ret == ATLAS_RET_BREGMAN) return 1.f / (1.f + expf(-m));
-    if (ret == ATLAS_RET_KL) return expf(m);
-    return m;
-  };
   const float* alpha = p.alpha + (long)head * p.N;
   const float* eta = p.eta + (long)head * p.N;
   const float* theta = p.theta + (long)head * p.N;
@@ -226,10 +628,9 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
   const long kbase = ((long)head * (p.N + p.nh) + p.nh) * dk;
   const long vbase = ((long)head * (p.N + p.nh) + p.nh) * dv;
   const long qbase = (long)head * p.N * dk;
-  const long ybase = (long)head * p.N * dv;
-  const int lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
-  float* Z = sm + L.Z;
+  float* Yh = p.Y + (long)head * p.N * dv + r0;
   const float logc = ret == ATLAS_RET_KL ? logf(p.rp) : 0.f;
+  const int cls = rows_class(rv);
 
   for (int t0 = 0; t0 < p.N; t0 += p.b) {
     const int t1 = min(p.N, t0 + p.b);
@@ -237,8 +638,10 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
     const int i0 = max(-p.nh, t0 - p.c + 1);
     const int Lw = t1 - i0;
     __syncthreads();
-    for (int x = tid; x < Lw * dk; x += nt) Kw[x] = ld_in(p.K, kbase + (long)i0 * dk + x, p.bf16);
-    for (int x = tid; x < nb * dk; x += nt) Qc[x] = ld_in(p.Q, qbase + (long)t0 * dk + x, p.bf16);
+    for (int x = tid; x < Lw * dk; x += nt)
+      Kw[(x / dk) * dkp + x % dk] = ld_in(p.K, kbase + (long)i0 * dk + x, p.bf16);
+    for (int x = tid; x < nb * dk; x += nt)
+      Qc[(x / dk) * dkp + x % dk] = ld_in(p.Q, qbase + (long)t0 * dk + x, p.bf16);
     for (int x = tid; x < Lw * rv; x += nt) {
       const int i = x / rv, r = x % rv;
       Vw[x] = ld_in(p.V, vbase + (long)(i0 + i) * dv + r0 + r, p.bf16);
@@ -257,30 +660,33 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
     // l_q: Z[r] = 1 / ||A_r||_q^(q-2) of the chunk-start accumulator (1 for a zero row)
     if (ret == ATLAS_RET_LQ) {
       for (int r = warp; r < rv; r += nw) {
-        const float* m = Ms + (long)r * D;
+        const float* m = Ms + (long)r * Dp;
         float acc = 0.f;
         for (int j = lane; j < D; j += 32) acc += powf(fabsf(m[j]), p.rp);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+        acc = warp_sum(acc);
         if (lane == 0) Z[r] = acc > 0.f ? 1.f / powf(acc, (p.rp - 2.f) / p.rp) : 1.f;
       }
     }
     __syncthreads();
     // errors at the chunk-start memory
-    for (int x = tid; x < Lw * rv; x += nt) {
-      const int i = x / rv, r = x % rv;
-      float e;
-      if (p.dot) {
-        e = -Vw[x];
+    if (p.dot) {
+      for (int x = tid; x < Lw * rv; x += nt) E[x] = -Vw[x];
+    } else {
+      const bool lq = ret == ATLAS_RET_LQ;
+      auto fe = [&](int i, int r, float acc) {
+        const float s = lq ? acc * Z[r] : acc;
+        E[i * rv + r] = bias_grad(s - Vw[i * rv + r], p.lk, p.lp);
+      };
+      if (mk == 0) {
+        auto fb = [&](int j, int r) { return Ms[r * Dp + j]; };
+        gemm_by_rows(cls, Lw, rv, D, fk, fb, fe);
+      } else if (mk == 1) {
+        auto fb = [&](int j, int r) { return mem_entry<1>(Ms[r * Dp + j]); };
+        gemm_by_rows(cls, Lw, rv, D, fk, fb, fe);
       } else {
-        const float* m = Ms + (long)r * D;
-        const float* k = Kw + i * dk;
-        float s = 0.f;
-        for (int j = 0; j < D; ++j) s += mem_of(m[j]) * feat(k, j);
-        if (ret == ATLAS_RET_LQ) s *= Z[r];
-        e = bias_grad(s - Vw[x], p.lk, p.lp);
+        auto fb = [&](int j, int r) { return mem_entry<2>(Ms[r * Dp + j]); };
+        gemm_by_rows(cls, Lw, rv, D, fk, fb, fe);
       }
-      E[x] = e;
     }
     if (p.lk == ATLAS_LOSS_ROBUST) {
       float* NR = sm + L.NR;
@@ -289,8 +695,7 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
         const float* e = E + i * rv;
         float ss = 0.f;
         for (int r = lane; r < rv; r += 32) ss += e[r] * e[r];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+        ss = warp_sum(ss);
         if (lane == 0) NR[i] = ss;
       }
       namespace cg = cooperative_groups;
@@ -305,9 +710,7 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
         } else if (lane == 0) {
           part = NR[i];
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o);
-        const float f = robust_scale(sqrtf(part), p.lp);
+        const float f = robust_scale(sqrtf(warp_sum(part)), p.lp);
         float* e = E + i * rv;
         for (int r = lane; r < rv; r += 32) e[r] *= f;
       }
@@ -315,28 +718,40 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
     }
     if (serial) {
       __syncthreads();
-      // token by token; warp w owns rows w, w + nw, ... for the whole chunk
+      if (D <= 128) {
+        const int jpl = (D + 31) / 32;
+        if (ret == ATLAS_RET_ELASTIC)
+          serial_chunk_dispatch<ATLAS_RET_ELASTIC>(jpl, nb, t0, i0, p.c, rv, D, Dp, Ms, Ss, E, fq,
+                                                   fk, sa, se, sb, Urun, p.rp, logc, Yh, dv);
+        else if (ret == ATLAS_RET_BREGMAN)
+          serial_chunk_dispatch<ATLAS_RET_BREGMAN>(jpl, nb, t0, i0, p.c, rv, D, Dp, Ms, Ss, E, fq,
+                                                   fk, sa, se, sb, Urun, p.rp, logc, Yh, dv);
+        else
+          serial_chunk_dispatch<ATLAS_RET_KL>(jpl, nb, t0, i0, p.c, rv, D, Dp, Ms, Ss, E, fq, fk,
+                                              sa, se, sb, Urun, p.rp, logc, Yh, dv);
+        continue;
+      }
+      // wide feature maps: one warp per row, lanes over the columns
       for (int n = 0; n < nb; ++n) {
         const int t = t0 + n;
         const float keep = 1.f - sa[n], et = se[n], th2 = 2.f * sb[n];
         const int hi = t - i0, lo = max(0, hi - p.c + 1);  // window rows of token t
-        const float* q = Qc + n * dk;
         for (int r = warp; r < rv; r += nw) {
-          float* m = Ms + (long)r * D;
-          float* sr = Ss + (long)r * D;
+          float* m = Ms + (long)r * Dp;
+          float* sr = Ss + (long)r * Dp;
           float acc = 0.f, mx = -INFINITY, den = 0.f;
           for (int j = lane; j < D; j += 32) {
             float g = 0.f;
-            for (int i = lo; i <= hi; ++i) g += Urun[hi - i] * E[i * rv + r] * feat(Kw + i * dk, j);
+            for (int i = lo; i <= hi; ++i) g += Urun[hi - i] * E[i * rv + r] * fk(i, j);
             const float sv = et * sr[j] - th2 * g;
             sr[j] = sv;
             float u = keep * m[j] + sv;
             if (ret == ATLAS_RET_ELASTIC) {
               const float a = fabsf(u) - p.rp;
               u = a > 0.f ? copysignf(a, u) : 0.f;
-              acc += u * feat(q, j);
+              acc += u * fq(n, j);
             } else if (ret == ATLAS_RET_BREGMAN) {
-              acc += feat(q, j) / (1.f + expf(-u));
+              acc += fq(n, j) / (1.f + expf(-u));
             } else {  // KL: running max and sum of exp for the row's softmax
               if (u > mx) {
                 den = den * expf(mx - u) + 1.f;
@@ -348,91 +763,63 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
             m[j] = u;
           }
           if (ret == ATLAS_RET_KL) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-              const float om = __shfl_xor_sync(0xFFFFFFFFu, mx, o);
-              const float od = __shfl_xor_sync(0xFFFFFFFFu, den, o);
-              const float nm = fmaxf(mx, om);
-              den = (den > 0.f ? den * expf(mx - nm) : 0.f) + (od > 0.f ? od * expf(om - nm) : 0.f);
-              mx = nm;
-            }
-            // log M = u - logsumexp(u) + log c
-            const float shift = mx + logf(den) - logc;
+            warp_lse(mx, den);
+            const float shift = mx + logf(den) - logc;  // log M = u - lse(u) + log c
             for (int j = lane; j < D; j += 32) {
               const float lm = m[j] - shift;
               m[j] = lm;
-              acc += expf(lm) * feat(q, j);
+              acc += expf(lm) * fq(n, j);
             }
           }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-          if (lane == 0) p.Y[ybase + (long)t * dv + r0 + r] = acc;
+          acc = warp_sum(acc);
+          if (lane == 0) Yh[(long)t * dv + r] = acc;
         }
       }
       continue;
     }
     // masked query-key products P[n,i] = W[n,i] * Phi(q_n).Phi(k_i)
-    for (int x = tid; x < nb * Lw; x += nt) {
-      const int n = x / Lw, i = x % Lw;
-      const float w = P[n * L.Lmax + i];
-      float v = 0.f;
-      if (w != 0.f) {
-        const float* q = Qc + n * dk;
-        const float* k = Kw + i * dk;
-        if (p.pgen) {
-          v = phi_gated_dot(q, k, dk, p.pcoef, p.pdeg);
-        } else {
-          float s = 0.f, s2 = 0.f;
-          for (int j = 0; j < dk; ++j) {
-            const float qk = q[j] * k[j];
-            s += qk;
-            s2 += qk * qk;
-          }
-          v = p.poly ? s + 0.5f * (s * s + s2) : s;
-        }
-        v *= w;
-      }
-      P[n * L.Lmax + i] = v;
-    }
+    if (p.pgen)
+      qk_tile<4>(nb, Lw, dk, Qc, Kw, dkp, P, L.Lmax, 2, coef, p.pdeg);
+    else if (p.poly)
+      qk_tile<2>(nb, Lw, dk, Qc, Kw, dkp, P, L.Lmax, 1, coef, 0);
+    else
+      qk_tile<1>(nb, Lw, dk, Qc, Kw, dkp, P, L.Lmax, 0, coef, 0);
     __syncthreads();
     // readout y_n = M_n Phi(q_n) (l_q: the accumulator's row times Z)
-    for (int x = tid; x < nb * rv; x += nt) {
-      const int n = x / rv, r = x % rv;
-      const float* q = Qc + n * dk;
-      const float* m = Ms + (long)r * D;
-      const float* s = Ss + (long)r * D;
-      float ym = 0.f, ys = 0.f;
-      for (int j = 0; j < D; ++j) {
-        const float f = feat(q, j);
-        ym += m[j] * f;
-        ys += s[j] * f;
+    {
+      bool with_s = false;
+      for (int n = 0; n < nb; ++n) with_s |= sb[n] != 0.f;
+      const float* zr = ret == ATLAS_RET_LQ ? Z : nullptr;
+      float* Yc = Yh + (long)t0 * dv;
+      switch (cls) {
+        case 0: readout_tile<8, 4, 1>(nb, rv, D, Lw, fq, Ms, Ss, Dp, P, L.Lmax, E, sa, sb, with_s, zr, Yc, dv); break;
+        case 1: readout_tile<16, 4, 1>(nb, rv, D, Lw, fq, Ms, Ss, Dp, P, L.Lmax, E, sa, sb, with_s, zr, Yc, dv); break;
+        case 2: readout_tile<16, 4, 2>(nb, rv, D, Lw, fq, Ms, Ss, Dp, P, L.Lmax, E, sa, sb, with_s, zr, Yc, dv); break;
+        case 3: readout_tile<16, 4, 4>(nb, rv, D, Lw, fq, Ms, Ss, Dp, P, L.Lmax, E, sa, sb, with_s, zr, Yc, dv); break;
+        default: readout_tile<16, 4, 8>(nb, rv, D, Lw, fq, Ms, Ss, Dp, P, L.Lmax, E, sa, sb, with_s, zr, Yc, dv); break;
       }
-      float acc = 0.f;
-      for (int i = 0; i < Lw; ++i) acc += P[n * L.Lmax + i] * E[i * rv + r];
-      float y = sa[n] * ym + sb[n] * ys - 2.f * acc;
-      if (ret == ATLAS_RET_LQ) y *= Z[r];
-      p.Y[ybase + (long)(t0 + n) * dv + r0 + r] = y;
     }
     __syncthreads();
     // carry the state to the end of the chunk
-    const float a_b = sa[nb - 1], e_b = se[nb - 1], b_b = sb[nb - 1];
-    for (long x = tid; x < (long)rv * D; x += nt) {
-      const int r = (int)(x / D), j = (int)(x % D);
-      float gw = 0.f, gu = 0.f;
-      for (int i = 0; i < Lw; ++i) {
-        const float f = E[i * rv + r] * feat(Kw + i * dk, j);
-        gw += Wrun[i] * f;
-        gu += Urun[i] * f;
+    {
+      const float a_b = sa[nb - 1], e_b = se[nb - 1], b_b = sb[nb - 1];
+      switch (cls) {
+        case 0: carry_tile<32, 1, 4>(rv, D, Lw, fk, E, Wrun, Urun, Ms, Ss, Dp, a_b, b_b, e_b); break;
+        case 1: carry_tile<16, 1, 8>(rv, D, Lw, fk, E, Wrun, Urun, Ms, Ss, Dp, a_b, b_b, e_b); break;
+        case 2: carry_tile<16, 2, 8>(rv, D, Lw, fk, E, Wrun, Urun, Ms, Ss, Dp, a_b, b_b, e_b); break;
+        case 3: carry_tile<16, 4, 8>(rv, D, Lw, fk, E, Wrun, Urun, Ms, Ss, Dp, a_b, b_b, e_b); break;
+        default: carry_tile<16, 8, 4>(rv, D, Lw, fk, E, Wrun, Urun, Ms, Ss, Dp, a_b, b_b, e_b); break;
       }
-      const float m0 = Ms[x], s0 = Ss[x];
-      Ms[x] = a_b * m0 + b_b * s0 - 2.f * gw;
-      Ss[x] = e_b * s0 - 2.f * gu;
     }
   }
   __syncthreads();
   for (long x = tid; x < (long)rv * D; x += nt) {
-    Mg[x] = serial ? mem_of(Ms[x]) : Ms[x];
-    if (Sg) Sg[x] = Ss[x];
+    const long xs = (x / D) * Dp + x % D;
+    float m = Ms[xs];
+    if (mk == 1) m = mem_entry<1>(m);
+    if (mk == 2) m = mem_entry<2>(m);
+    Mg[x] = m;
+    if (Sg) Sg[x] = Ss[xs];
   }
 }
 

@@ -219,6 +219,11 @@ def flop_per_token(w: Workload) -> float:
     D, dv, b = w.D, w.d_v, w.b
     L = b + w.c - 1
     momentum = w.eta[1] > 0
+    if w.mem == MEM_LINEAR and w.retention in (RET_ELASTIC, RET_BREGMAN, RET_KL):
+        # the token-serial chunk: errors at the chunk-start memory over the window,
+        # then per token the window gradient sum (c rank-1 terms), the momentum and
+        # state steps and the readout, 2 D d_v each
+        return 2.0 * L * D * dv / b + 2.0 * w.c * D * dv + 6.0 * D * dv
     if w.mem == MEM_LINEAR:
         per_chunk = (2.0 * L * D * dv            # errors Phi M0^T over the window
                      + 2.0 * b * D * dv          # Q M0^T
