@@ -262,7 +262,10 @@ def run_reference(args, w):
 _TC = ["tc_primitives.cuh", "common.cuh", "kernels.h"]
 KERNEL_OF_PATH = {
     "linear_tc": (["linear_tc.cu", "linear_simt.cu"] + _TC, "linear_tc_{wname}.md"),
-    "linear_simt": (["linear_simt.cu", "common.cuh", "kernels.h"], "linear_simt_{wname}.md"),
+    "linear_simt": (["linear_simt.cu", "simt_tiles.cuh", "common.cuh", "kernels.h"],
+                    "linear_simt_{wname}.md"),
+    "linear_wide": (["linear_wide.cu", "simt_tiles.cuh", "common.cuh", "kernels.h"],
+                    "linear_wide_{wname}.md"),
     "linear_seq": (["linear_seq.cu", "common.cuh", "kernels.h"], "linear_seq_{wname}.md"),
     "linear_chunk": (["linear_chunk.cu", "tc_gemm.cu"] + _TC, "linear_chunk_{wname}.md"),
     "mlp_simt": (["mlp_simt.cu", "tc_gemm.cu", "ns_fused.cu"] + _TC, "mlp_simt_{wname}.md"),
@@ -362,9 +365,10 @@ def roofline(w, path, kernel_s):
     bytes_launch = tokens * W.bytes_per_token(w) + 2 * 4 * w.heads * w.state_size
     flops_launch = tokens * W.flop_per_token(w)
     ridge = tf * 1e12 / (hbm * 1e9)
-    # fp32 FMAs on CUDA cores: the token-serial and CUDA-core linear kernels, and the
+    # fp32 FMAs on CUDA cores: the token-serial, CUDA-core and wide-map linear kernels, and the
     # CUDA-core MLP path when no Newton-Schulz products go to the tensor cores
-    if path in ("linear_seq", "linear_simt") or (path == "mlp_simt" and w.ns_steps == 0):
+    if path in ("linear_seq", "linear_simt", "linear_wide") or (path == "mlp_simt" and
+                                                                  w.ns_steps == 0):
         peak = fp32_alu_peak_tflops()
         achieved = flops_launch / kernel_s / 1e12
         roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

@@ -12,7 +12,7 @@ namespace {
 
 enum Path {
   PATH_INVALID = 0, PATH_LINEAR_SIMT, PATH_LINEAR_TC, PATH_LINEAR_SEQ, PATH_LINEAR_CHUNK,
-  PATH_MLP_SIMT, PATH_MLP_TC
+  PATH_MLP_SIMT, PATH_MLP_TC, PATH_LINEAR_WIDE
 };
 
 // Monomials of degree exactly e in d variables: C(d + e - 1, e).
@@ -138,6 +138,11 @@ Path choose_path(const atlas_mem_cfg* c) {
   }
   LinArgs a = lin_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, c,
                        nullptr, nullptr);
+  const int heads = c->B * c->H;
+  // wide feature maps (the degree-2 map, the gated map): the fused cluster kernel
+  if (linear_wide_supported(a, heads) && !(a.nh == 0 && linear_tc_supported(a)) &&
+      !linear_seq_supported(a))
+    return PATH_LINEAR_WIDE;
   // the gated polynomial map, the retention gates and the robust bias: CUDA-core kernel only
   if (a.pgen || a.ret != ATLAS_RET_L2 || a.lk == ATLAS_LOSS_ROBUST) {
     int RV;
@@ -188,6 +193,7 @@ const char* atlas_mem_path(const atlas_mem_cfg* cfg) {
     case PATH_LINEAR_TC: return "linear_tc";
     case PATH_LINEAR_SEQ: return "linear_seq";
     case PATH_LINEAR_CHUNK: return "linear_chunk";
+    case PATH_LINEAR_WIDE: return "linear_wide";
     case PATH_MLP_SIMT: return "mlp_simt";
     case PATH_MLP_TC: return "mlp_tc";
     default: return "";
@@ -198,6 +204,7 @@ long atlas_mem_launch_count(const atlas_mem_cfg* cfg) {
   switch (choose_path(cfg)) {
     case PATH_LINEAR_SIMT:
     case PATH_LINEAR_SEQ:
+    case PATH_LINEAR_WIDE:
     case PATH_MLP_TC:
       return (long)cfg->B * cfg->H > 0 ? 1 : 0;
     case PATH_LINEAR_TC:
@@ -250,6 +257,7 @@ int atlas_mem_forward(const void* K, const void* Q, const void* V, const float* 
     return linear_tc_launch(a, (int)heads, cfg->status_dev, cfg->workspace, st);
   }
   if (path == PATH_LINEAR_SEQ) return linear_seq_launch(a, (int)heads, st);
+  if (path == PATH_LINEAR_WIDE) return linear_wide_launch(a, (int)heads, st);
   if (path == PATH_LINEAR_CHUNK) {
     const size_t need = linear_chunk_workspace_bytes(a, (int)heads);
     if (!cfg->workspace || cfg->workspace_bytes < need) return ATLAS_ERR_WORKSPACE;

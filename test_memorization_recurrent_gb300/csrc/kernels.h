@@ -39,6 +39,11 @@ int linear_simt_plan(const LinArgs& a, int heads, int* RV_out, size_t* smem_out)
 bool linear_seq_supported(const LinArgs& a);
 int linear_seq_launch(const LinArgs& a, int heads, cudaStream_t st);
 
+// Fused path for linear memories with a wide feature map (D >= 256): one
+// thread-block cluster per head, feature columns split over its CTAs.
+bool linear_wide_supported(const LinArgs& a, int heads);
+int linear_wide_launch(const LinArgs& a, int heads, cudaStream_t st);
+
 // Host-driven path for linear memories with a wide feature map (D >= 256, the
 // degree-2 map): per chunk, batched tensor-core GEMMs over all heads.
 bool linear_chunk_supported(const LinArgs& a);

@@ -52,8 +52,8 @@ def test_state_size_and_path(lib, wid):
     w = W.workload(wid)
     cfg = cfg_for(w, w.heads, w.N)
     assert A.atlas_mem_state_size(cfg) == w.state_size
-    assert A.atlas_mem_path(cfg) in ("linear_simt", "linear_seq", "linear_chunk", "linear_tc", "mlp_simt",
-                                      "mlp_tc")
+    assert A.atlas_mem_path(cfg) in ("linear_simt", "linear_seq", "linear_chunk", "linear_tc",
+                                      "linear_wide", "mlp_simt", "mlp_tc")
     assert A.atlas_mem_launch_count(cfg) >= 1
     nbytes = A.atlas_mem_workspace_bytes(cfg)
     assert nbytes >= 0
@@ -134,7 +134,7 @@ def test_alternative_biases_choose_paths_that_apply_them(lib):
     their l2 paths."""
     from test_memorization_recurrent_gb300.harness import cfg_for
     for loss, prm in ((A.LOSS_LP, 3.0), (A.LOSS_HUBER, 0.5)):
-        for wid, path in ((1, "linear_seq"), (2, "linear_tc"), (3, "linear_chunk"),
+        for wid, path in ((1, "linear_seq"), (2, "linear_tc"), (3, "linear_wide"),
                           (4, "mlp_tc"), (5, "mlp_simt")):
             w = W.workload(wid)
             w = w.__class__(**{**w.__dict__, "loss": loss, "loss_param": prm})
@@ -143,11 +143,11 @@ def test_alternative_biases_choose_paths_that_apply_them(lib):
 
 
 def test_bias_launches_are_counted():
-    """The wide-feature and CUDA-core MLP paths add one elementwise launch per chunk for
-    an l_p or Huber bias; the other paths apply it inside their kernels."""
+    """The host-driven wide-feature and CUDA-core MLP paths add one elementwise launch
+    per chunk for an l_p or Huber bias; the other paths apply it inside their kernels."""
     from test_memorization_recurrent_gb300.harness import cfg_for
     N = 64 * 3 + 5  # four chunks
-    for wid, extra in ((1, 0), (2, 0), (3, 4), (4, 0), (5, 4)):
+    for wid, extra in ((1, 0), (2, 0), (3, 0), (4, 0), (5, 4)):
         w = W.workload(wid)
         base = A.atlas_mem_launch_count(cfg_for(w, 2, N))
         wb = w.__class__(**{**w.__dict__, "loss": A.LOSS_HUBER, "loss_param": 0.3})
@@ -184,14 +184,15 @@ def test_backward_workspace_and_missing_workspace(lib):
 
 
 def test_gated_polynomial_map_sizes(lib):
-    """D counts the monomials of every degree whose coefficient is non-zero, and the
-    gated map always runs on the CUDA-core linear kernel."""
+    """D counts the monomials of every degree whose coefficient is non-zero; the
+    gated map runs on the CUDA-core linear kernels (the fused cluster kernel once
+    D >= 256)."""
     import math
     for d, coef in ((8, (0, 1, 1, 1)), (6, (0.5, 1, 0, 0.8, 0.4)), (32, (0, 1, 1))):
         cfg = A.make_cfg(B=1, H=2, N=64, d_k=d, d_v=16, phi=A.PHI_POLY, phi_coef=coef, c=2, b=8)
         D = sum(math.comb(d + e - 1, e) for e, a in enumerate(coef) if a != 0)
         assert A.atlas_mem_state_size(cfg) == 16 * D
-        assert A.atlas_mem_path(cfg) == "linear_simt"
+        assert A.atlas_mem_path(cfg) == ("linear_wide" if D >= 256 else "linear_simt")
     # a = (0, 1, 1) describes the same features as the degree-2 map
     g = A.make_cfg(B=1, H=1, N=8, d_k=32, d_v=64, phi=A.PHI_POLY, phi_coef=(0, 1, 1))
     p2 = A.make_cfg(B=1, H=1, N=8, d_k=32, d_v=64, phi=A.PHI_POLY2)
@@ -227,9 +228,10 @@ def test_gated_memory_runs_on_the_cuda_core_mlp_path(lib):
 
 
 def test_retention_gates_and_robust_bias_run_on_the_cuda_core_kernels(lib):
-    """Every retention gate other than l2 and the robust bias select the CUDA-core
-    linear kernel (one launch); the robust bias on an MLP memory the CUDA-core MLP
-    path, one row-scaling launch per chunk where the l2 bias has none."""
+    """Every retention gate other than l2 selects the CUDA-core linear kernel (one
+    launch), as does the robust bias on a narrow map (a wide one keeps the fused
+    cluster kernel, whose error rows are whole); on an MLP memory the robust bias
+    takes the CUDA-core MLP path, one row-scaling launch per chunk."""
     from test_memorization_recurrent_gb300.harness import cfg_for
     for ret, prm in ((A.RET_ELASTIC, 0.01), (A.RET_BREGMAN, 0.0), (A.RET_KL, 1.0),
                      (A.RET_LQ, 3.0)):
@@ -239,9 +241,9 @@ def test_retention_gates_and_robust_bias_run_on_the_cuda_core_kernels(lib):
             assert A.atlas_mem_path(cfg) == "linear_simt", (wid, ret)
             assert A.atlas_mem_launch_count(cfg) == 1
             assert A.atlas_mem_state_size(cfg) == w.state_size
-    for wid in (1, 2, 3):
+    for wid, path in ((1, "linear_simt"), (2, "linear_simt"), (3, "linear_wide")):
         w = W.workload(wid, loss=A.LOSS_ROBUST, loss_param=0.5)
-        assert A.atlas_mem_path(cfg_for(w, 2, 256)) == "linear_simt"
+        assert A.atlas_mem_path(cfg_for(w, 2, 256)) == path
     N = 64 * 3 + 5  # four chunks
     for wid, extra in ((4, 4), (5, 4)):
         w = W.workload(wid)
@@ -260,3 +262,17 @@ def test_robust_bias_on_wide_memories_is_planned_in_clusters(lib):
                      loss_param=0.5)
     assert A.atlas_mem_path(cfg) == "linear_simt"
     assert A.atlas_mem_workspace_bytes(cfg) == 0
+
+
+def test_wide_maps_choose_the_fused_cluster_kernel(lib):
+    """The degree-2 workload and the gated degree-3 map (D = 968) run as one launch
+    of the fused kernel; more than 128 value rows fall back to the host-driven path."""
+    from test_memorization_recurrent_gb300.harness import cfg_for
+    w = W.workload(3)
+    cfg = cfg_for(w, w.heads, w.N)
+    assert A.atlas_mem_path(cfg) == "linear_wide"
+    assert A.atlas_mem_launch_count(cfg) == 1
+    assert A.atlas_mem_workspace_bytes(cfg) == 0
+    g = w.with_(d_k=16, phi=A.PHI_POLY, phi_coef=(0.0, 1.0, 1.0, 1.0))
+    assert A.atlas_mem_path(cfg_for(g, 32, 2048)) == "linear_wide"
+    assert A.atlas_mem_path(cfg_for(w.with_(d_v=160), 2, 256)) == "linear_chunk"

@@ -367,13 +367,14 @@ def test_alternative_biases(wid, N, heads, loss, prm):
 ])
 def test_gated_polynomial_map(d_k, coef, c, b, N, heads):
     """The gated polynomial map of degree 3 and 4 ("논문 리뷰 Google ATLAS" §3.1,
-    Polynomial Feature Mapping and Input gating) on the CUDA-core linear kernel,
+    Polynomial Feature Mapping and Input gating) on the CUDA-core linear kernels,
     against the oracle; momentum and decay as in the poly2 workload (bounded step)."""
     from test_memorization_recurrent_gb300.harness import cfg_for
     import test_memorization_recurrent_gb300 as A
     w = W.workload(3, bounded=True, d_k=d_k, phi=W.PHI_POLY, phi_coef=coef, c=c, b=b, N=N,
                    theta_scale=0.002)
-    assert A.atlas_mem_path(cfg_for(w, len(heads), N)) == "linear_simt"
+    path = "linear_wide" if w.D >= 256 else "linear_simt"  # the fused cluster kernel when wide
+    assert A.atlas_mem_path(cfg_for(w, len(heads), N)) == path
     inp = W.generate(w, heads=heads, n_tokens=N)
     Yo, Mo, So = run_oracle(w, inp)
     Yg, Mg, Sg = gpu_run(w, inp, with_S=True)
@@ -498,7 +499,7 @@ def test_retention_gates_from_a_random_state(ret, prm):
 @pytest.mark.parametrize("wid,kw,N,heads,path", [
     (2, dict(eta=(0.5, 0.9)), 64 + 13, [0, 5], "linear_simt"),    # 8-CTA clusters per head
     (1, dict(), 120, [0], "linear_simt"),                          # fp32 recurrence, c = 4
-    (3, dict(), 64 + 9, [0], "linear_simt"),                       # degree-2 map, d_v = 64
+    (3, dict(), 64 + 9, [0], "linear_wide"),                       # degree-2 map, d_v = 64
     (2, dict(retention=W.RET_ELASTIC, ret_param=0.01), 64 + 5, [3], "linear_simt"),
     (4, dict(), 64 + 19, [0, 7], "mlp_simt"),                      # MLP memory, momentum
     (4, dict(mem=W.MEM_MLP_LN), 64 + 5, [1], "mlp_simt"),          # through LN
@@ -516,3 +517,22 @@ def test_robust_bias(wid, kw, N, heads, path):
     Yo, Mo, _ = run_oracle(w, inp)
     Yg, Mg, _ = gpu_run(w, inp)
     check(w, Yg, Mg, Yo, Mo, f"workload {wid} robust {kw}")
+
+
+@pytest.mark.parametrize("kw,N,heads,path", [
+    (dict(d_v=160), 64 + 9, [0, 1], "linear_chunk"),   # too many value rows for the cluster
+    (dict(), 64 * 2 + 5, [0, 31], "linear_wide"),       # 4-CTA clusters, momentum, window 64
+    (dict(d_v=24, c=3, b=16), 70, [2], "linear_wide"),  # other widths, window, chunk
+])
+def test_wide_feature_map_paths(kw, N, heads, path):
+    """The degree-2 map (D = 560) on the fused cluster kernel and, beyond its row
+    limit, on the host-driven batched path, against the oracle with momentum S."""
+    from test_memorization_recurrent_gb300.harness import cfg_for
+    import test_memorization_recurrent_gb300 as A
+    w = W.workload(3, bounded=True, **kw)
+    assert A.atlas_mem_path(cfg_for(w, len(heads), N)) == path
+    inp = W.generate(w, heads=heads, n_tokens=N)
+    Yo, Mo, So = run_oracle(w, inp)
+    Yg, Mg, Sg = gpu_run(w, inp, with_S=True)
+    check(w, Yg, Mg, Yo, Mo, f"wide map {kw}")
+    assert rel_err(Sg, So, w.bf16) <= tol(w)
