@@ -66,8 +66,8 @@ extern "C" {
  * with a_e = cfg->phi_coef[e]; each degree's monomials appear once (no
  * multinomial weights), in lexicographic order of their sorted index tuples; a
  * degree whose a_e is 0 is left out, so D = sum over kept e of C(d_k + e - 1, e).
- * a = (0, 1, 1) is ATLAS_PHI_POLY2.  Runs on the CUDA-core linear kernel;
- * d_k <= 255, D <= 16384. */
+ * a = (0, 1, 1) is ATLAS_PHI_POLY2.  Runs on the CUDA-core linear kernels (the
+ * fused cluster kernel once D >= 256 and d_v <= 128); d_k <= 255, D <= 16384. */
 #define ATLAS_PHI_POLY 2
 #define ATLAS_PHI_MAX_DEGREE 4
 /* attentional bias */
@@ -81,8 +81,10 @@ extern "C" {
 /* Robust bias against a value shift of norm at most Delta = loss_param >= 0,
  * read as its worst case (||e|| + Delta)^2 over the whole value vector e:
  * gradient 2 e (1 + Delta / ||e||), 0 at e = 0.  Delta = 0 is ATLAS_LOSS_L2.
- * Couples the d_v coordinates of a token, so the CUDA-core kernels run it
- * (linear memory: one CTA holds all d_v rows of a head). */
+ * Couples the d_v coordinates of a token, so the CUDA-core kernels run it (linear
+ * memory: a head's row blocks form one thread-block cluster and add their
+ * partial norms; wide feature maps: the fused cluster kernel, whose error rows
+ * are whole; MLP memories: the CUDA-core MLP path). */
 #define ATLAS_LOSS_ROBUST 4
 /* Retention gate of the linear memory ("It's All Connected: ... (Miras)", #2
  * Alternative Retention Gates), the map from (M_{t-1}, alpha_t, U_t), U_t the
@@ -246,8 +248,8 @@ int atlas_mem_forward_noalloc(const void* K, const void* Q, const void* V, const
 const char* atlas_mem_strerror(int status);
 
 /* Name of the kernel family atlas_mem_forward would launch for cfg (for
- * reports): "linear_tc", "linear_seq", "linear_chunk", "linear_simt", "mlp_tc",
- * "mlp_simt", or "" if invalid. */
+ * reports): "linear_tc", "linear_seq", "linear_wide", "linear_chunk",
+ * "linear_simt", "mlp_tc", "mlp_simt", or "" if invalid. */
 const char* atlas_mem_path(const atlas_mem_cfg* cfg);
 
 /* Number of kernel launches atlas_mem_forward makes for cfg (for reports). */
