@@ -261,9 +261,10 @@ def run_reference(args, w):
 # only while all of them are unchanged) and the summary's file name.
 _TC = ["tc_primitives.cuh", "common.cuh", "kernels.h"]
 KERNEL_OF_PATH = {
-    "linear_tc": (["linear_tc.cu", "linear_simt.cu"] + _TC, "linear_tc_{wname}.md"),
-    "linear_simt": (["linear_simt.cu", "simt_tiles.cuh", "common.cuh", "kernels.h"],
-                    "linear_simt_{wname}.md"),
+    "linear_tc": (["linear_tc.cu", "linear_simt.cu", "linear_simt_body.cuh"] + _TC,
+                  "linear_tc_{wname}.md"),
+    "linear_simt": (["linear_simt.cu", "linear_simt_serial.cu", "linear_simt_body.cuh",
+                     "simt_tiles.cuh", "common.cuh", "kernels.h"], "linear_simt_{wname}.md"),
     "linear_wide": (["linear_wide.cu", "simt_tiles.cuh", "common.cuh", "kernels.h"],
                     "linear_wide_{wname}.md"),
     "linear_seq": (["linear_seq.cu", "common.cuh", "kernels.h"], "linear_seq_{wname}.md"),
