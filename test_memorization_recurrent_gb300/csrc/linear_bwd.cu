@@ -38,6 +38,7 @@
 //   bwd_finish_kernel  (head x chunk): sums the partials, dP, the gate scans, dK, dQ.
 #include "common.cuh"
 #include "kernels.h"
+#include "simt_tiles.cuh"
 
 namespace atlas {
 
@@ -130,12 +131,6 @@ __device__ __forceinline__ float bias_grad2(float e, int kind, float prm) {
   return 1.f;
 }
 
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
-  return x;
-}
-
 // K, Q rows of chunk j (tokens t0.., zero past N) into fp32 shared memory with
 // row strides ldk, ldq.
 __device__ __forceinline__ void load_kq(const BwdArgs& p, int h, int t0, int nb, float* sK,
@@ -224,14 +219,142 @@ __global__ void __launch_bounds__(kThreads) bwd_tables_kernel(BwdArgs p) {
 }
 
 // ------------------------------------------------- row-block recursion
+//
+// Every product of the recursion is a small dense contraction over shared
+// memory, computed by register tiles (simt_tiles.cuh): 256 threads as a 16 x 16
+// grid, each accumulating a few outputs spaced 16 apart, so a k-step loads a
+// handful of operands for several FMAs.  The three phases that share operands
+// accumulate their products together.
+
+// t = K M0^T, z = K dMe^T, mq = Q M0^T for the chunk's 64 tokens x 32 rows
+// (thread: tokens ty + 16 u, rows tx + 16 v).
+template <class FE>
+__device__ __forceinline__ void bwd_tile_tzq(const float* sK, const float* sQ, const float* sM0,
+                                             const float* sDM, const FE& fe) {
+  constexpr int TM = 4, TN = 2;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float at[TM][TN], az[TM][TN], aq[TM][TN];
+#pragma unroll
+  for (int u = 0; u < TM; ++u)
+#pragma unroll
+    for (int v = 0; v < TN; ++v) at[u][v] = az[u][v] = aq[u][v] = 0.f;
+  for (int f = 0; f < kD; ++f) {
+    float k[TM], q[TM], m[TN], d[TN];
+#pragma unroll
+    for (int u = 0; u < TM; ++u) {
+      k[u] = sK[(ty + 16 * u) * kPad + f];
+      q[u] = sQ[(ty + 16 * u) * kPad + f];
+    }
+#pragma unroll
+    for (int v = 0; v < TN; ++v) {
+      m[v] = sM0[(tx + 16 * v) * kPad + f];
+      d[v] = sDM[(tx + 16 * v) * kPad + f];
+    }
+#pragma unroll
+    for (int u = 0; u < TM; ++u)
+#pragma unroll
+      for (int v = 0; v < TN; ++v) {
+        at[u][v] = fmaf(k[u], m[v], at[u][v]);
+        az[u][v] = fmaf(k[u], d[v], az[u][v]);
+        aq[u][v] = fmaf(q[u], m[v], aq[u][v]);
+      }
+  }
+#pragma unroll
+  for (int u = 0; u < TM; ++u)
+#pragma unroll
+    for (int v = 0; v < TN; ++v) fe(ty + 16 * u, tx + 16 * v, at[u][v], az[u][v], aq[u][v]);
+}
+
+// s1 = dT M0, s2 = E dMe, s3 = dY M0 for 64 tokens x 128 features (two column
+// blocks of 64; thread: tokens ty + 16 u, features tx + 16 v).
+template <class FE>
+__device__ __forceinline__ void bwd_tile_kq(const float* sDT, const float* sE, const float* sDY,
+                                            const float* sM0, const float* sDM, const FE& fe) {
+  constexpr int TM = 4, TN = 4;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  for (int f0 = 0; f0 < kD; f0 += 16 * TN) {
+    float s1[TM][TN], s2[TM][TN], s3[TM][TN];
+#pragma unroll
+    for (int u = 0; u < TM; ++u)
+#pragma unroll
+      for (int v = 0; v < TN; ++v) s1[u][v] = s2[u][v] = s3[u][v] = 0.f;
+    for (int r = 0; r < kRB; ++r) {
+      float dt[TM], e[TM], dy[TM], m[TN], d[TN];
+#pragma unroll
+      for (int u = 0; u < TM; ++u) {
+        const int i = ty + 16 * u;
+        dt[u] = sDT[i * kPadB + r];
+        e[u] = sE[i * kPadB + r];
+        dy[u] = sDY[i * kPadB + r];
+      }
+#pragma unroll
+      for (int v = 0; v < TN; ++v) {
+        m[v] = sM0[r * kPad + f0 + tx + 16 * v];
+        d[v] = sDM[r * kPad + f0 + tx + 16 * v];
+      }
+#pragma unroll
+      for (int u = 0; u < TM; ++u)
+#pragma unroll
+        for (int v = 0; v < TN; ++v) {
+          s1[u][v] = fmaf(dt[u], m[v], s1[u][v]);
+          s2[u][v] = fmaf(e[u], d[v], s2[u][v]);
+          s3[u][v] = fmaf(dy[u], m[v], s3[u][v]);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < TM; ++u)
+#pragma unroll
+      for (int v = 0; v < TN; ++v)
+        fe(ty + 16 * u, f0 + tx + 16 * v, s1[u][v], s2[u][v], s3[u][v]);
+  }
+}
+
+// dMe[v][f] <- a_63 dMe[v][f] + sum_n (a_n dY[n][v] Q[n][f] + dT[n][v] K[n][f])
+// (thread: rows ty + 16 u, features tx + 16 v).
+__device__ __forceinline__ void bwd_tile_dm(const float* sA, const float* sDY, const float* sDT,
+                                            const float* sQ, const float* sK, float* sDM) {
+  constexpr int TM = 2, TN = 8;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float acc[TM][TN];
+#pragma unroll
+  for (int u = 0; u < TM; ++u)
+#pragma unroll
+    for (int v = 0; v < TN; ++v) acc[u][v] = 0.f;
+  for (int n = 0; n < kB; ++n) {
+    const float an = sA[n];
+    float ay[TM], dt[TM], q[TN], k[TN];
+#pragma unroll
+    for (int u = 0; u < TM; ++u) {
+      ay[u] = an * sDY[n * kPadB + ty + 16 * u];
+      dt[u] = sDT[n * kPadB + ty + 16 * u];
+    }
+#pragma unroll
+    for (int v = 0; v < TN; ++v) {
+      q[v] = sQ[n * kPad + tx + 16 * v];
+      k[v] = sK[n * kPad + tx + 16 * v];
+    }
+#pragma unroll
+    for (int u = 0; u < TM; ++u)
+#pragma unroll
+      for (int v = 0; v < TN; ++v) acc[u][v] = fmaf(ay[u], q[v], fmaf(dt[u], k[v], acc[u][v]));
+  }
+  const float a63 = sA[kB - 1];
+#pragma unroll
+  for (int u = 0; u < TM; ++u)
+#pragma unroll
+    for (int v = 0; v < TN; ++v) {
+      float* x = sDM + (ty + 16 * u) * kPad + tx + 16 * v;
+      *x = a63 * *x + acc[u][v];
+    }
+}
 
 __global__ void __launch_bounds__(kThreads, 1) bwd_rows_kernel(BwdArgs p) {
   extern __shared__ float sm[];
   float* sM0 = sm;                    // [kRB][kPad] state rows
   float* sDM = sM0 + kRB * kPad;      // [kRB][kPad] dMe rows
-  float* sK = sDM + kRB * kPad;       // [kB][kD]
-  float* sQ = sK + kB * kD;           // [kB][kD]
-  float* sV = sQ + kB * kD;           // [kB][kPadB] V[i][v]
+  float* sK = sDM + kRB * kPad;       // [kB][kPad]
+  float* sQ = sK + kB * kPad;         // [kB][kPad]
+  float* sV = sQ + kB * kPad;         // [kB][kPadB] V[i][v]
   float* sDY = sV + kB * kPadB;       // [kB][kPadB]
   float* sE = sDY + kB * kPadB;       // [kB][kPadB]
   float* sBP = sE + kB * kPadB;       // [kB][kPadB] bias'
@@ -265,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_rows_kernel(BwdArgs p) {
       const int v = x / kD, f = x % kD;
       ck[(size_t)(v0 + v) * kD + f] = sM0[v * kPad + f];
     }
-    load_kq(p, h, t0, nb, sK, kD, nullptr, 0);
+    load_kq(p, h, t0, nb, sK, kPad, nullptr, 0);
     for (int x = tid; x < kB * kRB; x += kThreads) {
       const int i = x / kRB, v = x % kRB;
       sV[i * kPadB + v] = i < nb ? ld_in(p.V, (hN + t0 + i) * kD + v0 + v, p.bf16) : 0.f;
@@ -275,27 +398,23 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_rows_kernel(BwdArgs p) {
       sWb[tid] = p.tW[cb * kB * kB + (kB - 1) * kB + tid];
     }
     __syncthreads();
-    {  // E[i][v] = bias(K M0^T - V), weighted by wb_i
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const int i = warp + 8 * r;
-        float t = 0.f;
-        for (int f = 0; f < kD; ++f) t += sK[i * kD + f] * sM0[lane * kPad + f];
-        const float e = t - sV[i * kPadB + lane];
-        sE[i * kPadB + lane] = sWb[i] * bias_grad(e, p.lk, p.lp);
-      }
+    {  // E[i][v] = wb_i bias(K M0^T - V)
+      auto fa = [&](int i, int f) { return sK[i * kPad + f]; };
+      auto fb = [&](int f, int v) { return sM0[v * kPad + f]; };
+      auto fe = [&](int i, int v, float t) {
+        sE[i * kPadB + v] = sWb[i] * bias_grad(t - sV[i * kPadB + v], p.lk, p.lp);
+      };
+      tile_gemm<16, 4, 2>(kB, kRB, kD, fa, fb, fe);
     }
     __syncthreads();
     {  // M_end[v][f] = a_63 M0[v][f] - 2 sum_i (wb E)[i][v] k_i[f]
-      const int f = tid & (kD - 1), vg = tid >> 7;
       const float a63 = sA[kB - 1];
-#pragma unroll 4
-      for (int r = 0; r < kRB / 2; ++r) {
-        const int v = vg + 2 * r;
-        float s = 0.f;
-        for (int i = 0; i < kB; ++i) s += sE[i * kPadB + v] * sK[i * kD + f];
+      auto fa = [&](int v, int i) { return sE[i * kPadB + v]; };
+      auto fb = [&](int i, int f) { return sK[i * kPad + f]; };
+      auto fe = [&](int v, int f, float s) {
         sM0[v * kPad + f] = a63 * sM0[v * kPad + f] - 2.f * s;
-      }
+      };
+      tile_gemm<16, 2, 8>(kRB, kD, kB, fa, fb, fe);
     }
   }
   // ------------------------------------------------------------ reverse
@@ -314,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_rows_kernel(BwdArgs p) {
       const int v = x / kD, f = x % kD;
       sM0[v * kPad + f] = ck[(size_t)(v0 + v) * kD + f];
     }
-    load_kq(p, h, t0, nb, sK, kD, sQ, kD);
+    load_kq(p, h, t0, nb, sK, kPad, sQ, kPad);
     for (int x = tid; x < kB * kRB; x += kThreads) {
       const int i = x / kRB, v = x % kRB;
       const bool ok = i < nb;
@@ -329,47 +448,40 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_rows_kernel(BwdArgs p) {
     if (tid <= kB) sRp[tid] = p.tR[cb * (kB + 1) + tid];
     if (tid < kD) sKp[tid] = j > 0 ? ld_in(p.K, (hN + t0 - 1) * kD + tid, p.bf16) : 0.f;
     __syncthreads();
-    // -- T, E, bias'; Z = K dMe^T; Mq = M0 q  (thread: v = lane, token = warp + 8 r)
-    {
-#pragma unroll 2
-      for (int r = 0; r < 8; ++r) {
-        const int i = warp + 8 * r;
-        float t = 0.f, z = 0.f, mq = 0.f;
-        for (int f = 0; f < kD; ++f) {
-          const float m = sM0[lane * kPad + f];
-          t += sK[i * kD + f] * m;
-          z += sK[i * kD + f] * sDM[lane * kPad + f];
-          mq += sQ[i * kD + f] * m;
-        }
-        const float e = t - sV[i * kPadB + lane];
-        const float E = bias_grad(e, p.lk, p.lp);
-        sE[i * kPadB + lane] = E;
-        sBP[i * kPadB + lane] = bias_grad2(e, p.lk, p.lp);
-        sZ[i * kPadB + lane] = z;
-        sMq[i * kPadB + lane] = mq;
-        if (i == kB - 1 && have_x) {
-          // <dM_{t0'} k_{t0'-1}, e_{t0'-1}> of the chunk after this one (its
-          // first token's momentum term), with e_{t0'-1} = this chunk's last error
-          const float s = warp_sum(sX[lane] * E);
-          if (lane == 0) p.pE0[((size_t)rb * p.heads + h) * nch + j + 1] = s;
-        }
-      }
-    }
+    // -- T, E, bias'; Z = K dMe^T; Mq = M0 q
+    bwd_tile_tzq(sK, sQ, sM0, sDM, [&](int i, int v, float t, float z, float mq) {
+      const float e = t - sV[i * kPadB + v];
+      sE[i * kPadB + v] = bias_grad(e, p.lk, p.lp);
+      sBP[i * kPadB + v] = bias_grad2(e, p.lk, p.lp);
+      sZ[i * kPadB + v] = z;
+      sMq[i * kPadB + v] = mq;
+    });
     __syncthreads();
-    // -- dE, dT, dV; dwb and da partials (thread: v = lane, token = warp + 8 r)
+    if (warp == 0 && have_x) {
+      // <dM_{t0'} k_{t0'-1}, e_{t0'-1}> of the chunk after this one (its first
+      // token's momentum term), with e_{t0'-1} = this chunk's last error
+      const float s = warp_sum(sX[lane] * sE[(kB - 1) * kPadB + lane]);
+      if (lane == 0) p.pE0[((size_t)rb * p.heads + h) * nch + j + 1] = s;
+    }
+    // -- dE, dT, dV (dE = -2 C^T dY - 2 wb Z)
+    {
+      auto fa = [&](int i, int n) { return sC[n * kB + i]; };
+      auto fb = [&](int n, int v) { return sDY[n * kPadB + v]; };
+      auto fe = [&](int i, int v, float s) {
+        const float dE = -2.f * s - 2.f * sWb[i] * sZ[i * kPadB + v];
+        const float dT = dE * sBP[i * kPadB + v];
+        sDT[i * kPadB + v] = dT;
+        if (i < nb) p.dV[(hN + t0 + i) * kD + v0 + v] = -dT;
+      };
+      tile_gemm<16, 4, 2>(kB, kRB, kB, fa, fb, fe);
+    }
+    // -- dwb and da partials (warp: tokens warp + 8 r; lane: row v)
     {
       const size_t pb = ((size_t)rb * p.heads + h) * nch + j;
 #pragma unroll 2
       for (int r = 0; r < 8; ++r) {
         const int i = warp + 8 * r;
-        float s = 0.f;
-        for (int n = 0; n < kB; ++n) s += sC[n * kB + i] * sDY[n * kPadB + lane];
-        const float z = sZ[i * kPadB + lane];
-        const float dE = -2.f * s - 2.f * sWb[i] * z;
-        const float dT = dE * sBP[i * kPadB + lane];
-        sDT[i * kPadB + lane] = dT;
-        if (i < nb) p.dV[(hN + t0 + i) * kD + v0 + lane] = -dT;
-        const float wbp = warp_sum(sE[i * kPadB + lane] * z);
+        const float wbp = warp_sum(sE[i * kPadB + lane] * sZ[i * kPadB + lane]);
         float ap = sDY[i * kPadB + lane] * sMq[i * kPadB + lane];
         if (i == kB - 1) {  // a_63 also scales M0 in M_end
           for (int f = 0; f < kD; ++f) ap += sDM[lane * kPad + f] * sM0[lane * kPad + f];
@@ -384,32 +496,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_rows_kernel(BwdArgs p) {
     __syncthreads();
     // -- dK, dQ, dC partials; the first token's momentum vector x
     {
-      const int f = tid & (kD - 1), ig = tid >> 7;
       const size_t ob = ((size_t)rb * p.heads + h) * N;
-      for (int r = 0; r < kB / 2; ++r) {
-        const int i = ig + 2 * r;
-        float s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll 8
-        for (int v = 0; v < kRB; ++v) {
-          const float m = sM0[v * kPad + f];
-          s1 += sDT[i * kPadB + v] * m;
-          s2 += sE[i * kPadB + v] * sDM[v * kPad + f];
-          s3 += sDY[i * kPadB + v] * m;
-        }
+      bwd_tile_kq(sDT, sE, sDY, sM0, sDM, [&](int i, int f, float s1, float s2, float s3) {
         if (i < nb) {
           p.pK[(ob + t0 + i) * kD + f] = s1 - 2.f * sWb[i] * s2;
           p.pQ[(ob + t0 + i) * kD + f] = sA[i] * s3;
         }
-      }
-      const int ii = tid & 63, ng = tid >> 6;
+      });
       const size_t cbo = (((size_t)rb * p.heads + h) * nch + j) * kB * kB;
-      for (int r = 0; r < 16; ++r) {
-        const int n = ng + 4 * r;
-        float s = 0.f;
-#pragma unroll 8
-        for (int v = 0; v < kRB; ++v) s += sDY[n * kPadB + v] * sE[ii * kPadB + v];
-        p.pC[cbo + n * kB + ii] = -2.f * s;
-      }
+      auto fa = [&](int n, int v) { return sDY[n * kPadB + v]; };
+      auto fb = [&](int v, int i) { return sE[i * kPadB + v]; };
+      auto fe = [&](int n, int i, float s) { p.pC[cbo + n * kB + i] = -2.f * s; };
+      tile_gemm<16, 4, 4>(kB, kB, kRB, fa, fb, fe);
       if (warp == 0) {
         // x[v] = (dM_{t0} k_{t0-1})[v]: dM_{t0} = sum_m r[m][0] dy_m q_m^T + r[63][0] dMe
         float s = 0.f;
@@ -421,19 +519,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_rows_kernel(BwdArgs p) {
     }
     have_x = j > 0;
     __syncthreads();
-    // -- dMe <- a_63 dMe + dY^T diag(a) Q + dT^T K  (thread: f, rows vg + 2 r)
-    {
-      const int f = tid & (kD - 1), vg = tid >> 7;
-      const float a63 = sA[kB - 1];
-#pragma unroll 2
-      for (int r = 0; r < kRB / 2; ++r) {
-        const int v = vg + 2 * r;
-        float s = 0.f;
-        for (int n = 0; n < kB; ++n)
-          s += sA[n] * sDY[n * kPadB + v] * sQ[n * kD + f] + sDT[n * kPadB + v] * sK[n * kD + f];
-        sDM[v * kPad + f] = a63 * sDM[v * kPad + f] + s;
-      }
-    }
+    // -- dMe <- a_63 dMe + dY^T diag(a) Q + dT^T K
+    bwd_tile_dm(sA, sDY, sDT, sQ, sK, sDM);
   }
   __syncthreads();
   for (int x = tid; x < kRB * kD; x += kThreads) {
@@ -554,7 +641,7 @@ namespace {
 
 constexpr size_t kTablesSmem = sizeof(float) * ((size_t)kB * kPad + kB * kD + kD + 2 * kB +
                                                 kB * kB + kB);
-constexpr size_t kRowsSmem = sizeof(float) * ((size_t)2 * kRB * kPad + 2 * kB * kD +
+constexpr size_t kRowsSmem = sizeof(float) * ((size_t)2 * kRB * kPad + 2 * kB * kPad +
                                               7 * kB * kPadB + kB * kB + 3 * kB + 1 + kD + kRB);
 constexpr size_t kFinishSmem = sizeof(float) * ((size_t)2 * kB * kD + 3 * kB * kB + 5 * kB);
 
