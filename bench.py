@@ -263,8 +263,9 @@ _TC = ["tc_primitives.cuh", "common.cuh", "kernels.h"]
 KERNEL_OF_PATH = {
     "linear_tc": (["linear_tc.cu", "linear_simt.cu", "linear_simt_body.cuh"] + _TC,
                   "linear_tc_{wname}.md"),
-    "linear_simt": (["linear_simt.cu", "linear_simt_serial.cu", "linear_simt_body.cuh",
-                     "simt_tiles.cuh", "common.cuh", "kernels.h"], "linear_simt_{wname}.md"),
+    "linear_simt": (["linear_simt.cu", "linear_simt_elastic.cu", "linear_simt_bregman.cu",
+                     "linear_simt_kl.cu", "linear_simt_body.cuh", "simt_tiles.cuh", "common.cuh",
+                     "kernels.h"], "linear_simt_{wname}.md"),
     "linear_wide": (["linear_wide.cu", "simt_tiles.cuh", "common.cuh", "kernels.h"],
                     "linear_wide_{wname}.md"),
     "linear_seq": (["linear_seq.cu", "common.cuh", "kernels.h"], "linear_seq_{wname}.md"),

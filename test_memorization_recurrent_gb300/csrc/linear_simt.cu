@@ -46,8 +46,6 @@ static int launch(const LinArgs& a, int heads, const int* flags, cudaStream_t st
   if (rc) return rc;
   if (flags && s.ncl > 1) return ATLAS_ERR_UNSUPPORTED;
   const size_t smem = s.bytes();
-  const bool serial =
-      a.ret == ATLAS_RET_ELASTIC || a.ret == ATLAS_RET_BREGMAN || a.ret == ATLAS_RET_KL;
   const int rows = flags ? 1 : (s.ncl > 1 ? s.ncl : (a.d_v + s.RV - 1) / s.RV);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(heads, rows);
@@ -63,15 +61,14 @@ static int launch(const LinArgs& a, int heads, const int* flags, cudaStream_t st
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  if (serial) {
-    if (linear_simt_serial_launch(&cfg, a, s, flags) != cudaSuccess) return ATLAS_ERR_CUDA;
-  } else {
-    if (cudaFuncSetAttribute(linear_simt_kernel<false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-      return ATLAS_ERR_CUDA;
-    if (cudaLaunchKernelEx(&cfg, linear_simt_kernel<false>, a, s, flags) != cudaSuccess)
-      return ATLAS_ERR_CUDA;
+  cudaError_t e;
+  switch (a.ret) {
+    case ATLAS_RET_ELASTIC: e = linear_simt_elastic_launch(&cfg, a, s, flags); break;
+    case ATLAS_RET_BREGMAN: e = linear_simt_bregman_launch(&cfg, a, s, flags); break;
+    case ATLAS_RET_KL: e = linear_simt_kl_launch(&cfg, a, s, flags); break;
+    default: e = linear_simt_launch_gate<ATLAS_RET_L2>(&cfg, a, s, flags); break;
   }
+  if (e != cudaSuccess) return ATLAS_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? ATLAS_OK : ATLAS_ERR_CUDA;
 }
 

@@ -1,8 +1,8 @@
 // linear_simt_body.cuh -- chunked Omega-rule update of a linear matrix memory on
 // CUDA cores (fp32), for any feature map, window, chunk and gate setting: the
-// kernel body, instantiated once for the chunk-table gates (linear_simt.cu) and
-// once for the token-serial gates (linear_simt_serial.cu), so the two compile in
-// parallel.
+// kernel body, instantiated once per gate family -- the chunk tables (l2, l_q;
+// linear_simt.cu) and each token-serial gate (linear_simt_elastic.cu,
+// linear_simt_bregman.cu, linear_simt_kl.cu) -- so that they compile in parallel.
 //
 // The memory y = M Phi(x) decomposes over the rows of M: the error
 // e_i[r] = M[r,:] . Phi(k_i) - v_i[r] and the readout y_n[r] = M_n[r,:] . Phi(q_n)
@@ -44,9 +44,9 @@
 // accumulates TM x TN outputs spaced TY and TX apart, so a k-step loads TM + TN
 // operands for TM TN FMAs.  Rows of M, S, K and Q are stored with odd strides,
 // which keeps the column walks free of bank conflicts.  The token-serial walk
-// has a fast form for D <= 128: each lane holds the features of its (at most
-// four) columns of q and of the window keys in registers and a warp steps two
-// rows at a time.
+// has a fast form for D <= 128 and at most 64 rows: four lanes share a row and
+// keep its M and S in registers for the whole chunk (32 columns each), so each
+// row's sums take two shuffle steps.
 //
 // The robust bias scales each window token's error row by 1 + Delta/||e||, which
 // needs the norm over all d_v rows of the head.  Its row blocks therefore form
@@ -281,137 +281,144 @@ __device__ __forceinline__ void warp_lse(float& mx, float& den) {
   }
 }
 
-// One token of the token-serial walk for a non-linear gate (RK: ATLAS_RET_*),
-// D <= 32 JPL: lane l holds columns l + 32 u (those >= D are skipped).  Two rows
-// (r, r + 8) per step.
-// kf: window-key features by lag (lags < 4), ge: gamma by lag.
-template <int JPL, int RK>
-__device__ __forceinline__ void serial_token_fast(int rv, int D, int Dp, float* Ms, float* Ss,
-                                                  const float* E, int hi, int nwin,
-                                                  const float (&qf)[JPL],
-                                                  const float (&kf)[4][JPL], const float* gam,
-                                                  const Feat& fk, float keep, float et, float th2,
-                                                  float lam, float logc, float* Yrow) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nw4 = min(nwin, 4);
-  for (int rb = warp; rb < rv; rb += 16) {
-    const int rr[2] = {rb, rb + 8};
-    float uval[2][JPL], acc[2] = {0.f, 0.f}, mx[2] = {-INFINITY, -INFINITY}, den[2] = {0.f, 0.f};
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int r = rr[h];
-      if (r >= rv) continue;
-      float ge[4];
-#pragma unroll
-      for (int w = 0; w < 4; ++w) ge[w] = w < nw4 ? gam[w] * E[(hi - w) * rv + r] : 0.f;
-#pragma unroll
-      for (int u = 0; u < JPL; ++u) {
-        const int j = lane + 32 * u;
-        uval[h][u] = 0.f;
-        if (j >= D) continue;
-        float g = 0.f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) g = fmaf(ge[w], kf[w][u], g);
-        for (int w = 4; w < nwin; ++w) g = fmaf(gam[w] * E[(hi - w) * rv + r], fk(hi - w, j), g);
-        const long x = (long)r * Dp + j;
-        const float sv = et * Ss[x] - th2 * g;
-        Ss[x] = sv;
-        float v = fmaf(keep, Ms[x], sv);
-        if (RK == ATLAS_RET_ELASTIC) {
-          const float a = fabsf(v) - lam;
-          v = a > 0.f ? copysignf(a, v) : 0.f;
-          acc[h] = fmaf(v, qf[u], acc[h]);
-        } else if (RK == ATLAS_RET_BREGMAN) {
-          acc[h] = fmaf(qf[u], 1.f / (1.f + expf(-v)), acc[h]);
-        } else {
-          if (v > mx[h]) {
-            den[h] = den[h] * expf(mx[h] - v) + 1.f;
-            mx[h] = v;
-          } else {
-            den[h] += expf(v - mx[h]);
-          }
-        }
-        uval[h][u] = v;
-        if (RK != ATLAS_RET_KL) Ms[x] = v;
-      }
-    }
-    if (RK == ATLAS_RET_KL) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) warp_lse(mx[h], den[h]);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int r = rr[h];
-        if (r >= rv) continue;
-        const float shift = mx[h] + logf(den[h]) - logc;  // log M = u - lse(u) + log c
-#pragma unroll
-        for (int u = 0; u < JPL; ++u) {
-          const int j = lane + 32 * u;
-          if (j >= D) continue;
-          const float lm = uval[h][u] - shift;
-          Ms[(long)r * Dp + j] = lm;
-          acc[h] = fmaf(expf(lm), qf[u], acc[h]);
-        }
-      }
-    }
-    const float y0 = warp_sum(acc[0]), y1 = warp_sum(acc[1]);
-    if (lane == 0) {
-      Yrow[rr[0]] = y0;
-      if (rr[1] < rv) Yrow[rr[1]] = y1;
-    }
-  }
+// Token-serial walk of one chunk for a non-linear gate (RK: ATLAS_RET_*), D <= 128,
+// at most 64 rows.  Four lanes share a row (warp w holds rows 8 w .. 8 w + 7), each
+// keeping 32 of its columns (sub + 4 u) of M and S in registers for the whole
+// chunk, so a row's sums take two shuffle steps.  Per token: the window gradient
+// from the chunk-start errors (the current key's features in registers, earlier
+// window keys read from shared memory), the momentum and state steps, the gate
+// and the row readout; the rows go back to shared memory at the chunk end.
+__device__ __forceinline__ float quad_sum(float x) {
+  x += __shfl_xor_sync(0xFFFFFFFFu, x, 1);
+  return x + __shfl_xor_sync(0xFFFFFFFFu, x, 2);
 }
 
-template <int JPL, int RK>
-__device__ __forceinline__ void serial_chunk_fast(int nb, int t0, int i0, int c, int rv, int D,
+// The identity map read straight from the rows of x (row stride ld).
+struct FeatId {
+  const float* x;
+  int ld;
+  __device__ __forceinline__ float operator()(int row, int j) const { return x[row * ld + j]; }
+};
+
+template <int RK, class FT>
+__device__ __forceinline__ void serial_chunk_quad(int nb, int t0, int i0, int c, int rv, int D,
                                                   int Dp, float* Ms, float* Ss, const float* E,
-                                                  const Feat& fq, const Feat& fk,
+                                                  const FT& fq, const FT& fk,
                                                   const float* sa, const float* se,
                                                   const float* sb, const float* gam, float lam,
                                                   float logc, float* Y, int dv) {
-  const int lane = threadIdx.x & 31;
+  constexpr int CPL = 32;  // columns per lane
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane & 3, row = warp * 8 + (lane >> 2);
+  const bool live = row < rv;
+  const int rr = live ? row : 0;  // a valid row index for the loads of idle lanes
+  float m[CPL], sv[CPL];
+#pragma unroll
+  for (int u = 0; u < CPL; ++u) {
+    const int j = sub + 4 * u;
+    const bool ok = live && j < D;
+    m[u] = ok ? Ms[rr * Dp + j] : 0.f;
+    sv[u] = ok ? Ss[rr * Dp + j] : 0.f;
+  }
   for (int n = 0; n < nb; ++n) {
     const int t = t0 + n;
     const int hi = t - i0, nwin = min(c, hi + 1);  // window rows hi, hi - 1, ... of token t
-    float qf[JPL], kf[4][JPL];
+    const float keep = 1.f - sa[n], et = se[n], th2 = 2.f * sb[n];
+    const float e0 = gam[0] * E[hi * rv + rr];
+    float acc = 0.f, mx = -INFINITY, den = 0.f;
 #pragma unroll
-    for (int u = 0; u < JPL; ++u) {
-      const int j = min(lane + 32 * u, D - 1);
-      qf[u] = fq(n, j);
+    for (int h = 0; h < CPL; h += CPL / 2) {  // two halves of the lane's columns
+      float g[CPL / 2];
 #pragma unroll
-      for (int w = 0; w < 4; ++w) kf[w][u] = w < nwin ? fk(hi - w, j) : 0.f;
+      for (int u = 0; u < CPL / 2; ++u) g[u] = e0 * fk(hi, min(sub + 4 * (h + u), D - 1));
+      for (int w = 1; w < nwin; ++w) {
+        const float ew = gam[w] * E[(hi - w) * rv + rr];
+#pragma unroll
+        for (int u = 0; u < CPL / 2; ++u)
+          g[u] = fmaf(ew, fk(hi - w, min(sub + 4 * (h + u), D - 1)), g[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < CPL / 2; ++u) {
+        const int j = sub + 4 * (h + u);
+        if (j >= D) continue;
+        const float s1 = et * sv[h + u] - th2 * g[u];
+        sv[h + u] = s1;
+        float v = fmaf(keep, m[h + u], s1);
+        if (RK == ATLAS_RET_ELASTIC) {
+          const float a = fabsf(v) - lam;
+          v = a > 0.f ? copysignf(a, v) : 0.f;
+          acc = fmaf(v, fq(n, j), acc);
+        } else if (RK == ATLAS_RET_BREGMAN) {
+          acc = fmaf(fq(n, j), __fdividef(1.f, 1.f + __expf(-v)), acc);
+        } else {  // KL: the row's maximum first
+          mx = fmaxf(mx, v);
+        }
+        m[h + u] = v;
+      }
     }
-    serial_token_fast<JPL, RK>(rv, D, Dp, Ms, Ss, E, hi, nwin, qf, kf, gam, fk, 1.f - sa[n],
-                               se[n], 2.f * sb[n], lam, logc, Y + (long)t * dv);
+    if (RK == ATLAS_RET_KL) {
+      // M = c softmax(u): with the row maximum mx, den = sum exp(u - mx) and
+      // num = sum exp(u - mx) q, the readout is c num / den and log M = u - shift
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+      float num = 0.f;
+#pragma unroll
+      for (int u = 0; u < CPL; ++u) {
+        const int j = sub + 4 * u;
+        if (j >= D) continue;
+        const float e = __expf(m[u] - mx);
+        den += e;
+        num = fmaf(e, fq(n, j), num);
+      }
+      den = quad_sum(den);
+      num = quad_sum(num);
+      const float shift = mx + __logf(den) - logc;
+#pragma unroll
+      for (int u = 0; u < CPL; ++u) m[u] -= shift;
+      acc = lam * num / den;  // lam carries the gate's parameter, here the row mass c
+    } else {
+      acc = quad_sum(acc);
+    }
+    if (sub == 0 && live) Y[(long)t * dv + row] = acc;
+  }
+#pragma unroll
+  for (int u = 0; u < CPL; ++u) {
+    const int j = sub + 4 * u;
+    if (live && j < D) {
+      Ms[row * Dp + j] = m[u];
+      Ss[row * Dp + j] = sv[u];
+    }
   }
 }
 
-// One CTA: rows [r0, r0 + RV) of one head, the whole sequence.  SERIAL: the
-// elastic-net, Bregman and KL gates (token-serial walk); else the chunk tables.
-template <bool SERIAL>
+// One CTA: rows [r0, r0 + RV) of one head, the whole sequence.  GATE: ATLAS_RET_L2
+// for the chunk tables (the l2 and l_q gates), else the token-serial gate it names.
+template <int GATE>
 __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimtSmem& L, int head,
                                                  int r0);
 
 // flags != nullptr: only the heads whose flag is set (the heads the tensor-core
 // kernel leaves, which it marks); every other head returns at once, and each
 // CTA walks all row blocks of its head so that the grid stays one CTA per head.
-template <bool SERIAL>
+template <int GATE>
 __global__ void __launch_bounds__(256) linear_simt_kernel(LinArgs p, LinSimtSmem L,
                                                           const int* flags) {
   const int head = blockIdx.x;
   if (flags) {
     if (flags[head] == 0) return;
     for (int r0 = 0; r0 < p.d_v; r0 += L.RV) {
-      linear_simt_rows<SERIAL>(p, L, head, r0);
+      linear_simt_rows<GATE>(p, L, head, r0);
       __syncthreads();
     }
     return;
   }
-  linear_simt_rows<SERIAL>(p, L, head, blockIdx.y * L.RV);
+  linear_simt_rows<GATE>(p, L, head, blockIdx.y * L.RV);
 }
 
-template <bool SERIAL>
+template <int GATE>
 __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimtSmem& L, int head,
                                                  int r0) {
+  constexpr bool SERIAL = GATE != ATLAS_RET_L2;
   extern __shared__ float sm[];
   float* Ms = sm + L.Ms;
   float* Ss = sm + L.Ss;
@@ -577,16 +584,13 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
     }
     if constexpr (SERIAL) {
       __syncthreads();
-      if (D <= 128) {
-        if (ret == ATLAS_RET_ELASTIC)
-          serial_chunk_fast<4, ATLAS_RET_ELASTIC>(nb, t0, i0, p.c, rv, D, Dp, Ms, Ss, E, fq, fk, sa,
-                                                  se, sb, Urun, p.rp, logc, Yh, dv);
-        else if (ret == ATLAS_RET_BREGMAN)
-          serial_chunk_fast<4, ATLAS_RET_BREGMAN>(nb, t0, i0, p.c, rv, D, Dp, Ms, Ss, E, fq, fk, sa,
-                                                  se, sb, Urun, p.rp, logc, Yh, dv);
+      if (D <= 128 && rv <= 64) {
+        if (!p.poly && !p.pgen)  // the identity map: features are the key and query entries
+          serial_chunk_quad<GATE>(nb, t0, i0, p.c, rv, D, Dp, Ms, Ss, E, FeatId{Qc, dkp},
+                                  FeatId{Kw, dkp}, sa, se, sb, Urun, p.rp, logc, Yh, dv);
         else
-          serial_chunk_fast<4, ATLAS_RET_KL>(nb, t0, i0, p.c, rv, D, Dp, Ms, Ss, E, fq, fk, sa, se,
-                                             sb, Urun, p.rp, logc, Yh, dv);
+          serial_chunk_quad<GATE>(nb, t0, i0, p.c, rv, D, Dp, Ms, Ss, E, fq, fk, sa, se, sb, Urun,
+                                  p.rp, logc, Yh, dv);
         continue;
       }
       // wide feature maps: one warp per row, lanes over the columns
@@ -681,8 +685,23 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
   }
 }
 
-// Launch of the token-serial instantiation (linear_simt_serial.cu).
-cudaError_t linear_simt_serial_launch(const cudaLaunchConfig_t* cfg, const LinArgs& a,
-                                      const LinSimtSmem& s, const int* flags);
+// Launches of the token-serial instantiations (one translation unit each).
+cudaError_t linear_simt_elastic_launch(const cudaLaunchConfig_t* cfg, const LinArgs& a,
+                                       const LinSimtSmem& s, const int* flags);
+cudaError_t linear_simt_bregman_launch(const cudaLaunchConfig_t* cfg, const LinArgs& a,
+                                       const LinSimtSmem& s, const int* flags);
+cudaError_t linear_simt_kl_launch(const cudaLaunchConfig_t* cfg, const LinArgs& a,
+                                  const LinSimtSmem& s, const int* flags);
+
+// Sets the kernel's shared-memory limit and launches it.
+template <int GATE>
+cudaError_t linear_simt_launch_gate(const cudaLaunchConfig_t* cfg, const LinArgs& a,
+                                    const LinSimtSmem& s, const int* flags) {
+  const cudaError_t e = cudaFuncSetAttribute(linear_simt_kernel<GATE>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)cfg->dynamicSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(cfg, linear_simt_kernel<GATE>, a, s, flags);
+}
 
 }  // namespace atlas
