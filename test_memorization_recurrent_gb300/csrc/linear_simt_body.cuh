@@ -293,13 +293,6 @@ __device__ __forceinline__ float quad_sum(float x) {
   return x + __shfl_xor_sync(0xFFFFFFFFu, x, 2);
 }
 
-// The identity map read straight from the rows of x (row stride ld).
-struct FeatId {
-  const float* x;
-  int ld;
-  __device__ __forceinline__ float operator()(int row, int j) const { return x[row * ld + j]; }
-};
-
 template <int RK, class FT>
 __device__ __forceinline__ void serial_chunk_quad(int nb, int t0, int i0, int c, int rv, int D,
                                                   int Dp, float* Ms, float* Ss, const float* E,

@@ -79,9 +79,22 @@ static WideSmem wide_layout(const LinArgs& a, int CL) {
 
 constexpr size_t kWideSmemLimit = 225 * 1024;
 
+// The degree-2 map alone (no gated-map branch): x_j, then the pair products.
+struct FeatP2 {
+  const float* x;
+  int ld, dk;
+  const uint8_t* pp;
+  const uint8_t* pq;
+  __device__ __forceinline__ float operator()(int row, int j) const {
+    const float* r = x + row * ld;
+    return j < dk ? r[j] : r[pp[j - dk]] * r[pq[j - dk]];
+  }
+};
+
 // Features of a column slice: feature j0 + j of row `row`.
+template <class F>
 struct FeatSlice {
-  Feat f;
+  F f;
   int j0;
   __device__ __forceinline__ float operator()(int row, int j) const { return f(row, j0 + j); }
 };
@@ -91,8 +104,8 @@ __device__ __forceinline__ int share_lo(int n, int CL, int c) { return (int)((lo
 
 // Partial readout of the slice: YP[n, r] = sa_n Phi(q_n).M[r] + sb_n Phi(q_n).S[r]
 // (slice columns only; the S term skipped when every sb_n is 0).
-template <int TX, int TM, int TN>
-__device__ __forceinline__ void readout_partial(int nb, int dv, int dj, const FeatSlice& fq,
+template <int TX, int TM, int TN, class FQ>
+__device__ __forceinline__ void readout_partial(int nb, int dv, int dj, const FQ& fq,
                                                 const float* Ms, const float* Ss, int DJp,
                                                 const float* sa, const float* sb, bool with_s,
                                                 float* YP) {
@@ -140,6 +153,8 @@ __device__ __forceinline__ void readout_partial(int nb, int dv, int dj, const Fe
     }
 }
 
+// FEAT: 0 the identity map, 1 the degree-2 map, 2 the gated polynomial map.
+template <int FEAT>
 __global__ void __launch_bounds__(256, 1) linear_wide_kernel(LinArgs p, WideSmem L) {
   extern __shared__ float sm[];
   cg::cluster_group cl = cg::this_cluster();
@@ -192,8 +207,16 @@ __global__ void __launch_bounds__(256, 1) linear_wide_kernel(LinArgs p, WideSmem
       }
     }
   }
-  const FeatSlice fk{{Kw, dkp, dk, p.poly, p.pgen, pp, pq, ftab, coef}, j0};
-  const FeatSlice fq{{Qc, dkp, dk, p.poly, p.pgen, pp, pq, ftab, coef}, j0};
+  auto make = [&](const float* x) {
+    if constexpr (FEAT == 0)
+      return FeatSlice<FeatId>{FeatId{x, dkp}, j0};
+    else if constexpr (FEAT == 1)
+      return FeatSlice<FeatP2>{FeatP2{x, dkp, dk, pp, pq}, j0};
+    else
+      return FeatSlice<Feat>{Feat{x, dkp, dk, p.poly, p.pgen, pp, pq, ftab, coef}, j0};
+  };
+  const auto fk = make(Kw);
+  const auto fq = make(Qc);
   float* Mg = p.M + head * state;
   float* Sg = p.S ? p.S + head * state : nullptr;
   for (long x = tid; x < (long)dv * dj; x += nt) {
@@ -388,8 +411,11 @@ int linear_wide_launch(const LinArgs& a, int heads, cudaStream_t st) {
   WideSmem s;
   wide_plan(a, heads, &s);
   const size_t smem = s.bytes();
-  if (cudaFuncSetAttribute(linear_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
+  const int feat = a.pgen ? 2 : a.poly ? 1 : 0;
+  auto kern = feat == 2 ? linear_wide_kernel<2> : feat == 1 ? linear_wide_kernel<1>
+                                                            : linear_wide_kernel<0>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
     return ATLAS_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(s.CL, heads);
@@ -403,7 +429,7 @@ int linear_wide_launch(const LinArgs& a, int heads, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, linear_wide_kernel, a, s) != cudaSuccess) return ATLAS_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kern, a, s) != cudaSuccess) return ATLAS_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? ATLAS_OK : ATLAS_ERR_CUDA;
 }
 

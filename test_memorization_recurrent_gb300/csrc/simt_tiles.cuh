@@ -39,6 +39,13 @@ struct Feat {
   }
 };
 
+// The identity map read straight from the rows of x (row stride ld).
+struct FeatId {
+  const float* x;
+  int ld;
+  __device__ __forceinline__ float operator()(int row, int j) const { return x[row * ld + j]; }
+};
+
 // C = A B over k < K for an m x n output: thread (ty, tx) of a TY x TX grid
 // (TY TX = 256) owns rows ty + TY u and columns tx + TX v of each block; fe
 // receives each finished output.  Operand indices are clamped into range, so
