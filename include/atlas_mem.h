@@ -186,20 +186,19 @@ size_t atlas_mem_backward_workspace_bytes(const atlas_mem_cfg* cfg);
  *     L = sum_t <dY_t, y_t> + <dM_N, M_N>
  * it returns dL/dK, dL/dQ, dL/dV, dL/dalpha, dL/deta, dL/dtheta and dL/dM_0.
  * Covered: linear memory, identity map, d_k = d_v = 128, b = 64, c = 1, the
- * l2, l_p or Huber bias, no history rows, cfg->S_state = NULL (the forward
- * starts from zero momentum; its final momentum gets no gradient), and a
- * forward without momentum: every eta must be 0 (the gradient with respect to
- * eta is still returned).  Anything else returns ATLAS_ERR_UNSUPPORTED before
- * any launch; a non-zero eta found on the device sets *cfg->status_dev to
- * ATLAS_ERR_UNSUPPORTED (the results are then not meaningful).  The window
- * weight gamma[0] is an input but gets no gradient.
+ * l2, l_p or Huber bias, momentum and decay with any gates, no history rows,
+ * cfg->S_state = NULL (the forward starts from zero momentum; its final
+ * momentum gets no gradient).  Anything else returns ATLAS_ERR_UNSUPPORTED
+ * before any launch.  The window weight gamma[0] is an input but gets no
+ * gradient.
  *   K, Q, V, alpha, eta, theta, gamma: as for atlas_mem_forward
  *   M0     [B,H,d_v,d_k] fp32 in: the forward's initial state
  *   dY     [B,H,N,d_v]   fp32 in: dL/dY
  *   dM     [B,H,d_v,d_k] fp32 in/out: dL/dM_N on entry, dL/dM_0 on return
  *   dK, dQ [B,H,N,d_k], dV [B,H,N,d_v], dalpha, deta, dtheta [B,H,N]: fp32 out
  * Workspace: cfg->workspace of at least atlas_mem_backward_workspace_bytes()
- * (the chunk-start states, gate tables and partial sums; ~6.9 KB per token).
+ * (the chunk-start states and momenta, gate tables and partial sums; ~8.2 KB
+ * per token).
  * Three kernel launches on `stream`; returns ATLAS_OK or an ATLAS_ERR_* code. */
 int atlas_mem_backward(const void* K, const void* Q, const void* V, const float* alpha,
                        const float* eta, const float* theta, const float* gamma,

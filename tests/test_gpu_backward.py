@@ -1,5 +1,6 @@
 """Parity of the backward pass (atlas_mem_backward, called through the C ABI)
-with the fp64 backward oracle on the same seeded inputs and upstream gradients:
+with the fp64 backward oracle on the same seeded inputs and upstream gradients,
+with and without momentum in the forward:
 dK, dQ, dV, dalpha, deta, dtheta and dM_0, each within the bf16-input tolerance
 (max |x - y| / RMS(y) <= 2e-2).  Small cases span several chunks and a ragged
 tail; the full-size case runs every head of the DeltaNet-like workload in one
@@ -73,16 +74,26 @@ def test_backward_full_size_sampled():
     check(w, got, ref, "full size")
 
 
-def test_backward_reports_momentum_in_the_forward():
-    """A non-zero eta is outside what the backward covers: the status word says so."""
-    from test_memorization_recurrent_gb300 import ERR_UNSUPPORTED
-    from test_memorization_recurrent_gb300.harness import BackwardRunner, to_device
-    w = W.workload(2, N=100)
+@pytest.mark.parametrize("N", [64 + 9, 64 * 3])
+@pytest.mark.parametrize("loss,prm", [(W.LOSS_L2, 0.0), (W.LOSS_HUBER, 0.3)])
+def test_backward_with_momentum(N, loss, prm):
+    """Momentum in the forward (eta ~ U(0.5, 0.9), as the other workloads draw it):
+    the momentum's own tables and their gradients, the chunk-start momentum carried
+    through the reverse, and eta's gradient against the oracle."""
+    w = W.workload(2, N=N, loss=loss, loss_param=prm, eta=(0.5, 0.9))
+    inp = W.generate(w, heads=[0, 5, 9])
+    inp["M0"] = (np.random.default_rng(N).standard_normal(inp["M0"].shape) * 0.05).astype(np.float32)
+    dY, dMN = upstream(w, 3, N)
+    got, ref = run_both(w, inp, dY, dMN)
+    check(w, got, ref, f"momentum N={N} loss={loss}")
+
+
+def test_backward_momentum_on_some_tokens_only():
+    """eta non-zero on a few tokens of one head, zero elsewhere (the DeltaNet gates
+    with a momentum burst), including the first token of a chunk."""
+    w = W.workload(2, N=64 * 2 + 30)
     inp = W.generate(w, heads=[0, 1])
-    inp["eta"][1, 70] = 0.5
-    d = to_device(w, inp)
-    r = BackwardRunner(w, 2, w.N)
+    inp["eta"][1, [5, 63, 64, 65, 100]] = 0.7
     dY, dMN = upstream(w, 2, w.N)
-    r(d, torch.from_numpy(dY).cuda(), torch.from_numpy(dMN).cuda())
-    torch.cuda.synchronize()
-    assert int(r.status.item()) == ERR_UNSUPPORTED
+    got, ref = run_both(w, inp, dY, dMN)
+    check(w, got, ref, "momentum burst")
