@@ -523,6 +523,9 @@ def test_robust_bias(wid, kw, N, heads, path):
     (dict(d_v=160), 64 + 9, [0, 1], "linear_chunk"),   # too many value rows for the cluster
     (dict(), 64 * 2 + 5, [0, 31], "linear_wide"),       # 4-CTA clusters, momentum, window 64
     (dict(d_v=24, c=3, b=16), 70, [2], "linear_wide"),  # other widths, window, chunk
+    (dict(loss=W.LOSS_DOT), 64 + 3, [4], "linear_wide"),  # dot-product bias (E = -V)
+    (dict(), 1, [7], "linear_wide"),                     # one token
+    (dict(d_k=24, d_v=128, c=8), 64 + 2, [0], "linear_wide"),  # 128 value rows, D = 324
 ])
 def test_wide_feature_map_paths(kw, N, heads, path):
     """The degree-2 map (D = 560) on the fused cluster kernel and, beyond its row
