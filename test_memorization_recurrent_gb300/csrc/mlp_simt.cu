@@ -436,6 +436,101 @@ __global__ void ns_normalize_kernel(float* X, long state, long half, float eps) 
   for (long i = threadIdx.x; i < half; i += blockDim.x) x[i] *= inv;
 }
 
+// Every momentum S_n of a chunk, streamed token by token (the Newton-Schulz
+// path needs each one): S_n = eta_n S_{n-1} - theta_n g_n with the window
+// gradient g_n = sum_{lag < c} gamma[lag] G_{n-lag}, G_i = 2 a_i b_i^T taken at
+// the chunk-start state (a, b: the two factor rows of weight block blk, E and the
+// hidden activation for W1, Delta (Delta3) and K for W2 (W3)).  With gamma
+// constant over the window, g_{n+1} = g_n + 2 gamma (G_{n+1} - G_{n+1-c}): two
+// rank-1 terms per token; otherwise the window is summed afresh for each token.
+// One CTA per (128 x 128 tile of a weight block, head); thread (ty, tx) of a
+// 16 x 16 grid holds rows ty + 16 u (u < 8) and columns 4 tx + 64 w .. + 3
+// (w < 2) of S and g in registers and writes S_n with 16-byte stores.
+struct MomStream {
+  int ra, cb;              // block shape: rows (the a factor's width), columns (b's)
+  long a_off, b_off;       // workspace offsets of the window rows [L][ra], [L][cb]
+  long blk_off;            // offset of the block in the state
+};
+
+__global__ void __launch_bounds__(256) mom_stream_kernel(MlpArgs p, MlpWs w, const float* ws,
+                                                         float* X, MomStream m0, MomStream m1,
+                                                         MomStream m2, int nblk, int t0, int nb,
+                                                         int i0) {
+  const int tiles_per_blk = 4;  // 128 x 512 blocks in 128 x 128 tiles
+  const int blk = blockIdx.x / tiles_per_blk, tile = blockIdx.x % tiles_per_blk;
+  if (blk >= nblk) return;
+  const MomStream& ms = blk == 0 ? m0 : blk == 1 ? m1 : m2;
+  const int h = blockIdx.y;
+  const float* base = ws + (long)h * w.per_head;
+  const float* A = base + ms.a_off;  // [L][ra]
+  const float* B = base + ms.b_off;  // [L][cb]
+  const long state = (long)(p.gated ? 3 : 2) * p.d * p.dh;
+  // the tile: rows [r0, r0 + 128) of a (ra) and columns [c0, c0 + 128) of b (cb)
+  const int r0 = ms.ra > 128 ? 128 * tile : 0, c0 = ms.ra > 128 ? 0 : 128 * tile;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int c = p.c;
+  const float* eta = p.eta + (long)h * p.N;
+  const float* theta = p.theta + (long)h * p.N;
+  bool gconst = true;
+  const float g0 = p.gamma[0];
+  for (int l = 1; l < c; ++l) gconst &= p.gamma[l] == g0;
+  float sv[8][8], gv[8][8];
+  const float* S0 = p.S + (long)h * state + ms.blk_off;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int r = r0 + ty + 16 * u;
+#pragma unroll
+    for (int wq = 0; wq < 2; ++wq) {
+      const float4 x = *reinterpret_cast<const float4*>(S0 + (long)r * ms.cb + c0 + 4 * tx + 64 * wq);
+      sv[u][4 * wq] = x.x; sv[u][4 * wq + 1] = x.y; sv[u][4 * wq + 2] = x.z; sv[u][4 * wq + 3] = x.w;
+    }
+  }
+  // g += f a_i b_i^T for the window row li
+  auto rank1 = [&](int li, float f) {
+    float a[8], b[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) a[u] = f * A[(long)li * ms.ra + r0 + ty + 16 * u];
+#pragma unroll
+    for (int wq = 0; wq < 2; ++wq) {
+      const float4 x = *reinterpret_cast<const float4*>(B + (long)li * ms.cb + c0 + 4 * tx + 64 * wq);
+      b[4 * wq] = x.x; b[4 * wq + 1] = x.y; b[4 * wq + 2] = x.z; b[4 * wq + 3] = x.w;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+#pragma unroll
+      for (int v = 0; v < 8; ++v) gv[u][v] = fmaf(a[u], b[v], gv[u][v]);
+  };
+  auto window = [&](int t) {  // g = 2 sum over the window of token t
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+#pragma unroll
+      for (int v = 0; v < 8; ++v) gv[u][v] = 0.f;
+    const int lo = max(i0, t - c + 1);
+    for (int i = lo; i <= t; ++i) rank1(i - i0, 2.f * p.gamma[t - i]);
+  };
+  for (int n = 0; n < nb; ++n) {
+    const int t = t0 + n;
+    if (n == 0 || !gconst) {
+      window(t);
+    } else {  // slide: token t enters, token t - c leaves (if it was in the window)
+      rank1(t - i0, 2.f * g0);
+      if (t - c >= i0) rank1(t - c - i0, -2.f * g0);
+    }
+    const float et = eta[t], th = theta[t];
+    float* Xn = X + ((long)h * nb + n) * state + ms.blk_off;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int r = r0 + ty + 16 * u;
+#pragma unroll
+      for (int v = 0; v < 8; ++v) sv[u][v] = et * sv[u][v] - th * gv[u][v];
+#pragma unroll
+      for (int wq = 0; wq < 2; ++wq)
+        *reinterpret_cast<float4*>(Xn + (long)r * ms.cb + c0 + 4 * tx + 64 * wq) =
+            make_float4(sv[u][4 * wq], sv[u][4 * wq + 1], sv[u][4 * wq + 2], sv[u][4 * wq + 3]);
+    }
+  }
+}
+
 // out[h][row][col] = S_{nb-1} of head h (the momentum carried to the next chunk).
 __global__ void ns_copy_last_kernel(float* S, const float* Sn, long state, int nb) {
   const int h = blockIdx.y;
@@ -514,7 +609,9 @@ long mlp_simt_launch_count(const MlpArgs& a) {
   // GELU(zq), three more products per block and step (unfused), and no fusion
   if (a.gated) extra += 3 + (a.ns_steps > 0 ? 5 + 3L * a.ns_steps : 3 + 1 + 2 + 2);
   const bool fused = ns_fused_supported(a.d, a.dh) && !a.gated;
-  if (a.ns_steps > 0) return 1 + chunks * (extra + (fused ? 16 : 16 + 6L * a.ns_steps));
+  // the momenta: one streamed launch for 128 x 512 blocks instead of one product per block
+  const long mom = (a.d == 128 && a.dh == 512) ? 1 - (a.gated ? 3 : 2) : 0;
+  if (a.ns_steps > 0) return 1 + chunks * (extra + mom + (fused ? 16 : 16 + 6L * a.ns_steps));
   return 1 + chunks * (extra + 4 + 1 + 3 + 1 + 4 + 4 + 1 + 4);
 }
 
@@ -537,6 +634,8 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
   float* W3 = p.M + 2 * half;  // gated memory only
   float* S3 = p.S + 2 * half;
   const long PH = w.per_head;
+  // the streamed momenta cover the 128 x 512 / 512 x 128 blocks in 128 x 128 tiles
+  const bool mom_stream_ok = d == 128 && dh == 512;
   for (int t0 = 0; t0 < p.N; t0 += p.b) {
     const int t1 = min(p.N, t0 + p.b), nb = t1 - t0;
     const int i0 = max(-p.nh, t0 - p.c + 1), L = t1 - i0;  // history rows enter windows
@@ -736,7 +835,15 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
       float* A2 = ws + w.nsA2;
       // S_n = eps_n S0 - 2 sum_i U[n,i] [e_i h_i^T | delta_i k_i^T]: eps_n S0 enters as
       // the products' addend (per-instance factor eps_n of the head's S0)
-      {  // instances (h, n): batch h * nb + n, per-head operands shared over n
+      if (mom_stream_ok) {  // streamed token by token
+        MomStream m[3];
+        m[0] = MomStream{(int)d, (int)dh, w.E, hid, 0};
+        m[1] = MomStream{(int)dh, (int)d, w.Dl, w.Kw, half};
+        m[2] = MomStream{(int)dh, (int)d, w.D3, w.Kw, 2 * half};
+        mom_stream_kernel<<<dim3((unsigned)(4 * nblk), (unsigned)H), 256, 0, st>>>(
+            p, w, ws, X, m[0], m[1], m[2], (int)nblk, t0, nb, i0);
+        CL();
+      } else {  // instances (h, n): batch h * nb + n, per-head operands shared over n
         TcGemm t = tc0();
         t.batch = (int)inst; t.bdiv = nb; t.M = (int)d; t.N = (int)dh; t.K = L;
         t.A = ws + w.E; t.sAb = PH; t.sAm = 1; t.sAk = d;
