@@ -367,10 +367,8 @@ def roofline(w, path, kernel_s):
     bytes_launch = tokens * W.bytes_per_token(w) + 2 * 4 * w.heads * w.state_size
     flops_launch = tokens * W.flop_per_token(w)
     ridge = tf * 1e12 / (hbm * 1e9)
-    # fp32 FMAs on CUDA cores: the token-serial, CUDA-core and wide-map linear kernels, and the
-    # CUDA-core MLP path when no Newton-Schulz products go to the tensor cores
-    if path in ("linear_seq", "linear_simt", "linear_wide") or (path == "mlp_simt" and
-                                                                  w.ns_steps == 0):
+    # fp32 FMAs on CUDA cores: the token-serial, CUDA-core and wide-map linear kernels
+    if path in ("linear_seq", "linear_simt", "linear_wide"):
         peak = fp32_alu_peak_tflops()
         achieved = flops_launch / kernel_s / 1e12
         roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

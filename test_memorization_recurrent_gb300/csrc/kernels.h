@@ -92,6 +92,9 @@ struct TcGemm {
   int ksplit;                               // > 1: K split over that many CTAs, their
                                             // terms added to C atomically (no D)
   int symmetric;
+  const float* emul; long sMb, sMb2, sMm, sMn;  // optional elementwise factor of the product
+  int epi;                                  // 1: C = GELU(pre), C2 = GELU'(pre), pre the
+  float* C2; long sC2b, sC2b2, sC2m, sC2n;  // value C would otherwise take
   int* status;                              // optional device status word (timeouts)
   int modeA, modeB;                         // set by tc_gemm_launch (operand load paths)
 };

@@ -1,7 +1,9 @@
 // mlp_simt.cu -- chunked update of the residual MLP memory
-// M(x) = x + W1 GELU(W2 x) on CUDA cores (fp32), host-driven per chunk, every
-// launch batched over all heads.  Handles any window c, chunk b, momentum and
-// the Newton-Schulz-orthogonalised momentum.
+// M(x) = x + W1 GELU(W2 x), host-driven per chunk, every launch batched over
+// all heads: the products as batched tensor-core GEMMs (tc_gemm.cu, bf16 hi/lo
+// operands, fp32 accumulation, with the GELU / GELU' and elementwise-factor
+// epilogues), the elementwise steps and tables on CUDA cores.  Handles any
+// window c, chunk b, momentum and the Newton-Schulz-orthogonalised momentum.
 //
 // Per chunk (window tokens i0..t1-1, L of them; "논문 리뷰 Google ATLAS" §3.3
 // and "It's All Connected (Miras)" Training: gradients at the chunk-start
@@ -49,6 +51,7 @@
 // Biases) scales each token's error row e by 1 + Delta / ||e|| (one warp per row;
 // for the layer-normalised memory inside the LN error kernel, on e = k + LN(u) - v).
 #include <math.h>
+#include <string.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -78,65 +81,6 @@ __device__ __forceinline__ float gelu_prime_f(float x) {
          x * 0.39894228040143268f * expf(-0.5f * x * x);
 }
 
-constexpr int GT = 64, GK = 16;
-
-__global__ void __launch_bounds__(256) gemm_kernel(Gemm g) {
-  __shared__ float As[GK][GT + 1];
-  __shared__ float Bs[GK][GT + 1];
-  const int bz = blockIdx.z;
-  const int m0 = blockIdx.y * GT, n0 = blockIdx.x * GT;
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  const float* A = g.A + bz * g.sAb;
-  const float* B = g.B + bz * g.sBb;
-  float acc[4][4] = {};
-  for (int k0 = 0; k0 < g.K; k0 += GK) {
-    for (int x = threadIdx.x; x < GK * GT; x += 256) {
-      const int kk = x / GT, mm = x % GT;
-      const int m = m0 + mm, k = k0 + kk;
-      As[kk][mm] = (m < g.M && k < g.K) ? A[m * g.sAm + k * g.sAk] : 0.f;
-      const int n = n0 + mm;
-      Bs[kk][mm] = (n < g.N && k < g.K) ? B[k * g.sBk + n * g.sBn] : 0.f;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int kk = 0; kk < GK; ++kk) {
-      float a[4], b[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        a[u] = As[kk][ty + 16 * u];
-        b[u] = Bs[kk][tx + 16 * u];
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int v = 0; v < 4; ++v) acc[u][v] += a[u] * b[v];
-    }
-    __syncthreads();
-  }
-  float* C = g.C + bz * g.sCb;
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int m = m0 + ty + 16 * u;
-    if (m >= g.M) continue;
-    const float rs = g.rowscale ? g.rowscale[bz * g.sRb + m] : 1.f;
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const int n = n0 + tx + 16 * v;
-      if (n >= g.N) continue;
-      float t = g.alpha * rs * acc[u][v];
-      if (g.emul) t *= g.emul[bz * g.sEb + m * g.sEm + n * g.sEn];
-      float* c = C + m * g.sCm + n * g.sCn;
-      const float pre = g.accumulate ? *c + t : t;
-      if (g.epi == 1) {
-        *c = gelu_f(pre);
-        if (g.C2) g.C2[bz * g.sC2b + m * g.sC2m + n * g.sC2n] = gelu_prime_f(pre);
-      } else {
-        *c = pre;
-      }
-    }
-  }
-}
-
 static Gemm gemm0() {
   Gemm g;
   memset(&g, 0, sizeof(g));
@@ -151,11 +95,23 @@ static TcGemm tc0() {
   return g;
 }
 
+// Every product of the path runs on the tensor cores (tc_gemm.cu, bf16 hi/lo
+// operands, fp32 accumulation) with the same epilogue: the elementwise factor,
+// accumulation and the GELU / GELU' pair.
 static int run_gemm(const Gemm& g, cudaStream_t st) {
   if (g.M <= 0 || g.N <= 0 || g.batch <= 0) return ATLAS_OK;
-  dim3 grid((g.N + GT - 1) / GT, (g.M + GT - 1) / GT, g.batch);
-  gemm_kernel<<<grid, 256, 0, st>>>(g);
-  return cudaGetLastError() == cudaSuccess ? ATLAS_OK : ATLAS_ERR_CUDA;
+  TcGemm t = tc0();
+  t.M = g.M; t.N = g.N; t.K = g.K; t.batch = g.batch;
+  t.A = g.A; t.sAb = g.sAb; t.sAm = g.sAm; t.sAk = g.sAk;
+  t.B = g.B; t.sBb = g.sBb; t.sBk = g.sBk; t.sBn = g.sBn;
+  t.C = g.C; t.sCb = g.sCb; t.sCm = g.sCm; t.sCn = g.sCn;
+  t.alpha = g.alpha;
+  t.rowscale = g.rowscale; t.sRb = g.sRb;
+  t.emul = g.emul; t.sMb = g.sEb; t.sMm = g.sEm; t.sMn = g.sEn;
+  t.accumulate = g.accumulate;
+  t.epi = g.epi;
+  t.C2 = g.C2; t.sC2b = g.sC2b; t.sC2m = g.sC2m; t.sC2n = g.sC2n;
+  return tc_gemm_launch(t, st);
 }
 
 // --------------------------------------------------------------- workspace

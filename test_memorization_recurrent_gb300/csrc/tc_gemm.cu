@@ -3,7 +3,8 @@
 // the window products of the MLP-memory path.
 //
 //   C[b](m, n) = alpha * rowscale[b](m) * sum_k A[b](m, k) kscale[b](k) B[b](k, n)
-//                + beta * dscale[b] * D[b](m, n)  (+ C[b](m, n) when accumulating)
+//                (* emul[b](m, n)) + beta * dscale[b] * D[b](m, n)  (+ C[b](m, n) when
+//                accumulating), then optionally C = GELU(that), C2 = GELU'(that)
 //
 // Each operand element is split into bf16 hi + lo (hi = rn(x), lo = rn(x - hi));
 // the product is accumulated in fp32 from hi*hi + hi*lo + lo*hi, which keeps
@@ -26,6 +27,14 @@ namespace atlas {
 using namespace tc;
 
 namespace {
+
+__device__ __forceinline__ float gelu_exact(float x) {
+  return 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
+}
+__device__ __forceinline__ float gelu_exact_prime(float x) {
+  return 0.5f * (1.f + erff(x * 0.70710678118654752f)) +
+         x * 0.39894228040143268f * expf(-0.5f * x * x);
+}
 
 constexpr int TB = 128;           // tile M = tile N
 constexpr int TK = 64;            // K block (one 128-byte bf16 row)
@@ -242,8 +251,17 @@ __global__ void __launch_bounds__(kThr, 3) tc_gemm_kernel(TcGemm g) {
           atomicAdd(crow + n, t);
           continue;
         }
+        if (g.emul) t *= g.emul[bo * g.sMb + bi * g.sMb2 + (long)m * g.sMm + (long)n * g.sMn];
         if (drow) t += db * drow[n];
-        crow[n] = g.accumulate ? crow[n] + t : t;
+        const float pre = g.accumulate ? crow[n] + t : t;
+        if (g.epi) {
+          crow[n] = gelu_exact(pre);
+          if (g.C2)
+            g.C2[bo * g.sC2b + bi * g.sC2b2 + (long)m * g.sC2m + (long)n * g.sC2n] =
+                gelu_exact_prime(pre);
+        } else {
+          crow[n] = pre;
+        }
       }
     }
   } else if (nkb > 0) {
@@ -266,9 +284,18 @@ __global__ void __launch_bounds__(kThr, 3) tc_gemm_kernel(TcGemm g) {
           const int n = n0 + c0 + x;
           if (n >= g.N) continue;
           float t = g.alpha * rs * acc[x];
+          if (g.emul) t *= g.emul[bo * g.sMb + bi * g.sMb2 + (long)m * g.sMm + (long)n * g.sMn];
           if (D) t += db * D[(long)m * g.sDm + (long)n * g.sDn];
           float* c = C + (long)m * g.sCm + (long)n * g.sCn;
-          *c = g.accumulate ? *c + t : t;
+          const float pre = g.accumulate ? *c + t : t;
+          if (g.epi) {
+            *c = gelu_exact(pre);
+            if (g.C2)
+              g.C2[bo * g.sC2b + bi * g.sC2b2 + (long)m * g.sC2m + (long)n * g.sC2n] =
+                  gelu_exact_prime(pre);
+          } else {
+            *c = pre;
+          }
         }
       }
     }
@@ -306,7 +333,7 @@ int tc_gemm_launch(const TcGemm& g0, cudaStream_t st) {
   TcGemm g = g0;
   if (g.symmetric && (g.M != TB || g.N != TB)) return ATLAS_ERR_UNSUPPORTED;
   const int nsplit = g.ksplit > 1 ? g.ksplit : 1;
-  if (nsplit > 1 && (g.D || g.sCn != 1)) return ATLAS_ERR_UNSUPPORTED;
+  if (nsplit > 1 && (g.D || g.sCn != 1 || g.emul || g.epi)) return ATLAS_ERR_UNSUPPORTED;
   g.modeA = pick_mode(g.A, g.sAm, g.sAk, g.sAb, g.sAb2, g.batch);
   g.modeB = pick_mode(g.B, g.sBn, g.sBk, g.sBb, g.sBb2, g.batch);
   // a per-k factor is applied elementwise: the vector paths handle it too
