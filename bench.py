@@ -438,12 +438,14 @@ def _bwd_prof(w):
     return files, prof.format(wname=w.name), w.tokens
 
 
-def measure_backward(steps, warmup, dev):
+def measure_backward(steps, warmup, dev, momentum=False):
     """The backward pass over the whole DeltaNet-like workload (every head, every
-    token): rate, and the fraction of the fp32 CUDA-core peak it reaches."""
+    token), or the same shape with momentum in the forward (eta ~ U(0.5, 0.9)):
+    rate, and the fraction of the fp32 CUDA-core peak it reaches."""
     import torch
     from test_memorization_recurrent_gb300.harness import BackwardRunner, to_device
-    w = W.workload(2)
+    w = W.workload(2, eta=(0.5, 0.9), name="linear-momentum-b64-bf16") if momentum else \
+        W.workload(2)
     inp = W.generate(w)
     d = to_device(w, inp, dev)
     r = np.random.default_rng(3)
@@ -644,9 +646,10 @@ def run_atlas(args, w):
                                      dev, not args.no_cpu_baseline)
                       for wid, n in PER_CONFIG if wid != w.wid]
 
-    backward = variants = None
+    backward = backward_momentum = variants = None
     if world == 1 and not args.no_per_config and not args.tokens and args.loss == "l2":
         backward = measure_backward(min(args.steps, 5), 2, dev)
+        backward_momentum = measure_backward(min(args.steps, 5), 2, dev, momentum=True)
         variants = [measure_config(v, None, min(args.steps, 5), 3, dev, not args.no_cpu_baseline)
                     for v in variant_workloads()]
 
@@ -684,6 +687,8 @@ def run_atlas(args, w):
         line["per_config"] = per_config
     if backward is not None:
         line["backward"] = backward
+    if backward_momentum is not None:
+        line["backward_momentum"] = backward_momentum
     if variants is not None:
         line["variants"] = variants
     print(json.dumps(line), flush=True)

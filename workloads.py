@@ -266,7 +266,9 @@ def bwd_flop_per_token(w: Workload) -> float:
     d, b = w.d_k, w.b
     X = 2.0 * b * d * d      # a (b x d) by (d x d) product
     Y = 2.0 * b * b * d      # a (b x b) by (b x d) product
-    return (10 * X + 5 * Y) / b
+    # with momentum: S_end in the replay, K dSe^T, Q S0^T, E dSe, dY S0 and the dS_0 term
+    mom = 6 * X if w.eta[1] > 0 else 0.0
+    return (10 * X + 5 * Y + mom) / b
 
 
 def bwd_bytes_per_token(w: Workload) -> float:
