@@ -756,8 +756,12 @@ def main(argv=None):
                     help="attentional bias: l2 (the workloads'), or the Miras l_p / Huber variants")
     ap.add_argument("--loss-param", type=float, default=0.0,
                     help="p of the l_p bias (default 3), delta of the Huber bias (default 0.3)")
+    ap.add_argument("--momentum", action="store_true",
+                    help="with --profile-call backward: momentum in the forward, eta ~ U(0.5, 0.9)")
     args = ap.parse_args(argv)
     w = W.workload(args.workload, bounded=True)
+    if args.momentum:
+        w = w.with_(eta=(0.5, 0.9), name="linear-momentum-b64-bf16")
     if args.tokens:
         w = w.with_(N=min(args.tokens, w.N))
     if args.loss != "l2":

@@ -62,23 +62,23 @@ __device__ __forceinline__ float phi_at(const float* x, int j, int d, const uint
 // with a_n = prod(1-alpha), eps_n = prod(eta), beta_n = (1-alpha_n) beta_{n-1} + eps_n,
 // U[n,i] = eta_n U[n-1,i] + theta_n gamma[t_n - t_i] (lag inside the window),
 // W[n,i] = (1-alpha_n) W[n-1,i] + U[n,i].
-// One warp builds them; lanes stride over the window tokens.  Urun/Wrun are
-// running rows of length L; Wt (nb x ldw) receives every W row; Ulast / Wlast
-// the last rows.
-__device__ __forceinline__ void chunk_tables_warp(const float* alpha, const float* eta,
-                                                  const float* theta, const float* gamma,
-                                                  int t0, int nb, int i0, int L, int c,
-                                                  float* Urun, float* Wrun, float* Wt, int ldw,
-                                                  float* Ut, float* a_out, float* e_out,
-                                                  float* b_out) {
-  const int lane = threadIdx.x & 31;
-  for (int i = lane; i < L; i += 32) {
+// Threads tid = 0 .. nthr - 1 (whole warps) share the window columns: each column's
+// recursion over n belongs to one thread, and every warp loads the gates of 32
+// tokens at a time and broadcasts them from lane to lane.  Urun/Wrun are running
+// rows of length L; Wt (nb x ldw) receives every W row, Ut every U row (either may
+// be null); thread 0 writes a_n, eps_n, beta_n.  The caller synchronises after.
+__device__ __forceinline__ void chunk_tables(const float* alpha, const float* eta,
+                                             const float* theta, const float* gamma, int t0,
+                                             int nb, int i0, int L, int c, float* Urun,
+                                             float* Wrun, float* Wt, int ldw, float* Ut,
+                                             float* a_out, float* e_out, float* b_out, int tid,
+                                             int nthr) {
+  const int lane = tid & 31;
+  for (int i = tid; i < L; i += nthr) {
     Urun[i] = 0.f;
     Wrun[i] = 0.f;
   }
   float pa = 1.f, pe = 1.f, pb = 0.f;
-  // the gates of 32 tokens at a time come in one load per lane (ahead of the
-  // sequential loop) and are broadcast from lane to lane
   float g_keep = 1.f, g_eta = 0.f, g_theta = 0.f;
   for (int n = 0; n < nb; ++n) {
     const int tn = t0 + n;
@@ -94,7 +94,7 @@ __device__ __forceinline__ void chunk_tables_warp(const float* alpha, const floa
     pa *= keep;
     pe *= et;
     pb = keep * pb + pe;
-    for (int i = lane; i < L; i += 32) {
+    for (int i = tid; i < L; i += nthr) {
       const int lag = tn - (i0 + i);
       const float g = (lag >= 0 && lag < c) ? gamma[lag] : 0.f;
       const float u = et * Urun[i] + th * g;
@@ -104,11 +104,22 @@ __device__ __forceinline__ void chunk_tables_warp(const float* alpha, const floa
       if (Wt) Wt[n * ldw + i] = w;
       if (Ut) Ut[n * ldw + i] = u;
     }
-    if (lane == 0) {
+    if (tid == 0) {
       a_out[n] = pa;
       e_out[n] = pe;
       b_out[n] = pb;
     }
   }
+}
+
+// The same tables built by one warp (the caller's lanes).
+__device__ __forceinline__ void chunk_tables_warp(const float* alpha, const float* eta,
+                                                  const float* theta, const float* gamma,
+                                                  int t0, int nb, int i0, int L, int c,
+                                                  float* Urun, float* Wrun, float* Wt, int ldw,
+                                                  float* Ut, float* a_out, float* e_out,
+                                                  float* b_out) {
+  chunk_tables(alpha, eta, theta, gamma, t0, nb, i0, L, c, Urun, Wrun, Wt, ldw, Ut, a_out, e_out,
+               b_out, threadIdx.x & 31, 32);
   __syncwarp();
 }

@@ -19,7 +19,7 @@
 //             - 2 sum_i W[n,i] (Phi(k_i).Phi(q_n)) E[i,r]
 //   M[r,:]  = a_b M0 + beta_b S0 - 2 sum_i W[b,i] E[i,r] Phi(k_i)
 //   S[r,:]  = eps_b S0 - 2 sum_i U[b,i] E[i,r] Phi(k_i)
-// with the scalar tables of chunk_tables_warp.  Phi(q).Phi(k) for the degree-2
+// with the scalar tables of chunk_tables.  Phi(q).Phi(k) for the degree-2
 // map is evaluated as s + (s^2 + sum_j q_j^2 k_j^2)/2 with s = q.k, which is the
 // same sum regrouped.  The gated polynomial map of any degree ("논문 리뷰 Google
 // ATLAS" §3.1, Input gating) keeps one 32-bit entry per feature (its sorted
@@ -512,9 +512,9 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
         sb[n] = theta[t0 + n];
       }
       for (int l = tid; l < p.c; l += nt) Urun[l] = p.gamma[l];
-    } else if (tid < 32) {
-      chunk_tables_warp(alpha, eta, theta, p.gamma, t0, nb, i0, Lw, p.c, Urun, Wrun, P, L.Lmax,
-                        nullptr, sa, se, sb);
+    } else {
+      chunk_tables(alpha, eta, theta, p.gamma, t0, nb, i0, Lw, p.c, Urun, Wrun, P, L.Lmax,
+                   nullptr, sa, se, sb, tid, nt);
     }
     // l_q: Z[r] = 1 / ||A_r||_q^(q-2) of the chunk-start accumulator (1 for a zero row)
     if (ret == ATLAS_RET_LQ) {

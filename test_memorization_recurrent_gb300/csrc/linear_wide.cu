@@ -11,7 +11,7 @@
 //   E[i,r]  = bias(M0[r,:].Phi(k_i) - v_i[r])
 //   y_n[r]  = a_n M0[r,:].Phi(q_n) + beta_n S0[r,:].Phi(q_n) - 2 sum_i W[n,i] (Phi(q_n).Phi(k_i)) E[i,r]
 //   M[r,:]  = a_b M0 + beta_b S0 - 2 sum_i W[b,i] E[i,r] Phi(k_i),  S likewise with U
-// (the scalar tables of chunk_tables_warp).  The products over the feature
+// (the scalar tables of chunk_tables).  The products over the feature
 // dimension split by column slice: each CTA forms the partial errors and the
 // partial readout of its slice, and the cluster adds them through distributed
 // shared memory -- CTA c sums the partials of every rank for its share of the
@@ -245,9 +245,8 @@ __global__ void __launch_bounds__(256, 1) linear_wide_kernel(LinArgs p, WideSmem
       Kw[(x / dk) * dkp + x % dk] = ld_in(p.K, kbase + (long)i0 * dk + x, p.bf16);
     for (int x = tid; x < nb * dk; x += nt)
       Qc[(x / dk) * dkp + x % dk] = ld_in(p.Q, qbase + (long)t0 * dk + x, p.bf16);
-    if (tid < 32)
-      chunk_tables_warp(alpha, eta, theta, p.gamma, t0, nb, i0, Lw, p.c, Urun, Wrun, Wt, Lmax,
-                        nullptr, sa, se, sb);
+    chunk_tables(alpha, eta, theta, p.gamma, t0, nb, i0, Lw, p.c, Urun, Wrun, Wt, Lmax, nullptr,
+                 sa, se, sb, tid, nt);
     __syncthreads();
     // 1. partial errors over this slice; P for this rank's queries (in place in Wt)
     if (!p.dot) {

@@ -210,16 +210,16 @@ __global__ void mlp_gather_kernel(MlpArgs p, MlpWs w, float* ws, int t0, int nb,
   }
   for (int x = threadIdx.x; x < nb * d; x += blockDim.x)
     base[w.Qc + x] = ld_in(p.Q, qb + (long)t0 * d + x, p.bf16);
-  if (threadIdx.x < 32) {
+  {  // every thread of the CTA takes window columns of the tables
     const long gb = (long)h * p.N;
     // U and W rows go to their tables; the running rows live in shared memory
     // when they fit (dynamic size 2 L floats), else in the P1/P2 scratch
     extern __shared__ float run_sm[];
     float* run_u = L <= kRunSmem ? run_sm : base + w.P1;
     float* run_w = L <= kRunSmem ? run_sm + L : base + w.P2;
-    chunk_tables_warp(p.alpha + gb, p.eta + gb, p.theta + gb, p.gamma, t0, nb, i0, L, p.c,
-                      run_u, run_w, base + w.W, L, base + w.U, base + w.ta, base + w.te,
-                      base + w.tb);
+    chunk_tables(p.alpha + gb, p.eta + gb, p.theta + gb, p.gamma, t0, nb, i0, L, p.c, run_u,
+                 run_w, base + w.W, L, base + w.U, base + w.ta, base + w.te, base + w.tb,
+                 threadIdx.x, blockDim.x);
   }
 }
 
