@@ -193,7 +193,8 @@ size_t mlp_simt_workspace_bytes(const MlpArgs& a) { return mlp_layout(a).bytes; 
 // Window lengths whose two running table rows fit in 48 KB of shared memory.
 constexpr int kRunSmem = 6144;
 
-// Window and chunk inputs as fp32, E preset to K - V, and the scalar tables.
+// Window and chunk inputs as fp32, E preset to K - V (CTAs (h, y) share head h's
+// elements), and the scalar tables (CTA (h, 0), after its share).
 __global__ void mlp_gather_kernel(MlpArgs p, MlpWs w, float* ws, int t0, int nb, int i0, int L) {
   const int h = blockIdx.x;
   float* base = ws + h * w.per_head;
@@ -201,15 +202,17 @@ __global__ void mlp_gather_kernel(MlpArgs p, MlpWs w, float* ws, int t0, int nb,
   // K, V: head stride (nh + N) rows, token 0 at row nh (i0 may be negative)
   const long kb = ((long)h * (p.N + p.nh) + p.nh) * d;
   const long qb = (long)h * p.N * d;
-  for (int x = threadIdx.x; x < L * d; x += blockDim.x) {
+  const int g = blockIdx.y * blockDim.x + threadIdx.x, ng = gridDim.y * blockDim.x;
+  for (int x = g; x < L * d; x += ng) {
     const float k = ld_in(p.K, kb + (long)i0 * d + x, p.bf16);
     const float v = ld_in(p.V, kb + (long)i0 * d + x, p.bf16);
     base[w.Kw + x] = k;
     base[w.Vw + x] = v;
     base[w.E + x] = k - v;
   }
-  for (int x = threadIdx.x; x < nb * d; x += blockDim.x)
+  for (int x = g; x < nb * d; x += ng)
     base[w.Qc + x] = ld_in(p.Q, qb + (long)t0 * d + x, p.bf16);
+  if (blockIdx.y != 0) return;
   {  // every thread of the CTA takes window columns of the tables
     const long gb = (long)h * p.N;
     // U and W rows go to their tables; the running rows live in shared memory
@@ -595,7 +598,8 @@ int mlp_simt_forward(const MlpArgs& p0, void* wsv, cudaStream_t st) {
   for (int t0 = 0; t0 < p.N; t0 += p.b) {
     const int t1 = min(p.N, t0 + p.b), nb = t1 - t0;
     const int i0 = max(-p.nh, t0 - p.c + 1), L = t1 - i0;  // history rows enter windows
-    mlp_gather_kernel<<<H, 256, L <= kRunSmem ? 2 * L * sizeof(float) : 0, st>>>(p, w, ws, t0, nb, i0, L);
+    mlp_gather_kernel<<<dim3(H, 8), 256, L <= kRunSmem ? 2 * L * sizeof(float) : 0, st>>>(
+        p, w, ws, t0, nb, i0, L);
     CL();
     // Z = K_w W2^T ; H = GELU(Z), Gp = GELU'(Z)
     Gemm g = gemm0();
