@@ -8,6 +8,16 @@
 
 #define ATLAS_HD __host__ __device__ __forceinline__
 
+// Programmatic dependent launch.  pdl_launch_dependents lets the next kernel on
+// the stream, when it was launched with programmatic stream serialisation, be
+// scheduled before this grid ends; pdl_wait returns once the grid this one
+// depends on has completed and its writes are visible (at once when there is
+// none), so everything before it may only touch on-chip state and parameters.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Element t of a K/Q/V tensor stored as fp32 or bf16.
 __device__ __forceinline__ float ld_in(const void* p, long idx, int bf16) {
   if (bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[idx]);

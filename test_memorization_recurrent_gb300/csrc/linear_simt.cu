@@ -60,6 +60,11 @@ static int launch(const LinArgs& a, int heads, const int* flags, cudaStream_t st
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+  } else if (flags) {  // after the tensor-core kernel: launch overlaps its tail
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
   }
   cudaError_t e;
   switch (a.ret) {

@@ -393,10 +393,14 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
 // flags != nullptr: only the heads whose flag is set (the heads the tensor-core
 // kernel leaves, which it marks); every other head returns at once, and each
 // CTA walks all row blocks of its head so that the grid stays one CTA per head.
+// Launched with programmatic stream serialisation when it follows the tensor-core
+// kernel: it lets its own successor be scheduled, then waits for its predecessor.
 template <int GATE>
 __global__ void __launch_bounds__(256) linear_simt_kernel(LinArgs p, LinSimtSmem L,
                                                           const int* flags) {
   const int head = blockIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
   if (flags) {
     if (flags[head] == 0) return;
     for (int r0 = 0; r0 < p.d_v; r0 += L.RV) {

@@ -236,9 +236,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int N = p.N;
   const int nchunks = (N + kChunk - 1) / kChunk;
 
-  // the head is this kernel's unless a chunk hands it off (momentum, reset gate)
-  if (tid == 0) p.flags[head] = 0;
-  if (nchunks == 0) return;
+  // the next launch (the CUDA-core kernel for handed-off heads) may be scheduled
+  // now: it waits for this grid's completion before it reads anything
+  pdl_launch_dependents();
+  if (nchunks == 0) {
+    pdl_wait();
+    if (tid == 0) p.flags[head] = 0;
+    return;
+  }
 
   if (tid == 0) {
     for (int b = 0; b < B_COUNT; ++b) {
@@ -258,6 +263,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, TM_COLS);
     tmem_relinquish();
   }
+  // the set-up above touched only on-chip state; the preceding launch's outputs
+  // (inputs, state, flags of this call) are complete from here
+  pdl_wait();
+  // the head is this kernel's unless a chunk hands it off (momentum, reset gate)
+  if (tid == 0) p.flags[head] = 0;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -766,8 +776,22 @@ int linear_tc_launch(const LinArgs& a, int heads, int* status, void* workspace, 
   if (cudaFuncSetAttribute(linear_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)SMEM_ALLOC) != cudaSuccess)
     return ATLAS_ERR_CUDA;
-  linear_tc_kernel<<<heads, kThreads, SMEM_ALLOC, st>>>(maps, p);
-  if (cudaGetLastError() != cudaSuccess) return ATLAS_ERR_CUDA;
+  // launched with programmatic stream serialisation: its launch and set-up overlap
+  // the tail of the preceding kernel, and it waits for that kernel before any
+  // global access
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(heads);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = SMEM_ALLOC;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, linear_tc_kernel, maps, p) != cudaSuccess ||
+      cudaGetLastError() != cudaSuccess)
+    return ATLAS_ERR_CUDA;
   // heads with a non-zero eta: the CUDA-core kernel takes exactly the flagged ones
   return linear_simt_launch_flagged(a, heads, p.flags, st);
 }
