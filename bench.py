@@ -513,8 +513,8 @@ def e2e_rate(w, d, run, steps, warmup, stream, world, dev, groups=8):
     device buffers used on alternate steps: its next copy-in overlaps its current
     update and copy-out, and the two copy directions run at once.  Events order
     each buffer's reuse.  The timed region starts before the first copy-in and
-    ends after the last copy-out.  Returns (seconds for all steps, h2d bytes per
-    step, d2h bytes per step)."""
+    ends after the last copy-out.  Returns (seconds for all steps, seconds for the
+    same steps with the copies alone, h2d bytes per step, d2h bytes per step)."""
     import torch
     import test_memorization_recurrent_gb300 as A
     from test_memorization_recurrent_gb300.harness import cfg_for
@@ -559,7 +559,7 @@ def e2e_rate(w, d, run, steps, warmup, stream, world, dev, groups=8):
                      ws))
     used = [[False, False] for _ in range(G)]
 
-    def steps_of(n, first):
+    def steps_of(n, first, compute=True):
         start = torch.cuda.Event()
         start.record(stream)
         for g in range(G):
@@ -577,11 +577,12 @@ def e2e_rate(w, d, run, steps, warmup, stream, world, dev, groups=8):
                 s_cp[g].wait_event(ev_in[g][par])
                 if used[g][par]:  # the outputs of this buffer have been copied out
                     s_cp[g].wait_event(ev_out[g][par])
-                with torch.cuda.stream(s_cp[g]):
-                    ov["M"].copy_(iv["M0"])
-                A.atlas_mem_forward(iv["K"], iv["Q"], iv["V"], iv["alpha"], iv["eta"],
-                                    iv["theta"], iv["gamma"], cfgs[g][0], ov["Y"], ov["M"],
-                                    s_cp[g])
+                if compute:
+                    with torch.cuda.stream(s_cp[g]):
+                        ov["M"].copy_(iv["M0"])
+                    A.atlas_mem_forward(iv["K"], iv["Q"], iv["V"], iv["alpha"], iv["eta"],
+                                        iv["theta"], iv["gamma"], cfgs[g][0], ov["Y"], ov["M"],
+                                        s_cp[g])
                 ev_cp[g][par].record(s_cp[g])
                 s_out[g].wait_event(ev_cp[g][par])
                 with torch.cuda.stream(s_out[g]):
@@ -594,17 +595,24 @@ def e2e_rate(w, d, run, steps, warmup, stream, world, dev, groups=8):
                 e.record(s_)
                 stream.wait_event(e)
 
-    steps_of(max(2, warmup), 0)
-    torch.cuda.synchronize()
-    barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    steps_of(steps, max(2, warmup))
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    return e0.elapsed_time(e1) / 1e3, h2d, d2h
+    def timed(compute):
+        steps_of(max(2, warmup), 0, compute)
+        torch.cuda.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        steps_of(steps, max(2, warmup), compute)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return e0.elapsed_time(e1) / 1e3
+
+    t = timed(True)
+    # the same copies, streams and events with no update: the rate the host link
+    # allows for this step's bytes, against which the end-to-end rate is read
+    t_copy = timed(False)
+    return t, t_copy, h2d, d2h
 
 
 def run_atlas(args, w):
@@ -633,8 +641,9 @@ def run_atlas(args, w):
         elapsed, kernel_s, flush = time_device(w, run, d, args.steps, args.warmup, stream, clk,
                                                world)
     elapsed_max = max_over_ranks(elapsed, world, dev)
-    e2e_s, h2d, d2h = e2e_rate(w, d, run, args.steps, args.warmup, stream, world, dev)
+    e2e_s, copy_s, h2d, d2h = e2e_rate(w, d, run, args.steps, args.warmup, stream, world, dev)
     e2e_s = max_over_ranks(e2e_s, world, dev)
+    copy_s = max_over_ranks(copy_s, world, dev)
     if int(run.status.item()) != 0:
         raise SystemExit(f"device status {int(run.status.item())} in the end-to-end leg")
 
@@ -679,7 +688,11 @@ def run_atlas(args, w):
         "roofline": roofline(w, path, kernel_s),
         "cpu_baseline": cpu,
         "e2e": {"value": aggregate(tokens, world, e2e_s, args.steps), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "copies_only": {"value": aggregate(tokens, world, copy_s, args.steps),
+                                "ms_per_step": copy_s * 1e3 / args.steps,
+                                "note": "the same pinned copies with no update: the "
+                                        "host-link bound of the end-to-end rate"}},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }

@@ -112,12 +112,17 @@ __device__ __forceinline__ void store_block(const Operand& o, const float* v, ui
   if (o.mode == M_RVEC) {
     // all lanes of a warp hold the same k chunk; rotating the row order by lane
     // spreads one store instruction over all eight 16-byte bank groups
+    // (the row is picked by selects, not by indexing v, so that v stays in registers)
     const int l = tid & 31, rb = 4 * l, c = tid >> 5;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int qq = (q + l) & 3;
+      float t[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        t[e] = (qq & 2) ? ((qq & 1) ? v[24 + e] : v[16 + e]) : ((qq & 1) ? v[8 + e] : v[e]);
       const uint32_t off = sw128_offset((uint32_t)(rb + qq), (uint32_t)c);
-      store_split8(hi + off, lo + off, v + 8 * qq);
+      store_split8(hi + off, lo + off, t);
     }
     return;
   }
@@ -130,7 +135,7 @@ __device__ __forceinline__ void store_block(const Operand& o, const float* v, ui
 
 }  // namespace
 
-__global__ void __launch_bounds__(kThr, 3) tc_gemm_kernel(TcGemm g) {
+__global__ void __launch_bounds__(kThr, 2) tc_gemm_kernel(TcGemm g) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
