@@ -418,7 +418,13 @@ __global__ void __launch_bounds__(256) mom_stream_kernel(MlpArgs p, MlpWs w, con
   const int tiles_per_blk = 4;  // 128 x 512 blocks in 128 x 128 tiles
   const int blk = blockIdx.x / tiles_per_blk, tile = blockIdx.x % tiles_per_blk;
   if (blk >= nblk) return;
-  const MomStream& ms = blk == 0 ? m0 : blk == 1 ? m1 : m2;
+  // field by field: a reference to a selected parameter would copy all three to local memory
+  MomStream ms;
+  ms.ra = blk == 0 ? m0.ra : blk == 1 ? m1.ra : m2.ra;
+  ms.cb = blk == 0 ? m0.cb : blk == 1 ? m1.cb : m2.cb;
+  ms.a_off = blk == 0 ? m0.a_off : blk == 1 ? m1.a_off : m2.a_off;
+  ms.b_off = blk == 0 ? m0.b_off : blk == 1 ? m1.b_off : m2.b_off;
+  ms.blk_off = blk == 0 ? m0.blk_off : blk == 1 ? m1.blk_off : m2.blk_off;
   const int h = blockIdx.y;
   const float* base = ws + (long)h * w.per_head;
   const float* A = base + ms.a_off;  // [L][ra]
@@ -444,9 +450,8 @@ __global__ void __launch_bounds__(256) mom_stream_kernel(MlpArgs p, MlpWs w, con
       sv[u][4 * wq] = x.x; sv[u][4 * wq + 1] = x.y; sv[u][4 * wq + 2] = x.z; sv[u][4 * wq + 3] = x.w;
     }
   }
-  // g += f a_i b_i^T for the window row li
-  auto rank1 = [&](int li, float f) {
-    float a[8], b[8];
+  // this thread's parts of the window row li: a (times f) and b
+  auto load_row = [&](int li, float f, float* a, float* b) {
 #pragma unroll
     for (int u = 0; u < 8; ++u) a[u] = f * A[(long)li * ms.ra + r0 + ty + 16 * u];
 #pragma unroll
@@ -454,6 +459,8 @@ __global__ void __launch_bounds__(256) mom_stream_kernel(MlpArgs p, MlpWs w, con
       const float4 x = *reinterpret_cast<const float4*>(B + (long)li * ms.cb + c0 + 4 * tx + 64 * wq);
       b[4 * wq] = x.x; b[4 * wq + 1] = x.y; b[4 * wq + 2] = x.z; b[4 * wq + 3] = x.w;
     }
+  };
+  auto add_row = [&](const float* a, const float* b) {  // g += a b^T
 #pragma unroll
     for (int u = 0; u < 8; ++u)
 #pragma unroll
@@ -464,16 +471,36 @@ __global__ void __launch_bounds__(256) mom_stream_kernel(MlpArgs p, MlpWs w, con
     for (int u = 0; u < 8; ++u)
 #pragma unroll
       for (int v = 0; v < 8; ++v) gv[u][v] = 0.f;
-    const int lo = max(i0, t - c + 1);
-    for (int i = lo; i <= t; ++i) rank1(i - i0, 2.f * p.gamma[t - i]);
+    int i = max(i0, t - c + 1);
+    for (; i + 3 <= t; i += 4) {  // four rows' loads in flight before their products
+      float a[4][8], b[4][8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) load_row(i + q - i0, 2.f * p.gamma[t - i - q], a[q], b[q]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) add_row(a[q], b[q]);
+    }
+    for (; i <= t; ++i) {
+      float a[8], b[8];
+      load_row(i - i0, 2.f * p.gamma[t - i], a, b);
+      add_row(a, b);
+    }
   };
+  // constant gamma: the rows entering (token t) and leaving (token t - c) the
+  // window of token t, loaded one token ahead
+  float ain[8], bin[8], aout[8], bout[8];
+  bool out_row = false;
   for (int n = 0; n < nb; ++n) {
     const int t = t0 + n;
     if (n == 0 || !gconst) {
       window(t);
     } else {  // slide: token t enters, token t - c leaves (if it was in the window)
-      rank1(t - i0, 2.f * g0);
-      if (t - c >= i0) rank1(t - c - i0, -2.f * g0);
+      add_row(ain, bin);
+      if (out_row) add_row(aout, bout);
+    }
+    if (gconst && n + 1 < nb) {
+      load_row(t + 1 - i0, 2.f * g0, ain, bin);
+      out_row = t + 1 - c >= i0;
+      if (out_row) load_row(t + 1 - c - i0, -2.f * g0, aout, bout);
     }
     const float et = eta[t], th = theta[t];
     float* Xn = X + ((long)h * nb + n) * state + ms.blk_off;
@@ -508,13 +535,13 @@ __global__ void ns_readout_add_kernel(float* out, long out_head, long ld, const 
   const long per = (long)rows * nb;
   for (long x = blockIdx.x * blockDim.x + threadIdx.x; x < per;
        x += (long)gridDim.x * blockDim.x) {
-    const int n = (int)(x / rows), j = (int)(x % rows);
-    const float* ph = P + (long)h * nb * per;
-    float acc = 0.f, r = 1.f;
-    for (int m = n; m >= 0; --m) {
-      acc += r * ph[(long)m * per + (long)j * nb + n];
-      r *= 1.f - alpha[(long)h * N + t0 + m];
-    }
+    // n fastest: a warp reads consecutive n of one row j of each P_m
+    const int n = (int)(x % nb), j = (int)(x / nb);
+    const float* ph = P + (long)h * nb * per + (long)j * nb + n;
+    // acc_k = (1 - alpha_k) acc_{k-1} + P_k, so acc_n = sum_{m<=n} r[n,m] P_m
+    float acc = 0.f;
+    for (int k = 0; k <= n; ++k)
+      acc = fmaf(1.f - alpha[(long)h * N + t0 + k], acc, ph[(long)k * per]);
     float* o = out + h * out_head + (long)n * ld + j;
     float v = *o + acc;
     if (gelu) v = 0.5f * v * (1.f + erff(v * 0.70710678118654752f));
