@@ -149,6 +149,39 @@ __device__ __forceinline__ float bias_grad2(float e, int kind, float prm) {
   return 1.f;
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* a) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+}
+
+// Into L2, ahead of their loads: the inputs of chunk j of head h that this CTA
+// (value rows [v0, v0 + kRB)) reads -- K, V and, in the reverse pass (rev), Q,
+// dY, the chunk-start state and momentum rows and C.  One 128-byte line each.
+__device__ __forceinline__ void prefetch_chunk(const BwdArgs& p, int h, int j, int v0, bool rev) {
+  const int t0 = j * kB, nb = min(kB, p.N - t0);
+  const int es = p.bf16 ? 2 : 4;
+  const long row0 = (long)h * p.N + t0;
+  const char* K = reinterpret_cast<const char*>(p.K) + row0 * kD * es;
+  const char* Q = reinterpret_cast<const char*>(p.Q) + row0 * kD * es;
+  const int lines = nb * kD * es / 128;
+  for (int x = threadIdx.x; x < lines; x += kThreads) {
+    prefetch_l2(K + 128 * (long)x);
+    if (rev) prefetch_l2(Q + 128 * (long)x);
+  }
+  for (int i = threadIdx.x; i < nb; i += kThreads) {
+    prefetch_l2(reinterpret_cast<const char*>(p.V) + ((row0 + i) * kD + v0) * es);
+    if (rev) prefetch_l2(p.dY + (row0 + i) * kD + v0);
+  }
+  if (!rev) return;
+  const long cb = (long)h * p.nch + j;
+  const size_t MS = (size_t)kD * kD;
+  for (int x = threadIdx.x; x < kRB * kD / 32; x += kThreads) {  // 32 floats a line
+    const size_t o = cb * MS + (size_t)v0 * kD + 32 * (size_t)x;
+    prefetch_l2(p.Mck + o);
+    prefetch_l2(p.Sck + o);
+  }
+  for (int x = threadIdx.x; x < kB * kB / 32; x += kThreads) prefetch_l2(p.tC + cb * kB * kB + 32 * x);
+}
+
 // K, Q rows of chunk j (tokens t0.., zero past N) into fp32 shared memory with
 // row strides ldk, ldq.
 __device__ __forceinline__ void load_kq(const BwdArgs& p, int h, int t0, int nb, float* sK,
@@ -493,6 +526,7 @@ __device__ __forceinline__ void bwd_rows_body(const BwdArgs& p) {
       sUb[tid] = p.tU[cb * kB * kB + (kB - 1) * kB + tid];
     }
     __syncthreads();
+    if (j + 1 < nch) prefetch_chunk(p, h, j + 1, v0, false);
     {  // E[i][v] = bias(K M0^T - V)
       auto fa = [&](int i, int f) { return sK[i * kPad + f]; };
       auto fb = [&](int f, int v) { return sM0[v * kPad + f]; };
@@ -541,6 +575,7 @@ __device__ __forceinline__ void bwd_rows_body(const BwdArgs& p) {
     for (int x = tid; x < 4 * kB + 3; x += kThreads) sAcc[x] = 0.f;
     const float e63 = p.tEp[cb * kB + kB - 1];
     __syncthreads();
+    if (j > 0) prefetch_chunk(p, h, j - 1, v0, true);
     // -- errors, bias', the weighted Z; da, db, dwb, dub summed over this block's rows
     bwd_tile_r1<MOM>(sK, sQ, sM0, sS0, sDM, sDS,
                 [&](int i, int v, float t, float z, float zs, float mq, float sq) {

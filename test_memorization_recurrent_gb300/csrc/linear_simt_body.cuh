@@ -384,6 +384,10 @@ __device__ __forceinline__ void serial_chunk_quad(int nb, int t0, int i0, int c,
   }
 }
 
+__device__ __forceinline__ void lin_prefetch_l2(const void* a) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+}
+
 // One CTA: rows [r0, r0 + RV) of one head, the whole sequence.  GATE: ATLAS_RET_L2
 // for the chunk tables (the l2 and l_q gates), else the token-serial gate it names.
 template <int GATE>
@@ -531,6 +535,20 @@ __device__ __forceinline__ void linear_simt_rows(const LinArgs& p, const LinSimt
       }
     }
     __syncthreads();
+    if (t1 < p.N) {  // the next chunk's own K, Q and V rows into L2 ahead of their loads
+      const int n1 = min(p.N, t1 + p.b), es = p.bf16 ? 2 : 4;
+      const char* Kn = reinterpret_cast<const char*>(p.K) + (kbase + (long)t1 * dk) * es;
+      const char* Qn = reinterpret_cast<const char*>(p.Q) + (qbase + (long)t1 * dk) * es;
+      const int kl = ((n1 - t1) * dk * es + 127) / 128;
+      for (int x = tid; x < kl; x += nt) {
+        lin_prefetch_l2(Kn + 128 * (long)x);
+        lin_prefetch_l2(Qn + 128 * (long)x);
+      }
+      const int segl = (rv * es + 127) / 128;  // lines of one V row segment
+      for (int x = tid; x < (n1 - t1) * segl; x += nt)
+        lin_prefetch_l2(reinterpret_cast<const char*>(p.V) +
+                        (vbase + (long)(t1 + x / segl) * dv + r0) * es + 128 * (x % segl));
+    }
     // errors at the chunk-start memory
     if (p.dot) {
       for (int x = tid; x < Lw * rv; x += nt) E[x] = -Vw[x];
