@@ -105,9 +105,11 @@ __device__ __forceinline__ void load_block(const Operand& o, int r0, int k0, flo
   }
 }
 
-// Split the block held in v into the hi / lo tiles.
+// Split the block held in v into the hi / lo tiles.  Rows at or past `rows` (the
+// operand's extent inside this tile) are left as they are: a row of A or B only
+// reaches the output row or column of the same index, which is never stored.
 __device__ __forceinline__ void store_block(const Operand& o, const float* v, uint32_t hi,
-                                            uint32_t lo) {
+                                            uint32_t lo, int rows) {
   const int tid = threadIdx.x;
   if (o.mode == M_RVEC) {
     // all lanes of a warp hold the same k chunk; rotating the row order by lane
@@ -122,12 +124,13 @@ __device__ __forceinline__ void store_block(const Operand& o, const float* v, ui
       for (int e = 0; e < 8; ++e)
         t[e] = (qq & 2) ? ((qq & 1) ? v[24 + e] : v[16 + e]) : ((qq & 1) ? v[8 + e] : v[e]);
       const uint32_t off = sw128_offset((uint32_t)(rb + qq), (uint32_t)c);
-      store_split8(hi + off, lo + off, t);
+      if (rb + qq < rows) store_split8(hi + off, lo + off, t);
     }
     return;
   }
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
+    if ((tid >> 3) + 32 * j >= rows) break;
     const uint32_t off = sw128_offset((uint32_t)((tid >> 3) + 32 * j), (uint32_t)(tid & 7));
     store_split8(hi + off, lo + off, v + 8 * j);
   }
@@ -189,8 +192,8 @@ __global__ void __launch_bounds__(kThr, 2) tc_gemm_kernel(TcGemm g) {
       tc_fence_after();
       if (!ok) break;
     }
-    store_block(oa, va, sb + OFF_AHI, sb + OFF_ALO);
-    if (!sym) store_block(ob, vb, sb + OFF_BHI, sb + OFF_BLO);
+    store_block(oa, va, sb + OFF_AHI, sb + OFF_ALO, min(TB, g.M - m0));
+    if (!sym) store_block(ob, vb, sb + OFF_BHI, sb + OFF_BLO, min(TB, g.N - n0));
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -221,19 +224,22 @@ __global__ void __launch_bounds__(kThr, 2) tc_gemm_kernel(TcGemm g) {
     if (tid == 0 && g.status) atomicExch(g.status, ATLAS_ERR_TIMEOUT);
   } else if (nkb > 0 && g.sCn == 1 && (!g.D || g.sDn == 1)) {
     // ---- epilogue through shared memory (the operand tiles are free): thread =
-    // row m, columns [64 (warp / 4), +64) into an fp32 [128][128] tile with the
-    // column index XOR (m % 32); then each warp writes whole rows, coalesced
+    // row m, columns [64 (warp / 4), +64) into an fp32 [128][128] tile in 16-byte
+    // groups, group g of row m at g XOR (m % 32); then each warp writes whole rows,
+    // four columns a lane
     float* tile = reinterpret_cast<float*>(sm);
     {
       const int q = warp & 3, half = warp >> 2;
       const int ml = q * 32 + lane;
       const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
-      for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
+      for (int c0 = 64 * half; c0 < 64 * half + 64 && n0 + c0 < g.N; c0 += 32) {
         float acc[32];
         tmem_ld32(tl + c0, acc);
 #pragma unroll
-        for (int x = 0; x < 32; ++x) tile[ml * TB + ((c0 + x) ^ lane)] = acc[x];
+        for (int g4 = 0; g4 < 8; ++g4)
+          *reinterpret_cast<float4*>(tile + ml * TB + 4 * (((c0 >> 2) + g4) ^ lane)) =
+              make_float4(acc[4 * g4], acc[4 * g4 + 1], acc[4 * g4 + 2], acc[4 * g4 + 3]);
       }
     }
     __syncthreads();
@@ -241,32 +247,57 @@ __global__ void __launch_bounds__(kThr, 2) tc_gemm_kernel(TcGemm g) {
     const float* D = g.D ? g.D + bo * g.sDb + bi * g.sDb2 : nullptr;
     const float db = g.beta * (g.dscale ? g.dscale[bo * g.sEb + bi * g.sEb2] : 1.f);
     const float* RS = g.rowscale ? g.rowscale + bo * g.sRb + bi * g.sRb2 : nullptr;
+    // rows of C start 16-byte aligned: whole groups go out as one vector
+    const bool cvec = ((reinterpret_cast<uintptr_t>(C) & 15) == 0) && (g.sCm & 3) == 0;
+    const int n = n0 + 4 * lane;  // this lane's columns n .. n + 3
     for (int ml = warp; ml < TB; ml += kThr / 32) {
       const int m = m0 + ml;
       if (m >= g.M) break;
+      if (n >= g.N) continue;
       const float rs = g.alpha * (RS ? RS[m] : 1.f);
+      const float4 t4 = *reinterpret_cast<const float4*>(tile + ml * TB + 4 * (lane ^ (ml & 31)));
+      float t[4] = {rs * t4.x, rs * t4.y, rs * t4.z, rs * t4.w};
       float* crow = C + (long)m * g.sCm;
-      const float* drow = D ? D + (long)m * g.sDm : nullptr;
+      if (nsplit > 1) {
 #pragma unroll
-      for (int j = 0; j < TB / 32; ++j) {
-        const int nl = 32 * j + lane, n = n0 + nl;
-        if (n >= g.N) continue;
-        float t = rs * tile[ml * TB + (nl ^ (ml & 31))];
-        if (nsplit > 1) {
-          atomicAdd(crow + n, t);
-          continue;
-        }
-        if (g.emul) t *= g.emul[bo * g.sMb + bi * g.sMb2 + (long)m * g.sMm + (long)n * g.sMn];
-        if (drow) t += db * drow[n];
-        const float pre = g.accumulate ? crow[n] + t : t;
-        if (g.epi) {
-          crow[n] = gelu_exact(pre);
-          if (g.C2)
-            g.C2[bo * g.sC2b + bi * g.sC2b2 + (long)m * g.sC2m + (long)n * g.sC2n] =
-                gelu_exact_prime(pre);
+        for (int e = 0; e < 4; ++e)
+          if (n + e < g.N) atomicAdd(crow + n + e, t[e]);
+        continue;
+      }
+      const bool full = cvec && n + 3 < g.N;
+      const float* drow = D ? D + (long)m * g.sDm : nullptr;
+      float cur[4] = {0.f, 0.f, 0.f, 0.f};
+      if (g.accumulate) {
+        if (full) {
+          const float4 c4 = *reinterpret_cast<const float4*>(crow + n);
+          cur[0] = c4.x; cur[1] = c4.y; cur[2] = c4.z; cur[3] = c4.w;
         } else {
-          crow[n] = pre;
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (n + e < g.N) cur[e] = crow[n + e];
         }
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (n + e >= g.N) break;
+        float x = t[e];
+        if (g.emul) x *= g.emul[bo * g.sMb + bi * g.sMb2 + (long)m * g.sMm + (long)(n + e) * g.sMn];
+        if (drow) x += db * drow[n + e];
+        float pre = g.accumulate ? cur[e] + x : x;
+        if (g.epi) {
+          if (g.C2)
+            g.C2[bo * g.sC2b + bi * g.sC2b2 + (long)m * g.sC2m + (long)(n + e) * g.sC2n] =
+                gelu_exact_prime(pre);
+          pre = gelu_exact(pre);
+        }
+        t[e] = pre;
+      }
+      if (full) {
+        *reinterpret_cast<float4*>(crow + n) = make_float4(t[0], t[1], t[2], t[3]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (n + e < g.N) crow[n + e] = t[e];
       }
     }
   } else if (nkb > 0) {
