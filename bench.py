@@ -473,7 +473,7 @@ def measure_backward(steps, warmup, dev, momentum=False):
     peak = fp32_alu_peak_tflops()
     rec = {"workload": w.name, "what": "backward pass (dK, dQ, dV, dalpha, deta, dtheta, dM_0)",
            "tokens_per_call": w.tokens, "steps": steps, "value": w.tokens / s, "unit": UNIT,
-           "ms_per_step": s * 1e3, "launches_per_call": 3,
+           "ms_per_step": s * 1e3, "launches_per_call": 4,
            "roofline": {"bound": "alu", "achieved": flops / s / 1e12, "peak": peak,
                         "unit": "TFLOP/s", "frac": flops / s / 1e12 / peak,
                         "peak_kind": "fp32 FMA peak from unit counts and clock",

@@ -199,7 +199,7 @@ size_t atlas_mem_backward_workspace_bytes(const atlas_mem_cfg* cfg);
  * Workspace: cfg->workspace of at least atlas_mem_backward_workspace_bytes()
  * (the chunk-start states and momenta, gate tables and partial sums; ~8.2 KB
  * per token).
- * Three kernel launches on `stream`; returns ATLAS_OK or an ATLAS_ERR_* code. */
+ * Four kernel launches on `stream`; returns ATLAS_OK or an ATLAS_ERR_* code. */
 int atlas_mem_backward(const void* K, const void* Q, const void* V, const float* alpha,
                        const float* eta, const float* theta, const float* gamma,
                        const atlas_mem_cfg* cfg, const float* M0, const float* dY, float* dM,

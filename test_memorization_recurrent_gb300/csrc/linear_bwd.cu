@@ -669,9 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_rows_kernel(BwdArgs p) {
 
 __global__ void __launch_bounds__(kThreads) bwd_finish_kernel(BwdArgs p) {
   extern __shared__ float sm[];
-  float* sK = sm;                 // [kB][kD]
-  float* sQ = sK + kB * kD;       // [kB][kD]
-  float* sW = sQ + kB * kD;       // [kB][kB] W, then the dalpha terms
+  float* sW = sm;                 // [kB][kB] W, then the dalpha terms
   float* sU = sW + kB * kB;       // [kB][kB] U, then the deta terms
   float* sDW = sU + kB * kB;      // [kB][kB] dW
   float* sDP = sDW + kB * kB;     // [kB][kB]
@@ -692,7 +690,6 @@ __global__ void __launch_bounds__(kThreads) bwd_finish_kernel(BwdArgs p) {
   const long g = (long)h * p.N + t0;
   const long cb = (long)h * p.nch + j;
   const size_t cbo = (size_t)cb * kB * kB;
-  load_kq(p, h, t0, nb, sK, kD, sQ, kD);
   for (int x = tid; x < kB * kB; x += kThreads) {
     const int n = x / kB, i = x % kB;
     float dc = 0.f;
@@ -781,24 +778,37 @@ __global__ void __launch_bounds__(kThreads) bwd_finish_kernel(BwdArgs p) {
     p.deta[g + n] = de;
     p.dtheta[g + n] = sTh[n];
   }
-  {  // dK[i] = sum of partials + sum_n dP[n][i] q_n; dQ[n] = ... + sum_i dP[n][i] k_i
-    const int f = tid & (kD - 1), ig = tid >> 7;
-    for (int r = 0; r < kB / 2; ++r) {
-      const int i = ig + 2 * r;
-      if (i >= nb) continue;
-      float sk = 0.f, sq = 0.f;
-      for (int n = 0; n < kB; ++n) {
-        sk += sDP[n * kB + i] * sQ[n * kD + f];
-        sq += sDP[i * kB + n] * sK[n * kD + f];
-      }
-      for (int rb = 0; rb < kR; ++rb) {
-        const size_t o = (((size_t)rb * p.heads + h) * p.N + t0 + i) * kD + f;
-        sk += p.pK[o];
-        sq += p.pQ[o];
-      }
-      p.dK[(g + i) * kD + f] = sk;
-      p.dQ[(g + i) * kD + f] = sq;
+  {  // dK[i] = sum_n dP[n][i] q_n, dQ[i] = sum_n dP[i][n] k_n (register-tiled: an 8 x 4
+     // block of (i, f) a thread; q_n and k_n straight from global memory, a warp reading
+     // 128 consecutive bytes, so that three CTAs fit an SM); the row-block partials are
+     // added by bwd_partials_kernel
+    auto row = [&](const void* X, int n, int f) {
+      return n < nb ? ld_in(X, (g + n) * kD + f, p.bf16) : 0.f;
+    };
+    tile_gemm<32, 8, 4>(nb, kD, kB, [&](int i, int n) { return sDP[n * kB + i]; },
+                        [&](int n, int f) { return row(p.Q, n, f); },
+                        [&](int i, int f, float s) { p.dK[(g + i) * kD + f] = s; });
+    tile_gemm<32, 8, 4>(nb, kD, kB, [&](int i, int n) { return sDP[i * kB + n]; },
+                        [&](int n, int f) { return row(p.K, n, f); },
+                        [&](int i, int f, float s) { p.dQ[(g + i) * kD + f] = s; });
+  }
+}
+
+// dK += the kR row-block partials of dK, dQ likewise, in row-block order: a
+// streaming pass over every head and token (the finish kernel, one large CTA
+// per SM, left too few loads in flight for it).
+__global__ void __launch_bounds__(kThreads) bwd_partials_kernel(BwdArgs p) {
+  const size_t T = (size_t)p.heads * p.N * kD;
+  for (size_t x = (size_t)blockIdx.x * kThreads + threadIdx.x; x < T;
+       x += (size_t)gridDim.x * kThreads) {
+    float sk = p.dK[x], sq = p.dQ[x];
+#pragma unroll
+    for (int rb = 0; rb < kR; ++rb) {
+      sk += p.pK[rb * T + x];
+      sq += p.pQ[rb * T + x];
     }
+    p.dK[x] = sk;
+    p.dQ[x] = sq;
   }
 }
 
@@ -809,7 +819,7 @@ namespace {
 constexpr size_t kTablesSmem = sizeof(float) * ((size_t)kB * kPad + kB * kD + 3 * kB + kB * kB);
 constexpr size_t kRowsSmem = sizeof(float) * ((size_t)4 * kRB * kPad + 2 * kB * kPad +
                                               6 * kB * kPadB + kB * kB + 4 * kB + 4 * kB + 3);
-constexpr size_t kFinishSmem = sizeof(float) * ((size_t)2 * kB * kD + 4 * kB * kB + 11 * kB);
+constexpr size_t kFinishSmem = sizeof(float) * ((size_t)4 * kB * kB + 11 * kB);
 
 }  // namespace
 
@@ -854,6 +864,7 @@ int linear_bwd_launch(const LinArgs& a, int heads, const float* M0, const float*
   bwd_tables_kernel<<<cells, kThreads, kTablesSmem, st>>>(p);
   bwd_rows_kernel<<<heads * kR, kThreads, kRowsSmem, st>>>(p);
   bwd_finish_kernel<<<cells, kThreads, kFinishSmem, st>>>(p);
+  bwd_partials_kernel<<<152 * 8, kThreads, 0, st>>>(p);
   return cudaGetLastError() == cudaSuccess ? ATLAS_OK : ATLAS_ERR_CUDA;
 }
 
