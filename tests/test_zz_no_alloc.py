@@ -10,7 +10,7 @@ in scratch, and checks four things on two calls in a row with different inputs
 reads would show): the outputs equal those of atlas_mem_forward bit for bit
 (same kernels, same inputs), they match the fp64 oracle within the bf16
 tolerance, the device status word stays 0, and the free device memory reported
-by the driver is the same before and after the two calls (nothing was
+by the CUDA driver (cudaMemGetInfo) is the same before and after the two calls (nothing was
 allocated).  This file is named to be collected last.
 """
 import ctypes
