@@ -41,7 +41,9 @@
 //   bwd_rows_kernel    (head x 32-row block): the forward once, keeping every
 //                      chunk-start state, then the reverse over the chunks;
 //                      writes dV, dM_0 and per-row-block partial sums;
-//   bwd_finish_kernel  (head x chunk): sums the partials, dP, the gate scans, dK, dQ.
+//   bwd_finish_kernel  (head x chunk): sums the gate-term partials, dP, the gate
+//                      scans, the dP products of dK and dQ;
+//   bwd_partials_kernel (streaming): adds the row-block partials of dK and dQ.
 #include "common.cuh"
 #include "kernels.h"
 #include "simt_tiles.cuh"
